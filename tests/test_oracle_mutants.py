@@ -1,0 +1,115 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check that
+at least one pin catches each: the pins are chosen so that a dropped term, a
+wrong sign or index, a transposed operand, a changed rounding order or a
+misread choice of the pages fails one of them."""
+import os
+
+import pytest
+
+import oracle
+import test_oracle_brute as tb
+import test_oracle_closed_form as tc
+import test_oracle_hand as th
+import test_oracle_invariants as ti
+import test_oracle_math as tm
+
+# (name, text in rnn_oracle.c, replacement)
+MUTANTS = [
+    ("k-descending dot", "for (long k = 0; k < K; ++k) acc = acc + x[k] * w[k];",
+     "for (long k = K - 1; k >= 0; --k) acc = acc + x[k] * w[k];"),
+    ("dot drops first term", "for (long k = 0; k < K; ++k) acc = acc + x[k] * w[k];",
+     "for (long k = 1; k < K; ++k) acc = acc + x[k] * w[k];"),
+    ("W index as [input, gates*hidden]", "xw[j] = o_dot(x, a->W + (d * GH + j) * a->I, a->I);",
+     "{ float s = 0.0f; for (long k = 0; k < a->I; ++k) s = s + x[k] * a->W[d * GH * a->I + k * GH + j]; xw[j] = s; }"),
+    ("RNN biases pre-summed", "if (a->B) { pre = pre + Wb[u]; pre = pre + Rb[u]; }",
+     "if (a->B) { pre = pre + (Wb[u] + Rb[u]); }"),
+    ("RNN drops Rb", "if (a->B) { pre = pre + Wb[u]; pre = pre + Rb[u]; }",
+     "if (a->B) { pre = pre + Wb[u]; }"),
+    ("GRU z/r swapped", "float pz = xw[u] + o_dot(h, Rd + u * H, H);",
+     "float pz = xw[H + u] + o_dot(h, Rd + (H + u) * H, H);"),
+    ("GRU update weights swapped", "hn[u] = (1.0f - z[u]) * ht + z[u] * h[u];",
+     "hn[u] = z[u] * ht + (1.0f - z[u]) * h[u];"),
+    ("GRU lbr0 without reset", "for (long k = 0; k < H; ++k) rh[k] = r[k] * h[k];",
+     "for (long k = 0; k < H; ++k) rh[k] = h[k];"),
+    ("GRU lbr1 biases exchanged", "ph = (xw[2 * H + u] + r[u] * (rec + Rb[2 * H + u])) + Wb[2 * H + u];",
+     "ph = (xw[2 * H + u] + r[u] * (rec + Wb[2 * H + u])) + Rb[2 * H + u];"),
+    ("LSTM o/f gates swapped", "float po = xw[H + u] + o_dot(h, Rd + (H + u) * H, H);",
+     "float po = xw[2 * H + u] + o_dot(h, Rd + (2 * H + u) * H, H);"),
+    ("LSTM Po with previous cell", "if (a->P) po = po + Po[u] * cn[u];",
+     "if (a->P) po = po + Po[u] * c[u];"),
+    ("LSTM drops Pf", "pf = pf + Pf[u] * c[u];", "pf = pf;"),
+    ("LSTM cell terms crossed", "cn[u] = fg * c[u] + ig * ct;", "cn[u] = fg * ct + ig * c[u];"),
+    ("input_forget uncoupled", "float fg = a->input_forget ? 1.0f - ig :", "float fg = a->input_forget ? ig :"),
+    ("LSTM h uses g", "hn[u] = og * o_act(&acts[2], cn[u]);", "hn[u] = og * o_act(&acts[1], cn[u]);"),
+    ("clip lower bound sign", "if (v < -a->clip) return -a->clip;", "if (v < -a->clip) return a->clip;"),
+    ("clip 0 clamps", "a.has_clip = clip > 0.0f;", "a.has_clip = clip >= 0.0f;"),
+    ("reverse ignores lens", "long t = reverse ? L - 1 - s : s;", "long t = reverse ? a->S - 1 - s : s;"),
+    ("len-0 row returns initial state", "yh[u] = L > 0 ? o_canon(h[u]) : 0.0f;", "yh[u] = o_canon(h[u]);"),
+    ("layout-1 Y index", "((n * a->S + t) * a->dirs + d) * a->H;", "((n * a->dirs + d) * a->S + t) * a->H;"),
+    ("layout-1 X index", "(n * a->S + t) * a->I;", "(t * a->N + n) * a->I;"),
+    ("beta shares the alpha cursor", "if (beta && cb < n_beta) list[i].beta = beta[cb];",
+     "if (beta && ca - 1 < n_beta && ca > 0) list[i].beta = beta[ca - 1];"),
+    ("second set ignored", "int base = (n_list == 2 * k && d == 1) ? k : 0;", "int base = 0;"),
+    ("exp drops r^3 term", "p = p * r + E3;", "p = p * r;"),
+    ("tanh large-range formula", "y = 1.0f - 2.0f / (e + 1.0f);", "y = 1.0f - 1.0f / (e + 1.0f);"),
+    ("sigmoid sign", "return 1.0f / (1.0f + oracle_exp(-x));", "return 1.0f / (1.0f + oracle_exp(x));"),
+    ("hardsigmoid upper clamp", "(v > 1.0f ? 1.0f : v)", "(v > 1.0f ? v : v)"),
+    ("softplus threshold", "x > 20.0f ? x : oracle_log", "x > 2.0f ? x : oracle_log"),
+    ("elu drops -1", "alpha * (oracle_exp(x) - 1.0f)", "alpha * oracle_exp(x)"),
+    ("relu drops NaN", "case OA_RELU:            return x < 0.0f ? 0.0f : x;",
+     "case OA_RELU:            return !(x >= 0.0f) ? 0.0f : x;"),
+    ("NaN not canonical", "return o_isnan(x) ? o_from_bits(0x7FC00000u) : x;", "return x;"),
+    ("leakyrelu default alpha", "case OA_LEAKYRELU: return 0.01f;", "case OA_LEAKYRELU: return 0.1f;"),
+]
+
+
+def _battery():
+    """Run the pins; return the names of those that fail."""
+    checks = []
+    for p in th.FILES:
+        checks.append((f"golden {os.path.basename(p)}", lambda p=p: th.test_golden_case(p)))
+    checks.append(("nan canonical", th.test_nan_outputs_are_canonical))
+    checks.append(("bidi lens hand", th.test_bidirectional_lens_combines_both_hand_cases))
+    for s in range(25):
+        checks.append((f"brute {s}", lambda s=s: tb.test_oracle_matches_float64_brute_force(s)))
+    checks.append(("closed form", lambda: tc.test_affine_rnn_matches_integer_closed_form(0)))
+    checks.append(("closed form reverse", tc.test_reverse_affine_closed_form))
+    for s in range(3):
+        checks.append((f"reverse {s}", lambda s=s: ti.test_reverse_is_forward_on_flipped_rows(s)))
+        checks.append((f"bidi {s}", lambda s=s: ti.test_bidirectional_is_two_directions(s)))
+        checks.append((f"layout {s}", lambda s=s: ti.test_layout1_is_transposed_layout0(s)))
+        checks.append((f"lens {s}", lambda s=s: ti.test_sequence_lens_semantics(s)))
+    checks.append(("resolve page case", ti.test_resolve_page_black_box_case))
+    checks.append(("resolve workload", ti.test_resolve_lstm_bidi_workload))
+    checks.append(("resolve defaults", ti.test_resolve_defaults_and_case_and_single_set))
+    checks.append(("rnncell3", lambda: ti.test_rnncell3_one_step("tanh")))
+    checks.append(("bnns gru", ti.test_bnns_gru_reset_after_matmul))
+    for fn in (tm.test_exp_special_values, tm.test_log_special_values, tm.test_tanh_special_values,
+               tm.test_relu_points, tm.test_leaky_thresholded_points,
+               tm.test_hardsigmoid_affine_softsign_points, tm.test_softplus_points,
+               tm.test_elu_scaledtanh_points):
+        checks.append((fn.__name__, fn))
+    checks.append(("sigmoid sweep", tm.test_sigmoid_accuracy_sweep))
+    checks.append(("tanh sweep", tm.test_tanh_accuracy_sweep))
+    checks.append(("softplus elu sweep", tm.test_softplus_elu_softsign_sweeps))
+    failed = []
+    for name, fn in checks:
+        try:
+            fn()
+        except Exception:
+            failed.append(name)
+    return failed
+
+
+def test_unmutated_oracle_passes_battery():
+    assert _battery() == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(name, old, new, tmp_path):
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation anchor not unique/present: {old!r}"
+    lib = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    with oracle.use_library(lib):
+        failed = _battery()
+    assert failed, f"no pin caught the planted mistake: {name}"
