@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Throughput of the ONNX-semantics recurrent operator on GB300.
+
+One step = one rnn_run (weight pack, input projection, state set-up,
+persistent recurrence, mask epilogue) over one batch of the workload, inputs
+resident in HBM.  The default workload is the LSTM forward layer (seq 64,
+batch 32, input 256, hidden 512, peepholes).  The metric is cell-steps per
+second (seq * batch * dirs per step), aggregated over ranks; each rank runs
+an independent replica (the operator has no exchange between GPUs).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--mode exact|fast]
+                  [--workload NAME] [--impl ours|reference]
+
+The L2 (129 MB) is flushed between timed steps by writing a 256 MiB buffer
+outside the timed events.  Per-kernel times come from CUDA events the library
+records on its own stream around each kernel during the timed steps.  The
+reference arm (--impl reference) times the CPU oracle on the host, one batch
+row of the workload per step.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "cell-steps/sec (seq*batch*dirs per s) at 1 GB300; % of roofline per kernel"
+UNIT = "cell-steps/s"
+DEFAULT_WORKLOAD = "lstm_fwd_s64_b32_i256_h512"
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--lbr", type=int, default=0)
+    ap.add_argument("--mode", default="exact", choices=["exact", "fast"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
+def emit(obj, out=None):
+    line = json.dumps(obj)
+    print(line, flush=True)
+    if out:
+        with open(out, "a") as f:
+            f.write(line + "\n")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------- roofline
+
+def algorithmic(case):
+    """FLOPs of the recurrent and projection products, per run."""
+    G, H, I, D = case.gates, case.hidden_size, case.input_size, case.dirs
+    valid_rows_steps = case.valid_cell_steps()           # sum of lengths * dirs
+    rec = 2.0 * valid_rows_steps * G * H * H
+    proj = 2.0 * case.seq * case.batch * D * G * H * I
+    proj_bytes = 4.0 * (case.seq * case.batch * I + D * G * H * I + case.seq * case.batch * D * G * H)
+    return rec, proj, proj_bytes
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "onnx_recurrent_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload, mode, digest):
+    """DRAM bytes per launch from a committed ncu summary of the same sources."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            text = f.read()
+        m = re.search(r"traffic_key:\s*(\S+)\s+(\S+)\s+(\S+)\s+(\S+)\s+(\d+)", text)
+        if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == mode \
+                and m.group(4) == digest:
+            return int(m.group(5))
+    return None
+
+
+# ------------------------------------------------------------ our arm
+
+def run_ours(args, ws, rank, local):
+    import numpy as np
+    import torch
+
+    import onnx_recurrent_gb300 as orc
+    from onnx_recurrent_gb300.synth import WORKLOADS, workload
+
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        orc.build()
+    if dist:
+        dist.barrier()
+    orc.build()
+    orc.load()
+
+    case = workload(args.workload, lbr=args.lbr)
+    dev = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in case.tensors().items()}
+    plan = orc.rnn_plan_create(case.op, case.direction, case.hidden_size, case.input_size,
+                               activations=case.activations, alpha=case.alpha, beta=case.beta,
+                               clip=case.clip, layout=case.layout,
+                               linear_before_reset=case.linear_before_reset,
+                               input_forget=case.input_forget)
+    orc.rnn_plan_set_mode(plan, args.mode)
+    Y = torch.empty(case.y_shape(), device="cuda")
+    Yh = torch.empty(case.state_shape(), device="cuda")
+    Yc = torch.empty(case.state_shape(), device="cuda") if case.op == "LSTM" else None
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        orc.rnn_run(plan, dev["X"], dev["W"], dev["R"], dev["B"], dev["sequence_lens"],
+                    dev["initial_h"], dev["initial_c"], dev["P"], Y, Yh, Yc, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    orc.rnn_plan_sync(plan)
+    launches_per_step = orc.rnn_plan_last_launch_count(plan)
+    geometry = orc.rnn_plan_get_launch(plan)
+
+    # ---- timed region: inputs resident, L2 flushed between steps
+    orc.rnn_plan_set_timing(plan, True)
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+    orc.rnn_plan_sync(plan)
+    total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    kern_ms, runs = orc.rnn_plan_timing_totals(plan)
+    orc.rnn_plan_set_timing(plan, False)
+
+    # ---- end to end: pinned host inputs -> device -> run -> host outputs
+    host_in = {k: (None if v is None else torch.from_numpy(v).pin_memory()) for k, v in case.tensors().items()}
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (Y, Yh, Yc) if t is not None]
+    dev_out = [t for t in (Y, Yh, Yc) if t is not None]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values() if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    E = K
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E)]
+    for i in range(E):
+        flush.zero_()
+        eev[i][0].record(stream)
+        for k, v in host_in.items():
+            if v is not None:
+                dev[k].copy_(v, non_blocking=True)
+        step()
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    orc.rnn_plan_sync(plan)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev)
+
+    if dist:
+        t = torch.tensor([total_ms, e2e_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    cells = case.cell_steps()
+    value = cells * K * ws / (total_ms / 1e3)
+    e2e_value = cells * E * ws / (e2e_ms / 1e3)
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sms = props.multi_processor_count
+    peaks = measured_peaks()
+    clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    exact = args.mode == "exact"
+    alu_peak = sms * 128 * (1 if exact else 2) * clock_mhz * 1e6          # FLOP/s
+    rec_flops, proj_flops, proj_bytes = algorithmic(case)
+    avg = {k: (v / runs if runs else 0.0) for k, v in kern_ms.items()}
+    dominant = max(avg, key=avg.get)
+    digest = source_digest()
+
+    def roof(kernel):
+        ms = avg[kernel]
+        if kernel == "recurrence":
+            ach = rec_flops / (ms / 1e3) / 1e12 if ms else 0.0
+            return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
+                    "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
+                    "traffic": profiled_traffic(kernel, args.workload, args.mode, digest),
+                    "kernel": "rnn_recurrent_kernel", "avg_ms": round(ms, 5),
+                    "algorithmic_flops_per_launch": rec_flops,
+                    "peak_note": f"{'no' if exact else 'fused'} multiply-add: {sms} SMs x 128 FP32 "
+                                 f"lanes x {'1' if exact else '2'} FLOP x {clock_mhz:.0f} MHz (derived)"}
+        if kernel == "projection":
+            ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
+            return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
+                    "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
+                    "traffic": profiled_traffic(kernel, args.workload, args.mode, digest),
+                    "kernel": "proj_gemm_kernel", "avg_ms": round(ms, 5),
+                    "algorithmic_flops_per_launch": proj_flops}
+        return {"kernel": kernel, "avg_ms": round(ms, 5)}
+
+    clocks = sampler.summary(t0, t1) if sampler else None
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, see synth.py)",
+        "config": {"workload": args.workload, "description": WORKLOADS.get(args.workload, ""),
+                   "op": case.op, "direction": case.direction, "seq": case.seq,
+                   "batch": case.batch, "input": case.input_size, "hidden": case.hidden_size,
+                   "mode": args.mode, "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas x{ws}", "geometry": geometry,
+                   "valid_cell_steps_per_step": case.valid_cell_steps()},
+        "roofline": roof(dominant),
+        "kernels": {k: roof(k) for k in avg if avg[k] > 0},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "impl": "ours",
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        result["cpu_baseline"] = cpu_baseline(case)
+    emit(result, args.out)
+    if dist:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(case, budget_s=12.0):
+    """The oracle, as it stands, single-threaded on this host, on a bounded
+    sample of the workload's batch rows."""
+    import oracle
+    from oracle import rnn as oracle_rnn
+    a = case.attrs()
+    t = case.tensors()
+
+    def rows(b, e):
+        return oracle_rnn(a["op"], a["direction"], a["hidden_size"], a["input_size"], t["X"], t["W"],
+                          t["R"], B=t["B"], sequence_lens=t["sequence_lens"], initial_h=t["initial_h"],
+                          initial_c=t["initial_c"], P=t["P"], activations=a["activations"],
+                          alpha=a["alpha"], beta=a["beta"], clip=a["clip"], layout=a["layout"],
+                          linear_before_reset=a["linear_before_reset"],
+                          input_forget=a["input_forget"], rows=(b, e))
+    oracle.build()
+    t0 = time.perf_counter()
+    rows(0, 1)
+    one = time.perf_counter() - t0
+    n = max(1, min(case.batch, int(budget_s / max(one, 1e-6))))
+    t0 = time.perf_counter()
+    rows(0, n)
+    dt = time.perf_counter() - t0
+    import numpy as np
+    valid = n * case.seq * case.dirs if case.sequence_lens is None else \
+        int(np.asarray(case.sequence_lens[:n], np.int64).sum()) * case.dirs
+    return {"value": round(n * case.seq * case.dirs / dt, 2), "unit": UNIT, "cores": 1,
+            "kind": "oracle", "sample": f"batch rows 0..{n - 1} of the workload, all {case.seq} steps "
+                                        f"({valid} valid cell-steps), {dt:.1f} s"}
+
+
+# ------------------------------------------------------ reference arm
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import oracle
+    from onnx_recurrent_gb300.synth import WORKLOADS, workload
+    case = workload(args.workload, lbr=args.lbr)
+    a = case.attrs()
+    t = case.tensors()
+    oracle.build()
+
+    def one_row(r):
+        oracle.rnn(a["op"], a["direction"], a["hidden_size"], a["input_size"], t["X"], t["W"],
+                   t["R"], B=t["B"], sequence_lens=t["sequence_lens"], initial_h=t["initial_h"],
+                   initial_c=t["initial_c"], P=t["P"], activations=a["activations"],
+                   alpha=a["alpha"], beta=a["beta"], clip=a["clip"], layout=a["layout"],
+                   linear_before_reset=a["linear_before_reset"], input_forget=a["input_forget"],
+                   rows=(r, r + 1))
+    for i in range(args.warmup):
+        one_row(i % case.batch)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one_row(i % case.batch)
+    dt = time.perf_counter() - t0
+    per_step = case.seq * case.dirs
+    value = per_step * args.steps / dt
+    emit({"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+          "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+          "data": "synthetic (seeded, see synth.py)",
+          "config": {"workload": args.workload, "description": WORKLOADS.get(args.workload, ""),
+                     "mode": "exact", "sample": "one batch row per step"},
+          "impl": "reference",
+          "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                           "sample": f"one batch row ({case.seq} steps) of the workload per step"},
+          "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0},
+          "gpu_launches": 0}, args.out)
+
+
+def main():
+    args = parse_args()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

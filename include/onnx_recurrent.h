@@ -1,0 +1,197 @@
+/*
+ * onnx_recurrent.h -- C ABI of the GB300 (sm_103a) ONNX RNN / GRU / LSTM
+ * sequence operator.
+ *
+ * The operator is the one defined by the page "Recurrent operators: RNN, GRU,
+ * LSTM" (sections Support, Computation, Activations, Choices the specification
+ * leaves open, Exact mode, Fast mode, Limits), with the input and output
+ * tables of the page "ai.onnx.RNN" (webgpu-kernels README, Inputs / Outputs /
+ * Attributes).  Every step of a run executes in this library's own CUDA
+ * kernels; nothing falls back to the CPU.
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers are DEVICE pointers owned by the caller, dense, fp32
+ *     (sequence_lens int32), in the shapes below for the plan's layout.
+ *     S = seq_length, N = batch_size, I = input_size, H = hidden_size,
+ *     D = 2 for bidirectional else 1, G = 1 (RNN), 3 (GRU), 4 (LSTM).
+ *       X          layout 0: [S, N, I]        layout 1: [N, S, I]
+ *       W          [D, G*H, I]     gate blocks LSTM i,o,f,c; GRU z,r,h
+ *       R          [D, G*H, H]
+ *       B          [D, 2*G*H]      all W biases (gate order) then all R biases
+ *       P          [D, 3*H]        peepholes i, o, f (LSTM only)
+ *       initial_h, initial_c, Y_h, Y_c
+ *                  layout 0: [D, N, H]        layout 1: [N, D, H]
+ *       Y          layout 0: [S, D, N, H]     layout 1: [N, S, D, H]
+ *       sequence_lens  [N] int32
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Runs are
+ *     stream-ordered and asynchronous.
+ *   - A plan is not re-entrant: one run at a time per plan (it owns scratch).
+ *   - No C++ exception crosses this boundary.  A failing call returns a
+ *     status and leaves a message for rnn_last_error() on the calling thread.
+ */
+#ifndef ONNX_RECURRENT_H
+#define ONNX_RECURRENT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct rnn_plan* rnn_plan_t;
+
+typedef enum {
+    RNN_OK = 0,
+    RNN_ERR_INVALID_ARGUMENT = 1, /* bad attribute, enum, shape or pointer      */
+    RNN_ERR_INVALID_INPUT = 2,    /* a sequence length outside [0, seq_length]  */
+    RNN_ERR_UNSUPPORTED = 3,      /* scratch limit, or a shape with no launch   */
+    RNN_ERR_CUDA = 4,             /* a CUDA runtime call failed                 */
+    RNN_ERR_OOM = 5,              /* device scratch allocation failed           */
+    RNN_ERR_TIMEOUT = 6           /* the device-wide step barrier gave up       */
+} rnn_status;
+
+enum { RNN_OP_RNN = 0, RNN_OP_GRU = 1, RNN_OP_LSTM = 2 };
+enum { RNN_DIR_FORWARD = 0, RNN_DIR_REVERSE = 1, RNN_DIR_BIDIRECTIONAL = 2 };
+
+/* Arithmetic modes (page "Recurrent operators", Exact mode / Fast mode).
+ *   EXACT: fp32, canonical order (one accumulator per output, k increasing
+ *          from +0, every multiply and add rounded separately), the library's
+ *          own IEEE-only transcendentals; bit-identical to the CPU oracle.
+ *   FAST:  same order; the two matrix products use fused multiply-add and the
+ *          elementwise functions use CUDA's expf/tanhf/logf.  The gate
+ *          arithmetic stays unfused. */
+enum { RNN_MODE_EXACT = 0, RNN_MODE_FAST = 1 };
+
+/* Activation function ids (page "Recurrent operators", Activations). */
+enum {
+    RNN_ACT_RELU = 0, RNN_ACT_TANH = 1, RNN_ACT_SIGMOID = 2, RNN_ACT_AFFINE = 3,
+    RNN_ACT_LEAKYRELU = 4, RNN_ACT_THRESHOLDEDRELU = 5, RNN_ACT_SCALEDTANH = 6,
+    RNN_ACT_HARDSIGMOID = 7, RNN_ACT_ELU = 8, RNN_ACT_SOFTSIGN = 9, RNN_ACT_SOFTPLUS = 10
+};
+
+/* Create a plan (no device work; callable without a GPU).
+ * Page "Recurrent operators": Support, Activations, Choices the specification
+ * leaves open (hidden_size), Computation (clip).
+ *   op            RNN_OP_*.
+ *   direction     RNN_DIR_*.
+ *   hidden_size   H > 0 (0 or negative: RNN_ERR_INVALID_ARGUMENT).
+ *   input_size    I >= 0 (0 gives an all-zero input projection).
+ *   activations   NULL/0 for the defaults (LSTM Sigmoid,Tanh,Tanh; GRU
+ *                 Sigmoid,Tanh; RNN Tanh), else k or 2k names (k = 3, 2, 1),
+ *                 matched case-insensitively; one set serves both directions
+ *                 of a bidirectional layer, two sets are forward then reverse
+ *                 (a unidirectional op uses the first set).
+ *   alpha, beta   activation_alpha / activation_beta (may be NULL/0); read
+ *                 with separate cursors in activation order; missing values
+ *                 take each activation's default.  The arrays are copied.
+ *   clip          applied to every gate input when > 0; NaN or <= 0: no clip.
+ *   layout        0 or 1.
+ *   linear_before_reset, input_forget   0 or 1 (ignored by the ops they do
+ *                 not apply to).
+ * On success *out receives a plan to be released with rnn_plan_destroy. */
+rnn_status rnn_plan_create(rnn_plan_t* out, int op, int direction,
+                           int64_t hidden_size, int64_t input_size,
+                           const char* const* activations, int n_activations,
+                           const float* alpha, int n_alpha,
+                           const float* beta, int n_beta,
+                           float clip, int layout, int linear_before_reset,
+                           int input_forget);
+
+/* Run the operator on device tensors (shapes above).
+ * Page "Recurrent operators": Computation (projection, recurrent product,
+ * GRU second product, gate order of operations), Choices the specification
+ * leaves open (sequence_lens, zero-size, omitted inputs), Exact mode (NaN
+ * written as 0x7FC00000), Limits.
+ *   seq_length, batch_size  S >= 0, N >= 0 (the C ABI needs them explicitly).
+ *   X, W, R       required (W and R may be NULL after rnn_plan_set_weights).
+ *   B, sequence_lens, initial_h, initial_c, P   optional (NULL = absent:
+ *                 bias adds and peepholes are skipped, states start at +0,
+ *                 every row runs all S steps).
+ *   Y, Y_h, Y_c   optional outputs (NULL = not written); Y_c is LSTM only.
+ * Zero-size (S == 0 or N == 0): nothing runs; Y_h/Y_c receive the initial
+ * states or zeros.  If sequence_lens is given it is copied to the host and
+ * checked first (the call waits for that copy on `stream`): a length outside
+ * [0, S] returns RNN_ERR_INVALID_INPUT and nothing is written.  A run whose
+ * per-direction scratch (S*N*G*H + 4*N*H + G*H*(I+H) floats, the last term
+ * dropped for constant weights) reaches 2^30 floats returns
+ * RNN_ERR_UNSUPPORTED.  Otherwise the kernels are queued on `stream` and the
+ * call returns RNN_OK; device-side failures (a barrier timeout) are reported
+ * by rnn_plan_sync(). */
+rnn_status rnn_run(rnn_plan_t plan, int64_t seq_length, int64_t batch_size,
+                   const float* X, const float* W, const float* R, const float* B,
+                   const int32_t* sequence_lens, const float* initial_h,
+                   const float* initial_c, const float* P,
+                   float* Y, float* Y_h, float* Y_c, void* stream);
+
+/* Release a plan and its device scratch (waits for its last run).  NULL is
+ * ignored. */
+void rnn_plan_destroy(rnn_plan_t plan);
+
+/* ---------------------------------------------------------------- extras */
+
+/* Select RNN_MODE_EXACT (default) or RNN_MODE_FAST (page "Recurrent
+ * operators", Exact mode / Fast mode). */
+rnn_status rnn_plan_set_mode(rnn_plan_t plan, int mode);
+
+/* Declare W and R constant (page "Recurrent operators", Computation: weights
+ * are transposed once per plan when they are constants).  Packs them now on
+ * `stream` into plan-owned device memory; later runs ignore their W and R
+ * arguments.  W [D, G*H, I] and R [D, G*H, H] are device pointers; the
+ * input_size used is the plan's. */
+rnn_status rnn_plan_set_weights(rnn_plan_t plan, const float* W, const float* R,
+                                void* stream);
+
+/* Wait for the plan's last run and report its device status: RNN_OK, or
+ * RNN_ERR_TIMEOUT if the step barrier gave up (the outputs are then
+ * incomplete).  Clears the status. */
+rnn_status rnn_plan_sync(rnn_plan_t plan);
+
+/* The resolved activation of slot `slot` (0 = f, 1 = g, 2 = h) of direction
+ * `dir`: its RNN_ACT_* id and alpha, beta (page "Recurrent operators",
+ * Activations).  Slots the op does not use report fn = -1. */
+rnn_status rnn_plan_get_activation(rnn_plan_t plan, int dir, int slot, int* fn,
+                                   float* alpha, float* beta);
+
+/* Launch geometry of the recurrent kernel.  rnn_plan_set_launch overrides the
+ * planner's choice (0 = automatic) for tuning and testing: CTAs per
+ * direction, batch rows per thread (1, 2, 4 or 8) and whether R is kept
+ * resident in shared memory (1), streamed through it (0) or chosen (-1).
+ * Results do not depend on the geometry.  rnn_plan_get_launch reports the
+ * geometry of the last run. */
+rnn_status rnn_plan_set_launch(rnn_plan_t plan, int ctas_per_dir, int rows_per_thread,
+                               int r_resident);
+rnn_status rnn_plan_get_launch(rnn_plan_t plan, int* ctas_per_dir, int* rows_per_thread,
+                               int* r_resident, int* threads_per_cta, int* smem_bytes);
+
+/* Per-kernel device time, in milliseconds, measured with CUDA events that the
+ * run records on its own stream around each kernel while timing is enabled:
+ * out[0] weight pack, out[1] input projection, out[2] state set-up,
+ * out[3] recurrence, out[4] mask epilogue (0 when a kernel did not run).
+ * rnn_plan_set_timing(plan, 1) enables timing and clears the totals.
+ * rnn_plan_last_timing reports the last run (waits for it).
+ * rnn_plan_timing_totals reports the sums over every run since timing was
+ * enabled or the totals were last read, stores their number in *runs, waits
+ * for them and clears the totals.  Back-to-back timed runs never wait on the
+ * device: each run's events are read at most once, after the run. */
+rnn_status rnn_plan_set_timing(rnn_plan_t plan, int enable);
+rnn_status rnn_plan_last_timing(rnn_plan_t plan, float* out, int n);
+rnn_status rnn_plan_timing_totals(rnn_plan_t plan, float* out, int n, int* runs);
+
+/* Test hook for the barrier's failure path: limit each device-wide barrier
+ * wait to `spin_limit_ns` nanoseconds (0 restores the default of 2 s) and,
+ * if skip_cta >= 0, make that CTA of the recurrent grid withhold its first
+ * arrival, so that the wait runs out and the run reports RNN_ERR_TIMEOUT
+ * through rnn_plan_sync() with the device still usable. */
+rnn_status rnn_plan_debug_barrier(rnn_plan_t plan, int64_t spin_limit_ns, int skip_cta);
+
+/* Number of kernel launches queued by the last rnn_run on this plan. */
+int rnn_plan_last_launch_count(rnn_plan_t plan);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* rnn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ONNX_RECURRENT_H */

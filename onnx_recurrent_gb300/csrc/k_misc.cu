@@ -1,0 +1,123 @@
+// Small bandwidth-bound kernels around the two products.
+//   pack        W and R transposed to k-major with gate-interleaved columns
+//               (page "Recurrent operators: RNN, GRU, LSTM", Computation:
+//               weights are transposed once per plan when constant, otherwise
+//               on each run into scratch);
+//   state_init  the first h exchange buffer from initial_h (omitted inputs
+//               are zeros: Choices the specification leaves open);
+//   mask_tail   Y = 0 at the steps no row reaches (sequence_lens: Y is zero
+//               at t >= len).
+#include "rnn_internal.h"
+
+namespace rnngb {
+
+namespace {
+
+// dst[k][dst_col0 + u*G + g] = src[g*H + u][k] for one direction.
+__global__ void pack_kernel(const float* __restrict__ src, float* __restrict__ dst, int G, int64_t H,
+                            int64_t K, int64_t dst_ld, int64_t dst_col0)
+{
+    __shared__ float tile[32][33];
+    const int64_t GH = (int64_t)G * H;
+    const int64_t c0 = (int64_t)blockIdx.x * 32;   // packed column tile
+    const int64_t k0 = (int64_t)blockIdx.y * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+    for (int j = ty; j < 32; j += 8) {
+        const int64_t cp = c0 + j;
+        const int64_t k = k0 + tx;
+        if (cp < GH && k < K) {
+            const int64_t u = cp / G, g = cp - u * G;
+            tile[j][tx] = src[(g * H + u) * K + k];
+        }
+    }
+    __syncthreads();
+    for (int j = ty; j < 32; j += 8) {
+        const int64_t k = k0 + j;
+        const int64_t cp = c0 + tx;
+        if (k < K && cp < GH) dst[k * dst_ld + dst_col0 + cp] = tile[tx][j];
+    }
+}
+
+__global__ void state_init_kernel(const RecParams p)
+{
+    const int64_t total = (int64_t)p.D * p.H * p.npad;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i % p.npad;
+        const int64_t u = (i / p.npad) % p.H;
+        const int64_t d = i / ((int64_t)p.npad * p.H);
+        float v = 0.0f;
+        if (n < p.N && p.h0) {
+            const int64_t si = p.layout == 0 ? (d * p.N + n) * p.H + u : (n * p.D + d) * p.H + u;
+            v = p.h0[si];
+        }
+        p.hbuf[((d * 2) * p.H + u) * p.npad + n] = v;
+        p.hbuf[((d * 2 + 1) * p.H + u) * p.npad + n] = 0.0f;
+        if (p.rhbuf) p.rhbuf[(d * p.H + u) * p.npad + n] = 0.0f;
+    }
+    if (blockIdx.x == 0 && threadIdx.x < p.D) p.bar[threadIdx.x] = 0u;
+}
+
+__global__ void mask_tail_kernel(float* __restrict__ Y, int layout, int64_t S, int64_t D, int64_t N,
+                                 int64_t H, int64_t t0)
+{
+    const int64_t DH = D * H;
+    if (layout == 0) {
+        const int64_t begin = t0 * D * N * H, end = S * D * N * H;
+        for (int64_t i = begin + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < end;
+             i += (int64_t)gridDim.x * blockDim.x)
+            Y[i] = 0.0f;
+    } else {
+        const int64_t per_row = (S - t0) * DH;
+        const int64_t total = N * per_row;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+             i += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t n = i / per_row, r = i - n * per_row;
+            Y[(n * S + t0) * DH + r] = 0.0f;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const float* W, const float* R, float* Wt, float* Rt, int D, int G, int64_t H,
+                        int64_t I, cudaStream_t stream)
+{
+    const int64_t GH = (int64_t)G * H;
+    const dim3 block(32, 8);
+    for (int d = 0; d < D; ++d) {
+        if (W && Wt && I > 0) {
+            const dim3 grid((unsigned)((GH + 31) / 32), (unsigned)((I + 31) / 32));
+            pack_kernel<<<grid, block, 0, stream>>>(W + (size_t)d * GH * I, Wt, G, H, I, (int64_t)D * GH,
+                                                    (int64_t)d * GH);
+        }
+        if (R && Rt) {
+            const dim3 grid((unsigned)((GH + 31) / 32), (unsigned)((H + 31) / 32));
+            pack_kernel<<<grid, block, 0, stream>>>(R + (size_t)d * GH * H, Rt + (size_t)d * H * GH, G, H, H,
+                                                    GH, 0);
+        }
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream)
+{
+    const int64_t total = (int64_t)p.D * p.H * p.npad;
+    int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
+    if (blocks < 1) blocks = 1;
+    state_init_kernel<<<blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mask_tail(float* Y, int layout, int64_t S, int64_t D, int64_t N, int64_t H, int64_t t0,
+                             cudaStream_t stream)
+{
+    if (!Y || t0 >= S) return cudaSuccess;
+    const int64_t total = (S - t0) * D * N * H;
+    int blocks = (int)std::min<int64_t>((total + 255) / 256, 8192);
+    if (blocks < 1) blocks = 1;
+    mask_tail_kernel<<<blocks, 256, 0, stream>>>(Y, layout, S, D, N, H, t0);
+    return cudaGetLastError();
+}
+
+}  // namespace rnngb

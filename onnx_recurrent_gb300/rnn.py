@@ -1,0 +1,286 @@
+"""Thin ctypes binding of the C ABI in include/onnx_recurrent.h.
+
+Argument marshalling only: every step of a run executes in the CUDA library.
+PyTorch supplies device memory and streams.  The library must have been built
+(``onnx_recurrent_gb300.build()``); there is no fallback when it is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from . import _build
+
+OPS = {"RNN": 0, "GRU": 1, "LSTM": 2}
+DIRECTIONS = {"forward": 0, "reverse": 1, "bidirectional": 2}
+MODES = {"exact": 0, "fast": 1}
+ACT_NAMES = ["relu", "tanh", "sigmoid", "affine", "leakyrelu", "thresholdedrelu",
+             "scaledtanh", "hardsigmoid", "elu", "softsign", "softplus"]
+STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARGUMENT", 2: "RNN_ERR_INVALID_INPUT",
+          3: "RNN_ERR_UNSUPPORTED", 4: "RNN_ERR_CUDA", 5: "RNN_ERR_OOM", 6: "RNN_ERR_TIMEOUT"}
+HEADER = os.path.join(_build.ROOT, "include", "onnx_recurrent.h")
+
+_lib = None
+
+
+class RNNError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load the built library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built ({p}); call onnx_recurrent_gb300.build()")
+    lib = ctypes.CDLL(p)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    fp = ctypes.POINTER(ctypes.c_float)
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.rnn_plan_create.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i64,
+                                    ctypes.POINTER(ctypes.c_char_p), i32, fp, i32, fp, i32,
+                                    f32, i32, i32, i32]
+    lib.rnn_run.argtypes = [vp, i64, i64] + [vp] * 11 + [vp]
+    lib.rnn_plan_destroy.argtypes = [vp]
+    lib.rnn_plan_destroy.restype = None
+    lib.rnn_plan_set_mode.argtypes = [vp, i32]
+    lib.rnn_plan_set_weights.argtypes = [vp, vp, vp, vp]
+    lib.rnn_plan_sync.argtypes = [vp]
+    lib.rnn_plan_get_activation.argtypes = [vp, i32, i32, ip, fp, fp]
+    lib.rnn_plan_set_launch.argtypes = [vp, i32, i32, i32]
+    lib.rnn_plan_get_launch.argtypes = [vp, ip, ip, ip, ip, ip]
+    lib.rnn_plan_set_timing.argtypes = [vp, i32]
+    lib.rnn_plan_last_timing.argtypes = [vp, fp, i32]
+    lib.rnn_plan_timing_totals.argtypes = [vp, fp, i32, ip]
+    lib.rnn_plan_debug_barrier.argtypes = [vp, i64, i32]
+    lib.rnn_plan_last_launch_count.argtypes = [vp]
+    lib.rnn_plan_last_launch_count.restype = i32
+    lib.rnn_last_error.argtypes = []
+    lib.rnn_last_error.restype = ctypes.c_char_p
+    for name in ("rnn_plan_create", "rnn_run", "rnn_plan_set_mode", "rnn_plan_set_weights",
+                 "rnn_plan_sync", "rnn_plan_get_activation", "rnn_plan_set_launch",
+                 "rnn_plan_get_launch", "rnn_plan_set_timing", "rnn_plan_last_timing",
+                 "rnn_plan_timing_totals",
+                 "rnn_plan_debug_barrier"):
+        getattr(lib, name).restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/onnx_recurrent.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rnn_\w+)\s*\(", text)))
+
+
+def rnn_last_error() -> str:
+    return load().rnn_last_error().decode()
+
+
+def _check(st: int):
+    if st != 0:
+        raise RNNError(st, rnn_last_error())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """A plan handle plus the attributes it was created with."""
+
+    def __init__(self, handle, op, direction, hidden_size, input_size, layout):
+        self.handle = handle
+        self.op = op
+        self.direction = direction
+        self.hidden_size = hidden_size
+        self.input_size = input_size
+        self.layout = layout
+
+    @property
+    def dirs(self):
+        return 2 if self.direction == "bidirectional" else 1
+
+    def __del__(self):
+        try:
+            if self.handle:
+                rnn_plan_destroy(self)
+        except Exception:
+            pass
+
+
+def rnn_plan_create(op, direction, hidden_size, input_size, activations=None, alpha=None,
+                    beta=None, clip=None, layout=0, linear_before_reset=0, input_forget=0) -> Plan:
+    lib = load()
+    h = ctypes.c_void_p()
+    acts = None
+    nacts = 0
+    if activations:
+        acts = (ctypes.c_char_p * len(activations))(*[a.encode() for a in activations])
+        nacts = len(activations)
+
+    def farr(v):
+        if not v:
+            return None, 0
+        return (ctypes.c_float * len(v))(*[float(x) for x in v]), len(v)
+    al, nal = farr(alpha)
+    be, nbe = farr(beta)
+    c = float("nan") if clip is None else float(clip)
+    st = lib.rnn_plan_create(ctypes.byref(h), OPS[op] if isinstance(op, str) else int(op),
+                             DIRECTIONS[direction] if isinstance(direction, str) else int(direction),
+                             int(hidden_size), int(input_size), acts, nacts, al, nal, be, nbe, c,
+                             int(layout), int(linear_before_reset), int(input_forget))
+    _check(st)
+    return Plan(h, op, direction, int(hidden_size), int(input_size), int(layout))
+
+
+def rnn_plan_destroy(plan: Plan):
+    if plan.handle:
+        load().rnn_plan_destroy(plan.handle)
+        plan.handle = None
+
+
+def rnn_plan_set_mode(plan: Plan, mode):
+    _check(load().rnn_plan_set_mode(plan.handle, MODES[mode] if isinstance(mode, str) else int(mode)))
+
+
+def rnn_plan_set_weights(plan: Plan, W, R, stream=None):
+    _check(load().rnn_plan_set_weights(plan.handle, _ptr(W), _ptr(R), _stream(stream)))
+
+
+def rnn_plan_sync(plan: Plan):
+    _check(load().rnn_plan_sync(plan.handle))
+
+
+def rnn_plan_get_activation(plan: Plan, d: int, slot: int):
+    fn = ctypes.c_int()
+    a = ctypes.c_float()
+    b = ctypes.c_float()
+    _check(load().rnn_plan_get_activation(plan.handle, d, slot, ctypes.byref(fn), ctypes.byref(a),
+                                          ctypes.byref(b)))
+    return (ACT_NAMES[fn.value] if fn.value >= 0 else None), a.value, b.value
+
+
+def rnn_plan_set_launch(plan: Plan, ctas_per_dir=0, rows_per_thread=0, r_resident=-1):
+    _check(load().rnn_plan_set_launch(plan.handle, int(ctas_per_dir), int(rows_per_thread),
+                                      int(r_resident)))
+
+
+def rnn_plan_get_launch(plan: Plan) -> dict:
+    v = [ctypes.c_int() for _ in range(5)]
+    _check(load().rnn_plan_get_launch(plan.handle, *[ctypes.byref(x) for x in v]))
+    return dict(zip(["ctas_per_dir", "rows_per_thread", "r_resident", "threads", "smem_bytes"],
+                    [x.value for x in v]))
+
+
+def rnn_plan_set_timing(plan: Plan, enable=True):
+    _check(load().rnn_plan_set_timing(plan.handle, int(bool(enable))))
+
+
+def rnn_plan_last_timing(plan: Plan) -> dict:
+    out = (ctypes.c_float * 5)()
+    _check(load().rnn_plan_last_timing(plan.handle, out, 5))
+    return dict(zip(["pack", "projection", "setup", "recurrence", "mask"], list(out)))
+
+
+def rnn_plan_timing_totals(plan: Plan) -> tuple[dict, int]:
+    """Per-kernel milliseconds summed over the runs since the last read."""
+    out = (ctypes.c_float * 5)()
+    runs = ctypes.c_int()
+    _check(load().rnn_plan_timing_totals(plan.handle, out, 5, ctypes.byref(runs)))
+    return dict(zip(["pack", "projection", "setup", "recurrence", "mask"], list(out))), runs.value
+
+
+def rnn_plan_debug_barrier(plan: Plan, spin_limit_ns=0, skip_cta=-1):
+    _check(load().rnn_plan_debug_barrier(plan.handle, int(spin_limit_ns), int(skip_cta)))
+
+
+def rnn_plan_last_launch_count(plan: Plan) -> int:
+    return int(load().rnn_plan_last_launch_count(plan.handle))
+
+
+def _need(t, shape, name, dtype="float32"):
+    import torch
+    if t is None:
+        return
+    want = torch.float32 if dtype == "float32" else torch.int32
+    if t.dtype != want:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def shapes(plan: Plan, seq, batch):
+    G = {"RNN": 1, "GRU": 3, "LSTM": 4}[plan.op] if isinstance(plan.op, str) else [1, 3, 4][plan.op]
+    D, H, I = plan.dirs, plan.hidden_size, plan.input_size
+    lay = plan.layout
+    return dict(
+        X=(seq, batch, I) if lay == 0 else (batch, seq, I),
+        W=(D, G * H, I), R=(D, G * H, H), B=(D, 2 * G * H), P=(D, 3 * H),
+        state=(D, batch, H) if lay == 0 else (batch, D, H),
+        Y=(seq, D, batch, H) if lay == 0 else (batch, seq, D, H),
+        lens=(batch,))
+
+
+def rnn_run(plan: Plan, X, W, R, B=None, sequence_lens=None, initial_h=None, initial_c=None,
+            P=None, Y=None, Y_h=None, Y_c=None, stream=None):
+    """Run on CUDA tensors; outputs are written into Y, Y_h, Y_c (each optional)."""
+    seq, batch = (X.shape[0], X.shape[1]) if plan.layout == 0 else (X.shape[1], X.shape[0])
+    sh = shapes(plan, seq, batch)
+    _need(X, sh["X"], "X")
+    _need(W, sh["W"], "W")
+    _need(R, sh["R"], "R")
+    _need(B, sh["B"], "B")
+    _need(P, sh["P"], "P")
+    _need(initial_h, sh["state"], "initial_h")
+    _need(initial_c, sh["state"], "initial_c")
+    _need(sequence_lens, sh["lens"], "sequence_lens", "int32")
+    _need(Y, sh["Y"], "Y")
+    _need(Y_h, sh["state"], "Y_h")
+    _need(Y_c, sh["state"], "Y_c")
+    st = load().rnn_run(plan.handle, int(seq), int(batch), _ptr(X), _ptr(W), _ptr(R), _ptr(B),
+                        _ptr(sequence_lens), _ptr(initial_h), _ptr(initial_c), _ptr(P), _ptr(Y),
+                        _ptr(Y_h), _ptr(Y_c), _stream(stream))
+    _check(st)
+
+
+def run(plan: Plan, X, W, R, B=None, sequence_lens=None, initial_h=None, initial_c=None, P=None,
+        stream=None, want_y=True):
+    """Allocate the outputs (torch.empty on X's device) and run; returns (Y, Y_h, Y_c)."""
+    import torch
+    seq, batch = (X.shape[0], X.shape[1]) if plan.layout == 0 else (X.shape[1], X.shape[0])
+    sh = shapes(plan, seq, batch)
+    Y = torch.empty(sh["Y"], dtype=torch.float32, device=X.device) if want_y else None
+    Yh = torch.empty(sh["state"], dtype=torch.float32, device=X.device)
+    is_lstm = plan.op in ("LSTM", 2)
+    Yc = torch.empty(sh["state"], dtype=torch.float32, device=X.device) if is_lstm else None
+    rnn_run(plan, X, W, R, B, sequence_lens, initial_h, initial_c, P, Y, Yh, Yc, stream)
+    return Y, Yh, Yc

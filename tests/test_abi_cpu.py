@@ -1,0 +1,110 @@
+"""The C-ABI library without a GPU: it builds, loads and exports every symbol
+include/onnx_recurrent.h declares; plan creation validates the attributes and
+resolves activations exactly as the oracle does; rnn_run rejects bad sizes and
+the scratch limit ("Recurrent operators: RNN, GRU, LSTM", Limits) before any
+device work."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import onnx_recurrent_gb300 as orc
+import oracle
+from onnx_recurrent_gb300 import rnn as rb
+from onnx_recurrent_gb300.synth import random_case, workload
+
+
+@pytest.fixture(scope="module")
+def lib():
+    orc.build()
+    return orc.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = rb.declared_functions()
+    assert "rnn_plan_create" in names and "rnn_run" in names and "rnn_plan_destroy" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_plan_create_and_destroy_without_gpu(lib):
+    p = orc.rnn_plan_create("LSTM", "bidirectional", 8, 4)
+    orc.rnn_plan_destroy(p)
+    orc.rnn_plan_destroy(p)   # idempotent in the binding
+
+
+@pytest.mark.parametrize("kw", [dict(hidden_size=0), dict(hidden_size=-3), dict(input_size=-1),
+                                dict(layout=2), dict(linear_before_reset=2), dict(input_forget=5),
+                                dict(activations=["Sigmoid"]),
+                                dict(activations=["Sigmoid", "Tanh", "NoSuch"]),
+                                dict(op=7), dict(direction=9)])
+def test_plan_create_rejects(lib, kw):
+    args = dict(op="LSTM", direction="forward", hidden_size=4, input_size=3)
+    args.update(kw)
+    with pytest.raises(rb.RNNError) as e:
+        orc.rnn_plan_create(**args)
+    assert e.value.status == 1
+    assert orc.rnn_last_error()
+
+
+def _resolved_lib(case):
+    p = orc.rnn_plan_create(case.op, case.direction, case.hidden_size, case.input_size,
+                            activations=case.activations, alpha=case.alpha, beta=case.beta)
+    k = {"RNN": 1, "GRU": 2, "LSTM": 3}[case.op]
+    out = [[orc.rnn_plan_get_activation(p, d, s) for s in range(k)] for d in range(case.dirs)]
+    orc.rnn_plan_destroy(p)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_activation_resolution_matches_oracle(lib, seed):
+    c = random_case(seed)
+    ref = oracle.resolve_activations(c.op, c.direction, c.activations, c.alpha, c.beta)
+    got = _resolved_lib(c)
+    assert got == ref
+
+
+def test_activation_resolution_workload(lib):
+    c = workload("lstm_bidi_s512_b128_i1024_h1024")
+    assert _resolved_lib(c) == oracle.resolve_activations(c.op, c.direction, c.activations,
+                                                          c.alpha, c.beta)
+
+
+def test_run_rejects_sizes_and_scratch_limit_before_device_work(lib):
+    p = orc.rnn_plan_create("LSTM", "bidirectional", 1024, 1024)
+    fake = ctypes.c_void_p(0x1000)
+    st = lib.rnn_run(p.handle, -1, 4, fake, fake, fake, None, None, None, None, None, None, None,
+                     None, None)
+    assert st == 1
+    # per direction: S*N*G*H + 4*N*H + G*H*(I+H) >= 2^30 floats -> Unsupported
+    st = lib.rnn_run(p.handle, 4096, 128, fake, fake, fake, None, None, None, None, None, None,
+                     None, None, None)
+    assert st == 3 and "2^30" in orc.rnn_last_error()
+    orc.rnn_plan_destroy(p)
+
+
+def test_set_launch_validation(lib):
+    p = orc.rnn_plan_create("GRU", "forward", 16, 8)
+    with pytest.raises(rb.RNNError):
+        orc.rnn_plan_set_launch(p, 4, 3, -1)
+    with pytest.raises(rb.RNNError):
+        orc.rnn_plan_set_launch(p, 4, 1, 2)
+    orc.rnn_plan_set_launch(p, 4, 2, 0)
+    with pytest.raises(rb.RNNError):
+        orc.rnn_plan_set_mode(p, 9)
+    orc.rnn_plan_set_mode(p, "fast")
+    orc.rnn_plan_destroy(p)
+
+
+def test_product_does_not_import_or_link_the_oracle():
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(root, "onnx_recurrent_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                with open(os.path.join(dirpath, f)) as fh:
+                    text = fh.read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "rnn_oracle" not in text and "liboracle" not in text, f

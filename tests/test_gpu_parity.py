@@ -1,0 +1,215 @@
+"""CUDA path vs the oracle, through the C ABI.
+
+Exact mode must be bit-identical to the oracle (page "Recurrent operators:
+RNN, GRU, LSTM", Exact mode); fast mode must stay within 1e-5 absolute (scaled
+by max(1, |value|) for the unbounded cell state).  Small cases cover the
+attribute space and several tiles with ragged tails; forced launch geometries
+(CTAs per direction, rows per thread, R resident or streamed) must all give
+the same bits; the five workloads run at full size and are compared on
+sampled batch rows, which the oracle computes independently (rows of a batch
+never interact)."""
+import numpy as np
+import pytest
+
+import onnx_recurrent_gb300 as orc
+from gpu_helpers import gpu_case, row_slice
+from helpers import assert_bits_equal, oracle_case
+from onnx_recurrent_gb300.synth import make_case, random_case, workload
+
+pytestmark = pytest.mark.gpu
+
+FAST_TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    orc.build()
+
+
+def _compare_exact(case, got, ref, what=""):
+    for name, g, r in zip(("Y", "Y_h", "Y_c"), got, ref):
+        if r is None or g is None:
+            continue
+        assert_bits_equal(g, r, f"{what} {name}")
+
+
+def _compare_fast(got, ref, tol=FAST_TOL):
+    for name, g, r in zip(("Y", "Y_h", "Y_c"), got, ref):
+        if r is None or g is None:
+            continue
+        scale = max(1.0, float(np.abs(r).max(initial=0.0))) if name == "Y_c" else 1.0
+        err = float(np.abs(g.astype(np.float64) - r).max(initial=0.0))
+        assert err <= tol * scale, f"{name}: max abs error {err:.3e} > {tol * scale:.3e}"
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_random_small_exact_is_bit_identical(seed):
+    c = random_case(seed)
+    _compare_exact(c, gpu_case(c, "exact"), oracle_case(c), f"seed {seed}")
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_small_fast_within_tolerance(seed):
+    c = random_case(seed)
+    _compare_fast(gpu_case(c, "fast"), oracle_case(c))
+
+
+GEOMETRIES = [(1, 1, 1), (2, 1, 1), (3, 2, 0), (5, 4, 1), (7, 8, 0), (13, 1, 0), (70, 2, 1),
+              (4, 8, 1), (9, 4, 0)]
+
+
+@pytest.mark.parametrize("op,direction,lbr", [("RNN", "bidirectional", 0), ("GRU", "forward", 0),
+                                              ("GRU", "bidirectional", 1), ("LSTM", "reverse", 0),
+                                              ("LSTM", "bidirectional", 0)])
+def test_every_launch_geometry_gives_the_same_bits(op, direction, lbr):
+    c = make_case(op, direction, 9, 11, 33, 70, seed=21, layout=1, with_P=True, h0_scale=0.5,
+                  c0_scale=0.5, lens=("uniform", 0, 9), linear_before_reset=lbr, clip=2.0,
+                  activations=None)
+    ref = oracle_case(c)
+    for g in GEOMETRIES:
+        _compare_exact(c, gpu_case(c, "exact", launch=g), ref, f"geometry {g}")
+
+
+@pytest.mark.parametrize("g", [(2, 1, 0), (5, 2, 1)])
+def test_fast_mode_is_geometry_independent(g):
+    c = make_case("LSTM", "bidirectional", 6, 9, 20, 37, seed=5, with_P=True, h0_scale=0.5)
+    a = gpu_case(c, "fast", launch=(1, 1, 1))
+    b = gpu_case(c, "fast", launch=g)
+    for x, y in zip(a, b):
+        assert_bits_equal(x, y, "fast mode across geometries")
+
+
+def test_constant_weights_path():
+    c = random_case(3, op="LSTM", direction="bidirectional")
+    _compare_exact(c, gpu_case(c, "exact", const_weights=True), oracle_case(c), "const")
+
+
+@pytest.mark.parametrize("want", [("Y",), ("Y_h",), ("Y_c",), ("Y_h", "Y_c")])
+def test_optional_outputs(want):
+    c = random_case(4, op="LSTM")
+    got = gpu_case(c, "exact", want=want)
+    ref = oracle_case(c)
+    for name, g, r in zip(("Y", "Y_h", "Y_c"), got, ref):
+        if name in want:
+            assert_bits_equal(g, r, name)
+        else:
+            assert g is None
+
+
+@pytest.mark.parametrize("op", ["RNN", "GRU", "LSTM"])
+def test_zero_size(op):
+    c = make_case(op, "bidirectional", 0, 3, 4, 5, seed=1, h0_scale=0.5, c0_scale=0.5)
+    Y, Yh, Yc = gpu_case(c)
+    assert Y.size == 0
+    assert_bits_equal(Yh, c.initial_h, "Y_h = initial_h")
+    if op == "LSTM":
+        assert_bits_equal(Yc, c.initial_c, "Y_c = initial_c")
+    c2 = c.with_(initial_h=None, initial_c=None)
+    _, Yh2, _ = gpu_case(c2)
+    assert np.all(Yh2 == 0)
+
+
+def test_invalid_lengths_write_nothing():
+    import torch
+    c = make_case("GRU", "forward", 4, 3, 2, 3, seed=2, lens=[1, 5, 2])
+    plan = orc.rnn_plan_create("GRU", "forward", 3, 2)
+    t = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in c.tensors().items()}
+    Y = torch.full(c.y_shape(), 7.0, device="cuda")
+    Yh = torch.full(c.state_shape(), 7.0, device="cuda")
+    with pytest.raises(orc.RNNError) as e:
+        orc.rnn_run(plan, t["X"], t["W"], t["R"], t["B"], t["sequence_lens"], Y=Y, Y_h=Yh)
+    assert e.value.status == 2
+    torch.cuda.synchronize()
+    assert bool((Y == 7.0).all()) and bool((Yh == 7.0).all())
+    orc.rnn_plan_destroy(plan)
+
+
+def test_barrier_timeout_is_reported_and_the_device_stays_usable():
+    # One CTA withholds its arrival at the first step barrier; every wait is
+    # bounded (50 ms here), so the grid exits and the status says TIMEOUT.
+    c = make_case("LSTM", "forward", 5, 4, 8, 64, seed=9, h0_scale=0.5)
+    plan = orc.rnn_plan_create("LSTM", "forward", 64, 8)
+    orc.rnn_plan_set_launch(plan, 4, 1, 1)
+    orc.rnn_plan_debug_barrier(plan, 50_000_000, 1)
+    import torch
+    t = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in c.tensors().items()}
+    Yh = torch.zeros(c.state_shape(), device="cuda")
+    orc.rnn_run(plan, t["X"], t["W"], t["R"], t["B"], initial_h=t["initial_h"], Y_h=Yh)
+    with pytest.raises(orc.RNNError) as e:
+        orc.rnn_plan_sync(plan)
+    assert e.value.status == 6
+    orc.rnn_plan_debug_barrier(plan, 0, -1)
+    got = gpu_case(c, "exact", plan=plan)
+    _compare_exact(c, got, oracle_case(c), "after timeout")
+    orc.rnn_plan_destroy(plan)
+
+
+def test_timing_and_launch_count():
+    c = random_case(8, op="GRU", lens=("uniform", 0, 3))
+    Y, Yh, Yc, plan = gpu_case(c, "exact", keep_plan=True)
+    orc.rnn_plan_set_timing(plan, True)
+    gpu_case(c, "exact", plan=plan)
+    tm = orc.rnn_plan_last_timing(plan)
+    assert tm["recurrence"] > 0 and tm["projection"] > 0
+    assert orc.rnn_plan_last_launch_count(plan) >= 4
+    orc.rnn_plan_destroy(plan)
+
+
+# ------------------------------------------------------------ workloads
+
+def _sample_rows(c, k):
+    N = c.batch
+    rows = {0, N - 1}
+    if c.sequence_lens is not None:
+        rows.add(int(np.argmax(c.sequence_lens)))
+        rows.add(int(np.argmin(c.sequence_lens)))
+    rng = np.random.default_rng(123)
+    while len(rows) < min(k, N):
+        rows.add(int(rng.integers(N)))
+    return sorted(rows)
+
+
+def _workload_check(c, rows, mode="exact"):
+    got = gpu_case(c, mode)
+    ref = oracle_case(c, rows=rows, threaded=True)
+    gs = (row_slice(c, rows, got[0], "Y"), row_slice(c, rows, got[1], "state"),
+          row_slice(c, rows, got[2], "state"))
+    rs = (row_slice(c, rows, ref[0], "Y"), row_slice(c, rows, ref[1], "state"),
+          row_slice(c, rows, ref[2], "state"))
+    if mode == "exact":
+        _compare_exact(c, gs, rs, c.name)
+    else:
+        _compare_fast(gs, rs)
+    # at any size: Y is +0 past every row's length
+    if c.sequence_lens is not None:
+        Y = got[0]
+        for n, L in enumerate(c.sequence_lens):
+            tail = Y[L:, :, n] if c.layout == 0 else Y[n, L:]
+            assert np.all(tail.view(np.uint32) == 0), f"row {n}: Y not zero past len {L}"
+    return got
+
+
+WORKLOAD_CASES = [("rnn_fwd_s8_b1_i16_h128", 0, 1), ("lstm_fwd_s64_b32_i256_h512", 0, 8),
+                  ("gru_bidi_s128_b64_i512_h1024", 0, 6), ("gru_bidi_s128_b64_i512_h1024", 1, 6),
+                  ("lstm_bidi_s512_b128_i1024_h1024", 0, 3), ("gru_rev_s4096_b4_i256_h2048", 1, 1)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,lbr,k", WORKLOAD_CASES, ids=[f"{w[0]}-lbr{w[1]}" for w in WORKLOAD_CASES])
+def test_workload_full_size_exact(name, lbr, k):
+    c = workload(name, lbr=lbr)
+    _workload_check(c, _sample_rows(c, k), "exact")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,lbr,k", WORKLOAD_CASES[:5], ids=[f"{w[0]}-lbr{w[1]}" for w in WORKLOAD_CASES[:5]])
+def test_workload_full_size_fast(name, lbr, k):
+    c = workload(name, lbr=lbr)
+    _workload_check(c, _sample_rows(c, min(k, 3)), "fast")
+
+
+def test_rnn_workload_absent_and_zero_initial_state():
+    a = gpu_case(workload("rnn_fwd_s8_b1_i16_h128"))
+    b = gpu_case(workload("rnn_fwd_s8_b1_i16_h128", initial_h_zero=True))
+    for x, y in zip(a[:2], b[:2]):
+        assert_bits_equal(x, y)
