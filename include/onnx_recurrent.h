@@ -187,6 +187,33 @@ rnn_status rnn_plan_debug_barrier(rnn_plan_t plan, int64_t spin_limit_ns, int sk
 /* Number of kernel launches queued by the last rnn_run on this plan. */
 int rnn_plan_last_launch_count(rnn_plan_t plan);
 
+/* rnn_run for callers that cannot allocate device memory while they run:
+ * for example a serving runtime that hands all of a GPU's memory to its own
+ * pool at start-up, or a latency-critical caller for which cudaMalloc and
+ * cudaFree (which synchronises the device) are not acceptable mid-run.  The
+ * pages describe no such entry point: it has no counterpart there.
+ * Same arguments, results and checks as rnn_run, but the call allocates
+ * nothing: its scratch comes from one fixed 32 MiB device array that every
+ * GPU loading this library holds until the process exits, and
+ * sequence_lens (at most 4096 rows) is checked through a stack buffer.
+ * A run whose scratch (256 bytes of control words, the packed weights unless
+ * they are constant, seq*batch*D*G*H floats of projection and the h exchange
+ * buffers) does not fit returns RNN_ERR_UNSUPPORTED before any device work.
+ * The first call on a device looks up the array's device address (once per
+ * device); make that first call before any stream capture.  Every call
+ * shares the one array and leaves its contents behind; what must start at
+ * zero is cleared by each call, so calls that overlap on the GPU (another
+ * stream, another thread or another plan) race and must be serialised by the
+ * caller.  Barrier waits are bounded as in rnn_run, but a timed-out run is
+ * not reported by rnn_plan_sync (its outputs are then incomplete), and
+ * rnn_plan_debug_barrier and timing do not apply. */
+rnn_status rnn_run_static_scratch(rnn_plan_t plan, int64_t seq_length, int64_t batch_size,
+                                  const float* X, const float* W, const float* R,
+                                  const float* B, const int32_t* sequence_lens,
+                                  const float* initial_h, const float* initial_c,
+                                  const float* P, float* Y, float* Y_h, float* Y_c,
+                                  void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* rnn_last_error(void);
 

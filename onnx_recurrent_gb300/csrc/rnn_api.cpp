@@ -698,4 +698,133 @@ rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const fl
     return RNN_OK;
 }
 
+// rnn_run without any device allocation: all scratch (control words, packed
+// weights, projection, h exchange buffers) is carved out of the library's
+// fixed device array, and sequence_lens is checked through a stack buffer.
+rnn_status rnn_run_static_scratch(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const float* W,
+                                  const float* R, const float* B, const int32_t* lens, const float* h0,
+                                  const float* c0, const float* P, float* Y, float* Yh, float* Yc,
+                                  void* stream)
+{
+    constexpr int64_t kMaxBatch = 4096;
+    g_error.clear();
+    if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
+    pl->last_launches = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (S < 0 || N < 0) return fail(RNN_ERR_INVALID_ARGUMENT, "seq_length and batch_size must be >= 0");
+    if (S > (1 << 30) || N > kMaxBatch)
+        return fail(RNN_ERR_UNSUPPORTED, "static-scratch runs take at most %lld batch rows", (long long)kMaxBatch);
+    const int64_t H = pl->H, I = pl->I, G = pl->G, D = pl->D, GH = G * H;
+    if (pl->op != RNN_OP_LSTM) { c0 = nullptr; P = nullptr; Yc = nullptr; }
+    const double per_dir = (double)S * N * GH + 4.0 * N * H + (pl->const_weights ? 0.0 : (double)GH * (I + H));
+    if (per_dir >= 1073741824.0)
+        return fail(RNN_ERR_UNSUPPORTED, "per-direction scratch of %.0f floats reaches the 2^30 limit", per_dir);
+    if (S == 0 || N == 0) {
+        const size_t sb = sizeof(float) * (size_t)D * N * H;
+        cudaError_t e = cudaSuccess;
+        if (Yh && sb) e = h0 ? cudaMemcpyAsync(Yh, h0, sb, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(Yh, 0, sb, st);
+        if (e == cudaSuccess && Yc && sb)
+            e = c0 ? cudaMemcpyAsync(Yc, c0, sb, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(Yc, 0, sb, st);
+        if (e != cudaSuccess) return cuda_fail(e, "zero-size copy");
+        return RNN_OK;
+    }
+    if (!X && I > 0) return fail(RNN_ERR_INVALID_ARGUMENT, "X is NULL");
+    if (!pl->const_weights && (!R || (!W && I > 0))) return fail(RNN_ERR_INVALID_ARGUMENT, "W and R are required");
+
+    DeviceInfo di;
+    rnn_status rs = device_info(&di);
+    if (rs != RNN_OK) return rs;
+    if (!di.coop) return fail(RNN_ERR_UNSUPPORTED, "device lacks cooperative launch");
+
+    int64_t max_len = S;
+    if (lens) {
+        int32_t host_lens[kMaxBatch];
+        cudaError_t e = cudaMemcpyAsync(host_lens, lens, sizeof(int32_t) * (size_t)N, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "copying sequence_lens");
+        max_len = 0;
+        for (int64_t n = 0; n < N; ++n) {
+            const int32_t L = host_lens[n];
+            if (L < 0 || (int64_t)L > S)
+                return fail(RNN_ERR_INVALID_INPUT, "sequence_lens[%lld] = %d is outside [0, %lld]", (long long)n, L,
+                            (long long)S);
+            max_len = std::max<int64_t>(max_len, L);
+        }
+    }
+
+    Geometry geo{};
+    rs = plan_geometry(pl, N, di, &geo);
+    if (rs != RNN_OK) return rs;
+
+    void* base = nullptr;
+    size_t cap = 0;
+    cudaError_t e = static_scratch(&base, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "looking up the static scratch");
+    const int64_t M = S * N;
+    size_t off = 256;   // control words: barrier counters, status
+    const size_t o_wt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)I * D * GH);
+    const size_t o_rt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)D * H * GH);
+    const size_t o_xw = off; off += align256(sizeof(float) * (size_t)M * D * GH);
+    const size_t o_hb = off; off += align256(sizeof(float) * (size_t)D * 2 * H * geo.npad);
+    const bool need_rh = pl->op == RNN_OP_GRU && pl->lbr == 0;
+    const size_t o_rh = off; off += need_rh ? align256(sizeof(float) * (size_t)D * H * geo.npad) : 0;
+    if (off > cap)
+        return fail(RNN_ERR_UNSUPPORTED, "run needs %zu bytes of scratch; the static scratch holds %zu", off, cap);
+    char* sb = (char*)base;
+
+    e = cudaMemsetAsync(sb + 64, 0, sizeof(int), st);   // status word starts at 0 on every call
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    float* wt = pl->const_weights ? pl->wt_const : (float*)(sb + o_wt);
+    float* rt = pl->const_weights ? pl->rt_const : (float*)(sb + o_rt);
+    float* xw = (float*)(sb + o_xw);
+    const bool exact = pl->mode == RNN_MODE_EXACT;
+    int launches = 0;
+    if (!pl->const_weights) {
+        e = launch_pack(W, R, wt, rt, (int)D, (int)G, H, I, st);
+        if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+        launches += (int)D * (I > 0 ? 2 : 1);
+    }
+    e = launch_projection(X, wt, xw, M, I, D * GH, exact, st);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    launches += 1;
+
+    RecParams p;
+    std::memset(&p, 0, sizeof p);
+    p.op = pl->op; p.G = (int)G; p.D = (int)D; p.N = (int)N; p.H = (int)H; p.S = (int)S;
+    p.layout = pl->layout; p.lbr = pl->lbr; p.input_forget = pl->input_forget;
+    p.has_B = B != nullptr; p.has_P = P != nullptr; p.has_h0 = h0 != nullptr; p.has_c0 = c0 != nullptr;
+    p.has_lens = lens != nullptr; p.has_clip = pl->has_clip; p.clip = pl->clip;
+    for (int d = 0; d < 2; ++d)
+        for (int s = 0; s < 3; ++s) p.act[d][s] = pl->act[d][s];
+    p.max_len = (int)max_len;
+    p.dir_reverse[0] = pl->direction == RNN_DIR_REVERSE ? 1 : 0;
+    p.dir_reverse[1] = 1;
+    p.ctas_per_dir = geo.ctas; p.umax = geo.umax; p.rows_per_thread = geo.tn; p.r_resident = geo.rres;
+    p.npad = geo.npad;
+    p.XW = xw; p.Rt = rt; p.B = B; p.P = P; p.h0 = h0; p.c0 = c0; p.lens = lens;
+    p.Y = Y; p.Yh = Yh; p.Yc = Yc;
+    p.hbuf = (float*)(sb + o_hb);
+    p.rhbuf = need_rh ? (float*)(sb + o_rh) : nullptr;
+    p.bar = (unsigned*)sb;           // zeroed by the state set-up kernel
+    p.status = (int*)(sb + 64);
+    p.spin_limit_ns = kDefaultSpinNs;
+    p.debug_skip_cta = -1;
+
+    e = launch_state_init(p, st);
+    if (e != cudaSuccess) return cuda_fail(e, "state set-up launch");
+    launches += 1;
+    e = launch_recurrent(p, exact, geo.threads, geo.smem, st);
+    if (e != cudaSuccess) return cuda_fail(e, "recurrent launch");
+    launches += 1;
+    if (Y && max_len < S) {
+        e = launch_mask_tail(Y, pl->layout, S, D, N, H, max_len, st);
+        if (e != cudaSuccess) return cuda_fail(e, "mask launch");
+        launches += 1;
+    }
+    pl->g_ctas = geo.ctas; pl->g_tn = geo.tn; pl->g_rres = geo.rres; pl->g_threads = geo.threads;
+    pl->g_smem = (int)geo.smem;
+    pl->last_launches = launches;
+    return RNN_OK;
+}
+
 }  // extern "C"

@@ -86,4 +86,8 @@ cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream);
 cudaError_t launch_mask_tail(float* Y, int layout, int64_t S, int64_t D, int64_t N, int64_t H,
                              int64_t t0, cudaStream_t stream);
 
+// Device address and size of the fixed scratch array used by
+// rnn_run_static_scratch (looked up once per device; see rnn_static.cu).
+cudaError_t static_scratch(void** ptr, size_t* bytes);
+
 }  // namespace rnngb

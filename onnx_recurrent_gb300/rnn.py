@@ -51,6 +51,7 @@ def load(path: str | None = None):
                                     ctypes.POINTER(ctypes.c_char_p), i32, fp, i32, fp, i32,
                                     f32, i32, i32, i32]
     lib.rnn_run.argtypes = [vp, i64, i64] + [vp] * 11 + [vp]
+    lib.rnn_run_static_scratch.argtypes = [vp, i64, i64] + [vp] * 11 + [vp]
     lib.rnn_plan_destroy.argtypes = [vp]
     lib.rnn_plan_destroy.restype = None
     lib.rnn_plan_set_mode.argtypes = [vp, i32]
@@ -67,7 +68,7 @@ def load(path: str | None = None):
     lib.rnn_plan_last_launch_count.restype = i32
     lib.rnn_last_error.argtypes = []
     lib.rnn_last_error.restype = ctypes.c_char_p
-    for name in ("rnn_plan_create", "rnn_run", "rnn_plan_set_mode", "rnn_plan_set_weights",
+    for name in ("rnn_plan_create", "rnn_run", "rnn_run_static_scratch", "rnn_plan_set_mode", "rnn_plan_set_weights",
                  "rnn_plan_sync", "rnn_plan_get_activation", "rnn_plan_set_launch",
                  "rnn_plan_get_launch", "rnn_plan_set_timing", "rnn_plan_last_timing",
                  "rnn_plan_timing_totals",
@@ -269,6 +270,23 @@ def rnn_run(plan: Plan, X, W, R, B=None, sequence_lens=None, initial_h=None, ini
     st = load().rnn_run(plan.handle, int(seq), int(batch), _ptr(X), _ptr(W), _ptr(R), _ptr(B),
                         _ptr(sequence_lens), _ptr(initial_h), _ptr(initial_c), _ptr(P), _ptr(Y),
                         _ptr(Y_h), _ptr(Y_c), _stream(stream))
+    _check(st)
+
+
+def rnn_run_static_scratch(plan: Plan, X, W, R, B=None, sequence_lens=None, initial_h=None,
+                           initial_c=None, P=None, Y=None, Y_h=None, Y_c=None, stream=None):
+    """rnn_run that allocates no device memory (the library's fixed scratch array)."""
+    seq, batch = (X.shape[0], X.shape[1]) if plan.layout == 0 else (X.shape[1], X.shape[0])
+    sh = shapes(plan, seq, batch)
+    for t, k, n in ((X, "X", "X"), (W, "W", "W"), (R, "R", "R"), (B, "B", "B"), (P, "P", "P"),
+                    (initial_h, "state", "initial_h"), (initial_c, "state", "initial_c"),
+                    (Y, "Y", "Y"), (Y_h, "state", "Y_h"), (Y_c, "state", "Y_c")):
+        _need(t, sh[k], n)
+    _need(sequence_lens, sh["lens"], "sequence_lens", "int32")
+    st = load().rnn_run_static_scratch(plan.handle, int(seq), int(batch), _ptr(X), _ptr(W), _ptr(R),
+                                       _ptr(B), _ptr(sequence_lens), _ptr(initial_h),
+                                       _ptr(initial_c), _ptr(P), _ptr(Y), _ptr(Y_h), _ptr(Y_c),
+                                       _stream(stream))
     _check(st)
 
 
