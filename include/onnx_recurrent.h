@@ -152,16 +152,24 @@ rnn_status rnn_plan_sync(rnn_plan_t plan);
 rnn_status rnn_plan_get_activation(rnn_plan_t plan, int dir, int slot, int* fn,
                                    float* alpha, float* beta);
 
-/* Launch geometry of the recurrent kernel.  rnn_plan_set_launch overrides the
- * planner's choice (0 = automatic) for tuning and testing: CTAs per
- * direction, batch rows per thread (1, 2, 4 or 8) and whether R is kept
- * resident in shared memory (1), streamed through it (0) or chosen (-1).
- * Results do not depend on the geometry.  rnn_plan_get_launch reports the
- * geometry of the last run. */
-rnn_status rnn_plan_set_launch(rnn_plan_t plan, int ctas_per_dir, int rows_per_thread,
-                               int r_resident);
-rnn_status rnn_plan_get_launch(rnn_plan_t plan, int* ctas_per_dir, int* rows_per_thread,
-                               int* r_resident, int* threads_per_cta, int* smem_bytes);
+/* Launch geometry of the recurrent product, for tuning and testing.
+ * rnn_plan_set_launch overrides the planner (0, or -1 for r_resident, means
+ * "choose"): kernel 1 is the staged kernel (CTAs hold all batch rows; h moves
+ * through a shared-memory ring; one device-wide barrier per step), kernel 2
+ * the dataflow kernel (CTAs tile unit groups x row groups; a loader warp
+ * fetches h with TMA bulk copies once the CTAs that produce it have
+ * published their per-step flags).  unit_groups: CTAs per direction along
+ * hidden units; row_groups: along batch rows (dataflow kernel only);
+ * rows_per_thread: 1, 2, 4 (or 8, staged kernel only); r_resident: R slice
+ * kept in shared memory (1) or streamed through it (0).  Every geometry gives
+ * the same results.  rnn_plan_get_launch reports the geometry of the last
+ * run; a shape the override cannot serve makes the run return
+ * RNN_ERR_UNSUPPORTED. */
+rnn_status rnn_plan_set_launch(rnn_plan_t plan, int unit_groups, int rows_per_thread,
+                               int r_resident, int row_groups, int kernel);
+rnn_status rnn_plan_get_launch(rnn_plan_t plan, int* unit_groups, int* rows_per_thread,
+                               int* r_resident, int* row_groups, int* kernel,
+                               int* threads_per_cta, int* smem_bytes);
 
 /* Per-kernel device time, in milliseconds, measured with CUDA events that the
  * run records on its own stream around each kernel while timing is enabled:
@@ -196,7 +204,7 @@ int rnn_plan_last_launch_count(rnn_plan_t plan);
  * nothing: its scratch comes from one fixed 32 MiB device array that every
  * GPU loading this library holds until the process exits, and
  * sequence_lens (at most 4096 rows) is checked through a stack buffer.
- * A run whose scratch (256 bytes of control words, the packed weights unless
+ * A run whose scratch (4 KiB of control words, the packed weights unless
  * they are constant, seq*batch*D*G*H floats of projection and the h exchange
  * buffers) does not fit returns RNN_ERR_UNSUPPORTED before any device work.
  * The first call on a device looks up the array's device address (once per

@@ -38,24 +38,50 @@ __global__ void pack_kernel(const float* __restrict__ src, float* __restrict__ d
     }
 }
 
+// Exchange buffers at the start of a run.  Staged kernel: hbuf[d][b][u][n]
+// (k-major).  Dataflow kernel: hbuf[d][b][cr][u / 32][rl][u % 32] with rows
+// of 36 floats (row n = cr*npad + rl).  Buffer 0 starts as initial_h (or 0);
+// buffer 1, padding rows and columns and rhbuf start as 0; barrier counters
+// and flags 0.
 __global__ void state_init_kernel(const RecParams p)
 {
-    const int64_t total = (int64_t)p.D * p.H * p.npad;
+    const bool df = p.kernel == 2;
+    const int64_t CR = p.row_groups;
+    const int64_t W = df ? (int64_t)p.hpad / kRecKC * kDfPitch : p.H;   // floats per row (all chunks)
+    const int64_t blk = (int64_t)p.npad * W;              // one row group's block
+    const int64_t total = (int64_t)p.D * CR * blk;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t n = i % p.npad;
-        const int64_t u = (i / p.npad) % p.H;
-        const int64_t d = i / ((int64_t)p.npad * p.H);
+        int64_t u, rl;
+        if (df) {
+            const int64_t e = i % blk, chunk = e / ((int64_t)p.npad * kDfPitch);
+            const int64_t r = e % ((int64_t)p.npad * kDfPitch);
+            rl = r / kDfPitch;
+            const int64_t col = r % kDfPitch;
+            u = col < kRecKC ? chunk * kRecKC + col : p.H;   // pitch padding: never a unit
+        }
+        else { rl = i % p.npad; u = (i / p.npad) % p.H; }
+        const int64_t cr = (i / blk) % CR;
+        const int64_t d = i / (blk * CR);
+        const int64_t n = cr * p.npad + rl;
         float v = 0.0f;
-        if (n < p.N && p.h0) {
+        if (n < p.N && u < p.H && p.h0) {
             const int64_t si = p.layout == 0 ? (d * p.N + n) * p.H + u : (n * p.D + d) * p.H + u;
             v = p.h0[si];
         }
-        p.hbuf[((d * 2) * p.H + u) * p.npad + n] = v;
-        p.hbuf[((d * 2 + 1) * p.H + u) * p.npad + n] = 0.0f;
-        if (p.rhbuf) p.rhbuf[(d * p.H + u) * p.npad + n] = 0.0f;
+        const int64_t off = i - d * CR * blk;             // offset inside direction d
+        p.hbuf[(d * 2) * CR * blk + off] = v;
+        p.hbuf[(d * 2 + 1) * CR * blk + off] = 0.0f;
+        if (p.rhbuf) {
+            p.rhbuf[(d * 2) * CR * blk + off] = 0.0f;
+            p.rhbuf[(d * 2 + 1) * CR * blk + off] = 0.0f;
+        }
     }
-    if (blockIdx.x == 0 && threadIdx.x < p.D) p.bar[threadIdx.x] = 0u;
+    if (blockIdx.x == 0) {
+        if (threadIdx.x < p.D) p.bar[threadIdx.x] = 0u;
+        const int nflags = p.D * p.row_groups * p.unit_groups;
+        for (int j = threadIdx.x; j < nflags && p.flags; j += blockDim.x) p.flags[j] = 0u;
+    }
 }
 
 __global__ void mask_tail_kernel(float* __restrict__ Y, int layout, int64_t S, int64_t D, int64_t N,
@@ -102,7 +128,7 @@ cudaError_t launch_pack(const float* W, const float* R, float* Wt, float* Rt, in
 
 cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream)
 {
-    const int64_t total = (int64_t)p.D * p.H * p.npad;
+    const int64_t total = (int64_t)p.D * p.row_groups * p.npad * (p.kernel == 2 ? p.hpad : p.H);
     int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
     if (blocks < 1) blocks = 1;
     state_init_kernel<<<blocks, 256, 0, stream>>>(p);

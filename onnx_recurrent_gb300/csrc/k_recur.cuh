@@ -143,6 +143,57 @@ __device__ __forceinline__ void load_cols(float (&rv)[NC], const float* p)
     }
 }
 
+// One full k-chunk (kRecKC rows) of the product for a thread's TN rows and NC
+// gate columns: acc[i][j] += h[k][i] * r[k][j], k ascending.  The shared-memory
+// operands go through registers in blocks of KB k-rows, block b+1 loaded
+// while block b is multiplied.
+template <int TN, int NC, bool EXACT>
+__device__ __forceinline__ void chunk_full(const float* hk, int hstride, const float* rk, int rstride,
+                                           float (&acc)[TN][NC])
+{
+    constexpr int KB = (TN * NC >= 16) ? 4 : 8;
+    constexpr int NB = kRecKC / KB;
+    float hv[2][KB][TN], rv[2][KB][NC];
+#pragma unroll
+    for (int j = 0; j < KB; ++j) {
+        load_rows<TN>(hv[0][j], hk + (size_t)j * hstride);
+        load_cols<NC>(rv[0][j], rk + (size_t)j * rstride);
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const int cur = b & 1;
+        if (b + 1 < NB) {
+#pragma unroll
+            for (int j = 0; j < KB; ++j) {
+                load_rows<TN>(hv[cur ^ 1][j], hk + (size_t)((b + 1) * KB + j) * hstride);
+                load_cols<NC>(rv[cur ^ 1][j], rk + (size_t)((b + 1) * KB + j) * rstride);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+#pragma unroll
+            for (int i = 0; i < TN; ++i)
+#pragma unroll
+                for (int g = 0; g < NC; ++g) acc[i][g] = mac<EXACT>(acc[i][g], hv[cur][j][i], rv[cur][j][g]);
+    }
+}
+
+// A partial chunk (the last one when H is not a multiple of kRecKC).
+template <int TN, int NC, bool EXACT>
+__device__ __forceinline__ void chunk_part(const float* hk, int hstride, const float* rk, int rstride, int kc,
+                                           float (&acc)[TN][NC])
+{
+    for (int kk = 0; kk < kc; ++kk) {
+        float hv[TN], rv[NC];
+        load_rows<TN>(hv, hk + (size_t)kk * hstride);
+        load_cols<NC>(rv, rk + (size_t)kk * rstride);
+#pragma unroll
+        for (int i = 0; i < TN; ++i)
+#pragma unroll
+            for (int j = 0; j < NC; ++j) acc[i][j] = mac<EXACT>(acc[i][j], hv[i], rv[j]);
+    }
+}
+
 // Shared per-CTA context of the kernel.
 struct RecCtx {
     int d, H, npad, G, GH, u0, UG, ugp, tid, nthreads, ul, rb;
@@ -200,28 +251,8 @@ __device__ __forceinline__ void accumulate(const RecParams& p, const RecCtx& x, 
             const float* rk = (p.r_resident ? x.Rs + (size_t)k0 * x.ugp
                                             : x.Rs + (size_t)slot * kRecKC * x.ugp) +
                               x.ul * x.G + col_off;
-            if (kc == kRecKC) {
-#pragma unroll 8
-                for (int kk = 0; kk < kRecKC; ++kk) {
-                    float hv[TN], rv[NC];
-                    load_rows<TN>(hv, hk + (size_t)kk * x.npad);
-                    load_cols<NC>(rv, rk + (size_t)kk * x.ugp);
-#pragma unroll
-                    for (int i = 0; i < TN; ++i)
-#pragma unroll
-                        for (int j = 0; j < NC; ++j) acc[i][j] = mac<EXACT>(acc[i][j], hv[i], rv[j]);
-                }
-            } else {
-                for (int kk = 0; kk < kc; ++kk) {
-                    float hv[TN], rv[NC];
-                    load_rows<TN>(hv, hk + (size_t)kk * x.npad);
-                    load_cols<NC>(rv, rk + (size_t)kk * x.ugp);
-#pragma unroll
-                    for (int i = 0; i < TN; ++i)
-#pragma unroll
-                        for (int j = 0; j < NC; ++j) acc[i][j] = mac<EXACT>(acc[i][j], hv[i], rv[j]);
-                }
-            }
+            if (kc == kRecKC) chunk_full<TN, NC, EXACT>(hk, x.npad, rk, x.ugp, acc);
+            else chunk_part<TN, NC, EXACT>(hk, x.npad, rk, x.ugp, kc, acc);
         }
     }
     cp_async_wait<0>();
@@ -364,7 +395,7 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
                 accumulate<TN, 2, EXACT>(p, x, hsrc, 0, az);
                 if (s + 1 < p.max_len) load_xw(s + 1);
                 float zg[TN];
-                float* rh = p.rhbuf + (size_t)d * p.H * x.npad;
+                float* rh = p.rhbuf + (size_t)d * 2 * p.H * x.npad;
 #pragma unroll
                 for (int i = 0; i < TN; ++i) {
                     const int n = x.rb * TN + i;

@@ -1,0 +1,697 @@
+// Persistent recurrent kernel, dataflow version: TMA bulk copies, a loader
+// warp and per-CTA publication flags instead of a device-wide barrier.
+//
+// Same arithmetic as the staged kernel in k_recur.cuh (page "Recurrent
+// operators: RNN, GRU, LSTM", Computation: one accumulator per output, k
+// increasing from +0; the gate epilogue in the written order), so both give
+// the same bits.  What changes is how h moves between steps:
+//
+//   * CTAs tile (unit group cu) x (row group cr).  CTA (cu, cr) owns hidden
+//     units [u0, u1) (all G gate columns of each) for the batch rows of group
+//     cr, so its slice of R serves only its own rows and it fetches only their
+//     h: hbuf is laid out [D][2][CR][H][NRP], one contiguous k-major block per
+//     row group.
+//   * Warp 0 is the loader.  Once per product it waits until every CTA of
+//     its row group has published the step (its lanes poll the flags in
+//     parallel with acquire loads), then issues one cp.async.bulk
+//     global->shared copy per k-chunk (plus, when R does not fit in shared
+//     memory, one bulk copy per k row of the CTA's R columns), each
+//     completing on the chunk's "full" mbarrier.  Lane j issues chunk j of a
+//     group in one converged instruction: bulk copies issued one after
+//     another by a single thread go out about one round trip apart.  A ring
+//     of slots with "empty" mbarriers lets the loader run ahead; when the
+//     whole block fits, every chunk of a product is in flight at once.
+//   * The other warps compute.  After the gate epilogue they write their h
+//     into the next buffer, meet at a named barrier, and one thread releases
+//     the CTA's flag (flags count publications: one per step, two for GRU with
+//     linear_before_reset = 0, whose r (.) h block is published in between).
+//   Two h buffers suffice: a CTA can only overwrite buffer b after every
+//   producer of its row group has published the step that reads b.
+//
+// Every wait is bounded (globaltimer): a CTA that gives up records
+// RNN_ERR_TIMEOUT in the status word; CTAs that see a non-zero status stop.
+// The compute warps leave only at a publish barrier, so no warp is left
+// waiting on a named barrier, and the loader waits for its own copies in
+// flight before it exits.
+#pragma once
+
+#include <cstdint>
+
+#include "k_recur.cuh"
+
+namespace rnngb {
+
+__device__ __forceinline__ unsigned smem_addr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                     smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, unsigned parity)
+{
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Tiled tensor copies global -> shared (TMA), completing on an mbarrier.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];" ::
+            "r"(smem_addr(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Bounded wait on an mbarrier phase.  Gives up (returning false) when the
+// CTA is aborting, another CTA reported a failure, or the limit passes.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, int* status, volatile int* abort_flag,
+                                          long long limit_ns)
+{
+    if (mbar_test(bar, parity)) return true;
+    if (*abort_flag) return false;
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned it = 0;
+    while (!mbar_test(bar, parity)) {
+        if ((++it & 15u) == 0u) {
+            if (*abort_flag) return false;
+            if (ld_relaxed_s32(status) != 0) { *abort_flag = 1; return false; }
+            if ((long long)(globaltimer_ns() - t0) > limit_ns) {
+                atomicCAS(status, 0, 6 /* RNN_ERR_TIMEOUT */);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// First hidden unit of unit group cu: groups hold multiples of `quant`
+// units, split as evenly as possible.
+__device__ __forceinline__ int unit_begin(int cu, int CU, int H, int quant)
+{
+    const int Q = H / quant;
+    return quant * (int)(((long long)cu * Q) / CU);
+}
+
+struct DfCtx {
+    int d, cu, cr, H, HP, G, GH, CU, CR, u0, U, umax, ugs, NR, NRP, nchunks, cpb, npieces, slots;
+    int ctid, ncompute, ul, rb;
+    bool active;
+    float* Rs;        // resident R: [umax][ugs] floats (unit-major, gate rows of H)
+    char* Rring;      // streamed R: slots x rslot bytes, each cpb chunks of [G][umax][36]
+    char* Hring;      // slots x hslot bytes, each [cpb][NRP][36]
+    int rslot, rsub, hslot; // bytes per slot (one piece: cpb chunks of 32 k), per R chunk
+    uint64_t* full;
+    uint64_t* empty;
+};
+
+// Loader: the chunk sequence of one product (one accumulate pass of the
+// compute warps).  `map` describes the h (or r (.) h) exchange buffer, `z` the
+// row group's block in it; every producer of the row group must have
+// published `target` times before the block may be read.  The lanes poll the
+// producers' flags in parallel (acquire loads); a warp barrier orders those
+// acquires before the copies, and a proxy fence orders the generic-proxy
+// writes they made visible before the tensor copies (async proxy) that read
+// them.  Chunks are issued by the lanes in parallel, lane j taking chunk
+// base + j, in groups no larger than the ring (so no two lanes of a group
+// share a slot).
+__device__ __forceinline__ bool load_product(const RecParams& p, const DfCtx& x, const CUtensorMap* map, int z,
+                                             unsigned target, const unsigned* flags, unsigned& q,
+                                             volatile int* abort_flag, int lane)
+{
+    if (target > 0) {
+        bool ready = true;
+        for (int j = lane; j < x.CU; j += 32) ready = ready && ld_acquire_u32(flags + j) >= target;
+        if (!__all_sync(0xffffffffu, ready)) {
+            const unsigned long long t0 = globaltimer_ns();
+            unsigned it = 0;
+            while (!__all_sync(0xffffffffu, ready)) {
+                // back off between polls: a tight acquire-load loop competes
+                // with the compute warps for the SM's load/store pipe
+                __nanosleep(64);
+                if (!ready) {
+                    ready = true;
+                    for (int j = lane; j < x.CU; j += 32) ready = ready && ld_acquire_u32(flags + j) >= target;
+                }
+                if ((++it & 15u) == 0u) {
+                    int bad = 0;
+                    if (lane == 0) {
+                        if (*abort_flag || ld_relaxed_s32(p.status) != 0) bad = 1;
+                        else if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) {
+                            atomicCAS(p.status, 0, 6 /* RNN_ERR_TIMEOUT */);
+                            bad = 1;
+                        }
+                    }
+                    if (__shfl_sync(0xffffffffu, bad, 0)) {
+                        if (lane == 0) *abort_flag = 1;
+                        return false;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        fence_proxy_async_global();
+        __syncwarp();
+    }
+    // One tensor copy per piece of cpb chunks: a box of many small copies
+    // lands one after another, a few large boxes land together.  Pieces are
+    // issued by the lanes in parallel, lane j taking piece base + j, in
+    // groups no larger than the ring (so no two lanes share a slot).
+    const int gsz = min(32, x.slots);
+    for (int base = 0; base < x.npieces; base += gsz) {
+        const int nmine = min(gsz, x.npieces - base);
+        const bool mine = lane < nmine;
+        const unsigned qq = q + (unsigned)lane;
+        const int slot = (int)(qq % (unsigned)x.slots);
+        const unsigned round = qq / (unsigned)x.slots;
+        bool ok = true;
+        if (mine) ok = mbar_wait(&x.empty[slot], (round & 1u) ^ 1u, p.status, abort_flag, p.spin_limit_ns);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        if (mine) {
+            const int c0 = (base + lane) * x.cpb;           // first chunk of the piece
+            const int nc = min(x.cpb, x.nchunks - c0);      // R chunks to copy (h: the whole box)
+            const unsigned hbytes = (unsigned)x.NRP * x.cpb * (kDfPitch * 4u);
+            const unsigned rbytes = p.r_resident ? 0u : (unsigned)(nc * x.G * x.umax) * (kDfPitch * 4u);
+            mbar_arrive_expect_tx(&x.full[slot], hbytes + rbytes);
+            tma_load_4d(x.Hring + (size_t)slot * x.hslot, map, 0, 0, c0, z, &x.full[slot]);
+            if (!p.r_resident)
+                for (int cl = 0; cl < nc; ++cl)
+                    tma_load_4d(x.Rring + (size_t)slot * x.rslot + (size_t)cl * x.rsub, &p.rmap, (c0 + cl) * kRecKC,
+                                x.u0, 0, x.d, &x.full[slot]);
+        }
+        q += (unsigned)nmine;
+    }
+    return true;
+}
+
+// The products of one piece for a thread's TN rows and NC gate columns:
+// acc[i][g] += h[row_i][k] * R[gate g][k] over the piece's k, ascending, 4 k
+// per vector load.  Operands are loaded PD groups of 4 k ahead (a ring of
+// PD + 1 register buffers that runs on across chunk boundaries); the ring
+// length divides the 8 groups of a chunk, so every buffer index is a
+// compile-time constant.  h rows (and streamed R rows) have a pitch of 36
+// floats; chunk cl of a piece is cl * hstep bytes (R: rsub bytes) further on.
+template <int TN, int NC, bool EXACT, bool RES>
+__device__ __forceinline__ void df_piece(const char* const (&hp)[TN], int hstep, const char* const (&rp)[NC],
+                                         int rstep, int ngroups, float (&acc)[TN][NC])
+{
+    constexpr int PD = TN == 1 ? 3 : 1;
+    constexpr int NB = PD + 1;
+    static_assert(8 % NB == 0 && PD < 8, "ring length must divide the groups of a chunk");
+    float4 hv[NB][TN], rv[NB][NC];
+    // group jc (compile-time, 0..7) of the chunk at byte offsets oh / orr
+    auto load = [&](int buf, int oh, int orr, int jc) {
+#pragma unroll
+        for (int i = 0; i < TN; ++i) hv[buf][i] = *reinterpret_cast<const float4*>(hp[i] + oh + jc * 16);
+#pragma unroll
+        for (int g = 0; g < NC; ++g) rv[buf][g] = *reinterpret_cast<const float4*>(rp[g] + orr + jc * 16);
+    };
+#pragma unroll
+    for (int b = 0; b < PD; ++b)
+        if (b < ngroups) load(b, 0, 0, b);
+    const int nch = (ngroups + 7) / 8;
+    for (int cl = 0; cl < nch; ++cl) {
+        const int oh = cl * hstep, orr = cl * rstep;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int jj = cl * 8 + j;
+            if (jj >= ngroups) break;
+            if (jj + PD < ngroups) {
+                if (j + PD < 8) load((j + PD) % NB, oh, orr, j + PD);
+                else load((j + PD) % NB, oh + hstep, orr + rstep, j + PD - 8);
+            }
+            const int b = j % NB;
+#pragma unroll
+            for (int i = 0; i < TN; ++i)
+#pragma unroll
+                for (int g = 0; g < NC; ++g) acc[i][g] = mac<EXACT>(acc[i][g], hv[b][i].x, rv[b][g].x);
+#pragma unroll
+            for (int i = 0; i < TN; ++i)
+#pragma unroll
+                for (int g = 0; g < NC; ++g) acc[i][g] = mac<EXACT>(acc[i][g], hv[b][i].y, rv[b][g].y);
+#pragma unroll
+            for (int i = 0; i < TN; ++i)
+#pragma unroll
+                for (int g = 0; g < NC; ++g) acc[i][g] = mac<EXACT>(acc[i][g], hv[b][i].z, rv[b][g].z);
+#pragma unroll
+            for (int i = 0; i < TN; ++i)
+#pragma unroll
+                for (int g = 0; g < NC; ++g) acc[i][g] = mac<EXACT>(acc[i][g], hv[b][i].w, rv[b][g].w);
+        }
+    }
+}
+
+// Compute warps: acc[i][j] += sum_k src[row_i][k] * R[gate col_off + j][k]
+// over the product's pieces (k ascending).  Returns false once the CTA is
+// aborting (the remaining pieces are then skipped, not waited for).
+template <int TN, int NC, bool EXACT>
+__device__ __forceinline__ bool consume_product(const RecParams& p, const DfCtx& x, int col_off,
+                                                float (&acc)[TN][NC], unsigned& q, volatile int* abort_flag,
+                                                int lane)
+{
+    bool ok = true;
+    for (int pc = 0; pc < x.npieces; ++pc, ++q) {
+        const int slot = (int)(q % (unsigned)x.slots);
+        const unsigned round = q / (unsigned)x.slots;
+        if (ok) ok = mbar_wait(&x.full[slot], round & 1u, p.status, abort_flag, p.spin_limit_ns);
+        if (ok && x.active) {
+            const int k0 = pc * x.cpb * kRecKC;
+            const int ngroups = (min(x.cpb * kRecKC, x.H - k0) + 3) / 4;
+            const char* hbox = x.Hring + (size_t)slot * x.hslot;
+            const char* hp[TN];
+#pragma unroll
+            for (int i = 0; i < TN; ++i) hp[i] = hbox + (size_t)(x.rb * TN + i) * (kDfPitch * 4);
+            const int hstep = x.NRP * kDfPitch * 4;
+            const char* rp[NC];
+            if (p.r_resident) {
+                const float* rbase = x.Rs + (size_t)x.ul * x.ugs + (size_t)col_off * x.H + k0;
+#pragma unroll
+                for (int g = 0; g < NC; ++g) rp[g] = reinterpret_cast<const char*>(rbase + (size_t)g * x.H);
+                df_piece<TN, NC, EXACT, true>(hp, hstep, rp, kRecKC * 4, ngroups, acc);
+            } else {
+                const char* rbox = x.Rring + (size_t)slot * x.rslot;
+#pragma unroll
+                for (int g = 0; g < NC; ++g)
+                    rp[g] = rbox + (size_t)((col_off + g) * x.umax + x.ul) * (kDfPitch * 4);
+                df_piece<TN, NC, EXACT, false>(hp, hstep, rp, x.rsub, ngroups, acc);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&x.empty[slot]);
+    }
+    return ok;
+}
+
+// Compute warps meet; one thread publishes the CTA's flag.  Returns false
+// (uniformly across the compute warps) when the CTA is aborting.
+__device__ __forceinline__ bool publish(const DfCtx& x, unsigned* my_flag, unsigned value,
+                                        volatile int* abort_flag, bool skip)
+{
+    named_barrier(1, x.ncompute);
+    const bool abort_now = *abort_flag != 0;
+    named_barrier(1, x.ncompute);   // everyone has read the abort flag
+    if (abort_now) return false;
+    if (x.ctid == 0 && !skip) {
+        fence_proxy_async_global();
+        st_release_u32(my_flag, value);   // the named barrier ordered every compute thread's writes first
+    }
+    return true;
+}
+
+// Threads per CTA: one row per thread keeps three groups of operands in
+// flight (up to 255 registers, 256 threads); wider tiles keep one group in
+// flight and more accumulators (up to 168 registers, 384 threads).
+template <int TN>
+struct DfBounds {
+    static constexpr int threads = TN == 1 ? 256 : 384;
+};
+
+// TWO: GRU with linear_before_reset = 0 (two products per step, the second
+// over r (.) h); a separate instance keeps its register allocation apart.
+template <int OP, int TN, bool EXACT, bool TWO>
+__global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(const __grid_constant__ RecParams p)
+{
+    constexpr int G = OP == 0 ? 1 : (OP == 1 ? 3 : 4);
+    extern __shared__ __align__(128) unsigned char df_smem[];
+    __shared__ __align__(8) uint64_t s_full[kMaxSlots];
+    __shared__ __align__(8) uint64_t s_empty[kMaxSlots];
+    __shared__ int s_abort;
+
+    DfCtx x;
+    const int per_dir = p.ctas_per_dir;           // CU * CR
+    x.d = blockIdx.x / per_dir;
+    const int c = blockIdx.x - x.d * per_dir;
+    x.CU = p.unit_groups;
+    x.CR = p.row_groups;
+    x.cr = c / x.CU;
+    x.cu = c - x.cr * x.CU;
+    x.H = p.H;
+    x.HP = p.hpad;
+    x.G = G;
+    x.GH = G * p.H;
+    x.u0 = unit_begin(x.cu, x.CU, p.H, 1);
+    x.U = unit_begin(x.cu + 1, x.CU, p.H, 1) - x.u0;
+    x.umax = p.umax;
+    x.ugs = p.unit_stride;
+    x.NRP = p.npad;                               // padded rows per group
+    x.NR = max(0, min(p.N - x.cr * x.NRP, x.NRP));
+    x.nchunks = (p.H + kRecKC - 1) / kRecKC;
+    x.cpb = p.chunks_per_piece;
+    x.npieces = (x.nchunks + x.cpb - 1) / x.cpb;
+    x.slots = p.slots;
+    x.hslot = x.NRP * x.cpb * kDfPitch * 4;
+    x.rsub = (int)df_rsub_bytes(x.umax, G);
+    x.rslot = p.r_resident ? 0 : x.cpb * x.rsub;
+    x.ncompute = blockDim.x - 32;
+    x.ctid = (int)threadIdx.x - 32;
+    const int RB = x.NRP / TN;
+    x.rb = x.ctid >= 0 ? x.ctid % RB : 0;
+    x.ul = x.ctid >= 0 ? x.ctid / RB : 0;
+    x.active = x.ctid >= 0 && x.ul < x.U && x.rb * TN < x.NR;
+    // tensor-copy destinations are 128-byte aligned
+    unsigned char* base = df_smem + ((128u - (smem_addr(df_smem) & 127u)) & 127u);
+    const size_t rbytes = p.r_resident ? (((size_t)x.umax * x.ugs * 4 + 127) / 128) * 128
+                                       : (size_t)x.slots * x.rslot;
+    x.Rs = reinterpret_cast<float*>(base);
+    x.Rring = reinterpret_cast<char*>(base);
+    x.Hring = reinterpret_cast<char*>(base + rbytes);
+    x.full = s_full;
+    x.empty = s_empty;
+
+    const int lane = threadIdx.x & 31;
+    const int d = x.d;
+    const bool rev = p.dir_reverse[d] != 0;
+    const int nwarps_compute = x.ncompute / 32;
+    const size_t blk = (size_t)x.NRP * (x.HP / kRecKC) * kDfPitch;   // one row group's block
+    // a unit's slot in a row group's block: [u / 32][row][u % 32], rows of 36
+    auto xoff = [&](int rl, int uu) { return ((size_t)(uu / kRecKC) * x.NRP + rl) * kDfPitch + (uu % kRecKC); };
+    const int zh0 = (d * 2 + 0) * x.CR + x.cr;                   // tensor-map block index, buffer 0
+    auto hblock = [&](int buf) { return p.hbuf + ((size_t)(d * 2 + buf) * x.CR + x.cr) * blk; };
+    auto rhblock = [&](int buf) { return p.rhbuf + ((size_t)(d * 2 + buf) * x.CR + x.cr) * blk; };
+    unsigned* flags = p.flags + (size_t)(d * x.CR + x.cr) * x.CU;
+    constexpr bool two_phase = TWO;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < x.slots; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], (unsigned)nwarps_compute);
+        }
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    if (p.r_resident) {
+        // R[d][g*H + u][k] -> Rs[(u - u0) * ugs + g*H + k]
+        const float* src = p.Rorig + (size_t)d * G * p.H * p.H;
+        const int per_unit = G * p.H;
+        const int tot = x.U * per_unit;
+        for (int i = threadIdx.x; i < tot; i += blockDim.x) {
+            const int ul = i / per_unit, r = i - ul * per_unit;
+            const int g = r / p.H, k = r - g * p.H;
+            x.Rs[(size_t)ul * x.ugs + r] = src[((size_t)g * p.H + x.u0 + ul) * p.H + k];
+        }
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ loader
+    if (threadIdx.x < 32) {
+        unsigned q = 0;
+        bool ok = true;
+        for (int s = 0; s < p.max_len && ok; ++s) {
+            const int zh = zh0 + (s & 1) * x.CR;
+            if (two_phase) {
+                ok = load_product(p, x, &p.hmap, zh, 2u * s, flags, q, &s_abort, lane);
+                if (ok) ok = load_product(p, x, &p.rhmap, zh, 2u * s + 1u, flags, q, &s_abort, lane);
+            } else {
+                ok = load_product(p, x, &p.hmap, zh, (unsigned)s, flags, q, &s_abort, lane);
+            }
+        }
+        // wait (bounded) for this CTA's copies still in flight before leaving
+        if (lane == 0) {
+            const unsigned issued = q;
+            for (int sl = 0; sl < x.slots && (unsigned)sl < issued; ++sl) {
+                const unsigned last = issued - 1u - (unsigned)((issued - 1u - sl) % (unsigned)x.slots);
+                const unsigned long long t0 = globaltimer_ns();
+                while (!mbar_test(&s_full[last % x.slots], (last / x.slots) & 1u)) {
+                    if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ compute
+    const int u = x.u0 + x.ul;
+    const ActSpec fA = p.act[d][0], gA = p.act[d][1], hA = p.act[d][2];
+    float wb[G], rbv[G];
+    float pI = 0.f, pO = 0.f, pF = 0.f;
+    float hown[TN], cown[TN], xw[TN][G];
+    int len[TN];
+#pragma unroll
+    for (int g = 0; g < G; ++g) { wb[g] = 0.f; rbv[g] = 0.f; }
+    if (x.active) {
+        if (p.has_B) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                wb[g] = p.B[(size_t)d * 2 * x.GH + (size_t)g * p.H + u];
+                rbv[g] = p.B[(size_t)d * 2 * x.GH + x.GH + (size_t)g * p.H + u];
+            }
+        }
+        if (OP == 2 && p.has_P) {
+            pI = p.P[(size_t)d * 3 * p.H + u];
+            pO = p.P[(size_t)d * 3 * p.H + p.H + u];
+            pF = p.P[(size_t)d * 3 * p.H + 2 * p.H + u];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < TN; ++i) {
+        const int rl = x.rb * TN + i;
+        const int n = x.cr * x.NRP + rl;
+        const bool ok = x.active && rl < x.NR;
+        len[i] = ok ? (p.has_lens ? p.lens[n] : p.S) : 0;
+        hown[i] = (ok && p.has_h0) ? p.h0[s_index(p, d, n, u)] : 0.f;
+        cown[i] = (ok && OP == 2 && p.has_c0) ? p.c0[s_index(p, d, n, u)] : 0.f;
+    }
+    const size_t xw_ld = (size_t)p.D * x.GH;
+    const size_t xw_col = (size_t)d * x.GH + (size_t)u * G;
+    auto load_xw = [&](int s) {
+#pragma unroll
+        for (int i = 0; i < TN; ++i) {
+            const int rl = x.rb * TN + i;
+            const int n = x.cr * x.NRP + rl;
+            if (x.active && rl < x.NR && s < len[i]) {
+                const int t = rev ? len[i] - 1 - s : s;
+                const size_t row = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
+                const float* q = p.XW + row * xw_ld + xw_col;
+#pragma unroll
+                for (int g = 0; g < G; ++g) xw[i][g] = __ldg(q + g);
+            } else {
+#pragma unroll
+                for (int g = 0; g < G; ++g) xw[i][g] = 0.f;
+            }
+        }
+    };
+
+    unsigned q = 0;
+    unsigned* my_flag = flags + x.cu;
+    const bool skip_first = p.debug_skip_cta == (int)blockIdx.x;
+    load_xw(0);
+    for (int s = 0; s < p.max_len; ++s) {
+        float xc[TN][G];
+#pragma unroll
+        for (int i = 0; i < TN; ++i)
+#pragma unroll
+            for (int g = 0; g < G; ++g) xc[i][g] = xw[i][g];
+        float* hdst = hblock((s + 1) & 1);
+
+        if constexpr (TWO) {
+            {
+                float az[TN][2];
+#pragma unroll
+                for (int i = 0; i < TN; ++i) { az[i][0] = 0.f; az[i][1] = 0.f; }
+                consume_product<TN, 2, EXACT>(p, x, 0, az, q, &s_abort, lane);
+                if (s + 1 < p.max_len) load_xw(s + 1);
+                float zg[TN];
+                float* rh = rhblock(s & 1);
+#pragma unroll
+                for (int i = 0; i < TN; ++i) {
+                    const int rl = x.rb * TN + i;
+                    zg[i] = 0.f;
+                    if (!(x.active && rl < x.NR)) continue;
+                    float rhv = 0.f;
+                    if (s < len[i]) {
+                        float pz = fadd(xc[i][0], az[i][0]);
+                        float pr = fadd(xc[i][1], az[i][1]);
+                        if (p.has_B) {
+                            pz = fadd(pz, wb[0]); pz = fadd(pz, rbv[0]);
+                            pr = fadd(pr, wb[1]); pr = fadd(pr, rbv[1]);
+                        }
+                        zg[i] = act<EXACT>(fA, clipv(p, pz));
+                        const float r = act<EXACT>(fA, clipv(p, pr));
+                        rhv = fmul(r, hown[i]);
+                    }
+                    rh[xoff(rl, u)] = rhv;
+                }
+                if (!publish(x, my_flag, 2u * s + 1u, &s_abort, skip_first && s == 0)) return;
+                float ah[TN][1];
+#pragma unroll
+                for (int i = 0; i < TN; ++i) ah[i][0] = 0.f;
+                consume_product<TN, 1, EXACT>(p, x, 2, ah, q, &s_abort, lane);
+#pragma unroll
+                for (int i = 0; i < TN; ++i) {
+                    const int rl = x.rb * TN + i;
+                    const int n = x.cr * x.NRP + rl;
+                    if (!(x.active && rl < x.NR)) continue;
+                    if (s < len[i]) {
+                        const int t = rev ? len[i] - 1 - s : s;
+                        float ph = fadd(xc[i][2], ah[i][0]);
+                        if (p.has_B) { ph = fadd(ph, wb[2]); ph = fadd(ph, rbv[2]); }
+                        const float ht = act<EXACT>(gA, clipv(p, ph));
+                        const float hn = fadd(fmul(fsub(1.0f, zg[i]), ht), fmul(zg[i], hown[i]));
+                        hown[i] = hn;
+                        if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
+                    } else if (p.Y) {
+                        p.Y[y_index(p, s, d, n, u)] = 0.f;
+                    }
+                    hdst[xoff(rl, u)] = hown[i];
+                }
+                if (!publish(x, my_flag, 2u * s + 2u, &s_abort, false)) return;
+            }
+        } else {
+            float acc[TN][G];
+#pragma unroll
+            for (int i = 0; i < TN; ++i)
+#pragma unroll
+                for (int g = 0; g < G; ++g) acc[i][g] = 0.f;
+            consume_product<TN, G, EXACT>(p, x, 0, acc, q, &s_abort, lane);
+            if (s + 1 < p.max_len) load_xw(s + 1);
+
+#pragma unroll
+            for (int i = 0; i < TN; ++i) {
+                const int rl = x.rb * TN + i;
+                const int n = x.cr * x.NRP + rl;
+                if (!(x.active && rl < x.NR)) continue;
+                if (s < len[i]) {
+                    const int t = rev ? len[i] - 1 - s : s;
+                    float hn;
+                    float pre[G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        pre[g] = fadd(xc[i][g], acc[i][g]);
+                        if (p.has_B) { pre[g] = fadd(pre[g], wb[g]); pre[g] = fadd(pre[g], rbv[g]); }
+                    }
+                    if constexpr (OP == 0) {
+                        hn = act<EXACT>(fA, clipv(p, pre[0]));
+                    } else if constexpr (OP == 1) {
+                        const float z = act<EXACT>(fA, clipv(p, pre[0]));
+                        const float r = act<EXACT>(fA, clipv(p, pre[1]));
+                        float ph;
+                        if (p.has_B) ph = fadd(fadd(xc[i][2], fmul(r, fadd(acc[i][2], rbv[2]))), wb[2]);
+                        else ph = fadd(xc[i][2], fmul(r, acc[i][2]));
+                        const float ht = act<EXACT>(gA, clipv(p, ph));
+                        hn = fadd(fmul(fsub(1.0f, z), ht), fmul(z, hown[i]));
+                    } else {
+                        float pi = pre[0], po = pre[1], pf = pre[2];
+                        const float pc = pre[3];
+                        if (p.has_P) {
+                            pi = fadd(pi, fmul(pI, cown[i]));
+                            pf = fadd(pf, fmul(pF, cown[i]));
+                        }
+                        const float ig = act<EXACT>(fA, clipv(p, pi));
+                        const float fg = p.input_forget ? fsub(1.0f, ig) : act<EXACT>(fA, clipv(p, pf));
+                        const float ct = act<EXACT>(gA, clipv(p, pc));
+                        const float cn = fadd(fmul(fg, cown[i]), fmul(ig, ct));
+                        if (p.has_P) po = fadd(po, fmul(pO, cn));
+                        const float og = act<EXACT>(fA, clipv(p, po));
+                        hn = fmul(og, act<EXACT>(hA, cn));
+                        cown[i] = cn;
+                    }
+                    hown[i] = hn;
+                    if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
+                } else if (p.Y) {
+                    p.Y[y_index(p, s, d, n, u)] = 0.f;
+                }
+                hdst[xoff(rl, u)] = hown[i];
+            }
+            if (!publish(x, my_flag, (unsigned)s + 1u, &s_abort, skip_first && s == 0)) return;
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < TN; ++i) {
+        const int rl = x.rb * TN + i;
+        const int n = x.cr * x.NRP + rl;
+        if (!(x.active && rl < x.NR)) continue;
+        const size_t si = s_index(p, d, n, u);
+        if (p.Yh) p.Yh[si] = len[i] > 0 ? canon_nan(hown[i]) : 0.f;
+        if (OP == 2 && p.Yc) p.Yc[si] = len[i] > 0 ? canon_nan(cown[i]) : 0.f;
+    }
+}
+
+template <int OP, bool TWO>
+const void* dataflow_kernel_ptr(int tn, bool exact)
+{
+    switch (tn * 2 + (exact ? 1 : 0)) {
+    case 2: return (const void*)rnn_dataflow_kernel<OP, 1, false, TWO>;
+    case 3: return (const void*)rnn_dataflow_kernel<OP, 1, true, TWO>;
+    case 4: return (const void*)rnn_dataflow_kernel<OP, 2, false, TWO>;
+    case 5: return (const void*)rnn_dataflow_kernel<OP, 2, true, TWO>;
+    case 8: return (const void*)rnn_dataflow_kernel<OP, 4, false, TWO>;
+    case 9: return (const void*)rnn_dataflow_kernel<OP, 4, true, TWO>;
+    default: return nullptr;
+    }
+}
+
+template <int OP>
+const void* dataflow_kernel_ptr(int tn, bool exact, bool two)
+{
+    if constexpr (OP == 1) {
+        if (two) return dataflow_kernel_ptr<OP, true>(tn, exact);
+    }
+    return dataflow_kernel_ptr<OP, false>(tn, exact);
+}
+
+template <int OP>
+cudaError_t launch_dataflow_op(const RecParams& p, bool exact, int threads, size_t smem, cudaStream_t stream)
+{
+    const void* fn = dataflow_kernel_ptr<OP>(p.rows_per_thread, exact, OP == 1 && p.lbr == 0);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    void* args[] = {(void*)&p};
+    return cudaLaunchCooperativeKernel(fn, dim3(p.D * p.ctas_per_dir), dim3(threads), args, smem, stream);
+}
+
+template <int OP>
+cudaError_t dataflow_occupancy_op(int tn, bool exact, bool two, int threads, size_t smem, int* blocks)
+{
+    const void* fn = dataflow_kernel_ptr<OP>(tn, exact, two);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, threads, smem);
+}
+
+}  // namespace rnngb

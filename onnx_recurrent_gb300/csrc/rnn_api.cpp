@@ -18,9 +18,9 @@ namespace rnngb {
 cudaError_t launch_recurrent_rnn(const RecParams&, bool, int, size_t, cudaStream_t);
 cudaError_t launch_recurrent_gru(const RecParams&, bool, int, size_t, cudaStream_t);
 cudaError_t launch_recurrent_lstm(const RecParams&, bool, int, size_t, cudaStream_t);
-cudaError_t recurrent_occupancy_rnn(int, bool, int, size_t, int*);
-cudaError_t recurrent_occupancy_gru(int, bool, int, size_t, int*);
-cudaError_t recurrent_occupancy_lstm(int, bool, int, size_t, int*);
+cudaError_t recurrent_occupancy_rnn(int, int, int, bool, int, size_t, int*);
+cudaError_t recurrent_occupancy_gru(int, int, int, bool, int, size_t, int*);
+cudaError_t recurrent_occupancy_lstm(int, int, int, bool, int, size_t, int*);
 
 cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t smem, cudaStream_t s)
 {
@@ -31,12 +31,12 @@ cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t
     }
 }
 
-cudaError_t recurrent_occupancy(int op, int tn, bool exact, int threads, size_t smem, int* blocks)
+cudaError_t recurrent_occupancy(int op, int lbr, int kernel, int tn, bool exact, int threads, size_t smem, int* blocks)
 {
     switch (op) {
-    case 0: return recurrent_occupancy_rnn(tn, exact, threads, smem, blocks);
-    case 1: return recurrent_occupancy_gru(tn, exact, threads, smem, blocks);
-    default: return recurrent_occupancy_lstm(tn, exact, threads, smem, blocks);
+    case 0: return recurrent_occupancy_rnn(kernel, lbr, tn, exact, threads, smem, blocks);
+    case 1: return recurrent_occupancy_gru(kernel, lbr, tn, exact, threads, smem, blocks);
+    default: return recurrent_occupancy_lstm(kernel, lbr, tn, exact, threads, smem, blocks);
     }
 }
 }  // namespace rnngb
@@ -64,7 +64,8 @@ rnn_status cuda_fail(cudaError_t e, const char* what)
                 cudaGetErrorString(e));
 }
 
-constexpr int kMaxThreads = 512;
+constexpr int kMaxThreads = 512;          // staged kernel
+constexpr int kMaxComputeThreads = 480;   // dataflow kernel (plus one loader warp)
 constexpr long long kDefaultSpinNs = 2000000000LL;   // 2 s per barrier wait
 
 int gates_of(int op) { return op == RNN_OP_RNN ? 1 : (op == RNN_OP_GRU ? 3 : 4); }
@@ -121,6 +122,7 @@ struct rnn_plan {
     bool const_weights = false;
     float* wt_const = nullptr;   // [I][D*G*H]
     float* rt_const = nullptr;   // [D][H][G*H]
+    float* r_orig_const = nullptr;   // R as given, [D][G*H][H] (the dataflow kernel reads this layout)
 
     // scratch
     char* scratch = nullptr;
@@ -131,8 +133,8 @@ struct rnn_plan {
     int device = -1;
 
     // launch overrides and record
-    int ov_ctas = 0, ov_tn = 0, ov_rres = -1;
-    int g_ctas = 0, g_tn = 0, g_rres = 0, g_threads = 0, g_smem = 0;
+    int ov_units = 0, ov_tn = 0, ov_rres = -1, ov_rows = 0, ov_kernel = 0;
+    int g_units = 0, g_tn = 0, g_rres = 0, g_rows = 0, g_kernel = 0, g_threads = 0, g_smem = 0;
     int last_launches = 0;
 
     // timing: a ring of event sets, one per run, harvested lazily so that
@@ -178,20 +180,35 @@ rnn_status device_info(DeviceInfo* out)
 }
 
 struct Geometry {
-    int ctas, umax, tn, threads, rres;
+    int kernel;       // 1 staged, 2 dataflow
+    int ctas;         // CTAs per direction
+    int units;        // unit groups
+    int rows;         // row groups
+    int quant;        // unit quantum
+    int slots;        // dataflow ring slots
+    int umax, tn, threads, rres;
     size_t smem;
-    int npad;
+    int npad;         // rows per row group (padded)
+    int hpad;         // dataflow: exchange-buffer row length
+    int cpb;          // dataflow: chunks per tensor copy
+    int ustride;      // dataflow: floats per unit of the resident R slice
 };
 
-// Launch geometry of the recurrent kernel for batch N.
-rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* g)
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Staged kernel: C CTAs per direction, all rows, device-wide barrier per step.
+rnn_status plan_staged(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* g)
 {
     const int64_t H = pl->H;
     const int G = pl->G, D = pl->D;
+    g->kernel = 1;
+    g->rows = 1;
+    g->quant = 1;
+    g->slots = 0;
     g->npad = (int)round_up(N, 8);
     int C;
-    if (pl->ov_ctas > 0) {
-        C = (int)std::min<int64_t>(pl->ov_ctas, H);
+    if (pl->ov_units > 0) {
+        C = (int)std::min<int64_t>(pl->ov_units, H);
     } else {
         const long long macs = (long long)N * G * H * H;
         const int64_t single_threads = H * ((N + 7) / 8);
@@ -203,12 +220,11 @@ rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
         C = (int)((H + umax0 - 1) / umax0);
     }
     g->ctas = C;
+    g->units = C;
     g->umax = (int)((H + C - 1) / C);
     const int tns[4] = {1, 2, 4, 8};
     g->tn = 0;
     if (pl->ov_tn > 0) {
-        if (pl->ov_tn != 1 && pl->ov_tn != 2 && pl->ov_tn != 4 && pl->ov_tn != 8)
-            return fail(RNN_ERR_INVALID_ARGUMENT, "rows_per_thread must be 1, 2, 4 or 8");
         g->tn = pl->ov_tn;
     } else {
         for (int tn : tns)
@@ -233,7 +249,7 @@ rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
         return fail(RNN_ERR_UNSUPPORTED, "recurrent kernel needs %zu bytes of shared memory (max %d)",
                     g->smem, di.smem_optin);
     int blocks = 0;
-    cudaError_t e = recurrent_occupancy(pl->op, g->tn, pl->mode == RNN_MODE_EXACT, g->threads, g->smem, &blocks);
+    cudaError_t e = recurrent_occupancy(pl->op, pl->lbr, 1, g->tn, pl->mode == RNN_MODE_EXACT, g->threads, g->smem, &blocks);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
     if (blocks < 1 || (int64_t)D * C > (int64_t)blocks * di.sms)
         return fail(RNN_ERR_UNSUPPORTED,
@@ -242,14 +258,148 @@ rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
     return RNN_OK;
 }
 
+// Dataflow kernel: CU unit groups x CR row groups per direction, TMA ring,
+// per-CTA flags.  Picks the cheapest feasible shape under a simple cost
+// model (cycles per step: k-loop issue + h/R bytes into the SM + epilogue +
+// a fixed latency for the flags and the first copy).
+rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out)
+{
+    const int64_t H = pl->H;
+    const int G = pl->G, D = pl->D;
+    const bool exact = pl->mode == RNN_MODE_EXACT;
+    const int nchunks = (int)ceil_div(H, kRecKC);
+    const int phases = (pl->op == RNN_OP_GRU && pl->lbr == 0) ? 2 : 1;
+    const size_t smem_cap = (size_t)di.smem_optin - 1024;   // static shared: mbarriers, flags
+    if (H % 4 != 0 || H > (1 << 20))
+        return fail(RNN_ERR_UNSUPPORTED, "the dataflow kernel needs hidden_size a multiple of 4");
+    double best_cost = 1e300;
+    bool found = false;
+    const int cr_auto[6] = {1, 2, 4, 8, 16, 32};
+    const int ncr = pl->ov_rows > 0 ? 1 : 6;
+    for (int cri = 0; cri < ncr; ++cri) {
+        const int CRc = pl->ov_rows > 0 ? pl->ov_rows : cr_auto[cri];
+        const int64_t NRP = round_up(ceil_div(N, CRc), 8);
+        const int CR = (int)ceil_div(N, NRP);
+        if (CR != CRc) continue;                                   // would leave an empty row group
+        if (NRP > 256) continue;                                   // a tensor-copy box spans at most 256 rows
+        const int64_t cu_cap = pl->ov_units > 0 ? pl->ov_units : di.sms / ((int64_t)D * CR);
+        if (cu_cap < 1) continue;
+        for (int rr = 1; rr >= 0; --rr) {
+            if (pl->ov_rres >= 0 && rr != pl->ov_rres) continue;
+            const int quant = 1;
+            const int64_t Q = H;
+            int64_t CU = std::min<int64_t>(cu_cap, Q);
+            const int64_t qmax = ceil_div(Q, CU);
+            if (pl->ov_units <= 0) CU = ceil_div(Q, qmax);
+            const int umax = (int)(qmax * quant);
+            if ((int64_t)D * CR * CU > kMaxFlags) continue;
+            int tn = 0;
+            const int tlist[3] = {1, 2, 4};
+            for (int t : tlist) {
+                if (pl->ov_tn > 0 && t != pl->ov_tn) continue;
+                if (NRP % t) continue;
+                const int cap = t == 1 ? 224 : 352;   // the kernel's launch bound, less the loader
+                if ((int64_t)umax * (NRP / t) <= cap) { tn = t; break; }
+            }
+            if (!tn) continue;
+            if (rr == 0 && (H < kDfPitch || umax > 256)) continue;   // R boxes: 36 k wide, <= 256 units
+            const int compute = (int)round_up((int64_t)umax * (NRP / tn), 32);
+            // pieces: about four tensor copies per product, fewer if the ring
+            // would not hold two pieces
+            int cpb = 0, slots = 0;
+            for (int c = (int)ceil_div(nchunks, 4); c >= 1; c /= 2) {
+                const size_t fixed = df_smem_bytes((int)H, umax, G, (int)NRP, rr, c, 0);
+                const size_t per_slot = df_smem_bytes((int)H, umax, G, (int)NRP, rr, c, 1) - fixed;
+                if (fixed + 2 * per_slot > smem_cap) continue;
+                const int np = (int)ceil_div(nchunks, c);
+                cpb = c;
+                slots = (int)std::min<size_t>(std::min<size_t>((size_t)kMaxSlots, (size_t)2 * np * phases),
+                                              (smem_cap - fixed) / per_slot);
+                break;
+            }
+            if (cpb == 0 || slots < 2) continue;
+            const size_t smem = df_smem_bytes((int)H, umax, G, (int)NRP, rr, cpb, slots);
+            const double wps = (double)ceil_div(compute / 32, 4);
+            const double per_k = ((exact ? 2.0 : 1.0) * 4.0 * tn * G + tn + G) / 4.0;
+            const double kloop = (double)H * per_k * wps;
+            const double bytes = (double)NRP * H * 4 * phases + (rr ? 0.0 : (double)H * umax * G * 4 * phases);
+            const double fetch = bytes / 64.0 * (slots >= (int)ceil_div(nchunks, cpb) * phases ? 0.5 : 1.0);
+            const double cost = kloop + fetch + 600.0 * tn * phases + 2500.0 * phases;
+            if (cost < best_cost) {
+                int blocks = 0;
+                cudaError_t e = recurrent_occupancy(pl->op, pl->lbr, 2, tn, exact, compute + 32, smem, &blocks);
+                if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+                if (blocks < 1 || (int64_t)D * CR * CU > (int64_t)blocks * di.sms) continue;
+                best_cost = cost;
+                found = true;
+                out->kernel = 2;
+                out->units = (int)CU;
+                out->rows = CR;
+                out->ctas = (int)CU * CR;
+                out->quant = quant;
+                out->slots = slots;
+                out->umax = umax;
+                out->tn = tn;
+                out->threads = compute + 32;
+                out->rres = rr;
+                out->smem = smem;
+                out->npad = (int)NRP;
+                out->hpad = (int)round_up(H, kRecKC);
+                out->cpb = cpb;
+                out->ustride = df_unit_stride((int)H, G);
+            }
+        }
+    }
+    if (!found)
+        return fail(RNN_ERR_UNSUPPORTED, "no dataflow launch fits batch %lld, hidden %lld", (long long)N,
+                    (long long)H);
+    return RNN_OK;
+}
+
+// Launch geometry of the recurrent kernel for batch N.
+rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, const float* R, Geometry* g)
+{
+    if (pl->ov_kernel == 1) return plan_staged(pl, N, di, g);
+    // the dataflow kernel reads R (as given) with TMA: 16-byte aligned base
+    const float* rsrc = pl->const_weights ? pl->r_orig_const : R;
+    if ((uintptr_t)rsrc % 16 != 0) {
+        if (pl->ov_kernel == 2) return fail(RNN_ERR_UNSUPPORTED, "the dataflow kernel needs R 16-byte aligned");
+        return plan_staged(pl, N, di, g);
+    }
+    if (pl->ov_kernel == 2) return plan_dataflow(pl, N, di, g);
+    const int64_t H = pl->H;
+    const long long macs = (long long)N * pl->G * H * H;
+    if (macs <= 262144 && H * ((N + 7) / 8) <= kMaxThreads && pl->ov_units <= 0 && pl->ov_rows <= 0)
+        return plan_staged(pl, N, di, g);                          // one CTA per direction
+    const std::string saved = g_error;
+    if (plan_dataflow(pl, N, di, g) == RNN_OK) {
+        // Measured on GB300: the dataflow kernel wins while a CTA's share of a
+        // step is small (its per-step latency dominates: 512 to 2048 hidden,
+        // a few rows); with more than about a million products per CTA and
+        // step the staged kernel, with more threads per CTA, keeps its
+        // arithmetic pipes busier.
+        const double work = (double)g->umax * pl->G * g->npad * (double)H;
+        if (work <= (double)(1 << 20)) return RNN_OK;
+        Geometry st{};
+        if (plan_staged(pl, N, di, &st) == RNN_OK) {
+            *g = st;
+            return RNN_OK;
+        }
+        g_error = saved;
+        return plan_dataflow(pl, N, di, g);
+    }
+    g_error = saved;
+    return plan_staged(pl, N, di, g);
+}
+
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 rnn_status ensure_scratch(rnn_plan* pl, size_t bytes)
 {
     if (!pl->ctrl) {
-        cudaError_t e = cudaMalloc((void**)&pl->ctrl, 256);
+        cudaError_t e = cudaMalloc((void**)&pl->ctrl, kCtrlBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(control)");
-        e = cudaMemset(pl->ctrl, 0, 256);
+        e = cudaMemset(pl->ctrl, 0, kCtrlBytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(control)");
     }
     if (bytes <= pl->scratch_bytes) return RNN_OK;
@@ -299,6 +449,207 @@ cudaError_t harvest(rnn_plan* pl, int slot)
     pl->totals_runs += 1;
     pl->slot_pending[slot] = false;
     return cudaSuccess;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on the driver library): a tiled fp32 map with 128-byte swizzle.
+typedef CUresult (*TmapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+rnn_status tmap_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box)
+{
+    static TmapEncodeFn fn = []() -> TmapEncodeFn {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<TmapEncodeFn>(f);
+    }();
+    if (!fn) return fail(RNN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(RNN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return RNN_OK;
+}
+
+struct RunArgs {
+    int64_t S, N;
+    const float *X, *W, *R, *B;
+    const int32_t* lens;
+    const float *h0, *c0, *P;
+    float *Y, *Yh, *Yc;
+    cudaStream_t st;
+};
+
+// Checks that need no device work: sizes, required pointers, the scratch
+// limit.  Sets *done when the zero-size rule applies (after queueing the
+// copies of the initial states).
+rnn_status check_run(rnn_plan* pl, RunArgs& a, bool* done)
+{
+    *done = false;
+    if (a.S < 0 || a.N < 0) return fail(RNN_ERR_INVALID_ARGUMENT, "seq_length and batch_size must be >= 0");
+    if (a.S > (1 << 30) || a.N > (1 << 24)) return fail(RNN_ERR_UNSUPPORTED, "seq_length or batch_size too large");
+    const int64_t H = pl->H, I = pl->I, GH = (int64_t)pl->G * H, D = pl->D;
+    if (pl->op != RNN_OP_LSTM) { a.c0 = nullptr; a.P = nullptr; a.Yc = nullptr; }
+    // Limits: per-direction scratch below 2^30 floats.
+    const double per_dir = (double)a.S * a.N * GH + 4.0 * a.N * H + (pl->const_weights ? 0.0 : (double)GH * (I + H));
+    if (per_dir >= 1073741824.0)
+        return fail(RNN_ERR_UNSUPPORTED, "per-direction scratch of %.0f floats reaches the 2^30 limit", per_dir);
+    // Zero-size: nothing runs; final states are the initial states or zeros.
+    if (a.S == 0 || a.N == 0) {
+        const size_t sb = sizeof(float) * (size_t)D * a.N * H;
+        cudaError_t e = cudaSuccess;
+        if (a.Yh && sb)
+            e = a.h0 ? cudaMemcpyAsync(a.Yh, a.h0, sb, cudaMemcpyDeviceToDevice, a.st) : cudaMemsetAsync(a.Yh, 0, sb, a.st);
+        if (e == cudaSuccess && a.Yc && sb)
+            e = a.c0 ? cudaMemcpyAsync(a.Yc, a.c0, sb, cudaMemcpyDeviceToDevice, a.st) : cudaMemsetAsync(a.Yc, 0, sb, a.st);
+        if (e != cudaSuccess) return cuda_fail(e, "zero-size copy");
+        *done = true;
+        return RNN_OK;
+    }
+    if (!a.X && I > 0) return fail(RNN_ERR_INVALID_ARGUMENT, "X is NULL");
+    if (!pl->const_weights && (!a.R || (!a.W && I > 0))) return fail(RNN_ERR_INVALID_ARGUMENT, "W and R are required");
+    return RNN_OK;
+}
+
+// sequence_lens already copied to `host`: check every length, find the longest.
+rnn_status check_lengths(const int32_t* host, int64_t N, int64_t S, int64_t* max_len)
+{
+    *max_len = 0;
+    for (int64_t n = 0; n < N; ++n) {
+        const int32_t L = host[n];
+        if (L < 0 || (int64_t)L > S)
+            return fail(RNN_ERR_INVALID_INPUT, "sequence_lens[%lld] = %d is outside [0, %lld]", (long long)n, L,
+                        (long long)S);
+        *max_len = std::max<int64_t>(*max_len, L);
+    }
+    return RNN_OK;
+}
+
+struct Layout {
+    size_t wt, rt, xw, hb, rh, total;
+    bool need_rh;
+};
+
+// Scratch layout after `base` bytes (control words live elsewhere).
+Layout scratch_layout(const rnn_plan* pl, const Geometry& geo, int64_t S, int64_t N, size_t base)
+{
+    const int64_t H = pl->H, I = pl->I, GH = (int64_t)pl->G * H, D = pl->D;
+    Layout L;
+    size_t off = base;
+    L.wt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)I * D * GH);
+    L.rt = off; off += (pl->const_weights || geo.kernel == 2) ? 0 : align256(sizeof(float) * (size_t)D * H * GH);
+    L.xw = off; off += align256(sizeof(float) * (size_t)S * N * D * GH);
+    const size_t row = geo.kernel == 2 ? (size_t)geo.hpad / kRecKC * kDfPitch : (size_t)H;
+    const size_t hbuf = sizeof(float) * (size_t)D * 2 * geo.rows * geo.npad * row;
+    L.hb = off; off += align256(hbuf);
+    L.need_rh = pl->op == RNN_OP_GRU && pl->lbr == 0;
+    L.rh = off; off += L.need_rh ? align256(hbuf) : 0;
+    L.total = off;
+    return L;
+}
+
+// Queue the kernels of one run.  `scratch` holds the layout, `ctrl` the
+// control block (the set-up kernel zeroes its counters and flags).
+rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t max_len, char* scratch,
+                   const Layout& L, char* ctrl, bool timed, long long spin_ns, int skip_cta, int* launches_out)
+{
+    const int64_t H = pl->H, I = pl->I, G = pl->G, D = pl->D, GH = G * H;
+    const int64_t M = a.S * a.N;
+    float* wt = pl->const_weights ? pl->wt_const : (float*)(scratch + L.wt);
+    float* rt = pl->const_weights ? pl->rt_const : (float*)(scratch + L.rt);
+    float* xw = (float*)(scratch + L.xw);
+    const bool exact = pl->mode == RNN_MODE_EXACT;
+    int launches = 0;
+    cudaError_t e;
+    if (timed) record(pl, 0, a.st);
+    if (!pl->const_weights) {
+        const bool pack_r = geo.kernel != 2;   // the dataflow kernel reads R as given
+        e = launch_pack(a.W, pack_r ? a.R : nullptr, wt, pack_r ? rt : nullptr, (int)D, (int)G, H, I, a.st);
+        if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+        launches += (int)D * ((I > 0 ? 1 : 0) + (pack_r ? 1 : 0));
+    }
+    if (timed) record(pl, 1, a.st);
+    e = launch_projection(a.X, wt, xw, M, I, D * GH, exact, a.st);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    launches += 1;
+    if (timed) record(pl, 2, a.st);
+
+    RecParams p;
+    std::memset(&p, 0, sizeof p);
+    p.op = pl->op; p.G = (int)G; p.D = (int)D; p.N = (int)a.N; p.H = (int)H; p.S = (int)a.S;
+    p.layout = pl->layout; p.lbr = pl->lbr; p.input_forget = pl->input_forget;
+    p.has_B = a.B != nullptr; p.has_P = a.P != nullptr; p.has_h0 = a.h0 != nullptr; p.has_c0 = a.c0 != nullptr;
+    p.has_lens = a.lens != nullptr; p.has_clip = pl->has_clip; p.clip = pl->clip;
+    for (int d = 0; d < 2; ++d)
+        for (int s = 0; s < 3; ++s) p.act[d][s] = pl->act[d][s];
+    p.max_len = (int)max_len;
+    p.dir_reverse[0] = pl->direction == RNN_DIR_REVERSE ? 1 : 0;
+    p.dir_reverse[1] = 1;
+    p.kernel = geo.kernel;
+    p.ctas_per_dir = geo.ctas; p.unit_groups = geo.units; p.row_groups = geo.rows; p.unit_quant = geo.quant;
+    p.slots = geo.slots; p.umax = geo.umax; p.rows_per_thread = geo.tn; p.r_resident = geo.rres;
+    p.npad = geo.npad;
+    p.hpad = geo.hpad;
+    p.chunks_per_piece = geo.cpb;
+    p.unit_stride = geo.ustride;
+    p.XW = xw; p.Rt = rt; p.Rorig = pl->const_weights ? pl->r_orig_const : a.R; p.B = a.B; p.P = a.P; p.h0 = a.h0; p.c0 = a.c0; p.lens = a.lens;
+    p.Y = a.Y; p.Yh = a.Yh; p.Yc = a.Yc;
+    p.hbuf = (float*)(scratch + L.hb);
+    p.rhbuf = L.need_rh ? (float*)(scratch + L.rh) : nullptr;
+    p.bar = (unsigned*)ctrl;
+    p.status = (int*)(ctrl + kCtrlStatusOffset);
+    p.flags = (unsigned*)(ctrl + kCtrlFlagsOffset);
+    p.spin_limit_ns = spin_ns;
+    p.debug_skip_cta = skip_cta;
+    if (geo.kernel == 2) {
+        // h / r (.) h exchange buffers [D*2*CR blocks][hpad/32 chunks][npad rows][36],
+        // box 36 x npad x cpb x 1 (one piece of one row group, contiguous)
+        const cuuint64_t nck = (cuuint64_t)(geo.hpad / kRecKC);
+        const cuuint64_t hdims[4] = {(cuuint64_t)kDfPitch, (cuuint64_t)geo.npad, nck, (cuuint64_t)(D * 2 * geo.rows)};
+        const cuuint64_t hstrides[3] = {(cuuint64_t)kDfPitch * 4, (cuuint64_t)geo.npad * kDfPitch * 4,
+                                        nck * geo.npad * kDfPitch * 4};
+        const cuuint32_t hbox[4] = {(cuuint32_t)kDfPitch, (cuuint32_t)geo.npad, (cuuint32_t)geo.cpb, 1};
+        rnn_status rs = tmap_encode(&p.hmap, p.hbuf, 4, hdims, hstrides, hbox);
+        if (rs != RNN_OK) return rs;
+        rs = tmap_encode(&p.rhmap, p.rhbuf ? p.rhbuf : p.hbuf, 4, hdims, hstrides, hbox);
+        if (rs != RNN_OK) return rs;
+        if (!geo.rres) {
+            // R as given [D][G][H units][H k], box 36 x umax x G x 1 (one chunk; k past H reads 0)
+            const cuuint64_t rdims[4] = {(cuuint64_t)H, (cuuint64_t)H, (cuuint64_t)G, (cuuint64_t)D};
+            const cuuint64_t rstrides[3] = {(cuuint64_t)H * 4, (cuuint64_t)H * H * 4, (cuuint64_t)G * H * H * 4};
+            const cuuint32_t rbox[4] = {(cuuint32_t)kDfPitch, (cuuint32_t)geo.umax, (cuuint32_t)G, 1};
+            rs = tmap_encode(&p.rmap, p.Rorig, 4, rdims, rstrides, rbox);
+            if (rs != RNN_OK) return rs;
+        } else {
+            p.rmap = p.hmap;   // unused
+        }
+    }
+
+    e = launch_state_init(p, a.st);
+    if (e != cudaSuccess) return cuda_fail(e, "state set-up launch");
+    launches += 1;
+    if (timed) record(pl, 3, a.st);
+    e = launch_recurrent(p, exact, geo.threads, geo.smem, a.st);
+    if (e != cudaSuccess) return cuda_fail(e, "recurrent launch");
+    launches += 1;
+    if (timed) record(pl, 4, a.st);
+    if (a.Y && max_len < a.S) {
+        e = launch_mask_tail(a.Y, pl->layout, a.S, D, a.N, H, max_len, a.st);
+        if (e != cudaSuccess) return cuda_fail(e, "mask launch");
+        launches += 1;
+    }
+    if (timed) record(pl, 5, a.st);
+    pl->g_units = geo.units; pl->g_tn = geo.tn; pl->g_rres = geo.rres; pl->g_rows = geo.rows;
+    pl->g_kernel = geo.kernel; pl->g_threads = geo.threads; pl->g_smem = (int)geo.smem;
+    *launches_out = launches;
+    return RNN_OK;
 }
 
 }  // namespace
@@ -394,6 +745,7 @@ void rnn_plan_destroy(rnn_plan_t pl)
     if (pl->ctrl) cudaFree(pl->ctrl);
     if (pl->wt_const) cudaFree(pl->wt_const);
     if (pl->rt_const) cudaFree(pl->rt_const);
+    if (pl->r_orig_const) cudaFree(pl->r_orig_const);
     if (pl->lens_host) cudaFreeHost(pl->lens_host);
     if (pl->events_ready)
         for (auto& set : pl->ev)
@@ -422,28 +774,38 @@ rnn_status rnn_plan_get_activation(rnn_plan_t pl, int dir, int slot, int* fn, fl
     return RNN_OK;
 }
 
-rnn_status rnn_plan_set_launch(rnn_plan_t pl, int ctas_per_dir, int rows_per_thread, int r_resident)
+rnn_status rnn_plan_set_launch(rnn_plan_t pl, int unit_groups, int rows_per_thread, int r_resident,
+                               int row_groups, int kernel)
 {
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
-    if (ctas_per_dir < 0 || rows_per_thread < 0 || r_resident < -1 || r_resident > 1)
+    if (unit_groups < 0 || rows_per_thread < 0 || r_resident < -1 || r_resident > 1 || row_groups < 0 ||
+        kernel < 0 || kernel > 2)
         return fail(RNN_ERR_INVALID_ARGUMENT, "bad launch override");
     if (rows_per_thread != 0 && rows_per_thread != 1 && rows_per_thread != 2 && rows_per_thread != 4 &&
         rows_per_thread != 8)
         return fail(RNN_ERR_INVALID_ARGUMENT, "rows_per_thread must be 0, 1, 2, 4 or 8");
-    pl->ov_ctas = ctas_per_dir;
+    if (kernel == 1 && row_groups > 1) return fail(RNN_ERR_INVALID_ARGUMENT, "the staged kernel has one row group");
+    if (kernel == 2 && rows_per_thread == 8)
+        return fail(RNN_ERR_INVALID_ARGUMENT, "the dataflow kernel takes 1, 2 or 4 rows per thread");
+    pl->ov_units = unit_groups;
     pl->ov_tn = rows_per_thread;
     pl->ov_rres = r_resident;
+    pl->ov_rows = row_groups;
+    pl->ov_kernel = kernel;
     return RNN_OK;
 }
 
-rnn_status rnn_plan_get_launch(rnn_plan_t pl, int* ctas, int* tn, int* rres, int* threads, int* smem)
+rnn_status rnn_plan_get_launch(rnn_plan_t pl, int* unit_groups, int* rows_per_thread, int* r_resident,
+                               int* row_groups, int* kernel, int* threads, int* smem_bytes)
 {
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
-    if (ctas) *ctas = pl->g_ctas;
-    if (tn) *tn = pl->g_tn;
-    if (rres) *rres = pl->g_rres;
+    if (unit_groups) *unit_groups = pl->g_units;
+    if (rows_per_thread) *rows_per_thread = pl->g_tn;
+    if (r_resident) *r_resident = pl->g_rres;
+    if (row_groups) *row_groups = pl->g_rows;
+    if (kernel) *kernel = pl->g_kernel;
     if (threads) *threads = pl->g_threads;
-    if (smem) *smem = pl->g_smem;
+    if (smem_bytes) *smem_bytes = pl->g_smem;
     return RNN_OK;
 }
 
@@ -511,11 +873,11 @@ rnn_status rnn_plan_sync(rnn_plan_t pl)
     cudaError_t e = pl->done_ready ? cudaEventSynchronize(pl->done) : cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "waiting for the run");
     int st = 0;
-    e = cudaMemcpy(&st, pl->ctrl + 64, sizeof st, cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(&st, pl->ctrl + kCtrlStatusOffset, sizeof st, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
     if (st != 0) {
         const int zero = 0;
-        cudaMemcpy(pl->ctrl + 64, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        cudaMemcpy(pl->ctrl + kCtrlStatusOffset, &zero, sizeof zero, cudaMemcpyHostToDevice);
         if (st == RNN_ERR_TIMEOUT)
             return fail(RNN_ERR_TIMEOUT, "the device-wide step barrier timed out; outputs are incomplete");
         return fail((rnn_status)st, "device reported status %d", st);
@@ -537,7 +899,14 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
             if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(W pack)");
         }
     }
-    cudaError_t e = launch_pack(W, R, pl->wt_const, pl->rt_const, pl->D, pl->G, pl->H, pl->I, s);
+    if (!pl->r_orig_const) {
+        cudaError_t e = cudaMalloc((void**)&pl->r_orig_const, sizeof(float) * (size_t)pl->D * GH * pl->H);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(R copy)");
+    }
+    cudaError_t e = cudaMemcpyAsync(pl->r_orig_const, R, sizeof(float) * (size_t)pl->D * GH * pl->H,
+                                    cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "copying R");
+    e = launch_pack(W, R, pl->wt_const, pl->rt_const, pl->D, pl->G, pl->H, pl->I, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     pl->const_weights = true;
     return RNN_OK;
@@ -550,32 +919,13 @@ rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const fl
     g_error.clear();
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
     pl->last_launches = 0;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (S < 0 || N < 0) return fail(RNN_ERR_INVALID_ARGUMENT, "seq_length and batch_size must be >= 0");
-    if (S > (1 << 30) || N > (1 << 24)) return fail(RNN_ERR_UNSUPPORTED, "seq_length or batch_size too large");
-    const int64_t H = pl->H, I = pl->I, G = pl->G, D = pl->D, GH = G * H;
-    if (pl->op != RNN_OP_LSTM) { c0 = nullptr; P = nullptr; Yc = nullptr; }
-
-    // Limits: per-direction scratch below 2^30 floats.
-    const double per_dir = (double)S * N * GH + 4.0 * N * H + (pl->const_weights ? 0.0 : (double)GH * (I + H));
-    if (per_dir >= 1073741824.0)
-        return fail(RNN_ERR_UNSUPPORTED, "per-direction scratch of %.0f floats reaches the 2^30 limit", per_dir);
-
-    // Zero-size: nothing runs; final states are the initial states or zeros.
-    if (S == 0 || N == 0) {
-        const size_t sb = sizeof(float) * (size_t)D * N * H;
-        cudaError_t e = cudaSuccess;
-        if (Yh && sb) e = h0 ? cudaMemcpyAsync(Yh, h0, sb, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(Yh, 0, sb, st);
-        if (e == cudaSuccess && Yc && sb)
-            e = c0 ? cudaMemcpyAsync(Yc, c0, sb, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(Yc, 0, sb, st);
-        if (e != cudaSuccess) return cuda_fail(e, "zero-size copy");
-        return RNN_OK;
-    }
-    if (!X && I > 0) return fail(RNN_ERR_INVALID_ARGUMENT, "X is NULL");
-    if (!pl->const_weights && (!R || (!W && I > 0))) return fail(RNN_ERR_INVALID_ARGUMENT, "W and R are required");
+    RunArgs a{S, N, X, W, R, B, lens, h0, c0, P, Y, Yh, Yc, (cudaStream_t)stream};
+    bool done = false;
+    rnn_status rs = check_run(pl, a, &done);
+    if (rs != RNN_OK || done) return rs;
 
     DeviceInfo di;
-    rnn_status rs = device_info(&di);
+    rs = device_info(&di);
     if (rs != RNN_OK) return rs;
     if (!di.coop) return fail(RNN_ERR_UNSUPPORTED, "device lacks cooperative launch");
 
@@ -589,33 +939,18 @@ rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const fl
             if (e != cudaSuccess) { pl->lens_cap = 0; return cuda_fail(e, "cudaMallocHost(lens)"); }
             pl->lens_cap = N;
         }
-        cudaError_t e = cudaMemcpyAsync(pl->lens_host, lens, sizeof(int32_t) * (size_t)N, cudaMemcpyDeviceToHost, st);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        cudaError_t e = cudaMemcpyAsync(pl->lens_host, lens, sizeof(int32_t) * (size_t)N, cudaMemcpyDeviceToHost, a.st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(a.st);
         if (e != cudaSuccess) return cuda_fail(e, "copying sequence_lens");
-        max_len = 0;
-        for (int64_t n = 0; n < N; ++n) {
-            const int32_t L = pl->lens_host[n];
-            if (L < 0 || (int64_t)L > S)
-                return fail(RNN_ERR_INVALID_INPUT, "sequence_lens[%lld] = %d is outside [0, %lld]", (long long)n, L,
-                            (long long)S);
-            max_len = std::max<int64_t>(max_len, L);
-        }
+        rs = check_lengths(pl->lens_host, N, S, &max_len);
+        if (rs != RNN_OK) return rs;
     }
 
     Geometry geo{};
-    rs = plan_geometry(pl, N, di, &geo);
+    rs = plan_geometry(pl, N, di, R, &geo);
     if (rs != RNN_OK) return rs;
-
-    // scratch layout
-    const int64_t M = S * N;
-    size_t off = 0;
-    const size_t o_wt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)I * D * GH);
-    const size_t o_rt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)D * H * GH);
-    const size_t o_xw = off; off += align256(sizeof(float) * (size_t)M * D * GH);
-    const size_t o_hb = off; off += align256(sizeof(float) * (size_t)D * 2 * H * geo.npad);
-    const bool need_rh = pl->op == RNN_OP_GRU && pl->lbr == 0;
-    const size_t o_rh = off; off += need_rh ? align256(sizeof(float) * (size_t)D * H * geo.npad) : 0;
-    rs = ensure_scratch(pl, std::max<size_t>(off, 256));
+    const Layout L = scratch_layout(pl, geo, S, N, 0);
+    rs = ensure_scratch(pl, std::max<size_t>(L.total, 256));
     if (rs != RNN_OK) return rs;
     if (pl->device < 0) cudaGetDevice(&pl->device);
     if (pl->timing && !pl->events_ready) {
@@ -633,67 +968,13 @@ rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const fl
         if (eh != cudaSuccess) return cuda_fail(eh, "reading timing events");
         for (bool& u : pl->ev_used[pl->slot]) u = false;
     }
-
-    float* wt = pl->const_weights ? pl->wt_const : (float*)(pl->scratch + o_wt);
-    float* rt = pl->const_weights ? pl->rt_const : (float*)(pl->scratch + o_rt);
-    float* xw = (float*)(pl->scratch + o_xw);
-    const bool exact = pl->mode == RNN_MODE_EXACT;
     int launches = 0;
-    cudaError_t e;
-
-    record(pl, 0, st);
-    if (!pl->const_weights) {
-        e = launch_pack(W, R, wt, rt, (int)D, (int)G, H, I, st);
-        if (e != cudaSuccess) return cuda_fail(e, "pack launch");
-        launches += (int)D * (I > 0 ? 2 : 1);
-    }
-    record(pl, 1, st);
-    e = launch_projection(X, wt, xw, M, I, D * GH, exact, st);
-    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-    launches += 1;
-    record(pl, 2, st);
-
-    RecParams p;
-    std::memset(&p, 0, sizeof p);
-    p.op = pl->op; p.G = (int)G; p.D = (int)D; p.N = (int)N; p.H = (int)H; p.S = (int)S;
-    p.layout = pl->layout; p.lbr = pl->lbr; p.input_forget = pl->input_forget;
-    p.has_B = B != nullptr; p.has_P = P != nullptr; p.has_h0 = h0 != nullptr; p.has_c0 = c0 != nullptr;
-    p.has_lens = lens != nullptr; p.has_clip = pl->has_clip; p.clip = pl->clip;
-    for (int d = 0; d < 2; ++d)
-        for (int s = 0; s < 3; ++s) p.act[d][s] = pl->act[d][s];
-    p.max_len = (int)max_len;
-    p.dir_reverse[0] = pl->direction == RNN_DIR_REVERSE ? 1 : 0;
-    p.dir_reverse[1] = 1;
-    p.ctas_per_dir = geo.ctas; p.umax = geo.umax; p.rows_per_thread = geo.tn; p.r_resident = geo.rres;
-    p.npad = geo.npad;
-    p.XW = xw; p.Rt = rt; p.B = B; p.P = P; p.h0 = h0; p.c0 = c0; p.lens = lens;
-    p.Y = Y; p.Yh = Yh; p.Yc = Yc;
-    p.hbuf = (float*)(pl->scratch + o_hb);
-    p.rhbuf = need_rh ? (float*)(pl->scratch + o_rh) : nullptr;
-    p.bar = (unsigned*)pl->ctrl;
-    p.status = (int*)(pl->ctrl + 64);
-    p.spin_limit_ns = pl->spin_limit_ns;
-    p.debug_skip_cta = pl->skip_cta;
-
-    e = launch_state_init(p, st);
-    if (e != cudaSuccess) return cuda_fail(e, "state set-up launch");
-    launches += 1;
-    record(pl, 3, st);
-    e = launch_recurrent(p, exact, geo.threads, geo.smem, st);
-    if (e != cudaSuccess) return cuda_fail(e, "recurrent launch");
-    launches += 1;
-    record(pl, 4, st);
-    if (Y && max_len < S) {
-        e = launch_mask_tail(Y, pl->layout, S, D, N, H, max_len, st);
-        if (e != cudaSuccess) return cuda_fail(e, "mask launch");
-        launches += 1;
-    }
-    record(pl, 5, st);
+    rs = enqueue(pl, a, geo, max_len, pl->scratch, L, pl->ctrl, pl->timing, pl->spin_limit_ns, pl->skip_cta,
+                 &launches);
+    if (rs != RNN_OK) return rs;
     if (pl->timing) pl->slot_pending[pl->slot] = true;
-    cudaEventRecord(pl->done, st);
+    cudaEventRecord(pl->done, a.st);
     pl->ran = true;
-    pl->g_ctas = geo.ctas; pl->g_tn = geo.tn; pl->g_rres = geo.rres; pl->g_threads = geo.threads;
-    pl->g_smem = (int)geo.smem;
     pl->last_launches = launches;
     return RNN_OK;
 }
@@ -710,119 +991,45 @@ rnn_status rnn_run_static_scratch(rnn_plan_t pl, int64_t S, int64_t N, const flo
     g_error.clear();
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
     pl->last_launches = 0;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (S < 0 || N < 0) return fail(RNN_ERR_INVALID_ARGUMENT, "seq_length and batch_size must be >= 0");
-    if (S > (1 << 30) || N > kMaxBatch)
+    if (N > kMaxBatch)
         return fail(RNN_ERR_UNSUPPORTED, "static-scratch runs take at most %lld batch rows", (long long)kMaxBatch);
-    const int64_t H = pl->H, I = pl->I, G = pl->G, D = pl->D, GH = G * H;
-    if (pl->op != RNN_OP_LSTM) { c0 = nullptr; P = nullptr; Yc = nullptr; }
-    const double per_dir = (double)S * N * GH + 4.0 * N * H + (pl->const_weights ? 0.0 : (double)GH * (I + H));
-    if (per_dir >= 1073741824.0)
-        return fail(RNN_ERR_UNSUPPORTED, "per-direction scratch of %.0f floats reaches the 2^30 limit", per_dir);
-    if (S == 0 || N == 0) {
-        const size_t sb = sizeof(float) * (size_t)D * N * H;
-        cudaError_t e = cudaSuccess;
-        if (Yh && sb) e = h0 ? cudaMemcpyAsync(Yh, h0, sb, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(Yh, 0, sb, st);
-        if (e == cudaSuccess && Yc && sb)
-            e = c0 ? cudaMemcpyAsync(Yc, c0, sb, cudaMemcpyDeviceToDevice, st) : cudaMemsetAsync(Yc, 0, sb, st);
-        if (e != cudaSuccess) return cuda_fail(e, "zero-size copy");
-        return RNN_OK;
-    }
-    if (!X && I > 0) return fail(RNN_ERR_INVALID_ARGUMENT, "X is NULL");
-    if (!pl->const_weights && (!R || (!W && I > 0))) return fail(RNN_ERR_INVALID_ARGUMENT, "W and R are required");
+    RunArgs a{S, N, X, W, R, B, lens, h0, c0, P, Y, Yh, Yc, (cudaStream_t)stream};
+    bool done = false;
+    rnn_status rs = check_run(pl, a, &done);
+    if (rs != RNN_OK || done) return rs;
 
     DeviceInfo di;
-    rnn_status rs = device_info(&di);
+    rs = device_info(&di);
     if (rs != RNN_OK) return rs;
     if (!di.coop) return fail(RNN_ERR_UNSUPPORTED, "device lacks cooperative launch");
 
     int64_t max_len = S;
     if (lens) {
         int32_t host_lens[kMaxBatch];
-        cudaError_t e = cudaMemcpyAsync(host_lens, lens, sizeof(int32_t) * (size_t)N, cudaMemcpyDeviceToHost, st);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        cudaError_t e = cudaMemcpyAsync(host_lens, lens, sizeof(int32_t) * (size_t)N, cudaMemcpyDeviceToHost, a.st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(a.st);
         if (e != cudaSuccess) return cuda_fail(e, "copying sequence_lens");
-        max_len = 0;
-        for (int64_t n = 0; n < N; ++n) {
-            const int32_t L = host_lens[n];
-            if (L < 0 || (int64_t)L > S)
-                return fail(RNN_ERR_INVALID_INPUT, "sequence_lens[%lld] = %d is outside [0, %lld]", (long long)n, L,
-                            (long long)S);
-            max_len = std::max<int64_t>(max_len, L);
-        }
+        rs = check_lengths(host_lens, N, S, &max_len);
+        if (rs != RNN_OK) return rs;
     }
 
     Geometry geo{};
-    rs = plan_geometry(pl, N, di, &geo);
+    rs = plan_geometry(pl, N, di, R, &geo);
     if (rs != RNN_OK) return rs;
 
     void* base = nullptr;
     size_t cap = 0;
     cudaError_t e = static_scratch(&base, &cap);
     if (e != cudaSuccess) return cuda_fail(e, "looking up the static scratch");
-    const int64_t M = S * N;
-    size_t off = 256;   // control words: barrier counters, status
-    const size_t o_wt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)I * D * GH);
-    const size_t o_rt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)D * H * GH);
-    const size_t o_xw = off; off += align256(sizeof(float) * (size_t)M * D * GH);
-    const size_t o_hb = off; off += align256(sizeof(float) * (size_t)D * 2 * H * geo.npad);
-    const bool need_rh = pl->op == RNN_OP_GRU && pl->lbr == 0;
-    const size_t o_rh = off; off += need_rh ? align256(sizeof(float) * (size_t)D * H * geo.npad) : 0;
-    if (off > cap)
-        return fail(RNN_ERR_UNSUPPORTED, "run needs %zu bytes of scratch; the static scratch holds %zu", off, cap);
+    const Layout L = scratch_layout(pl, geo, S, N, kCtrlBytes);   // control words first
+    if (L.total > cap)
+        return fail(RNN_ERR_UNSUPPORTED, "run needs %zu bytes of scratch; the static scratch holds %zu", L.total, cap);
     char* sb = (char*)base;
-
-    e = cudaMemsetAsync(sb + 64, 0, sizeof(int), st);   // status word starts at 0 on every call
+    e = cudaMemsetAsync(sb + kCtrlStatusOffset, 0, sizeof(int), a.st);   // status starts at 0 on every call
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
-    float* wt = pl->const_weights ? pl->wt_const : (float*)(sb + o_wt);
-    float* rt = pl->const_weights ? pl->rt_const : (float*)(sb + o_rt);
-    float* xw = (float*)(sb + o_xw);
-    const bool exact = pl->mode == RNN_MODE_EXACT;
     int launches = 0;
-    if (!pl->const_weights) {
-        e = launch_pack(W, R, wt, rt, (int)D, (int)G, H, I, st);
-        if (e != cudaSuccess) return cuda_fail(e, "pack launch");
-        launches += (int)D * (I > 0 ? 2 : 1);
-    }
-    e = launch_projection(X, wt, xw, M, I, D * GH, exact, st);
-    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
-    launches += 1;
-
-    RecParams p;
-    std::memset(&p, 0, sizeof p);
-    p.op = pl->op; p.G = (int)G; p.D = (int)D; p.N = (int)N; p.H = (int)H; p.S = (int)S;
-    p.layout = pl->layout; p.lbr = pl->lbr; p.input_forget = pl->input_forget;
-    p.has_B = B != nullptr; p.has_P = P != nullptr; p.has_h0 = h0 != nullptr; p.has_c0 = c0 != nullptr;
-    p.has_lens = lens != nullptr; p.has_clip = pl->has_clip; p.clip = pl->clip;
-    for (int d = 0; d < 2; ++d)
-        for (int s = 0; s < 3; ++s) p.act[d][s] = pl->act[d][s];
-    p.max_len = (int)max_len;
-    p.dir_reverse[0] = pl->direction == RNN_DIR_REVERSE ? 1 : 0;
-    p.dir_reverse[1] = 1;
-    p.ctas_per_dir = geo.ctas; p.umax = geo.umax; p.rows_per_thread = geo.tn; p.r_resident = geo.rres;
-    p.npad = geo.npad;
-    p.XW = xw; p.Rt = rt; p.B = B; p.P = P; p.h0 = h0; p.c0 = c0; p.lens = lens;
-    p.Y = Y; p.Yh = Yh; p.Yc = Yc;
-    p.hbuf = (float*)(sb + o_hb);
-    p.rhbuf = need_rh ? (float*)(sb + o_rh) : nullptr;
-    p.bar = (unsigned*)sb;           // zeroed by the state set-up kernel
-    p.status = (int*)(sb + 64);
-    p.spin_limit_ns = kDefaultSpinNs;
-    p.debug_skip_cta = -1;
-
-    e = launch_state_init(p, st);
-    if (e != cudaSuccess) return cuda_fail(e, "state set-up launch");
-    launches += 1;
-    e = launch_recurrent(p, exact, geo.threads, geo.smem, st);
-    if (e != cudaSuccess) return cuda_fail(e, "recurrent launch");
-    launches += 1;
-    if (Y && max_len < S) {
-        e = launch_mask_tail(Y, pl->layout, S, D, N, H, max_len, st);
-        if (e != cudaSuccess) return cuda_fail(e, "mask launch");
-        launches += 1;
-    }
-    pl->g_ctas = geo.ctas; pl->g_tn = geo.tn; pl->g_rres = geo.rres; pl->g_threads = geo.threads;
-    pl->g_smem = (int)geo.smem;
+    rs = enqueue(pl, a, geo, max_len, sb, L, sb, false, kDefaultSpinNs, -1, &launches);
+    if (rs != RNN_OK) return rs;
     pl->last_launches = launches;
     return RNN_OK;
 }

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace rnngb {
@@ -15,6 +16,10 @@ struct ActSpec {
 // Arguments of the persistent recurrent kernel (one launch covers all
 // directions; CTAs [d*ctas_per_dir, (d+1)*ctas_per_dir) serve direction d).
 struct RecParams {
+    // dataflow kernel: TMA descriptors of the h and r (.) h exchange buffers
+    // ([blocks][hpad/32 chunks][rows][36], box 36 x rows x cpb x 1) and of R
+    // as given ([D][G][H units][H], box 36 x units x G x 1), no swizzle
+    CUtensorMap hmap, rhmap, rmap;
     int op, G, D, N, H, S, layout;
     int lbr, input_forget;
     int has_B, has_P, has_h0, has_c0, has_lens, has_clip;
@@ -24,15 +29,24 @@ struct RecParams {
     int dir_reverse[2];          // per direction: 1 if it walks time backwards
 
     // geometry
-    int ctas_per_dir;            // C
-    int umax;                    // ceil(H / C): unit slots per CTA
+    int kernel;                  // 1: staged kernel, 2: dataflow kernel
+    int ctas_per_dir;            // CTAs per direction (unit_groups * row_groups)
+    int unit_groups;             // CU
+    int row_groups;              // CR (1 for the staged kernel)
+    int unit_quant;              // unit groups hold multiples of this many units
+    int slots;                   // dataflow kernel: ring slots (one piece each)
+    int chunks_per_piece;        // dataflow kernel: 32-k chunks per tensor copy
+    int umax;                    // most units in one group
     int rows_per_thread;         // TN (template parameter mirrored here)
     int r_resident;              // 1: R slice lives in shared memory
-    int npad;                    // N rounded up to a multiple of 4
+    int npad;                    // rows per row group, padded (staged kernel: N padded to 8)
+    int hpad;                    // dataflow kernel: H rounded up to 32 (chunks x 32)
+    int unit_stride;             // dataflow kernel: floats per unit of the resident R slice
 
     // tensors
     const float* XW;             // [S*N rows][D*G*H], columns u*G + g per direction
-    const float* Rt;             // [D][H (k)][G*H], columns u*G + g
+    const float* Rt;             // staged kernel: [D][H (k)][G*H], columns u*G + g
+    const float* Rorig;          // dataflow kernel: R as given, [D][G*H][H]
     const float* B;              // [D][2*G*H] (may be null)
     const float* P;              // [D][3*H]   (may be null)
     const float* h0;             // layout-dependent [D,N,H] / [N,D,H] (may be null)
@@ -41,17 +55,19 @@ struct RecParams {
     float* Y;                    // may be null
     float* Yh;
     float* Yc;
-    float* hbuf;                 // [D][2][H][npad]: h exchanged between steps
-    float* rhbuf;                // [D][H][npad]: r (.) h for GRU lbr = 0
+    float* hbuf;                 // staged: [D][2][H][npad]; dataflow: [D][2][row_groups][hpad/32][npad][36]
+    float* rhbuf;                // r (.) h for GRU lbr = 0, same layout as hbuf
     unsigned* bar;               // [D] barrier arrival counters (zeroed per run)
+    unsigned* flags;             // [D][row_groups][unit_groups] publication counts (zeroed per run)
     int* status;                 // device status word (0 ok, 6 timeout)
     long long spin_limit_ns;
     int debug_skip_cta;
 };
 
-// Shared-memory layout of the recurrent kernel, computed on the host.
-constexpr int kRecKC = 32;       // k rows per staged chunk
-constexpr int kRecStages = 4;    // chunks in the cp.async ring
+// Shared-memory layout of the recurrent kernels, computed on the host.
+constexpr int kRecKC = 32;       // k rows per chunk
+constexpr int kRecStages = 4;    // chunks in the cp.async ring (staged kernel)
+constexpr int kMaxSlots = 32;    // ring slots of the dataflow kernel
 
 __host__ __device__ inline int rec_ugp(int umax, int G) { return ((umax * G) + 3) / 4 * 4; }
 
@@ -63,10 +79,46 @@ inline size_t rec_smem_bytes(int H, int umax, int G, int npad, int r_resident)
     return rbytes + hbytes;
 }
 
-// Launchers (one per op; `exact` selects FMUL+FADD vs FFMA products).
+// Dataflow kernel: floats per unit of the resident R slice (G rows of H,
+// padded so that consecutive units start 16 bytes apart modulo the 128-byte
+// bank window: conflict-free 16-byte loads across units).
+inline int df_unit_stride(int H, int G)
+{
+    const int gh = G * H;
+    return gh + (((4 - gh) % 32) + 32) % 32;
+}
+
+// Dataflow kernel: a 32-k chunk of one operand row is stored with a pitch of
+// 36 floats (144 bytes), so that the rows read by the 8 (or 4) threads of a
+// quarter warp fall in distinct bank groups.  The exchange buffers are kept
+// in that form; tensor copies of R take 36 k (the 4 extra are never used).
+constexpr int kDfPitch = 36;
+
+// Bytes of one chunk of streamed R: G x umax rows of 144 bytes, 128-aligned.
+__host__ __device__ inline size_t df_rsub_bytes(int umax, int G) { return (((size_t)G * umax * kDfPitch * 4 + 127) / 128) * 128; }
+
+// Dataflow kernel: dynamic shared memory (128-byte alignment slack + R
+// resident or ring of R pieces + ring of h pieces; a slot holds one piece of
+// cpb chunks).
+inline size_t df_smem_bytes(int H, int umax, int G, int npad, int r_resident, int cpb, int slots)
+{
+    const size_t rres = (((size_t)umax * df_unit_stride(H, G) * 4 + 127) / 128) * 128;
+    const size_t rslot = (size_t)cpb * df_rsub_bytes(umax, G);
+    const size_t rbytes = r_resident ? rres : (size_t)slots * rslot;
+    return 128 + rbytes + (size_t)slots * npad * cpb * kDfPitch * 4;
+}
+
+// The control block: barrier counters, status word, publication flags.
+constexpr size_t kCtrlBytes = 4096;
+constexpr size_t kCtrlStatusOffset = 64;
+constexpr size_t kCtrlFlagsOffset = 256;
+constexpr int kMaxFlags = (int)((kCtrlBytes - kCtrlFlagsOffset) / 4);
+
+// Launchers (one per op; `exact` selects FMUL+FADD vs FFMA products;
+// p.kernel selects the staged or the dataflow kernel).
 cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t smem,
                              cudaStream_t stream);
-cudaError_t recurrent_occupancy(int op, int rows_per_thread, bool exact, int threads,
+cudaError_t recurrent_occupancy(int op, int lbr, int kernel, int rows_per_thread, bool exact, int threads,
                                 size_t smem, int* blocks_per_sm);
 
 // Input projection XW[M][ldc] = X[M][K] . Bt[K][ncols] (Bt row stride ldb).
@@ -78,7 +130,7 @@ cudaError_t launch_projection(const float* X, const float* Bt, float* XW, int64_
 cudaError_t launch_pack(const float* W, const float* R, float* Wt, float* Rt, int D, int G,
                         int64_t H, int64_t I, cudaStream_t stream);
 
-// hbuf[d][0][u][n] = initial_h (or 0), padding columns 0; bar[d] = 0.
+// Exchange buffer 0 = initial_h (or 0), everything else 0; bar, flags = 0.
 cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream);
 
 // Y = +0 at t >= t0 for every row (rows that ended earlier are written by

@@ -58,8 +58,8 @@ def load(path: str | None = None):
     lib.rnn_plan_set_weights.argtypes = [vp, vp, vp, vp]
     lib.rnn_plan_sync.argtypes = [vp]
     lib.rnn_plan_get_activation.argtypes = [vp, i32, i32, ip, fp, fp]
-    lib.rnn_plan_set_launch.argtypes = [vp, i32, i32, i32]
-    lib.rnn_plan_get_launch.argtypes = [vp, ip, ip, ip, ip, ip]
+    lib.rnn_plan_set_launch.argtypes = [vp, i32, i32, i32, i32, i32]
+    lib.rnn_plan_get_launch.argtypes = [vp, ip, ip, ip, ip, ip, ip, ip]
     lib.rnn_plan_set_timing.argtypes = [vp, i32]
     lib.rnn_plan_last_timing.argtypes = [vp, fp, i32]
     lib.rnn_plan_timing_totals.argtypes = [vp, fp, i32, ip]
@@ -186,16 +186,17 @@ def rnn_plan_get_activation(plan: Plan, d: int, slot: int):
     return (ACT_NAMES[fn.value] if fn.value >= 0 else None), a.value, b.value
 
 
-def rnn_plan_set_launch(plan: Plan, ctas_per_dir=0, rows_per_thread=0, r_resident=-1):
-    _check(load().rnn_plan_set_launch(plan.handle, int(ctas_per_dir), int(rows_per_thread),
-                                      int(r_resident)))
+def rnn_plan_set_launch(plan: Plan, unit_groups=0, rows_per_thread=0, r_resident=-1,
+                        row_groups=0, kernel=0):
+    _check(load().rnn_plan_set_launch(plan.handle, int(unit_groups), int(rows_per_thread),
+                                      int(r_resident), int(row_groups), int(kernel)))
 
 
 def rnn_plan_get_launch(plan: Plan) -> dict:
-    v = [ctypes.c_int() for _ in range(5)]
+    v = [ctypes.c_int() for _ in range(7)]
     _check(load().rnn_plan_get_launch(plan.handle, *[ctypes.byref(x) for x in v]))
-    return dict(zip(["ctas_per_dir", "rows_per_thread", "r_resident", "threads", "smem_bytes"],
-                    [x.value for x in v]))
+    return dict(zip(["unit_groups", "rows_per_thread", "r_resident", "row_groups", "kernel",
+                     "threads", "smem_bytes"], [x.value for x in v]))
 
 
 def rnn_plan_set_timing(plan: Plan, enable=True):

@@ -83,26 +83,51 @@ def test_random_small_fast_any_activation_normwise(seed):
         assert float(np.abs(g64[fin] - r64[fin]).max(initial=0.0)) <= 1e-4 * scale, name
 
 
-GEOMETRIES = [(1, 2, 1), (2, 1, 1), (3, 2, 0), (5, 4, 1), (7, 8, 0), (13, 1, 0), (70, 2, 1),
-              (4, 8, 1), (9, 4, 0)]
+# (unit_groups, rows_per_thread, r_resident, row_groups, kernel); kernel 1 is
+# the staged kernel, 2 the dataflow kernel; zeros and -1 let the planner choose.
+GEOMETRIES = [
+    (1, 2, 1, 0, 1), (2, 1, 1, 0, 1), (3, 2, 0, 0, 1), (5, 4, 1, 0, 1), (7, 8, 0, 0, 1),
+    (13, 1, 0, 0, 1), (72, 2, 1, 0, 1), (4, 8, 1, 0, 1),
+    (0, 0, -1, 0, 2), (8, 1, 1, 1, 2), (9, 2, 1, 2, 2), (5, 1, 0, 2, 2), (18, 4, 1, 1, 2),
+    (3, 1, 0, 2, 2), (36, 1, 1, 2, 2), (1, 4, 0, 1, 2), (3, 2, 0, 1, 2),
+]
 
 
 @pytest.mark.parametrize("op,direction,lbr", [("RNN", "bidirectional", 0), ("GRU", "forward", 0),
                                               ("GRU", "bidirectional", 1), ("LSTM", "reverse", 0),
-                                              ("LSTM", "bidirectional", 0)])
+                                              ("LSTM", "bidirectional", 0), ("GRU", "bidirectional", 0)])
 def test_every_launch_geometry_gives_the_same_bits(op, direction, lbr):
-    c = make_case(op, direction, 9, 11, 33, 70, seed=21, layout=1, with_P=True, h0_scale=0.5,
+    c = make_case(op, direction, 9, 11, 33, 72, seed=21, layout=1, with_P=True, h0_scale=0.5,
                   c0_scale=0.5, lens=("uniform", 0, 9), linear_before_reset=lbr, clip=2.0,
                   activations=None)
     ref = oracle_case(c)
     for g in GEOMETRIES:
+        try:
+            out = gpu_case(c, "exact", launch=g)
+        except orc.RNNError as e:
+            pytest.fail(f"geometry {g}: {e}")
+        _compare_exact(c, out, ref, f"geometry {g}")
+
+
+@pytest.mark.parametrize("op", ["RNN", "GRU", "LSTM"])
+def test_hidden_not_multiple_of_four(op):
+    # The dataflow kernel moves whole 16-byte groups of k, so it needs hidden
+    # a multiple of 4: the planner falls back to the staged kernel, and
+    # forcing the dataflow kernel is refused cleanly.
+    c = make_case(op, "bidirectional", 6, 7, 9, 37, seed=8, with_P=True, h0_scale=0.5,
+                  lens=("uniform", 1, 6))
+    ref = oracle_case(c)
+    for g in [(0, 0, -1, 0, 0), (5, 0, 0, 0, 0), (3, 2, 1, 0, 1)]:
         _compare_exact(c, gpu_case(c, "exact", launch=g), ref, f"geometry {g}")
+    with pytest.raises(orc.RNNError) as e:
+        gpu_case(c, "exact", launch=(0, 0, 1, 0, 2))
+    assert e.value.status == 3
 
 
-@pytest.mark.parametrize("g", [(2, 1, 0), (5, 2, 1)])
+@pytest.mark.parametrize("g", [(2, 1, 0, 0, 1), (5, 2, 1, 0, 1), (4, 1, 1, 2, 2), (3, 2, 0, 1, 2)])
 def test_fast_mode_is_geometry_independent(g):
-    c = make_case("LSTM", "bidirectional", 6, 9, 20, 37, seed=5, with_P=True, h0_scale=0.5)
-    a = gpu_case(c, "fast", launch=(1, 1, 1))
+    c = make_case("LSTM", "bidirectional", 6, 9, 20, 36, seed=5, with_P=True, h0_scale=0.5)
+    a = gpu_case(c, "fast", launch=(1, 1, 1, 0, 1))
     b = gpu_case(c, "fast", launch=g)
     for x, y in zip(a, b):
         assert_bits_equal(x, y, "fast mode across geometries")
@@ -153,12 +178,15 @@ def test_invalid_lengths_write_nothing():
     orc.rnn_plan_destroy(plan)
 
 
-def test_barrier_timeout_is_reported_and_the_device_stays_usable():
-    # One CTA withholds its arrival at the first step barrier; every wait is
-    # bounded (50 ms here), so the grid exits and the status says TIMEOUT.
-    c = make_case("LSTM", "forward", 5, 4, 8, 64, seed=9, h0_scale=0.5)
-    plan = orc.rnn_plan_create("LSTM", "forward", 64, 8)
-    orc.rnn_plan_set_launch(plan, 4, 1, 1)
+@pytest.mark.parametrize("kernel,lbr", [(1, 0), (2, 0), (2, 1)])
+def test_barrier_timeout_is_reported_and_the_device_stays_usable(kernel, lbr):
+    # One CTA withholds its first arrival (staged kernel) or its first flag
+    # (dataflow kernel); every wait is bounded (50 ms here), so the grid exits
+    # and the status says TIMEOUT.
+    op = "LSTM" if lbr == 0 else "GRU"
+    c = make_case(op, "forward", 5, 4, 8, 64, seed=9, h0_scale=0.5, linear_before_reset=lbr)
+    plan = orc.rnn_plan_create(op, "forward", 64, 8, linear_before_reset=lbr)
+    orc.rnn_plan_set_launch(plan, 4, 1, 1, 0, kernel)
     orc.rnn_plan_debug_barrier(plan, 50_000_000, 1)
     import torch
     t = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in c.tensors().items()}
