@@ -27,14 +27,15 @@ __device__ __forceinline__ float fdiv(float a, float b) { return __fdiv_rn(a, b)
 
 __device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
 
+// The special cases are selected after the fact rather than branched to, so
+// that independent calls can be interleaved; inside [-110, 89] the clamp is
+// the identity and the result is the polynomial path's.
 __device__ __forceinline__ float dx_exp(float x)
 {
-    if (x != x) return x;
-    if (x > 89.0f) return __int_as_float(0x7f800000);
-    if (x < -110.0f) return 0.0f;
-    const float t = fmul(x, 0x1.715476p+0f);                           // x / ln 2
+    const float xc = fminf(fmaxf(x, -110.0f), 89.0f);
+    const float t = fmul(xc, 0x1.715476p+0f);                          // x / ln 2
     const float kf = fsub(fadd(t, 0x1.8p+23f), 0x1.8p+23f);            // round to integer
-    const float r = fsub(fsub(x, fmul(kf, 0x1.62e4p-1f)), fmul(kf, 0x1.7f7d1cp-20f));
+    const float r = fsub(fsub(xc, fmul(kf, 0x1.62e4p-1f)), fmul(kf, 0x1.7f7d1cp-20f));
     float p = 0x1.a01a02p-13f;                                         // 1/5040
     p = fadd(fmul(p, r), 0x1.6c16c2p-10f);                             // 1/720
     p = fadd(fmul(p, r), 0x1.111112p-7f);                              // 1/120
@@ -46,7 +47,10 @@ __device__ __forceinline__ float dx_exp(float x)
     const int k = (int)kf;
     const int k1 = k / 2;
     const int k2 = k - k1;
-    return fmul(fmul(p, pow2i(k1)), pow2i(k2));
+    float v = fmul(fmul(p, pow2i(k1)), pow2i(k2));
+    v = x > 89.0f ? __int_as_float(0x7f800000) : v;
+    v = x < -110.0f ? 0.0f : v;
+    return x != x ? x : v;
 }
 
 __device__ __forceinline__ float dx_log(float x)
@@ -81,28 +85,24 @@ __device__ __forceinline__ float dx_log(float x)
     return fadd(fmul(ef, 0x1.62e4p-1f), fadd(lm, fmul(ef, 0x1.7f7d1cp-20f)));
 }
 
+// Both series are evaluated and the one for |x|'s range selected (no
+// divergent branches); each range's value is the same expression as above.
 __device__ __forceinline__ float dx_tanh(float x)
 {
-    if (x != x) return x;
     const unsigned sign = __float_as_uint(x) & 0x80000000u;
     const float a = __uint_as_float(__float_as_uint(x) & 0x7fffffffu);
-    float y;
-    if (a > 9.1f) {
-        y = 1.0f;
-    } else if (a < 0.4f) {
-        const float z = fmul(a, a);
-        float q = 0x1.d6d3d0p-9f;                                      // 21844/6081075
-        q = fadd(fmul(q, z), -0x1.226e36p-7f);                         // -1382/155925
-        q = fadd(fmul(q, z), 0x1.664f48p-6f);                          // 62/2835
-        q = fadd(fmul(q, z), -0x1.ba1ba2p-5f);                         // -17/315
-        q = fadd(fmul(q, z), 0x1.111112p-3f);                          // 2/15
-        q = fadd(fmul(q, z), -0x1.555556p-2f);                         // -1/3
-        y = fadd(a, fmul(a, fmul(q, z)));
-    } else {
-        const float e = dx_exp(fadd(a, a));
-        y = fsub(1.0f, fdiv(2.0f, fadd(e, 1.0f)));
-    }
-    return __uint_as_float(__float_as_uint(y) | sign);
+    const float z = fmul(a, a);
+    float q = 0x1.d6d3d0p-9f;                                          // 21844/6081075
+    q = fadd(fmul(q, z), -0x1.226e36p-7f);                             // -1382/155925
+    q = fadd(fmul(q, z), 0x1.664f48p-6f);                              // 62/2835
+    q = fadd(fmul(q, z), -0x1.ba1ba2p-5f);                             // -17/315
+    q = fadd(fmul(q, z), 0x1.111112p-3f);                              // 2/15
+    q = fadd(fmul(q, z), -0x1.555556p-2f);                             // -1/3
+    const float ys = fadd(a, fmul(a, fmul(q, z)));                     // |x| < 0.4
+    const float e = dx_exp(fadd(a, a));
+    const float yl = fsub(1.0f, fdiv(2.0f, fadd(e, 1.0f)));            // 0.4 <= |x| <= 9.1
+    const float y = a > 9.1f ? 1.0f : (a < 0.4f ? ys : yl);
+    return x != x ? x : __uint_as_float(__float_as_uint(y) | sign);
 }
 
 __device__ __forceinline__ float dx_sigmoid(float x) { return fdiv(1.0f, fadd(1.0f, dx_exp(-x))); }

@@ -79,7 +79,7 @@ __global__ void state_init_kernel(const RecParams p)
     }
     if (blockIdx.x == 0) {
         if (threadIdx.x < p.D) p.bar[threadIdx.x] = 0u;
-        const int nflags = p.D * p.row_groups * p.unit_groups;
+        const int nflags = p.D * p.row_groups;
         for (int j = threadIdx.x; j < nflags && p.flags; j += blockDim.x) p.flags[j] = 0u;
     }
 }

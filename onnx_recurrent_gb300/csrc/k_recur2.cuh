@@ -1,5 +1,6 @@
-// Persistent recurrent kernel, dataflow version: TMA bulk copies, a loader
-// warp and per-CTA publication flags instead of a device-wide barrier.
+// Persistent recurrent kernel, dataflow version: TMA tensor copies, a loader
+// warp and per-row-group publication counters instead of a device-wide
+// barrier.
 //
 // Same arithmetic as the staged kernel in k_recur.cuh (page "Recurrent
 // operators: RNN, GRU, LSTM", Computation: one accumulator per output, k
@@ -12,19 +13,23 @@
 //     h: hbuf is laid out [D][2][CR][H][NRP], one contiguous k-major block per
 //     row group.
 //   * Warp 0 is the loader.  Once per product it waits until every CTA of
-//     its row group has published the step (its lanes poll the flags in
-//     parallel with acquire loads), then issues one cp.async.bulk
-//     global->shared copy per k-chunk (plus, when R does not fit in shared
-//     memory, one bulk copy per k row of the CTA's R columns), each
-//     completing on the chunk's "full" mbarrier.  Lane j issues chunk j of a
-//     group in one converged instruction: bulk copies issued one after
-//     another by a single thread go out about one round trip apart.  A ring
-//     of slots with "empty" mbarriers lets the loader run ahead; when the
-//     whole block fits, every chunk of a product is in flight at once.
+//     its row group has published the step (one acquire-polled counter per
+//     row group that each CTA increments with a release add), then moves the
+//     row group's block of h in a few pieces of several 32-k chunks, one
+//     tensor copy (TMA) per piece (plus, when R does not fit in shared
+//     memory, one tensor copy of the CTA's R columns per chunk), each piece
+//     completing on its slot's "full" mbarrier.  Lane j issues piece j, so
+//     the copies of a product go out together.  A ring of slots with "empty"
+//     mbarriers lets the loader run ahead.  In global memory and in shared
+//     memory a 32-k chunk of a row has a pitch of 36 floats, which keeps the
+//     compute warps' 16-byte loads free of bank conflicts.
 //   * The other warps compute.  After the gate epilogue they write their h
-//     into the next buffer, meet at a named barrier, and one thread releases
-//     the CTA's flag (flags count publications: one per step, two for GRU with
+//     into the next buffer, meet at a named barrier, and one thread adds 1 to
+//     the row group's counter (one publication per step, two for GRU with
 //     linear_before_reset = 0, whose r (.) h block is published in between).
+//     A CTA can publish again only after reading every publication of the
+//     others, so the counter reaches target * (unit groups) exactly when
+//     every CTA of the row group has published `target` times.
 //   Two h buffers suffice: a CTA can only overwrite buffer b after every
 //   producer of its row group has published the step that reads b.
 //
@@ -36,6 +41,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 #include "k_recur.cuh"
 
@@ -95,11 +101,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
 
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ void named_barrier(int id, int threads)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -146,36 +147,32 @@ struct DfCtx {
     int rslot, rsub, hslot; // bytes per slot (one piece: cpb chunks of 32 k), per R chunk
     uint64_t* full;
     uint64_t* empty;
+    uint64_t* pub;    // completes a phase at each of this CTA's publications
 };
 
-// Loader: the chunk sequence of one product (one accumulate pass of the
-// compute warps).  `map` describes the h (or r (.) h) exchange buffer, `z` the
-// row group's block in it; every producer of the row group must have
-// published `target` times before the block may be read.  The lanes poll the
-// producers' flags in parallel (acquire loads); a warp barrier orders those
-// acquires before the copies, and a proxy fence orders the generic-proxy
-// writes they made visible before the tensor copies (async proxy) that read
-// them.  Chunks are issued by the lanes in parallel, lane j taking chunk
-// base + j, in groups no larger than the ring (so no two lanes of a group
-// share a slot).
+// Loader: the pieces of one product (one accumulate pass of the compute
+// warps).  `map` describes the h (or r (.) h) exchange buffer, `z` the row
+// group's block in it; every producer of the row group must have published
+// `target` times before the block may be read.  Every lane polls the row
+// group's counter (acquire loads); a proxy fence then orders the
+// generic-proxy writes that the acquire made visible before the tensor
+// copies (async proxy) that read them.
 __device__ __forceinline__ bool load_product(const RecParams& p, const DfCtx& x, const CUtensorMap* map, int z,
-                                             unsigned target, const unsigned* flags, unsigned& q,
+                                             unsigned target, const unsigned* counter, unsigned& q,
                                              volatile int* abort_flag, int lane)
 {
     if (target > 0) {
-        bool ready = true;
-        for (int j = lane; j < x.CU; j += 32) ready = ready && ld_acquire_u32(flags + j) >= target;
+        // This CTA's own publication comes first (the counter cannot be
+        // complete before it); waiting for it on the mbarrier keeps the
+        // loader off the memory pipe while the compute warps work.
+        if (!mbar_wait(x.pub, (target - 1u) & 1u, p.status, abort_flag, p.spin_limit_ns)) return false;
+        const unsigned need = target * (unsigned)x.CU;
+        bool ready = ld_acquire_u32(counter) >= need;
         if (!__all_sync(0xffffffffu, ready)) {
             const unsigned long long t0 = globaltimer_ns();
             unsigned it = 0;
             while (!__all_sync(0xffffffffu, ready)) {
-                // back off between polls: a tight acquire-load loop competes
-                // with the compute warps for the SM's load/store pipe
-                __nanosleep(64);
-                if (!ready) {
-                    ready = true;
-                    for (int j = lane; j < x.CU; j += 32) ready = ready && ld_acquire_u32(flags + j) >= target;
-                }
+                if (!ready) ready = ld_acquire_u32(counter) >= need;
                 if ((++it & 15u) == 0u) {
                     int bad = 0;
                     if (lane == 0) {
@@ -325,18 +322,49 @@ __device__ __forceinline__ bool consume_product(const RecParams& p, const DfCtx&
     return ok;
 }
 
-// Compute warps meet; one thread publishes the CTA's flag.  Returns false
-// (uniformly across the compute warps) when the CTA is aborting.
-__device__ __forceinline__ bool publish(const DfCtx& x, unsigned* my_flag, unsigned value,
-                                        volatile int* abort_flag, bool skip)
+// Gate activations: the ones the operator names (FX = false), or the default
+// set with its functions called directly (FX = true), which leaves the
+// compiler free to interleave the independent gates' chains.
+template <bool EXACT>
+__device__ __forceinline__ float sigmoid_fn(float v) { return EXACT ? dx_sigmoid(v) : df_sigmoid(v); }
+template <bool EXACT>
+__device__ __forceinline__ float tanh_fn(float v) { return EXACT ? dx_tanh(v) : df_tanh(v); }
+
+template <int OP, bool EXACT, bool FX>
+struct Acts {
+    ActSpec f, g, h;
+    __device__ __forceinline__ float F(float v) const
+    {
+        if constexpr (FX) return OP == 0 ? tanh_fn<EXACT>(v) : sigmoid_fn<EXACT>(v);
+        else return act<EXACT>(f, v);
+    }
+    __device__ __forceinline__ float Gf(float v) const
+    {
+        if constexpr (FX) return tanh_fn<EXACT>(v);
+        else return act<EXACT>(g, v);
+    }
+    __device__ __forceinline__ float Hf(float v) const
+    {
+        if constexpr (FX) return tanh_fn<EXACT>(v);
+        else return act<EXACT>(h, v);
+    }
+};
+
+// Compute warps meet; one thread publishes (adds 1 to the row group's
+// counter).  Returns false (uniformly across the compute warps) when the CTA
+// is aborting.
+__device__ __forceinline__ bool publish(const DfCtx& x, unsigned* counter, volatile int* abort_flag, bool skip)
 {
     named_barrier(1, x.ncompute);
     const bool abort_now = *abort_flag != 0;
     named_barrier(1, x.ncompute);   // everyone has read the abort flag
     if (abort_now) return false;
-    if (x.ctid == 0 && !skip) {
-        fence_proxy_async_global();
-        st_release_u32(my_flag, value);   // the named barrier ordered every compute thread's writes first
+    if (x.ctid == 0) {
+        if (!skip) {
+            fence_proxy_async_global();
+            red_release_add_u32(counter, 1u);   // the named barrier ordered every compute thread's writes first
+        }
+        mbar_arrive(x.pub);
     }
     return true;
 }
@@ -358,6 +386,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     extern __shared__ __align__(128) unsigned char df_smem[];
     __shared__ __align__(8) uint64_t s_full[kMaxSlots];
     __shared__ __align__(8) uint64_t s_empty[kMaxSlots];
+    __shared__ __align__(8) uint64_t s_pub, s_rfill;
     __shared__ int s_abort;
 
     DfCtx x;
@@ -400,6 +429,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     x.Hring = reinterpret_cast<char*>(base + rbytes);
     x.full = s_full;
     x.empty = s_empty;
+    x.pub = &s_pub;
 
     const int lane = threadIdx.x & 31;
     const int d = x.d;
@@ -411,7 +441,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     const int zh0 = (d * 2 + 0) * x.CR + x.cr;                   // tensor-map block index, buffer 0
     auto hblock = [&](int buf) { return p.hbuf + ((size_t)(d * 2 + buf) * x.CR + x.cr) * blk; };
     auto rhblock = [&](int buf) { return p.rhbuf + ((size_t)(d * 2 + buf) * x.CR + x.cr) * blk; };
-    unsigned* flags = p.flags + (size_t)(d * x.CR + x.cr) * x.CU;
+    unsigned* counter = p.flags + (size_t)(d * x.CR + x.cr);
     constexpr bool two_phase = TWO;
 
     if (threadIdx.x == 0) {
@@ -419,21 +449,26 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], (unsigned)nwarps_compute);
         }
+        mbar_init(&s_pub, 1);
+        mbar_init(&s_rfill, 1);
         s_abort = 0;
         mbar_fence_init();
     }
-    if (p.r_resident) {
-        // R[d][g*H + u][k] -> Rs[(u - u0) * ugs + g*H + k]
+    __syncthreads();
+    if (p.r_resident && threadIdx.x < 32) {
+        // R[d][g*H + u][k] -> Rs[(u - u0) * ugs + g*H + k]: one bulk copy of
+        // a row of H floats per (unit, gate), all completing on s_rfill
+        // (H is a multiple of 4 and ugs*4 of 16, so every copy is 16-byte
+        // aligned at both ends)
         const float* src = p.Rorig + (size_t)d * G * p.H * p.H;
-        const int per_unit = G * p.H;
-        const int tot = x.U * per_unit;
-        for (int i = threadIdx.x; i < tot; i += blockDim.x) {
-            const int ul = i / per_unit, r = i - ul * per_unit;
-            const int g = r / p.H, k = r - g * p.H;
-            x.Rs[(size_t)ul * x.ugs + r] = src[((size_t)g * p.H + x.u0 + ul) * p.H + k];
+        if (lane == 0) mbar_arrive_expect_tx(&s_rfill, (unsigned)(x.U * G * p.H) * 4u);
+        __syncwarp();
+        for (int j = lane; j < x.U * G; j += 32) {
+            const int ul = j / G, g = j - ul * G;
+            bulk_g2s(x.Rs + (size_t)ul * x.ugs + (size_t)g * p.H, src + ((size_t)g * p.H + x.u0 + ul) * p.H,
+                     (unsigned)p.H * 4u, &s_rfill);
         }
     }
-    __syncthreads();
 
     // ------------------------------------------------------------ loader
     if (threadIdx.x < 32) {
@@ -442,13 +477,18 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         for (int s = 0; s < p.max_len && ok; ++s) {
             const int zh = zh0 + (s & 1) * x.CR;
             if (two_phase) {
-                ok = load_product(p, x, &p.hmap, zh, 2u * s, flags, q, &s_abort, lane);
-                if (ok) ok = load_product(p, x, &p.rhmap, zh, 2u * s + 1u, flags, q, &s_abort, lane);
+                ok = load_product(p, x, &p.hmap, zh, 2u * s, counter, q, &s_abort, lane);
+                if (ok) ok = load_product(p, x, &p.rhmap, zh, 2u * s + 1u, counter, q, &s_abort, lane);
             } else {
-                ok = load_product(p, x, &p.hmap, zh, (unsigned)s, flags, q, &s_abort, lane);
+                ok = load_product(p, x, &p.hmap, zh, (unsigned)s, counter, q, &s_abort, lane);
             }
         }
         // wait (bounded) for this CTA's copies still in flight before leaving
+        if (lane == 0 && p.r_resident) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (!mbar_test(&s_rfill, 0u) && (long long)(globaltimer_ns() - t0) <= p.spin_limit_ns) {
+            }
+        }
         if (lane == 0) {
             const unsigned issued = q;
             for (int sl = 0; sl < x.slots && (unsigned)sl < issued; ++sl) {
@@ -465,6 +505,10 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     // ------------------------------------------------------------ compute
     const int u = x.u0 + x.ul;
     const ActSpec fA = p.act[d][0], gA = p.act[d][1], hA = p.act[d][2];
+    // the operator's default activations (RNN Tanh; GRU Sigmoid, Tanh; LSTM
+    // Sigmoid, Tanh, Tanh)
+    const bool fixed_acts = OP == 0 ? fA.fn == 1
+                                    : (OP == 1 ? fA.fn == 2 && gA.fn == 1 : fA.fn == 2 && gA.fn == 1 && hA.fn == 1);
     float wb[G], rbv[G];
     float pI = 0.f, pO = 0.f, pF = 0.f;
     float hown[TN], cown[TN], xw[TN][G];
@@ -515,8 +559,10 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     };
 
     unsigned q = 0;
-    unsigned* my_flag = flags + x.cu;
     const bool skip_first = p.debug_skip_cta == (int)blockIdx.x;
+    // the resident R slice must have landed (a failure here sets the abort
+    // flag, and the warps leave together at the first publication)
+    if (p.r_resident) mbar_wait(&s_rfill, 0u, p.status, &s_abort, p.spin_limit_ns);
     load_xw(0);
     for (int s = 0; s < p.max_len; ++s) {
         float xc[TN][G];
@@ -535,49 +581,61 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 if (s + 1 < p.max_len) load_xw(s + 1);
                 float zg[TN];
                 float* rh = rhblock(s & 1);
+                auto epi_r = [&](auto fx) {
+                    constexpr bool FX = decltype(fx)::value;
+                    const Acts<OP, EXACT, FX> A{fA, gA, hA};
 #pragma unroll
-                for (int i = 0; i < TN; ++i) {
-                    const int rl = x.rb * TN + i;
-                    zg[i] = 0.f;
-                    if (!(x.active && rl < x.NR)) continue;
-                    float rhv = 0.f;
-                    if (s < len[i]) {
-                        float pz = fadd(xc[i][0], az[i][0]);
-                        float pr = fadd(xc[i][1], az[i][1]);
-                        if (p.has_B) {
-                            pz = fadd(pz, wb[0]); pz = fadd(pz, rbv[0]);
-                            pr = fadd(pr, wb[1]); pr = fadd(pr, rbv[1]);
+                    for (int i = 0; i < TN; ++i) {
+                        const int rl = x.rb * TN + i;
+                        zg[i] = 0.f;
+                        if (!(x.active && rl < x.NR)) continue;
+                        float rhv = 0.f;
+                        if (s < len[i]) {
+                            float pz = fadd(xc[i][0], az[i][0]);
+                            float pr = fadd(xc[i][1], az[i][1]);
+                            if (p.has_B) {
+                                pz = fadd(pz, wb[0]); pz = fadd(pz, rbv[0]);
+                                pr = fadd(pr, wb[1]); pr = fadd(pr, rbv[1]);
+                            }
+                            zg[i] = A.F(clipv(p, pz));
+                            const float r = A.F(clipv(p, pr));
+                            rhv = fmul(r, hown[i]);
                         }
-                        zg[i] = act<EXACT>(fA, clipv(p, pz));
-                        const float r = act<EXACT>(fA, clipv(p, pr));
-                        rhv = fmul(r, hown[i]);
+                        rh[xoff(rl, u)] = rhv;
                     }
-                    rh[xoff(rl, u)] = rhv;
-                }
-                if (!publish(x, my_flag, 2u * s + 1u, &s_abort, skip_first && s == 0)) return;
+                };
+                if (fixed_acts) epi_r(std::true_type{});
+                else epi_r(std::false_type{});
+                if (!publish(x, counter, &s_abort, skip_first && s == 0)) return;
                 float ah[TN][1];
 #pragma unroll
                 for (int i = 0; i < TN; ++i) ah[i][0] = 0.f;
                 consume_product<TN, 1, EXACT>(p, x, 2, ah, q, &s_abort, lane);
+                auto epi = [&](auto fx) {
+                    constexpr bool FX = decltype(fx)::value;
+                    const Acts<OP, EXACT, FX> A{fA, gA, hA};
 #pragma unroll
-                for (int i = 0; i < TN; ++i) {
-                    const int rl = x.rb * TN + i;
-                    const int n = x.cr * x.NRP + rl;
-                    if (!(x.active && rl < x.NR)) continue;
-                    if (s < len[i]) {
-                        const int t = rev ? len[i] - 1 - s : s;
-                        float ph = fadd(xc[i][2], ah[i][0]);
-                        if (p.has_B) { ph = fadd(ph, wb[2]); ph = fadd(ph, rbv[2]); }
-                        const float ht = act<EXACT>(gA, clipv(p, ph));
-                        const float hn = fadd(fmul(fsub(1.0f, zg[i]), ht), fmul(zg[i], hown[i]));
-                        hown[i] = hn;
-                        if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
-                    } else if (p.Y) {
-                        p.Y[y_index(p, s, d, n, u)] = 0.f;
+                    for (int i = 0; i < TN; ++i) {
+                        const int rl = x.rb * TN + i;
+                        const int n = x.cr * x.NRP + rl;
+                        if (!(x.active && rl < x.NR)) continue;
+                        if (s < len[i]) {
+                            const int t = rev ? len[i] - 1 - s : s;
+                            float ph = fadd(xc[i][2], ah[i][0]);
+                            if (p.has_B) { ph = fadd(ph, wb[2]); ph = fadd(ph, rbv[2]); }
+                            const float ht = A.Gf(clipv(p, ph));
+                            const float hn = fadd(fmul(fsub(1.0f, zg[i]), ht), fmul(zg[i], hown[i]));
+                            hown[i] = hn;
+                            if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
+                        } else if (p.Y) {
+                            p.Y[y_index(p, s, d, n, u)] = 0.f;
+                        }
+                        hdst[xoff(rl, u)] = hown[i];
                     }
-                    hdst[xoff(rl, u)] = hown[i];
-                }
-                if (!publish(x, my_flag, 2u * s + 2u, &s_abort, false)) return;
+                };
+                if (fixed_acts) epi(std::true_type{});
+                else epi(std::false_type{});
+                if (!publish(x, counter, &s_abort, false)) return;
             }
         } else {
             float acc[TN][G];
@@ -588,54 +646,60 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
             consume_product<TN, G, EXACT>(p, x, 0, acc, q, &s_abort, lane);
             if (s + 1 < p.max_len) load_xw(s + 1);
 
+            auto epi = [&](auto fx) {
+                constexpr bool FX = decltype(fx)::value;
+                const Acts<OP, EXACT, FX> A{fA, gA, hA};
 #pragma unroll
-            for (int i = 0; i < TN; ++i) {
-                const int rl = x.rb * TN + i;
-                const int n = x.cr * x.NRP + rl;
-                if (!(x.active && rl < x.NR)) continue;
-                if (s < len[i]) {
-                    const int t = rev ? len[i] - 1 - s : s;
-                    float hn;
-                    float pre[G];
+                for (int i = 0; i < TN; ++i) {
+                    const int rl = x.rb * TN + i;
+                    const int n = x.cr * x.NRP + rl;
+                    if (!(x.active && rl < x.NR)) continue;
+                    if (s < len[i]) {
+                        const int t = rev ? len[i] - 1 - s : s;
+                        float hn;
+                        float pre[G];
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        pre[g] = fadd(xc[i][g], acc[i][g]);
-                        if (p.has_B) { pre[g] = fadd(pre[g], wb[g]); pre[g] = fadd(pre[g], rbv[g]); }
-                    }
-                    if constexpr (OP == 0) {
-                        hn = act<EXACT>(fA, clipv(p, pre[0]));
-                    } else if constexpr (OP == 1) {
-                        const float z = act<EXACT>(fA, clipv(p, pre[0]));
-                        const float r = act<EXACT>(fA, clipv(p, pre[1]));
-                        float ph;
-                        if (p.has_B) ph = fadd(fadd(xc[i][2], fmul(r, fadd(acc[i][2], rbv[2]))), wb[2]);
-                        else ph = fadd(xc[i][2], fmul(r, acc[i][2]));
-                        const float ht = act<EXACT>(gA, clipv(p, ph));
-                        hn = fadd(fmul(fsub(1.0f, z), ht), fmul(z, hown[i]));
-                    } else {
-                        float pi = pre[0], po = pre[1], pf = pre[2];
-                        const float pc = pre[3];
-                        if (p.has_P) {
-                            pi = fadd(pi, fmul(pI, cown[i]));
-                            pf = fadd(pf, fmul(pF, cown[i]));
+                        for (int g = 0; g < G; ++g) {
+                            pre[g] = fadd(xc[i][g], acc[i][g]);
+                            if (p.has_B) { pre[g] = fadd(pre[g], wb[g]); pre[g] = fadd(pre[g], rbv[g]); }
                         }
-                        const float ig = act<EXACT>(fA, clipv(p, pi));
-                        const float fg = p.input_forget ? fsub(1.0f, ig) : act<EXACT>(fA, clipv(p, pf));
-                        const float ct = act<EXACT>(gA, clipv(p, pc));
-                        const float cn = fadd(fmul(fg, cown[i]), fmul(ig, ct));
-                        if (p.has_P) po = fadd(po, fmul(pO, cn));
-                        const float og = act<EXACT>(fA, clipv(p, po));
-                        hn = fmul(og, act<EXACT>(hA, cn));
-                        cown[i] = cn;
+                        if constexpr (OP == 0) {
+                            hn = A.F(clipv(p, pre[0]));
+                        } else if constexpr (OP == 1) {
+                            const float z = A.F(clipv(p, pre[0]));
+                            const float r = A.F(clipv(p, pre[1]));
+                            float ph;
+                            if (p.has_B) ph = fadd(fadd(xc[i][2], fmul(r, fadd(acc[i][2], rbv[2]))), wb[2]);
+                            else ph = fadd(xc[i][2], fmul(r, acc[i][2]));
+                            const float ht = A.Gf(clipv(p, ph));
+                            hn = fadd(fmul(fsub(1.0f, z), ht), fmul(z, hown[i]));
+                        } else {
+                            float pi = pre[0], po = pre[1], pf = pre[2];
+                            const float pc = pre[3];
+                            if (p.has_P) {
+                                pi = fadd(pi, fmul(pI, cown[i]));
+                                pf = fadd(pf, fmul(pF, cown[i]));
+                            }
+                            const float ig = A.F(clipv(p, pi));
+                            const float fg = p.input_forget ? fsub(1.0f, ig) : A.F(clipv(p, pf));
+                            const float ct = A.Gf(clipv(p, pc));
+                            const float cn = fadd(fmul(fg, cown[i]), fmul(ig, ct));
+                            if (p.has_P) po = fadd(po, fmul(pO, cn));
+                            const float og = A.F(clipv(p, po));
+                            hn = fmul(og, A.Hf(cn));
+                            cown[i] = cn;
+                        }
+                        hown[i] = hn;
+                        if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
+                    } else if (p.Y) {
+                        p.Y[y_index(p, s, d, n, u)] = 0.f;
                     }
-                    hown[i] = hn;
-                    if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
-                } else if (p.Y) {
-                    p.Y[y_index(p, s, d, n, u)] = 0.f;
+                    hdst[xoff(rl, u)] = hown[i];
                 }
-                hdst[xoff(rl, u)] = hown[i];
-            }
-            if (!publish(x, my_flag, (unsigned)s + 1u, &s_abort, skip_first && s == 0)) return;
+            };
+            if (fixed_acts) epi(std::true_type{});
+            else epi(std::false_type{});
+            if (!publish(x, counter, &s_abort, skip_first && s == 0)) return;
         }
     }
 

@@ -292,7 +292,7 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
             const int64_t qmax = ceil_div(Q, CU);
             if (pl->ov_units <= 0) CU = ceil_div(Q, qmax);
             const int umax = (int)(qmax * quant);
-            if ((int64_t)D * CR * CU > kMaxFlags) continue;
+            if ((int64_t)D * CR > kMaxFlags) continue;
             int tn = 0;
             const int tlist[3] = {1, 2, 4};
             for (int t : tlist) {

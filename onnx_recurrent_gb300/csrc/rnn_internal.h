@@ -58,7 +58,7 @@ struct RecParams {
     float* hbuf;                 // staged: [D][2][H][npad]; dataflow: [D][2][row_groups][hpad/32][npad][36]
     float* rhbuf;                // r (.) h for GRU lbr = 0, same layout as hbuf
     unsigned* bar;               // [D] barrier arrival counters (zeroed per run)
-    unsigned* flags;             // [D][row_groups][unit_groups] publication counts (zeroed per run)
+    unsigned* flags;             // dataflow kernel: [D][row_groups] publication counters (zeroed per run)
     int* status;                 // device status word (0 ok, 6 timeout)
     long long spin_limit_ns;
     int debug_skip_cta;
