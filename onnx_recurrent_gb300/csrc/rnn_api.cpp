@@ -304,10 +304,11 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
             if (!tn) continue;
             if (rr == 0 && (H < kDfPitch || umax > 256)) continue;   // R boxes: 36 k wide, <= 256 units
             const int compute = (int)round_up((int64_t)umax * (NRP / tn), 32);
-            // pieces: about four tensor copies per product, fewer if the ring
-            // would not hold two pieces
+            // pieces: the whole block in one tensor copy per product (measured:
+            // every extra piece boundary costs more than the earlier start
+            // it buys), halved until the ring holds two pieces
             int cpb = 0, slots = 0;
-            for (int c = (int)ceil_div(nchunks, 4); c >= 1; c /= 2) {
+            for (int c = nchunks; c >= 1; c /= 2) {
                 const size_t fixed = df_smem_bytes((int)H, umax, G, (int)NRP, rr, c, 0);
                 const size_t per_slot = df_smem_bytes((int)H, umax, G, (int)NRP, rr, c, 1) - fixed;
                 if (fixed + 2 * per_slot > smem_cap) continue;
