@@ -157,8 +157,8 @@ rnn_status rnn_plan_get_activation(rnn_plan_t plan, int dir, int slot, int* fn,
  * "choose"): kernel 1 is the staged kernel (CTAs hold all batch rows; h moves
  * through a shared-memory ring; one device-wide barrier per step), kernel 2
  * the dataflow kernel (CTAs tile unit groups x row groups; a loader warp
- * fetches h with TMA bulk copies once the CTAs that produce it have
- * published their per-step flags).  unit_groups: CTAs per direction along
+ * fetches h with TMA tensor copies once every CTA of its row group has
+ * published the step on the row group's counter).  unit_groups: CTAs per direction along
  * hidden units; row_groups: along batch rows (dataflow kernel only);
  * rows_per_thread: 1, 2, 4 (or 8, staged kernel only); r_resident: R slice
  * kept in shared memory (1) or streamed through it (0).  Every geometry gives
