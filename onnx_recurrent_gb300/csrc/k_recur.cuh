@@ -31,6 +31,7 @@
 
 #include "exact_math.cuh"
 #include "rnn_internal.h"
+#include "tma.cuh"
 
 namespace rnngb {
 
@@ -51,13 +52,6 @@ __device__ __forceinline__ int ld_relaxed_s32(const int* p)
     int v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ unsigned long long globaltimer_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 __device__ __forceinline__ void cp_async16_cg(void* smem, const void* gmem)

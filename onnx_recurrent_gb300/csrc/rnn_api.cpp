@@ -453,13 +453,13 @@ cudaError_t harvest(rnn_plan* pl, int slot)
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// dependency on the driver library): a tiled fp32 map with 128-byte swizzle.
+// dependency on the driver library): a tiled fp32 map, no swizzle,
+// out-of-range elements read as zero.
 typedef CUresult (*TmapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-rnn_status tmap_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides, const cuuint32_t* box)
+TmapEncodeFn tmap_encoder()
 {
     static TmapEncodeFn fn = []() -> TmapEncodeFn {
         void* f = nullptr;
@@ -470,11 +470,25 @@ rnn_status tmap_encode(CUtensorMap* map, const void* base, int rank, const cuuin
             return nullptr;
         return reinterpret_cast<TmapEncodeFn>(f);
     }();
-    if (!fn) return fail(RNN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    return fn;
+}
+
+CUresult tmap_encode_raw(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                         const cuuint64_t* strides, const cuuint32_t* box)
+{
+    const TmapEncodeFn fn = tmap_encoder();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base), dims,
-                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+rnn_status tmap_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box)
+{
+    if (!tmap_encoder()) return fail(RNN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const CUresult r = tmap_encode_raw(map, base, rank, dims, strides, box);
     if (r != CUDA_SUCCESS) return fail(RNN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return RNN_OK;
 }
@@ -577,7 +591,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         launches += (int)D * ((I > 0 ? 1 : 0) + (pack_r ? 1 : 0));
     }
     if (timed) record(pl, 1, a.st);
-    e = launch_projection(a.X, wt, xw, M, I, D * GH, exact, a.st);
+    e = launch_projection(a.X, wt, xw, M, I, D * GH, exact, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
     launches += 1;
     if (timed) record(pl, 2, a.st);
@@ -880,7 +894,7 @@ rnn_status rnn_plan_sync(rnn_plan_t pl)
         const int zero = 0;
         cudaMemcpy(pl->ctrl + kCtrlStatusOffset, &zero, sizeof zero, cudaMemcpyHostToDevice);
         if (st == RNN_ERR_TIMEOUT)
-            return fail(RNN_ERR_TIMEOUT, "the device-wide step barrier timed out; outputs are incomplete");
+            return fail(RNN_ERR_TIMEOUT, "a device-side wait (step barrier or copy) timed out; outputs are incomplete");
         return fail((rnn_status)st, "device reported status %d", st);
     }
     return RNN_OK;
@@ -1036,3 +1050,13 @@ rnn_status rnn_run_static_scratch(rnn_plan_t pl, int64_t S, int64_t N, const flo
 }
 
 }  // extern "C"
+
+namespace rnngb {
+
+bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box)
+{
+    return tmap_encode_raw(map, base, rank, dims, strides, box) == CUDA_SUCCESS;
+}
+
+}  // namespace rnngb

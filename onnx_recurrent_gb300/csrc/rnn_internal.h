@@ -121,9 +121,16 @@ cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t
 cudaError_t recurrent_occupancy(int op, int lbr, int kernel, int rows_per_thread, bool exact, int threads,
                                 size_t smem, int* blocks_per_sm);
 
-// Input projection XW[M][ldc] = X[M][K] . Bt[K][ncols] (Bt row stride ldb).
+// Input projection XW[M][ncols] = X[M][K] . Bt[K][ncols].  A wait of the
+// tensor-copy loader that gives up writes RNN_ERR_TIMEOUT to *status.
 cudaError_t launch_projection(const float* X, const float* Bt, float* XW, int64_t M,
-                              int64_t K, int64_t ncols, bool exact, cudaStream_t stream);
+                              int64_t K, int64_t ncols, bool exact, int* status, long long limit_ns,
+                              cudaStream_t stream);
+
+// Encodes a tiled fp32 tensor map (no swizzle, out-of-range reads as zero);
+// false when the driver entry point is missing or rejects the shape.
+bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                       const cuuint64_t* strides, const cuuint32_t* box);
 
 // Pack: Wt[k][d*GH + u*G + g] = W[d][g*H + u][k]  (ld = D*GH),
 //       Rt[d][k][u*G + g]    = R[d][g*H + u][k].

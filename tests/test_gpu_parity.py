@@ -109,6 +109,25 @@ def test_every_launch_geometry_gives_the_same_bits(op, direction, lbr):
         _compare_exact(c, out, ref, f"geometry {g}")
 
 
+# Input projection through its tensor-copy loader: input sizes that are
+# multiples of 4 (16-byte rows) but not of the 16-k stage, row counts
+# (seq * batch) and column counts (dirs * gates * hidden) that are not
+# multiples of the 128 x 128 tile, so every edge of the zero-filled boxes is
+# crossed; and an input size that is not a multiple of 4 (register loader).
+@pytest.mark.parametrize("op,direction,seq,batch,inp,hid", [
+    ("LSTM", "forward", 7, 19, 20, 40), ("GRU", "bidirectional", 9, 15, 36, 44),
+    ("RNN", "reverse", 11, 13, 260, 68), ("LSTM", "bidirectional", 5, 29, 4, 36),
+    ("GRU", "forward", 6, 23, 34, 32)])
+def test_projection_tile_edges(op, direction, seq, batch, inp, hid):
+    c = make_case(op, direction, seq, batch, inp, hid, seed=31, with_P=True, h0_scale=0.5, c0_scale=0.5)
+    _compare_exact(c, gpu_case(c, "exact"), oracle_case(c), "exact")
+    ref = oracle_case(c)
+    for g, r in zip(gpu_case(c, "fast"), ref):
+        if g is None or r is None:
+            continue
+        assert float(np.abs(g.astype(np.float64) - r.astype(np.float64)).max(initial=0.0)) <= 1e-5
+
+
 @pytest.mark.parametrize("op", ["RNN", "GRU", "LSTM"])
 def test_hidden_not_multiple_of_four(op):
     # The dataflow kernel moves whole 16-byte groups of k, so it needs hidden
