@@ -104,7 +104,29 @@ __global__ void mask_tail_kernel(float* __restrict__ Y, int layout, int64_t S, i
     }
 }
 
+// Wk[r][k] = W[d*GH + g*H + u][k] for r = d*GH + u*G + g: whole rows of W,
+// reordered to the projection's interleaved column order.
+__global__ void pack_kmajor_kernel(const float* __restrict__ W, float* __restrict__ Wk, int G, int64_t H,
+                                   int64_t I, int64_t rows)
+{
+    const int64_t GH = (int64_t)G * H;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const int64_t d = r / GH, rem = r - d * GH, u = rem / G, g = rem - u * G;
+        const float* src = W + (d * GH + g * H + u) * I;
+        float* dst = Wk + r * I;
+        for (int64_t k = threadIdx.x; k < I; k += blockDim.x) dst[k] = src[k];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_kmajor(const float* W, float* Wk, int D, int G, int64_t H, int64_t I, cudaStream_t stream)
+{
+    const int64_t rows = (int64_t)D * G * H;
+    if (rows <= 0 || I <= 0) return cudaSuccess;
+    pack_kmajor_kernel<<<(unsigned)std::min<int64_t>(rows, 8192), 128, 0, stream>>>(W, Wk, G, H, I, rows);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pack(const float* W, const float* R, float* Wt, float* Rt, int D, int G, int64_t H,
                         int64_t I, cudaStream_t stream)

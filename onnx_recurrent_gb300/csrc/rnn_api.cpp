@@ -121,6 +121,7 @@ struct rnn_plan {
     // constant weights (rnn_plan_set_weights)
     bool const_weights = false;
     float* wt_const = nullptr;   // [I][D*G*H]
+    float* wk_const = nullptr;   // [D*G*H][I] (the tensor-core projection's operand)
     float* rt_const = nullptr;   // [D][H][G*H]
     float* r_orig_const = nullptr;   // R as given, [D][G*H][H] (the dataflow kernel reads this layout)
 
@@ -474,14 +475,15 @@ TmapEncodeFn tmap_encoder()
 }
 
 CUresult tmap_encode_raw(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                         const cuuint64_t* strides, const cuuint32_t* box)
+                         const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128 = false)
 {
     const TmapEncodeFn fn = tmap_encoder();
     if (!fn) return CUDA_ERROR_NOT_FOUND;
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
-              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 rnn_status tmap_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
@@ -578,6 +580,12 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     const int64_t H = pl->H, I = pl->I, G = pl->G, D = pl->D, GH = G * H;
     const int64_t M = a.S * a.N;
     float* wt = pl->const_weights ? pl->wt_const : (float*)(scratch + L.wt);
+    // tensor-core projection: W as K-major rows in the projection's column
+    // order (the same scratch bytes as the k-major pack)
+    float* wk = pl->const_weights ? pl->wk_const : (float*)(scratch + L.wt);
+    const bool use_tc = pl->mode == RNN_MODE_FAST_TF32 &&
+                        projection_tc_supported(a.X, wk ? wk : (const float*)scratch, (float*)(scratch + L.xw), M, I,
+                                                D * GH);
     float* rt = pl->const_weights ? pl->rt_const : (float*)(scratch + L.rt);
     float* xw = (float*)(scratch + L.xw);
     const bool exact = pl->mode == RNN_MODE_EXACT;
@@ -586,12 +594,21 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     if (timed) record(pl, 0, a.st);
     if (!pl->const_weights) {
         const bool pack_r = geo.kernel != 2;   // the dataflow kernel reads R as given
-        e = launch_pack(a.W, pack_r ? a.R : nullptr, wt, pack_r ? rt : nullptr, (int)D, (int)G, H, I, a.st);
+        e = launch_pack(use_tc ? nullptr : a.W, pack_r ? a.R : nullptr, wt, pack_r ? rt : nullptr, (int)D, (int)G, H,
+                        I, a.st);
         if (e != cudaSuccess) return cuda_fail(e, "pack launch");
-        launches += (int)D * ((I > 0 ? 1 : 0) + (pack_r ? 1 : 0));
+        launches += (int)D * ((I > 0 && !use_tc ? 1 : 0) + (pack_r ? 1 : 0));
+        if (use_tc) {
+            e = launch_pack_kmajor(a.W, wk, (int)D, (int)G, H, I, a.st);
+            if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+            launches += 1;
+        }
     }
     if (timed) record(pl, 1, a.st);
-    e = launch_projection(a.X, wt, xw, M, I, D * GH, exact, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
+    if (use_tc)
+        e = launch_projection_tc(a.X, wk, xw, M, I, D * GH, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
+    else
+        e = launch_projection(a.X, wt, xw, M, I, D * GH, exact, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
     launches += 1;
     if (timed) record(pl, 2, a.st);
@@ -759,6 +776,7 @@ void rnn_plan_destroy(rnn_plan_t pl)
     if (pl->scratch) cudaFree(pl->scratch);
     if (pl->ctrl) cudaFree(pl->ctrl);
     if (pl->wt_const) cudaFree(pl->wt_const);
+    if (pl->wk_const) cudaFree(pl->wk_const);
     if (pl->rt_const) cudaFree(pl->rt_const);
     if (pl->r_orig_const) cudaFree(pl->r_orig_const);
     if (pl->lens_host) cudaFreeHost(pl->lens_host);
@@ -772,7 +790,7 @@ void rnn_plan_destroy(rnn_plan_t pl)
 rnn_status rnn_plan_set_mode(rnn_plan_t pl, int mode)
 {
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
-    if (mode != RNN_MODE_EXACT && mode != RNN_MODE_FAST)
+    if (mode != RNN_MODE_EXACT && mode != RNN_MODE_FAST && mode != RNN_MODE_FAST_TF32)
         return fail(RNN_ERR_INVALID_ARGUMENT, "unknown mode %d", mode);
     pl->mode = mode;
     return RNN_OK;
@@ -912,6 +930,8 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
         if (pl->I > 0) {
             e = cudaMalloc((void**)&pl->wt_const, sizeof(float) * (size_t)pl->I * pl->D * GH);
             if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(W pack)");
+            e = cudaMalloc((void**)&pl->wk_const, sizeof(float) * (size_t)pl->I * pl->D * GH);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(W K-major pack)");
         }
     }
     if (!pl->r_orig_const) {
@@ -922,6 +942,7 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
                                     cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "copying R");
     e = launch_pack(W, R, pl->wt_const, pl->rt_const, pl->D, pl->G, pl->H, pl->I, s);
+    if (e == cudaSuccess && pl->wk_const) e = launch_pack_kmajor(W, pl->wk_const, pl->D, pl->G, pl->H, pl->I, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     pl->const_weights = true;
     return RNN_OK;
@@ -1054,9 +1075,9 @@ rnn_status rnn_run_static_scratch(rnn_plan_t pl, int64_t S, int64_t N, const flo
 namespace rnngb {
 
 bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides, const cuuint32_t* box)
+                       const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128)
 {
-    return tmap_encode_raw(map, base, rank, dims, strides, box) == CUDA_SUCCESS;
+    return tmap_encode_raw(map, base, rank, dims, strides, box, swizzle128) == CUDA_SUCCESS;
 }
 
 }  // namespace rnngb

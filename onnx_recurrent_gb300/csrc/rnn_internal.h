@@ -127,10 +127,21 @@ cudaError_t launch_projection(const float* X, const float* Bt, float* XW, int64_
                               int64_t K, int64_t ncols, bool exact, int* status, long long limit_ns,
                               cudaStream_t stream);
 
-// Encodes a tiled fp32 tensor map (no swizzle, out-of-range reads as zero);
-// false when the driver entry point is missing or rejects the shape.
+// Encodes a tiled fp32 tensor map (no swizzle, or 128-byte swizzle;
+// out-of-range reads as zero); false when the driver entry point is missing
+// or rejects the shape.
 bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides, const cuuint32_t* box);
+                       const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128 = false);
+
+// Input projection on the tensor cores (TF32 products, FP32 sums):
+// XW[M][ncols] = X[M][K] . Wk[ncols][K]^T with Wk K-major (see launch_pack_kmajor).
+bool projection_tc_supported(const float* X, const float* Wk, float* XW, int64_t M, int64_t K, int64_t ncols);
+cudaError_t launch_projection_tc(const float* X, const float* Wk, float* XW, int64_t M, int64_t K, int64_t ncols,
+                                 int* status, long long limit_ns, cudaStream_t stream);
+
+// Wk[d*G*H + u*G + g][k] = W[d][g*H + u][k]: W's rows in the projection's
+// column order, K contiguous.
+cudaError_t launch_pack_kmajor(const float* W, float* Wk, int D, int G, int64_t H, int64_t I, cudaStream_t stream);
 
 // Pack: Wt[k][d*GH + u*G + g] = W[d][g*H + u][k]  (ld = D*GH),
 //       Rt[d][k][u*G + g]    = R[d][g*H + u][k].

@@ -284,6 +284,44 @@ def test_workload_full_size_fast(name, lbr, k):
     _workload_check(c, _sample_rows(c, min(k, 3)), "fast")
 
 
+# TF32 mode: the input projection on the tensor cores (tcgen05), within 5e-3
+# of the oracle.  Shapes cross the 128 x 128 tile and the 32-k block edges;
+# an input size that is not a multiple of 4 takes the FP32 projection.
+TF32_TOL = 5e-3
+
+
+@pytest.mark.parametrize("op,direction,seq,batch,inp,hid,layout", [
+    ("LSTM", "forward", 7, 19, 20, 40, 0), ("GRU", "bidirectional", 9, 15, 36, 44, 1),
+    ("RNN", "reverse", 11, 13, 260, 68, 0), ("LSTM", "bidirectional", 5, 29, 4, 36, 1),
+    ("GRU", "forward", 6, 23, 34, 32, 0), ("LSTM", "forward", 3, 50, 96, 136, 0)])
+def test_tf32_mode_within_tolerance(op, direction, seq, batch, inp, hid, layout):
+    c = make_case(op, direction, seq, batch, inp, hid, seed=41, layout=layout, with_P=True, h0_scale=0.5,
+                  c0_scale=0.5)
+    _compare_fast(gpu_case(c, "tf32"), oracle_case(c), TF32_TOL)
+
+
+def test_tf32_mode_differs_from_fp32_only_by_the_projection():
+    # a zero input projection (X = 0) leaves nothing for TF32 to round: TF32
+    # and FAST must then agree bit for bit
+    c = make_case("LSTM", "forward", 5, 9, 24, 32, seed=3, with_P=True, h0_scale=0.5, c0_scale=0.5)
+    c.X[...] = 0.0
+    for g, f in zip(gpu_case(c, "tf32"), gpu_case(c, "fast")):
+        if g is not None:
+            assert_bits_equal(g, f, "tf32 vs fast with X = 0")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,lbr,k", [WORKLOAD_CASES[1], WORKLOAD_CASES[4]],
+                         ids=[f"{w[0]}-lbr{w[1]}" for w in (WORKLOAD_CASES[1], WORKLOAD_CASES[4])])
+def test_workload_full_size_tf32(name, lbr, k):
+    c = workload(name, lbr=lbr)
+    rows = _sample_rows(c, min(k, 3))
+    got = gpu_case(c, "tf32")
+    ref = oracle_case(c, rows=rows, threaded=True)
+    _compare_fast(tuple(row_slice(c, rows, g, kind) for g, kind in zip(got, ("Y", "state", "state"))),
+                  tuple(row_slice(c, rows, r, kind) for r, kind in zip(ref, ("Y", "state", "state"))), TF32_TOL)
+
+
 def test_rnn_workload_absent_and_zero_initial_state():
     a = gpu_case(workload("rnn_fwd_s8_b1_i16_h128"))
     b = gpu_case(workload("rnn_fwd_s8_b1_i16_h128", initial_h_zero=True))
