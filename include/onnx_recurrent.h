@@ -60,7 +60,7 @@ enum { RNN_DIR_FORWARD = 0, RNN_DIR_REVERSE = 1, RNN_DIR_BIDIRECTIONAL = 2 };
  *   FAST:  same order; the two matrix products use fused multiply-add and the
  *          elementwise functions use CUDA's expf/tanhf/logf.  The gate
  *          arithmetic stays unfused. */
-enum { RNN_MODE_EXACT = 0, RNN_MODE_FAST = 1, RNN_MODE_FAST_TF32 = 2 };
+enum { RNN_MODE_EXACT = 0, RNN_MODE_FAST = 1, RNN_MODE_FAST_TF32 = 2, RNN_MODE_FAST_BF16 = 3 };
 
 /* Activation function ids (page "Recurrent operators", Activations). */
 enum {
@@ -129,8 +129,8 @@ void rnn_plan_destroy(rnn_plan_t plan);
 
 /* ---------------------------------------------------------------- extras */
 
-/* Select RNN_MODE_EXACT (default), RNN_MODE_FAST or RNN_MODE_FAST_TF32
- * (page "Recurrent operators", Exact mode / Fast mode).
+/* Select RNN_MODE_EXACT (default), RNN_MODE_FAST, RNN_MODE_FAST_TF32 or
+ * RNN_MODE_FAST_BF16 (page "Recurrent operators", Exact mode / Fast mode).
  *   EXACT      bit-identical to the library's reference arithmetic: one
  *              accumulator per output, k ascending, every product and sum
  *              rounded separately, own IEEE-only transcendentals.
@@ -141,6 +141,10 @@ void rnn_plan_destroy(rnn_plan_t plan);
  *              within 5e-3 of EXACT.  Shapes the tensor-core path cannot take
  *              (input_size or G*H*D not a multiple of 4, unaligned pointers)
  *              run the FAST projection instead.
+ *   FAST_BF16  FAST, with X and W rounded to bf16 (nearest even) and the
+ *              input projection on the tensor cores, sums in FP32; within
+ *              5e-3 of EXACT; input_size must be a multiple of 8 (else the
+ *              FAST projection).  Scratch grows by 2 bytes per element of X.
  * An unknown mode returns RNN_ERR_INVALID_ARGUMENT. */
 rnn_status rnn_plan_set_mode(rnn_plan_t plan, int mode);
 

@@ -7,6 +7,8 @@
 //               are zeros: Choices the specification leaves open);
 //   mask_tail   Y = 0 at the steps no row reaches (sequence_lens: Y is zero
 //               at t >= len).
+#include <cuda_bf16.h>
+
 #include "rnn_internal.h"
 
 namespace rnngb {
@@ -105,26 +107,47 @@ __global__ void mask_tail_kernel(float* __restrict__ Y, int layout, int64_t S, i
 }
 
 // Wk[r][k] = W[d*GH + g*H + u][k] for r = d*GH + u*G + g: whole rows of W,
-// reordered to the projection's interleaved column order.
-__global__ void pack_kmajor_kernel(const float* __restrict__ W, float* __restrict__ Wk, int G, int64_t H,
-                                   int64_t I, int64_t rows)
+// reordered to the projection's interleaved column order (fp32 copy or bf16).
+template <typename T>
+__global__ void pack_kmajor_kernel(const float* __restrict__ W, T* __restrict__ Wk, int G, int64_t H, int64_t I,
+                                   int64_t rows)
 {
     const int64_t GH = (int64_t)G * H;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const int64_t d = r / GH, rem = r - d * GH, u = rem / G, g = rem - u * G;
         const float* src = W + (d * GH + g * H + u) * I;
-        float* dst = Wk + r * I;
-        for (int64_t k = threadIdx.x; k < I; k += blockDim.x) dst[k] = src[k];
+        T* dst = Wk + r * I;
+        for (int64_t k = threadIdx.x; k < I; k += blockDim.x) {
+            if constexpr (sizeof(T) == 4) dst[k] = src[k];
+            else dst[k] = __float2bfloat16_rn(src[k]);
+        }
     }
+}
+
+__global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = __float2bfloat16_rn(src[i]);
 }
 
 }  // namespace
 
-cudaError_t launch_pack_kmajor(const float* W, float* Wk, int D, int G, int64_t H, int64_t I, cudaStream_t stream)
+cudaError_t launch_pack_kmajor(const float* W, void* Wk, int D, int G, int64_t H, int64_t I, bool bf16,
+                               cudaStream_t stream)
 {
     const int64_t rows = (int64_t)D * G * H;
     if (rows <= 0 || I <= 0) return cudaSuccess;
-    pack_kmajor_kernel<<<(unsigned)std::min<int64_t>(rows, 8192), 128, 0, stream>>>(W, Wk, G, H, I, rows);
+    const unsigned blocks = (unsigned)std::min<int64_t>(rows, 8192);
+    if (bf16) pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (__nv_bfloat16*)Wk, G, H, I, rows);
+    else pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (float*)Wk, G, H, I, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t stream)
+{
+    if (n <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 16);
+    to_bf16_kernel<<<blocks, 256, 0, stream>>>(src, (__nv_bfloat16*)dst, n);
     return cudaGetLastError();
 }
 

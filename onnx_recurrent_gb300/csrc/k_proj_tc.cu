@@ -1,14 +1,20 @@
-// Input projection on the tensor cores (TF32): XW[M][NC] = X[M][K] . Wk[NC][K]^T
+// Input projection on the tensor cores: XW[M][NC] = X[M][K] . Wk[NC][K]^T
 // (page "Recurrent operators: RNN, GRU, LSTM", Computation: the projection
 // of every step as one matrix product; Fast mode: the product need not keep
-// the exact mode's rounding order).  Products are formed from the operands'
-// TF32 parts (10-bit mantissas) and summed in FP32 on the tensor cores.
+// the exact mode's rounding order).  Two operand kinds, sums in FP32 on the
+// tensor cores:
+//   * TF32: fp32 operands, products of their TF32 parts (10-bit mantissas),
+//     tcgen05.mma kind::tf32, K 8 per instruction;
+//   * BF16: operands converted to bf16 beforehand (round to nearest even),
+//     tcgen05.mma kind::f16 with both A and B bf16, K 16 per instruction.
+// Either way a k-block is 128 bytes of every row (32 fp32 or 64 bf16).
 //
 // One CTA per 128 x 128 output tile, 128 threads:
-//   * warp 0, one lane: tensor copies (TMA) of the A tile [128 rows][32 k]
-//     and the Wk tile [128 cols][32 k] of each k-block into a 4-stage ring,
-//     both with 128-byte swizzle (the layout the MMA descriptors describe);
-//   * warp 1, one lane: per k-block four tcgen05.mma (M 128, N 128, K 8)
+//   * warp 0, one lane: tensor copies (TMA) of the A tile [128 rows][k-block]
+//     and the Wk tile [128 cols][k-block] of each k-block into a 4-stage
+//     ring, both with 128-byte swizzle (the layout the MMA descriptors
+//     describe);
+//   * warp 1, one lane: per k-block four tcgen05.mma (M 128, N 128)
 //     accumulating in tensor memory, then tcgen05.commit to the stage's
 //     "empty" mbarrier (the ring slot is free once those MMAs have read it)
 //     and after the last k-block to the "done" mbarrier;
@@ -28,17 +34,17 @@ namespace rnngb {
 
 namespace {
 
-constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 32, TC_ST = 4;
-constexpr unsigned kTcTileA = TC_BM * TC_BK * 4, kTcTileB = TC_BN * TC_BK * 4;   // 16 KB each
+constexpr int TC_BM = 128, TC_BN = 128, TC_ROWB = 128, TC_ST = 4;   // TC_ROWB: bytes of a row per k-block
+constexpr unsigned kTcTileA = TC_BM * TC_ROWB, kTcTileB = TC_BN * TC_ROWB;   // 16 KB each
 constexpr unsigned kTcStage = kTcTileA + kTcTileB;
 constexpr size_t kTcSmem = (size_t)TC_ST * kTcStage + 1024;   // + alignment slack (1024 for the swizzle)
 constexpr unsigned kTmemCols = 128;
 
 struct TcArgs {
-    CUtensorMap amap;   // X  [M][K]:  dims {K, M},  box {32, 128}, 128-byte swizzle
-    CUtensorMap bmap;   // Wk [NC][K]: dims {K, NC}, box {32, 128}, 128-byte swizzle
+    CUtensorMap amap;   // X  [M][K]:  dims {K, M},  box {k-block, 128}, 128-byte swizzle
+    CUtensorMap bmap;   // Wk [NC][K]: dims {K, NC}, box {k-block, 128}, 128-byte swizzle
     float* C;
-    int M, NC, nk;      // nk: k-blocks of 32
+    int M, NC, nk;      // nk: k-blocks
     int* status;
     long long limit_ns;
 };
@@ -56,17 +62,28 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(unsigned saddr)
     return d;
 }
 
-// Instruction descriptor: D f32, A and B tf32, both K-major, M 128, N 128.
-constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(TC_BN >> 3) << 17) |
-                                ((uint32_t)(TC_BM >> 4) << 24);
+// Instruction descriptors: D f32, both operands K-major, M 128, N 128;
+// A and B tf32 (kind::tf32) or both bf16 (kind::f16).
+constexpr uint32_t kIdescShape = ((uint32_t)(TC_BN >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
+constexpr uint32_t kIdescTf32 = (1u << 4) | (2u << 7) | (2u << 10) | kIdescShape;
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | kIdescShape;
 
-__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+template <bool BF16>
+__device__ __forceinline__ void mma_issue(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdescTf32), "r"(accumulate)
-        : "memory");
+    if constexpr (BF16) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+            "l"(adesc), "l"(bdesc), "r"(kIdescBf16), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+            "l"(adesc), "l"(bdesc), "r"(kIdescTf32), "r"(accumulate)
+            : "memory");
+    }
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
@@ -113,8 +130,10 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, unsigned parity, long lon
     return true;
 }
 
+template <bool BF16>
 __global__ void __launch_bounds__(128, 1) proj_tc_kernel(const __grid_constant__ TcArgs a)
 {
+    constexpr int BKE = BF16 ? 64 : 32;   // elements of a row per k-block
     extern __shared__ __align__(1024) unsigned char tc_smem[];
     __shared__ __align__(8) uint64_t full[TC_ST], empty[TC_ST], done;
     __shared__ uint32_t tmem_slot;
@@ -156,8 +175,8 @@ __global__ void __launch_bounds__(128, 1) proj_tc_kernel(const __grid_constant__
             }
             unsigned char* st = base + (size_t)s * kTcStage;
             mbar_arrive_expect_tx(&full[s], kTcStage);
-            tma_load_2d(st, &a.amap, kb * TC_BK, m0, &full[s]);
-            tma_load_2d(st + kTcTileA, &a.bmap, kb * TC_BK, n0, &full[s]);
+            tma_load_2d(st, &a.amap, kb * BKE, m0, &full[s]);
+            tma_load_2d(st + kTcTileA, &a.bmap, kb * BKE, n0, &full[s]);
             ++issued;
         }
     } else if (warp == 1 && lane == 0) {
@@ -174,8 +193,9 @@ __global__ void __launch_bounds__(128, 1) proj_tc_kernel(const __grid_constant__
             const unsigned sa = smem_addr(base + (size_t)s * kTcStage);
             const unsigned sb = sa + kTcTileA;
 #pragma unroll
-            for (int j = 0; j < TC_BK / 8; ++j)   // K 8 per MMA = 32 bytes along the swizzled row
-                mma_tf32(tmem, sdesc_k_sw128(sa + 32u * j), sdesc_k_sw128(sb + 32u * j), (kb > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < 4; ++j)   // one MMA per 32 bytes along the swizzled row (K 8 tf32 / 16 bf16)
+                mma_issue<BF16>(tmem, sdesc_k_sw128(sa + 32u * j), sdesc_k_sw128(sb + 32u * j),
+                                (kb > 0 || j > 0) ? 1u : 0u);
             mma_commit(&empty[s]);
         }
         mma_commit(&done);   // arrives once every MMA issued above has completed
@@ -222,36 +242,41 @@ __global__ void __launch_bounds__(128, 1) proj_tc_kernel(const __grid_constant__
 
 }  // namespace
 
-bool projection_tc_supported(const float* X, const float* Wk, float* XW, int64_t M, int64_t K, int64_t ncols)
+bool projection_tc_supported(const void* X, const void* Wk, float* XW, int64_t M, int64_t K, int64_t ncols,
+                             bool bf16)
 {
-    return K > 0 && K % 4 == 0 && ncols % 4 == 0 && (uintptr_t)X % 16 == 0 && (uintptr_t)Wk % 16 == 0 &&
+    const int64_t kq = bf16 ? 8 : 4;   // 16-byte rows
+    return K > 0 && K % kq == 0 && ncols % 4 == 0 && (uintptr_t)X % 16 == 0 && (uintptr_t)Wk % 16 == 0 &&
            (uintptr_t)XW % 16 == 0 && M < (1ll << 31) && ncols < (1ll << 31) && K < (1ll << 31) &&
            (M + TC_BM - 1) / TC_BM <= 65535;
 }
 
-cudaError_t launch_projection_tc(const float* X, const float* Wk, float* XW, int64_t M, int64_t K, int64_t ncols,
-                                 int* status, long long limit_ns, cudaStream_t stream)
+cudaError_t launch_projection_tc(const void* X, const void* Wk, float* XW, int64_t M, int64_t K, int64_t ncols,
+                                 bool bf16, int* status, long long limit_ns, cudaStream_t stream)
 {
     if (M <= 0 || ncols <= 0) return cudaSuccess;
-    if (!projection_tc_supported(X, Wk, XW, M, K, ncols)) return cudaErrorInvalidValue;
+    if (!projection_tc_supported(X, Wk, XW, M, K, ncols, bf16)) return cudaErrorInvalidValue;
+    const int es = bf16 ? 2 : 4, bke = TC_ROWB / es;
     TcArgs ta;
     const cuuint64_t adims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t astr[1] = {(cuuint64_t)K * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)TC_BM};
+    const cuuint64_t astr[1] = {(cuuint64_t)K * es};
+    const cuuint32_t box[2] = {(cuuint32_t)bke, (cuuint32_t)TC_BM};
     const cuuint64_t bdims[2] = {(cuuint64_t)K, (cuuint64_t)ncols};
-    if (!encode_tensor_map(&ta.amap, X, 2, adims, astr, box, true) ||
-        !encode_tensor_map(&ta.bmap, Wk, 2, bdims, astr, box, true))
+    if (!encode_tensor_map(&ta.amap, X, 2, adims, astr, box, true, bf16) ||
+        !encode_tensor_map(&ta.bmap, Wk, 2, bdims, astr, box, true, bf16))
         return cudaErrorInvalidValue;
     ta.C = XW;
     ta.M = (int)M;
     ta.NC = (int)ncols;
-    ta.nk = (int)((K + TC_BK - 1) / TC_BK);
+    ta.nk = (int)((K + bke - 1) / bke);
     ta.status = status;
     ta.limit_ns = limit_ns;
-    cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    const void* fn = bf16 ? (const void*)proj_tc_kernel<true> : (const void*)proj_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((ncols + TC_BN - 1) / TC_BN), (unsigned)((M + TC_BM - 1) / TC_BM));
-    proj_tc_kernel<<<grid, 128, kTcSmem, stream>>>(ta);
+    if (bf16) proj_tc_kernel<true><<<grid, 128, kTcSmem, stream>>>(ta);
+    else proj_tc_kernel<false><<<grid, 128, kTcSmem, stream>>>(ta);
     return cudaGetLastError();
 }
 

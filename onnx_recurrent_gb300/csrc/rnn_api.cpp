@@ -122,6 +122,7 @@ struct rnn_plan {
     bool const_weights = false;
     float* wt_const = nullptr;   // [I][D*G*H]
     float* wk_const = nullptr;   // [D*G*H][I] (the tensor-core projection's operand)
+    void* wkb_const = nullptr;   // the same rounded to bf16
     float* rt_const = nullptr;   // [D][H][G*H]
     float* r_orig_const = nullptr;   // R as given, [D][G*H][H] (the dataflow kernel reads this layout)
 
@@ -475,12 +476,13 @@ TmapEncodeFn tmap_encoder()
 }
 
 CUresult tmap_encode_raw(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                         const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128 = false)
+                         const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128 = false,
+                         bool bf16 = false)
 {
     const TmapEncodeFn fn = tmap_encoder();
     if (!fn) return CUDA_ERROR_NOT_FOUND;
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -550,7 +552,7 @@ rnn_status check_lengths(const int32_t* host, int64_t N, int64_t S, int64_t* max
 }
 
 struct Layout {
-    size_t wt, rt, xw, hb, rh, total;
+    size_t wt, rt, xw, xb, hb, rh, total;
     bool need_rh;
 };
 
@@ -563,6 +565,7 @@ Layout scratch_layout(const rnn_plan* pl, const Geometry& geo, int64_t S, int64_
     L.wt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)I * D * GH);
     L.rt = off; off += (pl->const_weights || geo.kernel == 2) ? 0 : align256(sizeof(float) * (size_t)D * H * GH);
     L.xw = off; off += align256(sizeof(float) * (size_t)S * N * D * GH);
+    L.xb = off; off += pl->mode == RNN_MODE_FAST_BF16 ? align256((size_t)2 * S * N * I) : 0;   // X as bf16
     const size_t row = geo.kernel == 2 ? (size_t)geo.hpad / kRecKC * kDfPitch : (size_t)H;
     const size_t hbuf = sizeof(float) * (size_t)D * 2 * geo.rows * geo.npad * row;
     L.hb = off; off += align256(hbuf);
@@ -581,11 +584,14 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     const int64_t M = a.S * a.N;
     float* wt = pl->const_weights ? pl->wt_const : (float*)(scratch + L.wt);
     // tensor-core projection: W as K-major rows in the projection's column
-    // order (the same scratch bytes as the k-major pack)
-    float* wk = pl->const_weights ? pl->wk_const : (float*)(scratch + L.wt);
-    const bool use_tc = pl->mode == RNN_MODE_FAST_TF32 &&
-                        projection_tc_supported(a.X, wk ? wk : (const float*)scratch, (float*)(scratch + L.xw), M, I,
-                                                D * GH);
+    // order (the same scratch bytes as the k-major pack), and in BF16 mode X
+    // and W rounded to bf16
+    const bool bf16 = pl->mode == RNN_MODE_FAST_BF16;
+    void* wk = pl->const_weights ? (bf16 ? pl->wkb_const : (void*)pl->wk_const) : (void*)(scratch + L.wt);
+    const void* xin = bf16 ? (const void*)(scratch + L.xb) : (const void*)a.X;
+    const bool use_tc = (pl->mode == RNN_MODE_FAST_TF32 || bf16) &&
+                        projection_tc_supported(xin, wk ? wk : (const void*)scratch, (float*)(scratch + L.xw), M, I,
+                                                D * GH, bf16);
     float* rt = pl->const_weights ? pl->rt_const : (float*)(scratch + L.rt);
     float* xw = (float*)(scratch + L.xw);
     const bool exact = pl->mode == RNN_MODE_EXACT;
@@ -599,14 +605,19 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         if (e != cudaSuccess) return cuda_fail(e, "pack launch");
         launches += (int)D * ((I > 0 && !use_tc ? 1 : 0) + (pack_r ? 1 : 0));
         if (use_tc) {
-            e = launch_pack_kmajor(a.W, wk, (int)D, (int)G, H, I, a.st);
+            e = launch_pack_kmajor(a.W, wk, (int)D, (int)G, H, I, bf16, a.st);
             if (e != cudaSuccess) return cuda_fail(e, "pack launch");
             launches += 1;
         }
     }
+    if (use_tc && bf16) {
+        e = launch_to_bf16(a.X, scratch + L.xb, M * I, a.st);
+        if (e != cudaSuccess) return cuda_fail(e, "bf16 conversion launch");
+        launches += 1;
+    }
     if (timed) record(pl, 1, a.st);
     if (use_tc)
-        e = launch_projection_tc(a.X, wk, xw, M, I, D * GH, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
+        e = launch_projection_tc(xin, wk, xw, M, I, D * GH, bf16, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
     else
         e = launch_projection(a.X, wt, xw, M, I, D * GH, exact, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
@@ -777,6 +788,7 @@ void rnn_plan_destroy(rnn_plan_t pl)
     if (pl->ctrl) cudaFree(pl->ctrl);
     if (pl->wt_const) cudaFree(pl->wt_const);
     if (pl->wk_const) cudaFree(pl->wk_const);
+    if (pl->wkb_const) cudaFree(pl->wkb_const);
     if (pl->rt_const) cudaFree(pl->rt_const);
     if (pl->r_orig_const) cudaFree(pl->r_orig_const);
     if (pl->lens_host) cudaFreeHost(pl->lens_host);
@@ -790,7 +802,7 @@ void rnn_plan_destroy(rnn_plan_t pl)
 rnn_status rnn_plan_set_mode(rnn_plan_t pl, int mode)
 {
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
-    if (mode != RNN_MODE_EXACT && mode != RNN_MODE_FAST && mode != RNN_MODE_FAST_TF32)
+    if (mode != RNN_MODE_EXACT && mode != RNN_MODE_FAST && mode != RNN_MODE_FAST_TF32 && mode != RNN_MODE_FAST_BF16)
         return fail(RNN_ERR_INVALID_ARGUMENT, "unknown mode %d", mode);
     pl->mode = mode;
     return RNN_OK;
@@ -932,6 +944,8 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
             if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(W pack)");
             e = cudaMalloc((void**)&pl->wk_const, sizeof(float) * (size_t)pl->I * pl->D * GH);
             if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(W K-major pack)");
+            e = cudaMalloc(&pl->wkb_const, 2 * (size_t)pl->I * pl->D * GH);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(W bf16 pack)");
         }
     }
     if (!pl->r_orig_const) {
@@ -942,7 +956,8 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
                                     cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return cuda_fail(e, "copying R");
     e = launch_pack(W, R, pl->wt_const, pl->rt_const, pl->D, pl->G, pl->H, pl->I, s);
-    if (e == cudaSuccess && pl->wk_const) e = launch_pack_kmajor(W, pl->wk_const, pl->D, pl->G, pl->H, pl->I, s);
+    if (e == cudaSuccess && pl->wk_const) e = launch_pack_kmajor(W, pl->wk_const, pl->D, pl->G, pl->H, pl->I, false, s);
+    if (e == cudaSuccess && pl->wkb_const) e = launch_pack_kmajor(W, pl->wkb_const, pl->D, pl->G, pl->H, pl->I, true, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     pl->const_weights = true;
     return RNN_OK;
@@ -1075,9 +1090,9 @@ rnn_status rnn_run_static_scratch(rnn_plan_t pl, int64_t S, int64_t N, const flo
 namespace rnngb {
 
 bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128)
+                       const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128, bool bf16)
 {
-    return tmap_encode_raw(map, base, rank, dims, strides, box, swizzle128) == CUDA_SUCCESS;
+    return tmap_encode_raw(map, base, rank, dims, strides, box, swizzle128, bf16) == CUDA_SUCCESS;
 }
 
 }  // namespace rnngb

@@ -127,21 +127,29 @@ cudaError_t launch_projection(const float* X, const float* Bt, float* XW, int64_
                               int64_t K, int64_t ncols, bool exact, int* status, long long limit_ns,
                               cudaStream_t stream);
 
-// Encodes a tiled fp32 tensor map (no swizzle, or 128-byte swizzle;
-// out-of-range reads as zero); false when the driver entry point is missing
-// or rejects the shape.
+// Encodes a tiled tensor map of fp32 (or bf16) elements (no swizzle, or
+// 128-byte swizzle; out-of-range reads as zero); false when the driver entry
+// point is missing or rejects the shape.
 bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128 = false);
+                       const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128 = false,
+                       bool bf16 = false);
 
-// Input projection on the tensor cores (TF32 products, FP32 sums):
-// XW[M][ncols] = X[M][K] . Wk[ncols][K]^T with Wk K-major (see launch_pack_kmajor).
-bool projection_tc_supported(const float* X, const float* Wk, float* XW, int64_t M, int64_t K, int64_t ncols);
-cudaError_t launch_projection_tc(const float* X, const float* Wk, float* XW, int64_t M, int64_t K, int64_t ncols,
-                                 int* status, long long limit_ns, cudaStream_t stream);
+// Input projection on the tensor cores (TF32 products of fp32 operands, or
+// bf16 operands; FP32 sums): XW[M][ncols] = X[M][K] . Wk[ncols][K]^T with Wk
+// K-major (see launch_pack_kmajor).  X and Wk are fp32, or bf16 when `bf16`.
+bool projection_tc_supported(const void* X, const void* Wk, float* XW, int64_t M, int64_t K, int64_t ncols,
+                             bool bf16);
+cudaError_t launch_projection_tc(const void* X, const void* Wk, float* XW, int64_t M, int64_t K, int64_t ncols,
+                                 bool bf16, int* status, long long limit_ns, cudaStream_t stream);
 
 // Wk[d*G*H + u*G + g][k] = W[d][g*H + u][k]: W's rows in the projection's
-// column order, K contiguous.
-cudaError_t launch_pack_kmajor(const float* W, float* Wk, int D, int G, int64_t H, int64_t I, cudaStream_t stream);
+// column order, K contiguous; written as fp32, or rounded to bf16 when
+// `bf16` (Wk then holds 2-byte elements).
+cudaError_t launch_pack_kmajor(const float* W, void* Wk, int D, int G, int64_t H, int64_t I, bool bf16,
+                               cudaStream_t stream);
+
+// dst[i] = src[i] rounded to bf16 (nearest even), n elements.
+cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t stream);
 
 // Pack: Wt[k][d*GH + u*G + g] = W[d][g*H + u][k]  (ld = D*GH),
 //       Rt[d][k][u*G + g]    = R[d][g*H + u][k].

@@ -14,7 +14,7 @@ from . import _build
 
 OPS = {"RNN": 0, "GRU": 1, "LSTM": 2}
 DIRECTIONS = {"forward": 0, "reverse": 1, "bidirectional": 2}
-MODES = {"exact": 0, "fast": 1, "tf32": 2}
+MODES = {"exact": 0, "fast": 1, "tf32": 2, "bf16": 3}
 ACT_NAMES = ["relu", "tanh", "sigmoid", "affine", "leakyrelu", "thresholdedrelu",
              "scaledtanh", "hardsigmoid", "elu", "softsign", "softplus"]
 STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARGUMENT", 2: "RNN_ERR_INVALID_INPUT",

@@ -284,42 +284,55 @@ def test_workload_full_size_fast(name, lbr, k):
     _workload_check(c, _sample_rows(c, min(k, 3)), "fast")
 
 
-# TF32 mode: the input projection on the tensor cores (tcgen05), within 5e-3
-# of the oracle.  Shapes cross the 128 x 128 tile and the 32-k block edges;
-# an input size that is not a multiple of 4 takes the FP32 projection.
-TF32_TOL = 5e-3
+# TF32 and BF16 modes: the input projection on the tensor cores (tcgen05),
+# within 5e-3 of the oracle.  Shapes cross the 128 x 128 tile and the k-block
+# edges; input sizes that are not multiples of 4 (TF32) or 8 (BF16) take the
+# FP32 projection.
+TC_TOL = 5e-3
+TC_SHAPES = {
+    "tf32": [("LSTM", "forward", 7, 19, 20, 40, 0), ("GRU", "bidirectional", 9, 15, 36, 44, 1),
+             ("RNN", "reverse", 11, 13, 260, 68, 0), ("LSTM", "bidirectional", 5, 29, 4, 36, 1),
+             ("GRU", "forward", 6, 23, 34, 32, 0), ("LSTM", "forward", 3, 50, 96, 136, 0)],
+    "bf16": [("LSTM", "forward", 7, 19, 24, 40, 0), ("GRU", "bidirectional", 9, 15, 40, 44, 1),
+             ("RNN", "reverse", 11, 13, 264, 68, 0), ("LSTM", "bidirectional", 5, 29, 8, 36, 1),
+             ("GRU", "forward", 6, 23, 36, 32, 0), ("LSTM", "forward", 3, 50, 136, 136, 0)],
+}
 
 
-@pytest.mark.parametrize("op,direction,seq,batch,inp,hid,layout", [
-    ("LSTM", "forward", 7, 19, 20, 40, 0), ("GRU", "bidirectional", 9, 15, 36, 44, 1),
-    ("RNN", "reverse", 11, 13, 260, 68, 0), ("LSTM", "bidirectional", 5, 29, 4, 36, 1),
-    ("GRU", "forward", 6, 23, 34, 32, 0), ("LSTM", "forward", 3, 50, 96, 136, 0)])
-def test_tf32_mode_within_tolerance(op, direction, seq, batch, inp, hid, layout):
+@pytest.mark.parametrize("mode,op,direction,seq,batch,inp,hid,layout",
+                         [(m,) + sh for m in ("tf32", "bf16") for sh in TC_SHAPES[m]])
+def test_tensor_core_modes_within_tolerance(mode, op, direction, seq, batch, inp, hid, layout):
+    # weights scaled like the workloads' (1/sqrt of the longer of hidden and
+    # input): bf16's 8-bit mantissas leave an error of about
+    # 2^-8 * sqrt(input) * |x| * |w| in the projection, which the 5e-3 bound
+    # covers at that scale
     c = make_case(op, direction, seq, batch, inp, hid, seed=41, layout=layout, with_P=True, h0_scale=0.5,
-                  c0_scale=0.5)
-    _compare_fast(gpu_case(c, "tf32"), oracle_case(c), TF32_TOL)
+                  c0_scale=0.5, w_scale=1.0 / np.sqrt(max(hid, inp)))
+    _compare_fast(gpu_case(c, mode), oracle_case(c), TC_TOL)
 
 
-def test_tf32_mode_differs_from_fp32_only_by_the_projection():
-    # a zero input projection (X = 0) leaves nothing for TF32 to round: TF32
-    # and FAST must then agree bit for bit
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+def test_tensor_core_modes_differ_from_fp32_only_by_the_projection(mode):
+    # a zero input projection (X = 0) leaves nothing to round: the tensor-core
+    # modes and FAST must then agree bit for bit
     c = make_case("LSTM", "forward", 5, 9, 24, 32, seed=3, with_P=True, h0_scale=0.5, c0_scale=0.5)
     c.X[...] = 0.0
-    for g, f in zip(gpu_case(c, "tf32"), gpu_case(c, "fast")):
+    for g, f in zip(gpu_case(c, mode), gpu_case(c, "fast")):
         if g is not None:
-            assert_bits_equal(g, f, "tf32 vs fast with X = 0")
+            assert_bits_equal(g, f, f"{mode} vs fast with X = 0")
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
 @pytest.mark.parametrize("name,lbr,k", [WORKLOAD_CASES[1], WORKLOAD_CASES[4]],
                          ids=[f"{w[0]}-lbr{w[1]}" for w in (WORKLOAD_CASES[1], WORKLOAD_CASES[4])])
-def test_workload_full_size_tf32(name, lbr, k):
+def test_workload_full_size_tensor_core_modes(name, lbr, k, mode):
     c = workload(name, lbr=lbr)
     rows = _sample_rows(c, min(k, 3))
-    got = gpu_case(c, "tf32")
+    got = gpu_case(c, mode)
     ref = oracle_case(c, rows=rows, threaded=True)
     _compare_fast(tuple(row_slice(c, rows, g, kind) for g, kind in zip(got, ("Y", "state", "state"))),
-                  tuple(row_slice(c, rows, r, kind) for r, kind in zip(ref, ("Y", "state", "state"))), TF32_TOL)
+                  tuple(row_slice(c, rows, r, kind) for r, kind in zip(ref, ("Y", "state", "state"))), TC_TOL)
 
 
 def test_rnn_workload_absent_and_zero_initial_state():
