@@ -8,7 +8,7 @@ batch 32, input 256, hidden 512, peepholes).  The metric is cell-steps per
 second (seq * batch * dirs per step), aggregated over ranks; each rank runs
 an independent replica (the operator has no exchange between GPUs).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--mode exact|fast]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--mode exact|fast|tf32|bf16]
                   [--workload NAME] [--impl ours|reference]
 
 The L2 (129 MB) is flushed between timed steps by writing a 256 MiB buffer
@@ -45,7 +45,7 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--lbr", type=int, default=0)
-    ap.add_argument("--mode", default="exact", choices=["exact", "fast"])
+    ap.add_argument("--mode", default="exact", choices=["exact", "fast", "tf32", "bf16"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     return ap.parse_args()
@@ -307,12 +307,23 @@ def run_ours(args, ws, rank, local):
                     "algorithmic_flops_per_launch": rec_flops,
                     "peak_note": f"{'no' if exact else 'fused'} multiply-add: {sms} SMs x 128 FP32 "
                                  f"lanes x {'1' if exact else '2'} FLOP x {clock_mhz:.0f} MHz (derived)"}
+        if kernel == "projection" and args.mode in ("tf32", "bf16"):
+            # tensor cores: the measured bf16 burst peak, scaled by the nominal
+            # TF32 : bf16 ratio (1.1 : 2.25 PFLOP/s dense) for TF32
+            bf16 = float(peaks.get("bf16_tflops", 1900.0))
+            peak = bf16 if args.mode == "bf16" else bf16 * 1.1 / 2.25
+            ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
+            return {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
+                    "frac": round(ach / peak, 4) if ms else 0.0,
+                    "traffic": profiled_traffic(kernel, args.workload, args.mode, digest),
+                    "kernel": "proj_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": proj_flops,
+                    "peak_note": "of measured bf16 burst" + ("" if args.mode == "bf16" else " x 1.1/2.25 (TF32)")}
         if kernel == "projection":
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
                     "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
                     "traffic": profiled_traffic(kernel, args.workload, args.mode, digest),
-                    "kernel": "proj_gemm_kernel", "avg_ms": round(ms, 5),
+                    "kernel": "proj_tma_kernel", "avg_ms": round(ms, 5),
                     "algorithmic_flops_per_launch": proj_flops}
         return {"kernel": kernel, "avg_ms": round(ms, 5)}
 
@@ -320,7 +331,10 @@ def run_ours(args, ws, rank, local):
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, see synth.py)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"exact": "f32", "fast": "f32", "tf32": "f32 (tf32 projection)",
+                  "bf16": "f32 (bf16 projection)"}[args.mode],
+        "data": "synthetic (seeded, see synth.py)",
         "config": {"workload": args.workload, "description": WORKLOADS.get(args.workload, ""),
                    "op": case.op, "direction": case.direction, "seq": case.seq,
                    "batch": case.batch, "input": case.input_size, "hidden": case.hidden_size,
