@@ -9,9 +9,10 @@
 //     tcgen05.mma kind::f16 with both A and B bf16, K 16 per instruction.
 // Either way a k-block is 128 bytes of every row (32 fp32 or 64 bf16).
 //
-// One CTA per 128 x 128 output tile, 128 threads:
+// One CTA per 128 x 128 output tile, 128 threads, two CTAs per SM (so one
+// tile's read-out overlaps the other's MMAs):
 //   * warp 0, one lane: tensor copies (TMA) of the A tile [128 rows][k-block]
-//     and the Wk tile [128 cols][k-block] of each k-block into a 4-stage
+//     and the Wk tile [128 cols][k-block] of each k-block into a 3-stage
 //     ring, both with 128-byte swizzle (the layout the MMA descriptors
 //     describe);
 //   * warp 1, one lane: per k-block four tcgen05.mma (M 128, N 128)
@@ -34,7 +35,7 @@ namespace rnngb {
 
 namespace {
 
-constexpr int TC_BM = 128, TC_BN = 128, TC_ROWB = 128, TC_ST = 4;   // TC_ROWB: bytes of a row per k-block
+constexpr int TC_BM = 128, TC_BN = 128, TC_ROWB = 128, TC_ST = 3;   // TC_ROWB: bytes of a row per k-block
 constexpr unsigned kTcTileA = TC_BM * TC_ROWB, kTcTileB = TC_BN * TC_ROWB;   // 16 KB each
 constexpr unsigned kTcStage = kTcTileA + kTcTileB;
 constexpr size_t kTcSmem = (size_t)TC_ST * kTcStage + 1024;   // + alignment slack (1024 for the swizzle)
@@ -131,7 +132,7 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, unsigned parity, long lon
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(128, 1) proj_tc_kernel(const __grid_constant__ TcArgs a)
+__global__ void __launch_bounds__(128, 2) proj_tc_kernel(const __grid_constant__ TcArgs a)
 {
     constexpr int BKE = BF16 ? 64 : 32;   // elements of a row per k-block
     extern __shared__ __align__(1024) unsigned char tc_smem[];
