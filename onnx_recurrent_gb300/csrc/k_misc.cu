@@ -7,7 +7,10 @@
 //               are zeros: Choices the specification leaves open);
 //   mask_tail   Y = 0 at the steps no row reaches (sequence_lens: Y is zero
 //               at t >= len).
+#include <type_traits>
+
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "rnn_internal.h"
 
@@ -119,6 +122,7 @@ __global__ void pack_kmajor_kernel(const float* __restrict__ W, T* __restrict__ 
         T* dst = Wk + r * I;
         for (int64_t k = threadIdx.x; k < I; k += blockDim.x) {
             if constexpr (sizeof(T) == 4) dst[k] = src[k];
+            else if constexpr (std::is_same<T, __half>::value) dst[k] = __float2half_rn(src[k]);
             else dst[k] = __float2bfloat16_rn(src[k]);
         }
     }
@@ -132,13 +136,14 @@ __global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __r
 
 }  // namespace
 
-cudaError_t launch_pack_kmajor(const float* W, void* Wk, int D, int G, int64_t H, int64_t I, bool bf16,
+cudaError_t launch_pack_kmajor(const float* W, void* Wk, int D, int G, int64_t H, int64_t I, int dtype,
                                cudaStream_t stream)
 {
     const int64_t rows = (int64_t)D * G * H;
     if (rows <= 0 || I <= 0) return cudaSuccess;
     const unsigned blocks = (unsigned)std::min<int64_t>(rows, 8192);
-    if (bf16) pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (__nv_bfloat16*)Wk, G, H, I, rows);
+    if (dtype == 1) pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (__nv_bfloat16*)Wk, G, H, I, rows);
+    else if (dtype == 2) pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (__half*)Wk, G, H, I, rows);
     else pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (float*)Wk, G, H, I, rows);
     return cudaGetLastError();
 }
@@ -168,6 +173,38 @@ cudaError_t launch_pack(const float* W, const float* R, float* Wt, float* Rt, in
                                                     GH, 0);
         }
     }
+    return cudaGetLastError();
+}
+
+namespace {
+
+// Tensor-core kernel: hx[b][d][r][u] (fp16, 128 rows) = initial_h for b = 0
+// and r < N, else 0; step counters 0.
+__global__ void tc_state_init_kernel(const RecParams p)
+{
+    __half* hx = reinterpret_cast<__half*>(p.hbuf);
+    const int64_t total = (int64_t)2 * p.D * 128 * p.H;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t u = i % p.H, r = (i / p.H) % 128, d = (i / ((int64_t)p.H * 128)) % p.D;
+        const int64_t b = i / ((int64_t)p.H * 128 * p.D);
+        float v = 0.0f;
+        if (b == 0 && r < p.N && p.h0) {
+            const int64_t si = p.layout == 0 ? (d * p.N + r) * p.H + u : (r * p.D + d) * p.H + u;
+            v = p.h0[si];
+        }
+        hx[i] = __float2half_rn(v);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < p.D) p.bar[threadIdx.x] = 0u;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_state_init(const RecParams& p, cudaStream_t stream)
+{
+    const int64_t total = (int64_t)2 * p.D * 128 * p.H;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, 4096));
+    tc_state_init_kernel<<<blocks, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

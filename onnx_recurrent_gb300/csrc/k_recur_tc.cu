@@ -1,0 +1,424 @@
+// Persistent recurrent kernel on the tensor cores (the TF32 and BF16 modes,
+// batches of up to 128 rows).
+//
+// Page "Recurrent operators: RNN, GRU, LSTM", Computation: per step the
+// recurrent product Rec = H . R^T, then the gate arithmetic per batch row in
+// the written order (Fast mode: the product's order and rounding are free).
+// Here the product runs on the tensor cores with fp16 operands (h and R
+// rounded to nearest: 10-bit mantissas, as TF32) and FP32 sums.  The kernel
+// is used only when every h it produces is bounded (see the planner), so h
+// always fits fp16's range.
+//
+// One cooperative launch, one CTA per SM; CTA c of direction d owns hidden
+// units [u0, u0 + U) and their G gate columns (column ul*G + g, padded to NP,
+// a multiple of 16), for all batch rows (padded to 128: the MMA's M).
+//   * its slice of R (fp16, K-major, NP rows x H) is loaded once into shared
+//     memory by tensor copies (128-byte swizzle, one box per 64-k block) and
+//     stays there as the MMA's B operand;
+//   * warp 4 (one lane) waits each step for every CTA of the direction to
+//     have published the step (a release-add / acquire-poll counter), then
+//     moves h (fp16 [128 rows][H], the exchange buffer) through a 4-stage
+//     ring of 64-k blocks with tensor copies;
+//   * warp 5 (one lane) issues four tcgen05.mma (kind::f16, M 128, N NP,
+//     K 16) per block into tensor memory, commits each ring slot back to the
+//     producer and, after the last block, the accumulators to the epilogue;
+//   * warps 0-3 are the epilogue: thread t owns batch row t (tensor-memory
+//     lane t), reads its NP accumulators, adds XW and the biases, runs the
+//     gate arithmetic (FMA-based fast functions) with its cell state kept in
+//     registers, writes Y and its h (fp32 kept, fp16 to the exchange
+//     buffer), and the CTA publishes.
+// Every wait is bounded; on a failure the CTA records RNN_ERR_TIMEOUT and
+// its roles leave at the next uniform point, waiting (bounded) for their
+// copies and MMAs in flight before the tensor memory is freed.
+#include <cstdint>
+#include <type_traits>
+
+#include <cuda_fp16.h>
+
+#include "k_recur.cuh"
+#include "tma.cuh"
+
+namespace rnngb {
+
+namespace {
+
+constexpr int TR_M = 128;                       // MMA rows (batch rows, padded)
+constexpr int TR_KB = 64;                       // fp16 k per block (128-byte rows)
+constexpr int TR_ST = 4;                        // h ring stages
+constexpr unsigned kTrHStage = TR_M * 128;      // one h block: 16 KB
+constexpr int TR_NPMAX = 64;                    // most gate columns per CTA
+constexpr int TR_THREADS = 192;
+
+__device__ __forceinline__ uint64_t tr_sdesc(unsigned saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);    // start address
+    d |= (uint64_t)1u << 16;                     // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024u >> 4) << 32;           // stride byte offset: next 8-row group
+    d |= (uint64_t)1u << 46;                     // descriptor version
+    d |= (uint64_t)2u << 61;                     // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void tr_mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tr_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tr_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tr_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tr_bar(int id, int threads) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory"); }
+
+// Columns J .. J+15 of this thread's tensor-memory lane into acc[J .. J+15].
+template <int J>
+__device__ __forceinline__ void tr_ld16(uint32_t taddr, float (&acc)[TR_NPMAX])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[J + i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tr_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Bounded wait on an mbarrier phase; gives up when the limit passes, the CTA
+// is aborting, or another CTA reported a failure.
+__device__ __forceinline__ bool tr_wait(uint64_t* bar, unsigned parity, const RecParams& p, volatile int* abort_flag)
+{
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned it = 0;
+    while (!mbar_test(bar, parity)) {
+        if ((++it & 255u) == 0u) {
+            if (abort_flag && *abort_flag) return false;
+            if (ld_relaxed_s32(p.status) != 0) return false;
+            if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tr_fail(const RecParams& p, volatile int* abort_flag)
+{
+    atomicCAS(p.status, 0, 6 /* RNN_ERR_TIMEOUT */);
+    *abort_flag = 1;
+}
+
+template <int OP>
+__global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_constant__ RecParams p)
+{
+    constexpr int G = OP == 0 ? 1 : (OP == 1 ? 3 : 4);
+    constexpr int UMAX = TR_NPMAX / G;
+    extern __shared__ __align__(1024) unsigned char tr_smem[];
+    __shared__ __align__(8) uint64_t full[TR_ST], empty[TR_ST], r_ready, acc_ready, acc_free, mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_abort;
+    __shared__ float s_wb[TR_NPMAX], s_rb[TR_NPMAX], s_p[3][UMAX];
+
+    unsigned char* base = tr_smem + ((1024u - (smem_addr(tr_smem) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = p.ctas_per_dir;
+    const int d = blockIdx.x / C, c = blockIdx.x - d * C;
+    const int H = p.H, GH = G * H;
+    const int u0 = (int)(((long long)c * H) / C);
+    const int U = (int)(((long long)(c + 1) * H) / C) - u0;
+    const int NP = p.npad;                                  // padded gate columns (MMA N)
+    const int nkb = (H + TR_KB - 1) / TR_KB;
+    unsigned char* rsm = base;                              // R slice: nkb blocks of [NP rows][128 B]
+    unsigned char* hring = base + (size_t)nkb * NP * 128;   // TR_ST blocks of [128 rows][128 B]
+    const bool rev = p.dir_reverse[d] != 0;
+    unsigned* counter = p.bar + d;
+    const uint32_t idesc = (1u << 4) | ((uint32_t)(NP >> 3) << 17) | ((uint32_t)(TR_M >> 4) << 24);
+    int tmem_cols = 32;
+    while (tmem_cols < NP) tmem_cols *= 2;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < TR_ST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(&r_ready, 1);
+        mbar_init(&acc_ready, 1);
+        mbar_init(&acc_free, 4);   // one arrival per epilogue warp
+        mbar_init(&mma_done, 1);
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    // biases and peepholes of the CTA's columns (zero where absent)
+    for (int j = threadIdx.x; j < TR_NPMAX; j += blockDim.x) {
+        const int ul = j / G, g = j - ul * G;
+        const bool in = ul < U;
+        s_wb[j] = (in && p.has_B) ? p.B[(size_t)d * 2 * GH + (size_t)g * H + u0 + ul] : 0.f;
+        s_rb[j] = (in && p.has_B) ? p.B[(size_t)d * 2 * GH + GH + (size_t)g * H + u0 + ul] : 0.f;
+    }
+    for (int j = threadIdx.x; j < 3 * UMAX; j += blockDim.x) {
+        const int k = j / UMAX, ul = j - k * UMAX;
+        s_p[k][ul] = (OP == 2 && p.has_P && ul < U) ? p.P[(size_t)d * 3 * H + (size_t)k * H + u0 + ul] : 0.f;
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
+                     "r"(tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tr_fence_before();
+    __syncthreads();
+    tr_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&r_ready, (unsigned)(nkb * NP * 128));
+            for (int kb = 0; kb < nkb; ++kb)
+                tma_load_2d(rsm + (size_t)kb * NP * 128, &p.rmap, kb * TR_KB, d * GH + u0 * G, &r_ready);
+            unsigned q = 0;
+            bool ok = true;
+            for (int s = 0; s < p.max_len && ok; ++s) {
+                if (s > 0) {
+                    const unsigned need = (unsigned)s * (unsigned)C;
+                    const unsigned long long t0 = globaltimer_ns();
+                    unsigned it = 0;
+                    while (ld_acquire_u32(counter) < need) {
+                        if ((++it & 63u) == 0u) {
+                            if (s_abort || ld_relaxed_s32(p.status) != 0) { ok = false; break; }
+                            if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) {
+                                tr_fail(p, &s_abort);
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
+                    if (!ok) break;
+                    fence_proxy_async_global();
+                }
+                const int z = (s & 1) * p.D + d;
+                for (int kb = 0; kb < nkb; ++kb, ++q) {
+                    const int slot = (int)(q % TR_ST);
+                    if (q >= TR_ST && !tr_wait(&empty[slot], ((q / TR_ST) - 1u) & 1u, p, &s_abort)) {
+                        tr_fail(p, &s_abort);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[slot], kTrHStage);
+                    tma_load_3d(hring + (size_t)slot * kTrHStage, &p.hmap, kb * TR_KB, 0, z, &full[slot]);
+                }
+            }
+            // copies still in flight land before the CTA can leave
+            (void)tr_wait(&r_ready, 0u, p, nullptr);
+            for (unsigned k = (q > TR_ST ? q - TR_ST : 0u); k < q; ++k)
+                (void)tr_wait(&full[k % TR_ST], (k / TR_ST) & 1u, p, nullptr);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = tr_wait(&r_ready, 0u, p, &s_abort);
+            if (!ok) tr_fail(p, &s_abort);
+            unsigned q = 0;
+            for (int s = 0; s < p.max_len && ok; ++s) {
+                if (s > 0 && !tr_wait(&acc_free, (unsigned)(s - 1) & 1u, p, &s_abort)) {
+                    tr_fail(p, &s_abort);
+                    break;
+                }
+                tr_fence_after();
+                for (int kb = 0; kb < nkb; ++kb, ++q) {
+                    const int slot = (int)(q % TR_ST);
+                    if (!tr_wait(&full[slot], (q / TR_ST) & 1u, p, &s_abort)) {
+                        tr_fail(p, &s_abort);
+                        ok = false;
+                        break;
+                    }
+                    tr_fence_after();
+                    const unsigned sa = smem_addr(hring + (size_t)slot * kTrHStage);
+                    const unsigned sb = smem_addr(rsm + (size_t)kb * NP * 128);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)   // K 16 per MMA = 32 bytes along the swizzled rows
+                        tr_mma_f16(tmem, tr_sdesc(sa + 32u * j), tr_sdesc(sb + 32u * j), idesc,
+                                   (kb > 0 || j > 0) ? 1u : 0u);
+                    tr_commit(&empty[slot]);
+                }
+                if (!ok) break;
+                tr_commit(&acc_ready);
+            }
+            // completes once every MMA issued above has: waited for before the
+            // tensor memory is freed
+            tr_commit(&mma_done);
+            (void)tr_wait(&mma_done, 0u, p, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int n = warp * 32 + lane;                      // batch row = tensor-memory lane
+        const bool row = n < p.N;
+        const int len = row ? (p.has_lens ? p.lens[n] : p.S) : 0;
+        const ActSpec fA = p.act[d][0], gA = p.act[d][1], hA = p.act[d][2];
+        float hown[UMAX], cown[UMAX];
+#pragma unroll
+        for (int ul = 0; ul < UMAX; ++ul) {
+            hown[ul] = (row && ul < U && p.has_h0) ? p.h0[s_index(p, d, n, u0 + ul)] : 0.f;
+            cown[ul] = (row && ul < U && OP == 2 && p.has_c0) ? p.c0[s_index(p, d, n, u0 + ul)] : 0.f;
+        }
+        const size_t xw_ld = (size_t)p.D * GH;
+        const size_t xw_col = (size_t)d * GH + (size_t)u0 * G;
+        __half* hx = reinterpret_cast<__half*>(p.hbuf);
+        const bool skip_first = p.debug_skip_cta == (int)blockIdx.x;
+        bool alive = true;
+        for (int s = 0; s < p.max_len; ++s) {
+            // this step's XW row (independent of the product: loaded first)
+            float xw[TR_NPMAX];
+            const bool live = row && s < len;
+            const int t = live ? (rev ? len - 1 - s : s) : 0;
+            if (live) {
+                const size_t xrow = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
+                const float* src = p.XW + xrow * xw_ld + xw_col;
+#pragma unroll
+                for (int j = 0; j < TR_NPMAX; ++j) xw[j] = j < U * G ? __ldg(src + j) : 0.f;
+            }
+            // accumulators (warp-collective loads: the decision is warp-uniform)
+            const bool got = __all_sync(0xffffffffu, alive && tr_wait(&acc_ready, (unsigned)s & 1u, p, &s_abort));
+            float acc[TR_NPMAX];
+            if (got) {
+                tr_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+                tr_ld16<0>(taddr, acc);
+                if (NP > 16) tr_ld16<16>(taddr + 16u, acc);
+                if (NP > 32) tr_ld16<32>(taddr + 32u, acc);
+                if (NP > 48) tr_ld16<48>(taddr + 48u, acc);
+                tr_ld_wait();
+                tr_fence_before();
+            } else if (alive && lane == 0) {
+                tr_fail(p, &s_abort);
+            }
+            __syncwarp();
+            if (lane == 0 && got) mbar_arrive(&acc_free);
+            if (got && live) {
+#pragma unroll
+                for (int ul = 0; ul < UMAX; ++ul) {
+                    if (ul >= U) break;
+                    float pre[G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const int j = ul * G + g;
+                        pre[g] = (xw[j] + acc[j]) + s_wb[j] + s_rb[j];
+                    }
+                    float hn;
+                    if constexpr (OP == 0) {
+                        hn = act<false>(fA, clipv(p, pre[0]));
+                    } else if constexpr (OP == 1) {
+                        const float z = act<false>(fA, clipv(p, pre[0]));
+                        const float r = act<false>(fA, clipv(p, pre[1]));
+                        const int j = ul * G + 2;
+                        const float ph = p.has_B ? (xw[j] + r * (acc[j] + s_rb[j])) + s_wb[j] : xw[j] + r * acc[j];
+                        const float ht = act<false>(gA, clipv(p, ph));
+                        hn = (1.0f - z) * ht + z * hown[ul];
+                    } else {
+                        float pi = pre[0], po = pre[1], pf = pre[2];
+                        const float pc = pre[3];
+                        if (p.has_P) {
+                            pi += s_p[0][ul] * cown[ul];
+                            pf += s_p[2][ul] * cown[ul];
+                        }
+                        const float ig = act<false>(fA, clipv(p, pi));
+                        const float fg = p.input_forget ? 1.0f - ig : act<false>(fA, clipv(p, pf));
+                        const float ct = act<false>(gA, clipv(p, pc));
+                        const float cn = fg * cown[ul] + ig * ct;
+                        if (p.has_P) po += s_p[1][ul] * cn;
+                        const float og = act<false>(fA, clipv(p, po));
+                        hn = og * act<false>(hA, cn);
+                        cown[ul] = cn;
+                    }
+                    hown[ul] = hn;
+                    if (p.Y) p.Y[y_index(p, t, d, n, u0 + ul)] = canon_nan(hn);
+                }
+            } else if (got && row && p.Y) {
+                for (int ul = 0; ul < U; ++ul) p.Y[y_index(p, s, d, n, u0 + ul)] = 0.f;
+            }
+            if (got && row) {
+                __half* dst = hx + (((size_t)((s + 1) & 1) * p.D + d) * TR_M + n) * H + u0;
+#pragma unroll
+                for (int ul = 0; ul < UMAX; ++ul)
+                    if (ul < U) dst[ul] = __float2half_rn(hown[ul]);
+            }
+            // publish: every epilogue thread's h is written; leave together on a failure
+            tr_bar(1, 128);
+            const bool abort_now = s_abort != 0 || !got;
+            tr_bar(1, 128);
+            if (abort_now) {
+                alive = false;
+                break;
+            }
+            if (threadIdx.x == 0 && !(skip_first && s == 0)) {
+                fence_proxy_async_global();
+                red_release_add_u32(counter, 1u);
+            }
+        }
+        if (alive && row) {
+#pragma unroll
+            for (int ul = 0; ul < UMAX; ++ul) {
+                if (ul >= U) break;
+                const size_t si = s_index(p, d, n, u0 + ul);
+                if (p.Yh) p.Yh[si] = len > 0 ? canon_nan(hown[ul]) : 0.f;
+                if (OP == 2 && p.Yc) p.Yc[si] = len > 0 ? canon_nan(cown[ul]) : 0.f;
+            }
+        }
+    }
+
+    tr_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tr_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
+    }
+}
+
+template <int OP>
+const void* tc_kernel_ptr()
+{
+    return (const void*)rnn_tc_kernel<OP>;
+}
+
+}  // namespace
+
+size_t tc_recurrent_smem(int H, int npad) { return 1024 + (size_t)((H + TR_KB - 1) / TR_KB) * npad * 128 + (size_t)TR_ST * kTrHStage; }
+
+int tc_recurrent_threads() { return TR_THREADS; }
+
+int tc_recurrent_max_columns() { return TR_NPMAX; }
+
+cudaError_t tc_recurrent_occupancy(int op, size_t smem, int* blocks)
+{
+    const void* fn = op == 0 ? tc_kernel_ptr<0>() : (op == 1 ? tc_kernel_ptr<1>() : tc_kernel_ptr<2>());
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, TR_THREADS, smem);
+}
+
+cudaError_t launch_tc_recurrent(const RecParams& p, size_t smem, cudaStream_t stream)
+{
+    const void* fn = p.op == 0 ? tc_kernel_ptr<0>() : (p.op == 1 ? tc_kernel_ptr<1>() : tc_kernel_ptr<2>());
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    void* args[] = {(void*)&p};
+    return cudaLaunchCooperativeKernel(fn, dim3(p.D * p.ctas_per_dir), dim3(TR_THREADS), args, smem, stream);
+}
+
+}  // namespace rnngb

@@ -123,6 +123,7 @@ struct rnn_plan {
     float* wt_const = nullptr;   // [I][D*G*H]
     float* wk_const = nullptr;   // [D*G*H][I] (the tensor-core projection's operand)
     void* wkb_const = nullptr;   // the same rounded to bf16
+    void* rp16_const = nullptr;  // R [D*G*H][H] in the projection's column order, fp16 (tensor-core recurrence)
     float* rt_const = nullptr;   // [D][H][G*H]
     float* r_orig_const = nullptr;   // R as given, [D][G*H][H] (the dataflow kernel reads this layout)
 
@@ -359,10 +360,72 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
     return RNN_OK;
 }
 
+// The tensor-core recurrent kernel keeps h in fp16: it is used only when
+// every h the operator produces is bounded, i.e. the activation that makes h
+// is one of Tanh, Sigmoid, ScaledTanh, HardSigmoid, Softsign (and, for GRU,
+// the update gate z is in [0, 1]: Sigmoid or HardSigmoid).
+bool tc_bounded_h(const rnn_plan* pl)
+{
+    auto bounded = [](int fn) { return fn == 1 || fn == 2 || fn == 6 || fn == 7 || fn == 9; };
+    for (int d = 0; d < pl->D; ++d) {
+        const int f = pl->act[d][0].fn, g = pl->act[d][1].fn, h = pl->act[d][2].fn;
+        if (pl->op == RNN_OP_RNN && !bounded(f)) return false;
+        if (pl->op == RNN_OP_GRU && !((f == 2 || f == 7) && bounded(g))) return false;
+        if (pl->op == RNN_OP_LSTM && !(bounded(f) && bounded(h))) return false;
+    }
+    return true;
+}
+
+rnn_status plan_tc(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out)
+{
+    const int64_t H = pl->H;
+    const int G = pl->G, D = pl->D;
+    if (N > 128) return fail(RNN_ERR_UNSUPPORTED, "the tensor-core kernel takes at most 128 batch rows");
+    if (H % 8 != 0) return fail(RNN_ERR_UNSUPPORTED, "the tensor-core kernel needs hidden_size a multiple of 8");
+    if (pl->op == RNN_OP_GRU && pl->lbr == 0)
+        return fail(RNN_ERR_UNSUPPORTED, "the tensor-core kernel has no linear_before_reset = 0 path");
+    if (!tc_bounded_h(pl)) return fail(RNN_ERR_UNSUPPORTED, "the tensor-core kernel needs bounded h activations");
+    int64_t C = std::min<int64_t>(di.sms / D, H);
+    if (pl->ov_units > 0) C = std::min<int64_t>(pl->ov_units, H);
+    if (C < 1) return fail(RNN_ERR_UNSUPPORTED, "no SM for the tensor-core kernel");
+    const int64_t U = ceil_div(H, C);
+    C = ceil_div(H, U);
+    const int NP = (int)round_up(U * G, 16);
+    if (NP > tc_recurrent_max_columns())
+        return fail(RNN_ERR_UNSUPPORTED, "hidden_size %lld is too large for the tensor-core kernel", (long long)H);
+    const size_t smem = tc_recurrent_smem((int)H, NP);
+    if (smem > (size_t)di.smem_optin - 2048) return fail(RNN_ERR_UNSUPPORTED, "tensor-core kernel: shared memory");
+    int blocks = 0;
+    cudaError_t e = tc_recurrent_occupancy(pl->op, smem, &blocks);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (blocks < 1 || (int64_t)D * C > (int64_t)blocks * di.sms)
+        return fail(RNN_ERR_UNSUPPORTED, "tensor-core kernel: the grid does not fit");
+    *out = Geometry{};
+    out->kernel = 3;
+    out->units = (int)C;
+    out->rows = 1;
+    out->ctas = (int)C;
+    out->quant = 1;
+    out->umax = (int)U;
+    out->tn = 1;
+    out->threads = tc_recurrent_threads();
+    out->rres = 1;
+    out->smem = smem;
+    out->npad = NP;
+    return RNN_OK;
+}
+
 // Launch geometry of the recurrent kernel for batch N.
 rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, const float* R, Geometry* g)
 {
     if (pl->ov_kernel == 1) return plan_staged(pl, N, di, g);
+    if (pl->ov_kernel == 3) return plan_tc(pl, N, di, g);
+    // tensor-core modes: the tensor-core kernel for batches of 48..128 rows
+    if ((pl->mode == RNN_MODE_FAST_TF32 || pl->mode == RNN_MODE_FAST_BF16) && pl->ov_kernel == 0 && N >= 48) {
+        const std::string saved = g_error;
+        if (plan_tc(pl, N, di, g) == RNN_OK) return RNN_OK;
+        g_error = saved;
+    }
     // the dataflow kernel reads R (as given) with TMA: 16-byte aligned base
     const float* rsrc = pl->const_weights ? pl->r_orig_const : R;
     if ((uintptr_t)rsrc % 16 != 0) {
@@ -477,12 +540,15 @@ TmapEncodeFn tmap_encoder()
 
 CUresult tmap_encode_raw(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
                          const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128 = false,
-                         bool bf16 = false)
+                         int dtype = 0)
 {
     const TmapEncodeFn fn = tmap_encoder();
     if (!fn) return CUDA_ERROR_NOT_FOUND;
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
+    const CUtensorMapDataType dt = dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dtype == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return fn(map, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box,
               es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -552,7 +618,7 @@ rnn_status check_lengths(const int32_t* host, int64_t N, int64_t S, int64_t* max
 }
 
 struct Layout {
-    size_t wt, rt, xw, xb, hb, rh, total;
+    size_t wt, rt, rp, xw, xb, hb, rh, total;
     bool need_rh;
 };
 
@@ -563,11 +629,13 @@ Layout scratch_layout(const rnn_plan* pl, const Geometry& geo, int64_t S, int64_
     Layout L;
     size_t off = base;
     L.wt = off; off += pl->const_weights ? 0 : align256(sizeof(float) * (size_t)I * D * GH);
-    L.rt = off; off += (pl->const_weights || geo.kernel == 2) ? 0 : align256(sizeof(float) * (size_t)D * H * GH);
+    L.rt = off; off += (pl->const_weights || geo.kernel != 1) ? 0 : align256(sizeof(float) * (size_t)D * H * GH);
+    L.rp = off; off += (pl->const_weights || geo.kernel != 3) ? 0 : align256((size_t)2 * D * GH * H);   // R fp16
     L.xw = off; off += align256(sizeof(float) * (size_t)S * N * D * GH);
     L.xb = off; off += pl->mode == RNN_MODE_FAST_BF16 ? align256((size_t)2 * S * N * I) : 0;   // X as bf16
     const size_t row = geo.kernel == 2 ? (size_t)geo.hpad / kRecKC * kDfPitch : (size_t)H;
-    const size_t hbuf = sizeof(float) * (size_t)D * 2 * geo.rows * geo.npad * row;
+    const size_t hbuf = geo.kernel == 3 ? (size_t)2 * 2 * D * 128 * H   // fp16 [2][D][128][H]
+                                        : sizeof(float) * (size_t)D * 2 * geo.rows * geo.npad * row;
     L.hb = off; off += align256(hbuf);
     L.need_rh = pl->op == RNN_OP_GRU && pl->lbr == 0;
     L.rh = off; off += L.need_rh ? align256(hbuf) : 0;
@@ -599,7 +667,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     cudaError_t e;
     if (timed) record(pl, 0, a.st);
     if (!pl->const_weights) {
-        const bool pack_r = geo.kernel != 2;   // the dataflow kernel reads R as given
+        const bool pack_r = geo.kernel == 1;   // the dataflow kernel reads R as given, the tensor-core one fp16
         e = launch_pack(use_tc ? nullptr : a.W, pack_r ? a.R : nullptr, wt, pack_r ? rt : nullptr, (int)D, (int)G, H,
                         I, a.st);
         if (e != cudaSuccess) return cuda_fail(e, "pack launch");
@@ -609,6 +677,11 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
             if (e != cudaSuccess) return cuda_fail(e, "pack launch");
             launches += 1;
         }
+    }
+    if (geo.kernel == 3 && !pl->const_weights) {
+        e = launch_pack_kmajor(a.R, scratch + L.rp, (int)D, (int)G, H, H, 2, a.st);
+        if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+        launches += 1;
     }
     if (use_tc && bf16) {
         e = launch_to_bf16(a.X, scratch + L.xb, M * I, a.st);
@@ -651,6 +724,21 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     p.flags = (unsigned*)(ctrl + kCtrlFlagsOffset);
     p.spin_limit_ns = spin_ns;
     p.debug_skip_cta = skip_cta;
+    if (geo.kernel == 3) {
+        // h exchange buffer fp16 [2 buffers][D][128 rows][H]: box 64 k x 128 rows x 1;
+        // R fp16 [D*G*H columns][H]: box 64 k x npad columns; both 128-byte swizzled
+        const void* rp = pl->const_weights ? pl->rp16_const : (const void*)(scratch + L.rp);
+        const cuuint64_t hdims[3] = {(cuuint64_t)H, 128, (cuuint64_t)(2 * D)};
+        const cuuint64_t hstrides[2] = {(cuuint64_t)H * 2, (cuuint64_t)H * 2 * 128};
+        const cuuint32_t hbox[3] = {64, 128, 1};
+        const cuuint64_t rdims[2] = {(cuuint64_t)H, (cuuint64_t)(D * GH)};
+        const cuuint64_t rstrides[1] = {(cuuint64_t)H * 2};
+        const cuuint32_t rbox[2] = {64, (cuuint32_t)geo.npad};
+        if (!encode_tensor_map(&p.hmap, p.hbuf, 3, hdims, hstrides, hbox, true, 2) ||
+            !encode_tensor_map(&p.rmap, rp, 2, rdims, rstrides, rbox, true, 2))
+            return fail(RNN_ERR_CUDA, "tensor map for the tensor-core kernel");
+        p.rhmap = p.hmap;   // unused
+    }
     if (geo.kernel == 2) {
         // h / r (.) h exchange buffers [D*2*CR blocks][hpad/32 chunks][npad rows][36],
         // box 36 x npad x cpb x 1 (one piece of one row group, contiguous)
@@ -675,11 +763,11 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         }
     }
 
-    e = launch_state_init(p, a.st);
+    e = geo.kernel == 3 ? launch_tc_state_init(p, a.st) : launch_state_init(p, a.st);
     if (e != cudaSuccess) return cuda_fail(e, "state set-up launch");
     launches += 1;
     if (timed) record(pl, 3, a.st);
-    e = launch_recurrent(p, exact, geo.threads, geo.smem, a.st);
+    e = geo.kernel == 3 ? launch_tc_recurrent(p, geo.smem, a.st) : launch_recurrent(p, exact, geo.threads, geo.smem, a.st);
     if (e != cudaSuccess) return cuda_fail(e, "recurrent launch");
     launches += 1;
     if (timed) record(pl, 4, a.st);
@@ -789,6 +877,7 @@ void rnn_plan_destroy(rnn_plan_t pl)
     if (pl->wt_const) cudaFree(pl->wt_const);
     if (pl->wk_const) cudaFree(pl->wk_const);
     if (pl->wkb_const) cudaFree(pl->wkb_const);
+    if (pl->rp16_const) cudaFree(pl->rp16_const);
     if (pl->rt_const) cudaFree(pl->rt_const);
     if (pl->r_orig_const) cudaFree(pl->r_orig_const);
     if (pl->lens_host) cudaFreeHost(pl->lens_host);
@@ -824,8 +913,10 @@ rnn_status rnn_plan_set_launch(rnn_plan_t pl, int unit_groups, int rows_per_thre
 {
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
     if (unit_groups < 0 || rows_per_thread < 0 || r_resident < -1 || r_resident > 1 || row_groups < 0 ||
-        kernel < 0 || kernel > 2)
+        kernel < 0 || kernel > 3)
         return fail(RNN_ERR_INVALID_ARGUMENT, "bad launch override");
+    if (kernel == 3 && (row_groups > 1 || rows_per_thread > 1))
+        return fail(RNN_ERR_INVALID_ARGUMENT, "the tensor-core kernel has one row group and one row per thread");
     if (rows_per_thread != 0 && rows_per_thread != 1 && rows_per_thread != 2 && rows_per_thread != 4 &&
         rows_per_thread != 8)
         return fail(RNN_ERR_INVALID_ARGUMENT, "rows_per_thread must be 0, 1, 2, 4 or 8");
@@ -951,6 +1042,8 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
     if (!pl->r_orig_const) {
         cudaError_t e = cudaMalloc((void**)&pl->r_orig_const, sizeof(float) * (size_t)pl->D * GH * pl->H);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(R copy)");
+        e = cudaMalloc(&pl->rp16_const, 2 * (size_t)pl->D * GH * pl->H);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(R fp16 pack)");
     }
     cudaError_t e = cudaMemcpyAsync(pl->r_orig_const, R, sizeof(float) * (size_t)pl->D * GH * pl->H,
                                     cudaMemcpyDeviceToDevice, s);
@@ -958,6 +1051,7 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
     e = launch_pack(W, R, pl->wt_const, pl->rt_const, pl->D, pl->G, pl->H, pl->I, s);
     if (e == cudaSuccess && pl->wk_const) e = launch_pack_kmajor(W, pl->wk_const, pl->D, pl->G, pl->H, pl->I, false, s);
     if (e == cudaSuccess && pl->wkb_const) e = launch_pack_kmajor(W, pl->wkb_const, pl->D, pl->G, pl->H, pl->I, true, s);
+    if (e == cudaSuccess && pl->rp16_const) e = launch_pack_kmajor(R, pl->rp16_const, pl->D, pl->G, pl->H, pl->H, 2, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     pl->const_weights = true;
     return RNN_OK;
@@ -1090,9 +1184,9 @@ rnn_status rnn_run_static_scratch(rnn_plan_t pl, int64_t S, int64_t N, const flo
 namespace rnngb {
 
 bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                       const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128, bool bf16)
+                       const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128, int dtype)
 {
-    return tmap_encode_raw(map, base, rank, dims, strides, box, swizzle128, bf16) == CUDA_SUCCESS;
+    return tmap_encode_raw(map, base, rank, dims, strides, box, swizzle128, dtype) == CUDA_SUCCESS;
 }
 
 }  // namespace rnngb

@@ -29,7 +29,7 @@ struct RecParams {
     int dir_reverse[2];          // per direction: 1 if it walks time backwards
 
     // geometry
-    int kernel;                  // 1: staged kernel, 2: dataflow kernel
+    int kernel;                  // 1: staged kernel, 2: dataflow kernel, 3: tensor-core kernel
     int ctas_per_dir;            // CTAs per direction (unit_groups * row_groups)
     int unit_groups;             // CU
     int row_groups;              // CR (1 for the staged kernel)
@@ -127,12 +127,12 @@ cudaError_t launch_projection(const float* X, const float* Bt, float* XW, int64_
                               int64_t K, int64_t ncols, bool exact, int* status, long long limit_ns,
                               cudaStream_t stream);
 
-// Encodes a tiled tensor map of fp32 (or bf16) elements (no swizzle, or
-// 128-byte swizzle; out-of-range reads as zero); false when the driver entry
-// point is missing or rejects the shape.
+// Encodes a tiled tensor map (no swizzle, or 128-byte swizzle; out-of-range
+// reads as zero) of fp32 (dtype 0), bf16 (1) or fp16 (2) elements; false when
+// the driver entry point is missing or rejects the shape.
 bool encode_tensor_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
                        const cuuint64_t* strides, const cuuint32_t* box, bool swizzle128 = false,
-                       bool bf16 = false);
+                       int dtype = 0);
 
 // Input projection on the tensor cores (TF32 products of fp32 operands, or
 // bf16 operands; FP32 sums): XW[M][ncols] = X[M][K] . Wk[ncols][K]^T with Wk
@@ -143,9 +143,10 @@ cudaError_t launch_projection_tc(const void* X, const void* Wk, float* XW, int64
                                  bool bf16, int* status, long long limit_ns, cudaStream_t stream);
 
 // Wk[d*G*H + u*G + g][k] = W[d][g*H + u][k]: W's rows in the projection's
-// column order, K contiguous; written as fp32, or rounded to bf16 when
-// `bf16` (Wk then holds 2-byte elements).
-cudaError_t launch_pack_kmajor(const float* W, void* Wk, int D, int G, int64_t H, int64_t I, bool bf16,
+// column order, K contiguous; written as fp32 (dtype 0), or rounded to bf16
+// (1) or fp16 (2) (Wk then holds 2-byte elements).  Also packs R (I = H) for
+// the tensor-core recurrent kernel.
+cudaError_t launch_pack_kmajor(const float* W, void* Wk, int D, int G, int64_t H, int64_t I, int dtype,
                                cudaStream_t stream);
 
 // dst[i] = src[i] rounded to bf16 (nearest even), n elements.
@@ -155,6 +156,18 @@ cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t 
 //       Rt[d][k][u*G + g]    = R[d][g*H + u][k].
 cudaError_t launch_pack(const float* W, const float* R, float* Wt, float* Rt, int D, int G,
                         int64_t H, int64_t I, cudaStream_t stream);
+
+// Tensor-core recurrent kernel (kernel 3): shared memory for hidden size H
+// and npad padded gate columns, threads per CTA, the most gate columns a CTA
+// may own, occupancy, launch.  Its exchange buffer p.hbuf holds fp16
+// [2][D][128][H]; launch_tc_state_init fills buffer 0 from initial_h (rows
+// past the batch 0), buffer 1 with 0, and zeroes the step counters.
+size_t tc_recurrent_smem(int H, int npad);
+int tc_recurrent_threads();
+int tc_recurrent_max_columns();
+cudaError_t tc_recurrent_occupancy(int op, size_t smem, int* blocks_per_sm);
+cudaError_t launch_tc_recurrent(const RecParams& p, size_t smem, cudaStream_t stream);
+cudaError_t launch_tc_state_init(const RecParams& p, cudaStream_t stream);
 
 // Exchange buffer 0 = initial_h (or 0), everything else 0; bar, flags = 0.
 cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream);

@@ -324,8 +324,8 @@ def test_tensor_core_modes_differ_from_fp32_only_by_the_projection(mode):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
-@pytest.mark.parametrize("name,lbr,k", [WORKLOAD_CASES[1], WORKLOAD_CASES[4]],
-                         ids=[f"{w[0]}-lbr{w[1]}" for w in (WORKLOAD_CASES[1], WORKLOAD_CASES[4])])
+@pytest.mark.parametrize("name,lbr,k", [WORKLOAD_CASES[1], WORKLOAD_CASES[3], WORKLOAD_CASES[4]],
+                         ids=[f"{w[0]}-lbr{w[1]}" for w in (WORKLOAD_CASES[1], WORKLOAD_CASES[3], WORKLOAD_CASES[4])])
 def test_workload_full_size_tensor_core_modes(name, lbr, k, mode):
     c = workload(name, lbr=lbr)
     rows = _sample_rows(c, min(k, 3))
@@ -333,6 +333,70 @@ def test_workload_full_size_tensor_core_modes(name, lbr, k, mode):
     ref = oracle_case(c, rows=rows, threaded=True)
     _compare_fast(tuple(row_slice(c, rows, g, kind) for g, kind in zip(got, ("Y", "state", "state"))),
                   tuple(row_slice(c, rows, r, kind) for r, kind in zip(ref, ("Y", "state", "state"))), TC_TOL)
+
+
+# The tensor-core recurrent kernel (kernel 3: fp16 operands, FP32 sums),
+# chosen in the tensor-core modes for 48..128 batch rows with bounded h; on
+# smaller batches it is forced through the launch override.
+TC_REC_SHAPES = [
+    # op, direction, seq, batch, input, hidden, layout, lbr, lens, clip, launch override
+    ("LSTM", "bidirectional", 9, 64, 24, 128, 0, 0, ("uniform", 0, 9), None, None),
+    ("LSTM", "forward", 7, 128, 40, 200, 1, 0, None, 2.5, None),
+    ("GRU", "bidirectional", 8, 100, 16, 136, 1, 1, ("uniform", 1, 8), None, None),
+    ("GRU", "reverse", 6, 48, 32, 64, 0, 1, None, None, None),
+    ("RNN", "bidirectional", 10, 77, 8, 96, 0, 0, ("uniform", 0, 10), None, None),
+    ("LSTM", "reverse", 5, 9, 16, 64, 0, 0, None, None, (0, 0, -1, 0, 3)),
+    ("GRU", "forward", 4, 1, 8, 32, 1, 1, None, None, (3, 0, -1, 0, 3)),
+]
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", TC_REC_SHAPES, ids=[f"{s[0]}-{s[1]}-n{s[3]}-h{s[5]}" for s in TC_REC_SHAPES])
+def test_tensor_core_recurrence_within_tolerance(shape, mode):
+    op, direction, seq, batch, inp, hid, layout, lbr, lens, clip, launch = shape
+    c = make_case(op, direction, seq, batch, inp, hid, seed=57, layout=layout, with_P=True, h0_scale=0.5,
+                  c0_scale=0.5, lens=lens, linear_before_reset=lbr, clip=clip,
+                  w_scale=1.0 / np.sqrt(max(hid, inp)))
+    Y, Yh, Yc, plan = gpu_case(c, mode, launch=launch, keep_plan=True)
+    assert orc.rnn_plan_get_launch(plan)["kernel"] == 3
+    orc.rnn_plan_destroy(plan)
+    _compare_fast((Y, Yh, Yc), oracle_case(c), TC_TOL)
+
+
+@pytest.mark.parametrize("what", ["gru_lbr0", "relu", "too_many_rows"])
+def test_tensor_core_recurrence_falls_back(what):
+    # cases the fp16 tensor-core kernel does not take run on the FP32 kernels
+    if what == "gru_lbr0":
+        c = make_case("GRU", "forward", 4, 64, 16, 64, seed=5, linear_before_reset=0)
+    elif what == "relu":
+        c = make_case("RNN", "forward", 4, 64, 16, 64, seed=5, activations=["Relu"], w_scale=0.05)
+    else:
+        c = make_case("LSTM", "forward", 3, 130, 16, 64, seed=5)
+    Y, Yh, Yc, plan = gpu_case(c, "tf32", keep_plan=True)
+    assert orc.rnn_plan_get_launch(plan)["kernel"] != 3
+    orc.rnn_plan_destroy(plan)
+    _compare_fast((Y, Yh, Yc), oracle_case(c), TC_TOL)
+
+
+def test_tensor_core_recurrence_timeout_is_reported_and_the_device_stays_usable():
+    # one CTA withholds its first publication: the others' bounded waits
+    # (50 ms) expire, the status says TIMEOUT, and the next run is correct
+    c = make_case("LSTM", "forward", 5, 64, 8, 64, seed=9, h0_scale=0.5)
+    plan = orc.rnn_plan_create("LSTM", "forward", 64, 8)
+    orc.rnn_plan_set_mode(plan, "tf32")
+    orc.rnn_plan_set_launch(plan, 4, 0, -1, 0, 3)
+    orc.rnn_plan_debug_barrier(plan, 50_000_000, 1)
+    import torch
+    t = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in c.tensors().items()}
+    Yh = torch.zeros(c.state_shape(), device="cuda")
+    orc.rnn_run(plan, t["X"], t["W"], t["R"], t["B"], initial_h=t["initial_h"], Y_h=Yh)
+    with pytest.raises(orc.RNNError) as e:
+        orc.rnn_plan_sync(plan)
+    assert e.value.status == 6
+    orc.rnn_plan_debug_barrier(plan, 0, -1)
+    got = gpu_case(c, "tf32", plan=plan)
+    _compare_fast(got, oracle_case(c), TC_TOL)
+    orc.rnn_plan_destroy(plan)
 
 
 def test_rnn_workload_absent_and_zero_initial_state():
