@@ -25,8 +25,10 @@
 //   * warps 0-3 are the epilogue: thread t owns batch row t (tensor-memory
 //     lane t), reads its NP accumulators, adds XW and the biases, runs the
 //     gate arithmetic (FMA-based fast functions) with its cell state kept in
-//     registers, writes Y and its h (fp32 kept, fp16 to the exchange
-//     buffer), and the CTA publishes.
+//     registers (h kept in fp32 too), and stages its row of Y and of the
+//     fp16 h in shared memory; the four warps then write both tiles with
+//     consecutive threads on consecutive units (a thread per row would make
+//     every store instruction touch 32 rows), and the CTA publishes.
 // Every wait is bounded; on a failure the CTA records RNN_ERR_TIMEOUT and
 // its roles leave at the next uniform point, waiting (bounded) for their
 // copies and MMAs in flight before the tensor memory is freed.
@@ -122,11 +124,50 @@ __device__ __forceinline__ void tr_fail(const RecParams& p, volatile int* abort_
     *abort_flag = 1;
 }
 
+// v[k] = act(clip(v[k])) over a whole array for one activation id known at
+// compile time (the id's switch folds away: one formula per element).
+template <int FN, int K>
+__device__ __forceinline__ void tc_apply(const ActSpec& a, float (&v)[K])
+{
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = activation<false>(FN, a.alpha, a.beta, v[k]);
+}
+
+// KIND 1 and 2 call sigmoid and tanh directly; KIND 0 dispatches on the
+// activation id once for the array.
+template <int KIND, int K>
+__device__ __forceinline__ void tc_act_array(const ActSpec& a, float (&v)[K], const RecParams& p, bool clip)
+{
+    if (clip && p.has_clip) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) v[k] = v[k] > p.clip ? p.clip : (v[k] < -p.clip ? -p.clip : v[k]);
+    }
+    if constexpr (KIND == 1) {
+        tc_apply<2, K>(a, v);
+    } else if constexpr (KIND == 2) {
+        tc_apply<1, K>(a, v);
+    } else {
+        switch (a.fn) {
+        case 0: tc_apply<0, K>(a, v); break;
+        case 1: tc_apply<1, K>(a, v); break;
+        case 2: tc_apply<2, K>(a, v); break;
+        case 3: tc_apply<3, K>(a, v); break;
+        case 4: tc_apply<4, K>(a, v); break;
+        case 5: tc_apply<5, K>(a, v); break;
+        case 6: tc_apply<6, K>(a, v); break;
+        case 7: tc_apply<7, K>(a, v); break;
+        case 8: tc_apply<8, K>(a, v); break;
+        case 9: tc_apply<9, K>(a, v); break;
+        default: tc_apply<10, K>(a, v); break;
+        }
+    }
+}
+
 template <int OP>
 __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_constant__ RecParams p)
 {
     constexpr int G = OP == 0 ? 1 : (OP == 1 ? 3 : 4);
-    constexpr int UMAX = TR_NPMAX / G;
+    constexpr int UMAX = G == 1 ? 32 : TR_NPMAX / G;   // most units per CTA (register arrays)
     extern __shared__ __align__(1024) unsigned char tr_smem[];
     __shared__ __align__(8) uint64_t full[TR_ST], empty[TR_ST], r_ready, acc_ready, acc_free, mma_done;
     __shared__ uint32_t tmem_slot;
@@ -144,6 +185,10 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
     const int nkb = (H + TR_KB - 1) / TR_KB;
     unsigned char* rsm = base;                              // R slice: nkb blocks of [NP rows][128 B]
     unsigned char* hring = base + (size_t)nkb * NP * 128;   // TR_ST blocks of [128 rows][128 B]
+    // per-step staging of the CTA's output tiles: Y [128][umax] fp32, h [128][umax] fp16, t per row
+    float* s_y = reinterpret_cast<float*>(hring + (size_t)TR_ST * kTrHStage);
+    __half* s_h = reinterpret_cast<__half*>(s_y + (size_t)TR_M * p.umax);
+    int* s_t = reinterpret_cast<int*>(s_h + (size_t)TR_M * ((p.umax + 1) & ~1));
     const bool rev = p.dir_reverse[d] != 0;
     unsigned* counter = p.bar + d;
     const uint32_t idesc = (1u << 4) | ((uint32_t)(NP >> 3) << 17) | ((uint32_t)(TR_M >> 4) << 24);
@@ -271,6 +316,10 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
         const bool row = n < p.N;
         const int len = row ? (p.has_lens ? p.lens[n] : p.S) : 0;
         const ActSpec fA = p.act[d][0], gA = p.act[d][1], hA = p.act[d][2];
+        // the operator's default activations (RNN Tanh; GRU Sigmoid, Tanh; LSTM
+        // Sigmoid, Tanh, Tanh) are called directly
+        const bool fixed_acts = OP == 0 ? fA.fn == 1
+                                        : (OP == 1 ? fA.fn == 2 && gA.fn == 1 : fA.fn == 2 && gA.fn == 1 && hA.fn == 1);
         float hown[UMAX], cown[UMAX];
 #pragma unroll
         for (int ul = 0; ul < UMAX; ++ul) {
@@ -310,57 +359,119 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
             }
             __syncwarp();
             if (lane == 0 && got) mbar_arrive(&acc_free);
+            // pre-activations in place: acc = ((xw + rec) + Wb) + Rb, except the
+            // GRU candidate's column, whose xw is kept apart (it is added after
+            // r (.) (rec + Rb))
+            float xh[OP == 1 ? UMAX : 1];
             if (got && live) {
 #pragma unroll
-                for (int ul = 0; ul < UMAX; ++ul) {
-                    if (ul >= U) break;
-                    float pre[G];
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const int j = ul * G + g;
-                        pre[g] = (xw[j] + acc[j]) + s_wb[j] + s_rb[j];
-                    }
-                    float hn;
-                    if constexpr (OP == 0) {
-                        hn = act<false>(fA, clipv(p, pre[0]));
-                    } else if constexpr (OP == 1) {
-                        const float z = act<false>(fA, clipv(p, pre[0]));
-                        const float r = act<false>(fA, clipv(p, pre[1]));
-                        const int j = ul * G + 2;
-                        const float ph = p.has_B ? (xw[j] + r * (acc[j] + s_rb[j])) + s_wb[j] : xw[j] + r * acc[j];
-                        const float ht = act<false>(gA, clipv(p, ph));
-                        hn = (1.0f - z) * ht + z * hown[ul];
+                for (int j = 0; j < TR_NPMAX; ++j) {
+                    if (OP == 1 && j % 3 == 2) {
+                        if (j / 3 < UMAX) xh[j / 3] = xw[j];
                     } else {
-                        float pi = pre[0], po = pre[1], pf = pre[2];
-                        const float pc = pre[3];
-                        if (p.has_P) {
-                            pi += s_p[0][ul] * cown[ul];
-                            pf += s_p[2][ul] * cown[ul];
-                        }
-                        const float ig = act<false>(fA, clipv(p, pi));
-                        const float fg = p.input_forget ? 1.0f - ig : act<false>(fA, clipv(p, pf));
-                        const float ct = act<false>(gA, clipv(p, pc));
-                        const float cn = fg * cown[ul] + ig * ct;
-                        if (p.has_P) po += s_p[1][ul] * cn;
-                        const float og = act<false>(fA, clipv(p, po));
-                        hn = og * act<false>(hA, cn);
-                        cown[ul] = cn;
+                        acc[j] = (xw[j] + acc[j]) + s_wb[j] + s_rb[j];
                     }
-                    hown[ul] = hn;
-                    if (p.Y) p.Y[y_index(p, t, d, n, u0 + ul)] = canon_nan(hn);
                 }
-            } else if (got && row && p.Y) {
-                for (int ul = 0; ul < U; ++ul) p.Y[y_index(p, s, d, n, u0 + ul)] = 0.f;
             }
-            if (got && row) {
-                __half* dst = hx + (((size_t)((s + 1) & 1) * p.D + d) * TR_M + n) * H + u0;
+            if (got && live) {
+                // gate arithmetic gate-by-gate over the CTA's units: each
+                // activation is applied to a whole array, so its dispatch is
+                // paid once per gate and the units' chains run side by side
+                auto cells = [&](auto fx) {
+                    constexpr int KIND_F = decltype(fx)::value ? (OP == 0 ? 2 : 1) : 0;   // 1 sigmoid, 2 tanh
+                    constexpr int KIND_T = decltype(fx)::value ? 2 : 0;
+                    (void)KIND_T;
+                    if constexpr (OP == 0) {
+                        float a[UMAX];
+#pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul) a[ul] = acc[ul];
+                        tc_act_array<KIND_F, UMAX>(fA, a, p, true);
+#pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul) hown[ul] = ul < U ? a[ul] : hown[ul];
+                    } else if constexpr (OP == 1) {
+                        float z[UMAX], r[UMAX];
+#pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul) {
+                            z[ul] = acc[3 * ul];
+                            r[ul] = acc[3 * ul + 1];
+                        }
+                        tc_act_array<KIND_F, UMAX>(fA, z, p, true);
+                        tc_act_array<KIND_F, UMAX>(fA, r, p, true);
+#pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul) {
+                            const int j = 3 * ul + 2;
+                            r[ul] = p.has_B ? (xh[ul] + r[ul] * (acc[j] + s_rb[j])) + s_wb[j] : xh[ul] + r[ul] * acc[j];
+                        }
+                        tc_act_array<KIND_T, UMAX>(gA, r, p, true);   // r now holds the candidate
+#pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul)
+                            if (ul < U) hown[ul] = (1.0f - z[ul]) * r[ul] + z[ul] * hown[ul];
+                    } else {
+                        float gi[UMAX], gf[UMAX], gc[UMAX], go[UMAX];
+#pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul) {
+                            const int j = 4 * ul;
+                            gi[ul] = acc[j];
+                            go[ul] = acc[j + 1];
+                            gf[ul] = acc[j + 2];
+                            gc[ul] = acc[j + 3];
+                            if (p.has_P) {
+                                gi[ul] += s_p[0][ul] * cown[ul];
+                                gf[ul] += s_p[2][ul] * cown[ul];
+                            }
+                        }
+                        tc_act_array<KIND_F, UMAX>(fA, gi, p, true);
+                        if (p.input_forget) {
+#pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul) gf[ul] = 1.0f - gi[ul];
+                        } else {
+                            tc_act_array<KIND_F, UMAX>(fA, gf, p, true);
+                        }
+                        tc_act_array<KIND_T, UMAX>(gA, gc, p, true);
+#pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul) {
+                            const float cn = gf[ul] * cown[ul] + gi[ul] * gc[ul];
+                            if (ul < U) cown[ul] = cn;
+                            gc[ul] = cn;
+                            if (p.has_P) go[ul] += s_p[1][ul] * cn;
+                        }
+                        tc_act_array<KIND_F, UMAX>(fA, go, p, true);
+                        tc_act_array<KIND_T, UMAX>(hA, gc, p, false);   // the cell state is not clipped
+#pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul)
+                            if (ul < U) hown[ul] = go[ul] * gc[ul];
+                    }
+#pragma unroll
+                    for (int ul = 0; ul < UMAX; ++ul)
+                        if (ul < U) s_y[n * p.umax + ul] = canon_nan(hown[ul]);
+                };
+                if (fixed_acts) cells(std::true_type{});
+                else cells(std::false_type{});
+            } else if (got && row) {
 #pragma unroll
                 for (int ul = 0; ul < UMAX; ++ul)
-                    if (ul < U) dst[ul] = __float2half_rn(hown[ul]);
+                    if (ul < U) s_y[n * p.umax + ul] = 0.f;   // Y is +0 past the row's length
             }
-            // publish: every epilogue thread's h is written; leave together on a failure
+            if (got && row) {
+                s_t[n] = live ? t : s;
+#pragma unroll
+                for (int ul = 0; ul < UMAX; ++ul)
+                    if (ul < U) s_h[n * p.umax + ul] = __float2half_rn(hown[ul]);
+            }
             tr_bar(1, 128);
             const bool abort_now = s_abort != 0 || !got;
+            if (!abort_now) {
+                // the staged tiles, units fastest: a warp's stores cover a few
+                // contiguous row segments
+                __half* hdst = hx + ((size_t)((s + 1) & 1) * p.D + d) * TR_M * H + u0;
+                const int tot = p.N * U;
+                for (int i = threadIdx.x; i < tot; i += 128) {
+                    const int rn = i / U, ul = i - rn * U;
+                    if (p.Y) p.Y[y_index(p, s_t[rn], d, rn, u0 + ul)] = s_y[rn * p.umax + ul];
+                    hdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
+                }
+            }
+            // publish: every epilogue thread's writes are done; leave together on a failure
             tr_bar(1, 128);
             if (abort_now) {
                 alive = false;
@@ -398,11 +509,17 @@ const void* tc_kernel_ptr()
 
 }  // namespace
 
-size_t tc_recurrent_smem(int H, int npad) { return 1024 + (size_t)((H + TR_KB - 1) / TR_KB) * npad * 128 + (size_t)TR_ST * kTrHStage; }
+size_t tc_recurrent_smem(int H, int npad, int umax)
+{
+    return 1024 + (size_t)((H + TR_KB - 1) / TR_KB) * npad * 128 + (size_t)TR_ST * kTrHStage +
+           (size_t)TR_M * umax * 4 + (size_t)TR_M * ((umax + 1) & ~1) * 2 + (size_t)TR_M * 4;
+}
 
 int tc_recurrent_threads() { return TR_THREADS; }
 
 int tc_recurrent_max_columns() { return TR_NPMAX; }
+
+int tc_recurrent_max_units(int op) { return op == 0 ? 32 : TR_NPMAX / (op == 1 ? 3 : 4); }
 
 cudaError_t tc_recurrent_occupancy(int op, size_t smem, int* blocks)
 {

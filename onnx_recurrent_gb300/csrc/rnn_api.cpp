@@ -391,9 +391,9 @@ rnn_status plan_tc(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out)
     const int64_t U = ceil_div(H, C);
     C = ceil_div(H, U);
     const int NP = (int)round_up(U * G, 16);
-    if (NP > tc_recurrent_max_columns())
+    if (NP > tc_recurrent_max_columns() || U > tc_recurrent_max_units(pl->op))
         return fail(RNN_ERR_UNSUPPORTED, "hidden_size %lld is too large for the tensor-core kernel", (long long)H);
-    const size_t smem = tc_recurrent_smem((int)H, NP);
+    const size_t smem = tc_recurrent_smem((int)H, NP, (int)U);
     if (smem > (size_t)di.smem_optin - 2048) return fail(RNN_ERR_UNSUPPORTED, "tensor-core kernel: shared memory");
     int blocks = 0;
     cudaError_t e = tc_recurrent_occupancy(pl->op, smem, &blocks);
