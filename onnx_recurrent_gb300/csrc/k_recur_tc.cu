@@ -17,14 +17,15 @@
 //     stays there as the MMA's B operand;
 //   * warp 4 (one lane) waits each step for every CTA of the direction to
 //     have published the step (a release-add / acquire-poll counter), then
-//     moves h (fp16 [128 rows][H], the exchange buffer) through a 4-stage
-//     ring of 64-k blocks with tensor copies;
+//     moves h (fp16 [128 rows][H], the exchange buffer) through a ring of
+//     64-k blocks (up to 4 stages of 16 KB, fewer if shared memory is short)
+//     with tensor copies;
 //   * warp 5 (one lane) issues four tcgen05.mma (kind::f16, M 128, N NP,
 //     K 16) per block into tensor memory, commits each ring slot back to the
 //     producer and, after the last block, the accumulators to the epilogue;
 //   * warps 0-3 are the epilogue: thread t owns batch row t (tensor-memory
 //     lane t), reads its NP accumulators, adds XW and the biases, runs the
-//     gate arithmetic (FMA-based fast functions) with its cell state kept in
+//     gate arithmetic (FMA-based, hardware tanh) with its cell state kept in
 //     registers (h kept in fp32 too), and stages its row of Y and of the
 //     fp16 h in shared memory; the four warps then write both tiles with
 //     consecutive threads on consecutive units (a thread per row would make
@@ -46,7 +47,7 @@ namespace {
 
 constexpr int TR_M = 128;                       // MMA rows (batch rows, padded)
 constexpr int TR_KB = 64;                       // fp16 k per block (128-byte rows)
-constexpr int TR_ST = 4;                        // h ring stages
+constexpr int TR_STMAX = 4;                     // most h ring stages (measured: deeper rings are slower)
 constexpr unsigned kTrHStage = TR_M * 128;      // one h block: 16 KB
 constexpr int TR_NPMAX = 64;                    // most gate columns per CTA
 constexpr int TR_THREADS = 192;
@@ -124,13 +125,30 @@ __device__ __forceinline__ void tr_fail(const RecParams& p, volatile int* abort_
     *abort_flag = 1;
 }
 
-// v[k] = act(clip(v[k])) over a whole array for one activation id known at
-// compile time (the id's switch folds away: one formula per element).
+// The tensor-core modes promise 5e-3, so their tanh and sigmoid use the
+// hardware tanh (tanh.approx.f32, relative error about 2^-11, below the fp16
+// rounding of h): tanh(x), sigmoid(x) = 1/2 + tanh(x/2)/2, alpha*tanh(beta*x).
+__device__ __forceinline__ float tc_tanh(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float tc_sigmoid(float x) { return fmaf(0.5f, tc_tanh(0.5f * x), 0.5f); }
+
+// v[k] = act(v[k]) over a whole array for one activation id known at compile
+// time (the id's switch folds away: one formula per element).
 template <int FN, int K>
 __device__ __forceinline__ void tc_apply(const ActSpec& a, float (&v)[K])
 {
 #pragma unroll
-    for (int k = 0; k < K; ++k) v[k] = activation<false>(FN, a.alpha, a.beta, v[k]);
+    for (int k = 0; k < K; ++k) {
+        if constexpr (FN == 1) v[k] = tc_tanh(v[k]);
+        else if constexpr (FN == 2) v[k] = tc_sigmoid(v[k]);
+        else if constexpr (FN == 6) v[k] = a.alpha * tc_tanh(a.beta * v[k]);
+        else v[k] = activation<false>(FN, a.alpha, a.beta, v[k]);
+    }
 }
 
 // KIND 1 and 2 call sigmoid and tanh directly; KIND 0 dispatches on the
@@ -169,7 +187,7 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
     constexpr int G = OP == 0 ? 1 : (OP == 1 ? 3 : 4);
     constexpr int UMAX = G == 1 ? 32 : TR_NPMAX / G;   // most units per CTA (register arrays)
     extern __shared__ __align__(1024) unsigned char tr_smem[];
-    __shared__ __align__(8) uint64_t full[TR_ST], empty[TR_ST], r_ready, acc_ready, acc_free, mma_done;
+    __shared__ __align__(8) uint64_t full[TR_STMAX], empty[TR_STMAX], r_ready, acc_ready, acc_free, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_abort;
     __shared__ float s_wb[TR_NPMAX], s_rb[TR_NPMAX], s_p[3][UMAX];
@@ -184,9 +202,10 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
     const int NP = p.npad;                                  // padded gate columns (MMA N)
     const int nkb = (H + TR_KB - 1) / TR_KB;
     unsigned char* rsm = base;                              // R slice: nkb blocks of [NP rows][128 B]
-    unsigned char* hring = base + (size_t)nkb * NP * 128;   // TR_ST blocks of [128 rows][128 B]
+    const int nst = p.slots;                                // h ring stages
+    unsigned char* hring = base + (size_t)nkb * NP * 128;   // nst blocks of [128 rows][128 B]
     // per-step staging of the CTA's output tiles: Y [128][umax] fp32, h [128][umax] fp16, t per row
-    float* s_y = reinterpret_cast<float*>(hring + (size_t)TR_ST * kTrHStage);
+    float* s_y = reinterpret_cast<float*>(hring + (size_t)nst * kTrHStage);
     __half* s_h = reinterpret_cast<__half*>(s_y + (size_t)TR_M * p.umax);
     int* s_t = reinterpret_cast<int*>(s_h + (size_t)TR_M * ((p.umax + 1) & ~1));
     const bool rev = p.dir_reverse[d] != 0;
@@ -196,7 +215,7 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
     while (tmem_cols < NP) tmem_cols *= 2;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < TR_ST; ++i) {
+        for (int i = 0; i < nst; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
@@ -257,8 +276,8 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                 }
                 const int z = (s & 1) * p.D + d;
                 for (int kb = 0; kb < nkb; ++kb, ++q) {
-                    const int slot = (int)(q % TR_ST);
-                    if (q >= TR_ST && !tr_wait(&empty[slot], ((q / TR_ST) - 1u) & 1u, p, &s_abort)) {
+                    const int slot = (int)(q % nst);
+                    if (q >= (unsigned)nst && !tr_wait(&empty[slot], ((q / nst) - 1u) & 1u, p, &s_abort)) {
                         tr_fail(p, &s_abort);
                         ok = false;
                         break;
@@ -269,8 +288,8 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
             }
             // copies still in flight land before the CTA can leave
             (void)tr_wait(&r_ready, 0u, p, nullptr);
-            for (unsigned k = (q > TR_ST ? q - TR_ST : 0u); k < q; ++k)
-                (void)tr_wait(&full[k % TR_ST], (k / TR_ST) & 1u, p, nullptr);
+            for (unsigned k = (q > (unsigned)nst ? q - nst : 0u); k < q; ++k)
+                (void)tr_wait(&full[k % nst], (k / nst) & 1u, p, nullptr);
         }
         __syncwarp();
     } else if (warp == 5) {
@@ -286,8 +305,8 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                 }
                 tr_fence_after();
                 for (int kb = 0; kb < nkb; ++kb, ++q) {
-                    const int slot = (int)(q % TR_ST);
-                    if (!tr_wait(&full[slot], (q / TR_ST) & 1u, p, &s_abort)) {
+                    const int slot = (int)(q % nst);
+                    if (!tr_wait(&full[slot], (q / nst) & 1u, p, &s_abort)) {
                         tr_fail(p, &s_abort);
                         ok = false;
                         break;
@@ -509,11 +528,13 @@ const void* tc_kernel_ptr()
 
 }  // namespace
 
-size_t tc_recurrent_smem(int H, int npad, int umax)
+size_t tc_recurrent_smem(int H, int npad, int umax, int stages)
 {
-    return 1024 + (size_t)((H + TR_KB - 1) / TR_KB) * npad * 128 + (size_t)TR_ST * kTrHStage +
+    return 1024 + (size_t)((H + TR_KB - 1) / TR_KB) * npad * 128 + (size_t)stages * kTrHStage +
            (size_t)TR_M * umax * 4 + (size_t)TR_M * ((umax + 1) & ~1) * 2 + (size_t)TR_M * 4;
 }
+
+int tc_recurrent_max_stages() { return TR_STMAX; }
 
 int tc_recurrent_threads() { return TR_THREADS; }
 

@@ -393,8 +393,13 @@ rnn_status plan_tc(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out)
     const int NP = (int)round_up(U * G, 16);
     if (NP > tc_recurrent_max_columns() || U > tc_recurrent_max_units(pl->op))
         return fail(RNN_ERR_UNSUPPORTED, "hidden_size %lld is too large for the tensor-core kernel", (long long)H);
-    const size_t smem = tc_recurrent_smem((int)H, NP, (int)U);
-    if (smem > (size_t)di.smem_optin - 2048) return fail(RNN_ERR_UNSUPPORTED, "tensor-core kernel: shared memory");
+    // h ring: as many 16 KB stages as fit (at least 2)
+    const size_t cap = (size_t)di.smem_optin - 2048;
+    const size_t fixed = tc_recurrent_smem((int)H, NP, (int)U, 0);
+    const size_t per_stage = tc_recurrent_smem((int)H, NP, (int)U, 1) - fixed;
+    if (fixed + 2 * per_stage > cap) return fail(RNN_ERR_UNSUPPORTED, "tensor-core kernel: shared memory");
+    const int stages = (int)std::min<size_t>((size_t)tc_recurrent_max_stages(), (cap - fixed) / per_stage);
+    const size_t smem = tc_recurrent_smem((int)H, NP, (int)U, stages);
     int blocks = 0;
     cudaError_t e = tc_recurrent_occupancy(pl->op, smem, &blocks);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
@@ -412,6 +417,7 @@ rnn_status plan_tc(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out)
     out->rres = 1;
     out->smem = smem;
     out->npad = NP;
+    out->slots = stages;
     return RNN_OK;
 }
 

@@ -162,7 +162,8 @@ cudaError_t launch_pack(const float* W, const float* R, float* Wt, float* Rt, in
 // may own, occupancy, launch.  Its exchange buffer p.hbuf holds fp16
 // [2][D][128][H]; launch_tc_state_init fills buffer 0 from initial_h (rows
 // past the batch 0), buffer 1 with 0, and zeroes the step counters.
-size_t tc_recurrent_smem(int H, int npad, int umax);
+size_t tc_recurrent_smem(int H, int npad, int umax, int stages);
+int tc_recurrent_max_stages();
 int tc_recurrent_threads();
 int tc_recurrent_max_columns();
 int tc_recurrent_max_units(int op);
