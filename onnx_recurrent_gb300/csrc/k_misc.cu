@@ -71,7 +71,8 @@ __global__ void state_init_kernel(const RecParams p)
         const int64_t n = cr * p.npad + rl;
         float v = 0.0f;
         if (n < p.N && u < p.H && p.h0) {
-            const int64_t si = p.layout == 0 ? (d * p.N + n) * p.H + u : (n * p.D + d) * p.H + u;
+            const int64_t nr = p.perm ? p.perm[n] : n;    // the caller's row behind internal row n
+            const int64_t si = p.layout == 0 ? (d * p.N + nr) * p.H + u : (nr * p.D + d) * p.H + u;
             v = p.h0[si];
         }
         const int64_t off = i - d * CR * blk;             // offset inside direction d
@@ -178,6 +179,19 @@ cudaError_t launch_pack(const float* W, const float* R, float* Wt, float* Rt, in
 
 namespace {
 
+__global__ void rank_rows_kernel(const int32_t* __restrict__ lens, int32_t* __restrict__ perm, int N)
+{
+    for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
+        const int ln = lens[n];
+        int rank = 0;
+        for (int m = 0; m < N; ++m) {
+            const int lm = lens[m];
+            rank += (lm > ln || (lm == ln && m < n)) ? 1 : 0;
+        }
+        perm[rank] = n;
+    }
+}
+
 // Tensor-core kernel: hx[b][d][r][u] (fp16, 128 rows) = initial_h for b = 0
 // and r < N, else 0; step counters 0.
 __global__ void tc_state_init_kernel(const RecParams p)
@@ -199,6 +213,13 @@ __global__ void tc_state_init_kernel(const RecParams p)
 }
 
 }  // namespace
+
+cudaError_t launch_rank_rows(const int32_t* lens, int32_t* perm, int N, cudaStream_t stream)
+{
+    if (N <= 0) return cudaSuccess;
+    rank_rows_kernel<<<(N + 127) / 128, 128, 0, stream>>>(lens, perm, N);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_tc_state_init(const RecParams& p, cudaStream_t stream)
 {

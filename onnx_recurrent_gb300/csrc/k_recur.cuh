@@ -192,6 +192,7 @@ __device__ __forceinline__ void chunk_part(const float* hk, int hstride, const f
 struct RecCtx {
     int d, H, npad, G, GH, u0, UG, ugp, tid, nthreads, ul, rb;
     bool active;
+    bool live;   // this step: some row of the thread's tile has not finished
     float* Rs;   // resident [H][ugp] or ring [stages][KC][ugp]
     float* Hs;   // ring [stages][KC][npad]
 };
@@ -240,7 +241,7 @@ __device__ __forceinline__ void accumulate(const RecParams& p, const RecCtx& x, 
         const int slot = c % kRecStages;
         const int k0 = c * kRecKC;
         const int kc = min(kRecKC, x.H - k0);
-        if (x.active) {
+        if (x.active && x.live) {
             const float* hk = x.Hs + (size_t)slot * kRecKC * x.npad + x.rb * TN;
             const float* rk = (p.r_resident ? x.Rs + (size_t)k0 * x.ugp
                                             : x.Rs + (size_t)slot * kRecKC * x.ugp) +
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
     x.ul = x.tid % p.umax;
     x.rb = x.tid / p.umax;
     x.active = (x.ul < U) && (x.rb * TN < p.N);
+    x.live = true;
     x.Rs = smem;
     x.Hs = smem + (p.r_resident ? (size_t)p.H * x.ugp : (size_t)kRecStages * kRecKC * x.ugp);
 
@@ -341,13 +343,21 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
             pF = p.P[(size_t)d * 3 * p.H + 2 * p.H + u];
         }
     }
+    // Rows: the exchange buffers use the internal row index r = rb*TN + i;
+    // with sequence_lens the rows are sorted by length (longest first, so a
+    // tile whose first row has finished has finished altogether) and rown[i]
+    // is the caller's row behind r.
+    int rown[TN];
+    int tile_len = 0;
 #pragma unroll
     for (int i = 0; i < TN; ++i) {
-        const int n = x.rb * TN + i;
-        const bool ok = x.active && n < N;
-        len[i] = ok ? (p.has_lens ? p.lens[n] : p.S) : 0;
-        hown[i] = (ok && p.has_h0) ? p.h0[s_index(p, d, n, u)] : 0.f;
-        cown[i] = (ok && OP == 2 && p.has_c0) ? p.c0[s_index(p, d, n, u)] : 0.f;
+        const int r = x.rb * TN + i;
+        const bool ok = x.active && r < N;
+        rown[i] = ok ? (p.perm ? p.perm[r] : r) : 0;
+        len[i] = ok ? (p.has_lens ? p.lens[rown[i]] : p.S) : 0;
+        tile_len = len[i] > tile_len ? len[i] : tile_len;
+        hown[i] = (ok && p.has_h0) ? p.h0[s_index(p, d, rown[i], u)] : 0.f;
+        cown[i] = (ok && OP == 2 && p.has_c0) ? p.c0[s_index(p, d, rown[i], u)] : 0.f;
     }
 
     const size_t xw_ld = (size_t)p.D * x.GH;
@@ -355,8 +365,8 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
     auto load_xw = [&](int s) {
 #pragma unroll
         for (int i = 0; i < TN; ++i) {
-            const int n = x.rb * TN + i;
-            if (x.active && n < N && s < len[i]) {
+            const int n = rown[i];
+            if (x.active && x.rb * TN + i < N && s < len[i]) {
                 const int t = rev ? len[i] - 1 - s : s;
                 const size_t row = p.layout == 0 ? (size_t)t * N + n : (size_t)n * p.S + t;
                 const float* q = p.XW + row * xw_ld + xw_col;
@@ -379,6 +389,7 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
         for (int i = 0; i < TN; ++i)
 #pragma unroll
             for (int g = 0; g < G; ++g) xc[i][g] = xw[i][g];
+        x.live = s < tile_len;   // a finished tile skips its products (its rows stay frozen)
 
         if constexpr (OP == 1) {
             if (p.lbr == 0) {
@@ -392,7 +403,7 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
                 float* rh = p.rhbuf + (size_t)d * 2 * p.H * x.npad;
 #pragma unroll
                 for (int i = 0; i < TN; ++i) {
-                    const int n = x.rb * TN + i;
+                    const int n = x.rb * TN + i;   // internal row (exchange buffers)
                     zg[i] = 0.f;
                     if (!(x.active && n < N)) continue;
                     float rhv = 0.f;
@@ -419,7 +430,8 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
                 accumulate<TN, 1, EXACT>(p, x, rh, 2, ah);
 #pragma unroll
                 for (int i = 0; i < TN; ++i) {
-                    const int n = x.rb * TN + i;
+                    const int n = x.rb * TN + i;   // internal row (exchange buffers)
+                    const int nr = rown[i];        // the caller's row
                     if (!(x.active && n < N)) continue;
                     if (s < len[i]) {
                         const int t = rev ? len[i] - 1 - s : s;
@@ -428,9 +440,9 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
                         const float ht = act<EXACT>(gA, clipv(p, ph));
                         const float hn = fadd(fmul(fsub(1.0f, zg[i]), ht), fmul(zg[i], hown[i]));
                         hown[i] = hn;
-                        if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
+                        if (p.Y) p.Y[y_index(p, t, d, nr, u)] = canon_nan(hn);
                     } else if (p.Y) {
-                        p.Y[y_index(p, s, d, n, u)] = 0.f;
+                        p.Y[y_index(p, s, d, nr, u)] = 0.f;
                     }
                     hdst[(size_t)u * x.npad + n] = hown[i];
                 }
@@ -450,7 +462,8 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
 
 #pragma unroll
         for (int i = 0; i < TN; ++i) {
-            const int n = x.rb * TN + i;
+            const int n = x.rb * TN + i;   // internal row (exchange buffers)
+            const int nr = rown[i];        // the caller's row
             if (!(x.active && n < N)) continue;
             if (s < len[i]) {
                 const int t = rev ? len[i] - 1 - s : s;
@@ -490,9 +503,9 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
                     cown[i] = cn;
                 }
                 hown[i] = hn;
-                if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
+                if (p.Y) p.Y[y_index(p, t, d, nr, u)] = canon_nan(hn);
             } else if (p.Y) {
-                p.Y[y_index(p, s, d, n, u)] = 0.f;
+                p.Y[y_index(p, s, d, nr, u)] = 0.f;
             }
             hdst[(size_t)u * x.npad + n] = hown[i];
         }
@@ -506,7 +519,7 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
     for (int i = 0; i < TN; ++i) {
         const int n = x.rb * TN + i;
         if (!(x.active && n < N)) continue;
-        const size_t si = s_index(p, d, n, u);
+        const size_t si = s_index(p, d, rown[i], u);
         if (p.Yh) p.Yh[si] = len[i] > 0 ? canon_nan(hown[i]) : 0.f;
         if (OP == 2 && p.Yc) p.Yc[si] = len[i] > 0 ? canon_nan(cown[i]) : 0.f;
     }

@@ -426,8 +426,8 @@ rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, const fl
 {
     if (pl->ov_kernel == 1) return plan_staged(pl, N, di, g);
     if (pl->ov_kernel == 3) return plan_tc(pl, N, di, g);
-    // tensor-core modes: the tensor-core kernel for batches of 48..128 rows
-    if ((pl->mode == RNN_MODE_FAST_TF32 || pl->mode == RNN_MODE_FAST_BF16) && pl->ov_kernel == 0 && N >= 48) {
+    // tensor-core modes: the tensor-core kernel for batches of 32..128 rows
+    if ((pl->mode == RNN_MODE_FAST_TF32 || pl->mode == RNN_MODE_FAST_BF16) && pl->ov_kernel == 0 && N >= 32) {
         const std::string saved = g_error;
         if (plan_tc(pl, N, di, g) == RNN_OK) return RNN_OK;
         g_error = saved;
@@ -624,7 +624,7 @@ rnn_status check_lengths(const int32_t* host, int64_t N, int64_t S, int64_t* max
 }
 
 struct Layout {
-    size_t wt, rt, rp, xw, xb, hb, rh, total;
+    size_t wt, rt, rp, xw, xb, hb, rh, perm, total;
     bool need_rh;
 };
 
@@ -645,6 +645,7 @@ Layout scratch_layout(const rnn_plan* pl, const Geometry& geo, int64_t S, int64_
     L.hb = off; off += align256(hbuf);
     L.need_rh = pl->op == RNN_OP_GRU && pl->lbr == 0;
     L.rh = off; off += L.need_rh ? align256(hbuf) : 0;
+    L.perm = off; off += geo.kernel == 1 ? align256(sizeof(int32_t) * (size_t)N) : 0;   // rows by length
     L.total = off;
     return L;
 }
@@ -769,6 +770,14 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         }
     }
 
+    if (geo.kernel == 1 && a.lens) {
+        // the staged kernel takes the rows longest first, so that finished
+        // row tiles drop out of the products
+        p.perm = (const int32_t*)(scratch + L.perm);
+        e = launch_rank_rows(a.lens, (int32_t*)(scratch + L.perm), (int)a.N, a.st);
+        if (e != cudaSuccess) return cuda_fail(e, "row ranking launch");
+        launches += 1;
+    }
     e = geo.kernel == 3 ? launch_tc_state_init(p, a.st) : launch_state_init(p, a.st);
     if (e != cudaSuccess) return cuda_fail(e, "state set-up launch");
     launches += 1;

@@ -52,6 +52,8 @@ struct RecParams {
     const float* h0;             // layout-dependent [D,N,H] / [N,D,H] (may be null)
     const float* c0;
     const int32_t* lens;         // [N] device (may be null)
+    const int32_t* perm;         // staged kernel with lens: internal row r is the caller's row perm[r]
+                                 // (rows by length, longest first; null = identity)
     float* Y;                    // may be null
     float* Yh;
     float* Yc;
@@ -170,6 +172,10 @@ int tc_recurrent_max_units(int op);
 cudaError_t tc_recurrent_occupancy(int op, size_t smem, int* blocks_per_sm);
 cudaError_t launch_tc_recurrent(const RecParams& p, size_t smem, cudaStream_t stream);
 cudaError_t launch_tc_state_init(const RecParams& p, cudaStream_t stream);
+
+// perm[rank] = n, rank = the number of rows longer than n or as long and
+// before it: the rows sorted by length, longest first (stable).
+cudaError_t launch_rank_rows(const int32_t* lens, int32_t* perm, int N, cudaStream_t stream);
 
 // Exchange buffer 0 = initial_h (or 0), everything else 0; bar, flags = 0.
 cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream);
