@@ -26,6 +26,13 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Runs are
  *     stream-ordered and asynchronous.
  *   - A plan is not re-entrant: one run at a time per plan (it owns scratch).
+ *   - The recurrent kernel of a run keeps all its CTAs resident and they wait
+ *     on one another every step, so two of them must not share the SMs.  The
+ *     library orders recurrent launches on a device: each waits (through an
+ *     event, on its own stream) for the previous one from any plan or
+ *     stream; the rest of a run overlaps freely.  Launches queued under stream
+ *     capture get no such ordering: graphs that hold recurrent kernels must
+ *     not be replayed concurrently with each other or with uncaptured runs.
  *   - No C++ exception crosses this boundary.  A failing call returns a
  *     status and leaves a message for rnn_last_error() on the calling thread.
  */

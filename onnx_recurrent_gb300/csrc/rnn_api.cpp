@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -650,6 +651,49 @@ Layout scratch_layout(const rnn_plan* pl, const Geometry& geo, int64_t S, int64_
     return L;
 }
 
+// The recurrent kernels need every CTA of their grid resident at once (they
+// wait on one another every step).  Two of them launched on different streams
+// may each get only part of the SMs and then wait for CTAs that cannot be
+// placed until a wait limit runs out.  So recurrent launches on one device
+// are put in one order: each waits, through an event, for the previous one,
+// whichever stream or plan it came from.  Work captured into a graph is left
+// alone (an event from outside a capture cannot be waited on inside it).
+struct RecurrentGate {
+    std::mutex m;
+    cudaEvent_t last = nullptr;
+};
+
+cudaError_t launch_recurrent_ordered(const RecParams& p, const Geometry& geo, bool exact, cudaStream_t st)
+{
+    static RecurrentGate gates[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return e;
+    auto launch = [&]() {
+        return geo.kernel == 3 ? launch_tc_recurrent(p, geo.smem, st)
+                               : launch_recurrent(p, exact, geo.threads, geo.smem, st);
+    };
+    if (cs != cudaStreamCaptureStatusNone || dev < 0 || dev >= 64) return launch();
+    RecurrentGate& g = gates[dev];
+    std::lock_guard<std::mutex> lock(g.m);
+    if (!g.last) {
+        e = cudaEventCreateWithFlags(&g.last, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            g.last = nullptr;
+            return e;
+        }
+    } else {
+        e = cudaStreamWaitEvent(st, g.last, 0);
+        if (e != cudaSuccess) return e;
+    }
+    e = launch();
+    if (e != cudaSuccess) return e;
+    return cudaEventRecord(g.last, st);
+}
+
 // Queue the kernels of one run.  `scratch` holds the layout, `ctrl` the
 // control block (the set-up kernel zeroes its counters and flags).
 rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t max_len, char* scratch,
@@ -782,7 +826,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     if (e != cudaSuccess) return cuda_fail(e, "state set-up launch");
     launches += 1;
     if (timed) record(pl, 3, a.st);
-    e = geo.kernel == 3 ? launch_tc_recurrent(p, geo.smem, a.st) : launch_recurrent(p, exact, geo.threads, geo.smem, a.st);
+    e = launch_recurrent_ordered(p, geo, exact, a.st);
     if (e != cudaSuccess) return cuda_fail(e, "recurrent launch");
     launches += 1;
     if (timed) record(pl, 4, a.st);

@@ -231,6 +231,58 @@ def test_timing_and_launch_count():
     orc.rnn_plan_destroy(plan)
 
 
+CONCURRENT = {
+    # recurrent grids that fill the GPU: the staged kernel, the dataflow
+    # kernel, the tensor-core kernel
+    "staged": (dict(op="GRU", direction="bidirectional", seq=24, batch=64, input_size=32, hidden_size=1024,
+                    lens=("uniform", 1, 24)), "exact", 1),
+    "dataflow": (dict(op="LSTM", direction="forward", seq=24, batch=32, input_size=32, hidden_size=512,
+                      with_P=True), "exact", 2),
+    "tensor_core": (dict(op="GRU", direction="bidirectional", seq=24, batch=64, input_size=32, hidden_size=512,
+                         linear_before_reset=1), "tf32", 3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CONCURRENT))
+def test_two_plans_on_two_streams(name):
+    """Runs of two plans queued on two streams without host waits in between
+    give the same bits as one run alone, and none of them times out: the
+    recurrent kernels, which need all their CTAs resident at once, must not
+    split the SMs between them."""
+    import torch
+    kw, mode, kernel = CONCURRENT[name]
+    kw = dict(kw)
+    op, direction = kw.pop("op"), kw.pop("direction")
+    c = make_case(op, direction, kw.pop("seq"), kw.pop("batch"), kw.pop("input_size"), kw.pop("hidden_size"),
+                  seed=31, h0_scale=0.5, **kw)
+    ref = gpu_case(c, mode)
+    t = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in c.tensors().items()}
+    plans, outs = [], []
+    for _ in range(2):
+        pl = orc.rnn_plan_create(c.op, c.direction, c.hidden_size, c.input_size, clip=c.clip,
+                                 linear_before_reset=c.linear_before_reset)
+        orc.rnn_plan_set_mode(pl, mode)
+        orc.rnn_plan_debug_barrier(pl, 200_000_000, -1)     # a starved wait gives up after 0.2 s
+        plans.append(pl)
+        outs.append([torch.full(c.y_shape(), float("nan"), device="cuda"),
+                     torch.full(c.state_shape(), float("nan"), device="cuda"),
+                     torch.full(c.state_shape(), float("nan"), device="cuda") if c.op == "LSTM" else None])
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for pl, o, st in zip(plans, outs, streams):
+            orc.rnn_run(pl, t["X"], t["W"], t["R"], t["B"], t["sequence_lens"], t["initial_h"], t["initial_c"],
+                        t["P"], o[0], o[1], o[2], st)
+    torch.cuda.synchronize()
+    for pl, o in zip(plans, outs):
+        assert orc.rnn_plan_get_launch(pl)["kernel"] == kernel
+        orc.rnn_plan_sync(pl)
+        for x, y in zip(ref, o):
+            if x is not None:
+                assert_bits_equal(x, y.cpu().numpy())
+        orc.rnn_plan_destroy(pl)
+
+
 # ------------------------------------------------------------ workloads
 
 def _sample_rows(c, k):
