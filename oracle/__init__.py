@@ -74,6 +74,8 @@ def _configure(lib):
     lib.oracle_activation_n.restype = None
     lib.oracle_projection.argtypes = [L, L, L, fp, fp, fp]
     lib.oracle_projection.restype = None
+    lib.oracle_rnn_cell.argtypes = [L, L, ctypes.c_char_p, ctypes.c_float, L, fp, fp, fp, fp, fp, fp]
+    lib.oracle_rnn_cell.restype = ctypes.c_int
     return lib
 
 
@@ -296,3 +298,19 @@ def projection(X2, Wd):
     out = np.empty((rows, cols), np.float32)
     lib.oracle_projection(rows, I, cols, _fptr(X2), _fptr(Wd), _fptr(out))
     return out
+
+
+def rnn_cell(hidden_size, input_size, X, H, W, R, B, activation="Tanh", clip=float("inf")):
+    """One RNN cell (page "RNNCell", RNNCell-3): Ho = f(clip(X.W^T + H.R^T + B)),
+    B the summed bias, in the sequence operator's rounding order.
+    X [batch, I], H [batch, hidden], W [hidden, I], R [hidden, hidden], B [hidden]."""
+    lib = _load()
+    X, H, W, R, B = map(_f32, (X, H, W, R, B))
+    N = X.shape[0]
+    Ho = np.zeros((N, int(hidden_size)), np.float32)
+    st = lib.oracle_rnn_cell(int(hidden_size), int(input_size),
+                             None if activation is None else activation.encode(), float(clip), N,
+                             _fptr(X), _fptr(H), _fptr(W), _fptr(R), _fptr(B), _fptr(Ho))
+    if st != 0:
+        raise OracleError(st)
+    return Ho

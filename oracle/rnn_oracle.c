@@ -33,6 +33,9 @@
  * bit parity with that library is unpinned; accuracy is pinned by the tests
  * against double-precision math.
  *
+ * oracle_rnn_cell computes the single RNN cell of page "RNNCell" (RNNCell-3)
+ * in the same rounding order (its header gives the reading).
+ *
  * Status codes: 0 ok, 1 invalid argument, 2 invalid input.
  */
 #include <stdint.h>
@@ -589,6 +592,42 @@ int oracle_rnn(int op, int direction, long hidden_size, long input_size,
                            alpha, n_alpha, beta, n_beta, clip, layout, lbr,
                            input_forget, seq, batch, X, W, R, B, lens, h0, c0, P,
                            Y, Yh, Yc, 0, batch);
+}
+
+/* ------------------------------------------------------------ single cell */
+
+/* One RNN cell (page "RNNCell", RNNCell-3: Detailed description, Attributes,
+ * Inputs, Outputs): Ho = f(X.W^T + H.R^T + B), where B is the sum of the
+ * input and recurrence biases, given once, and clip (when not +infinity, its
+ * default) clamps f's input to [-clip, clip].  The page fixes no rounding
+ * order; this follows the sequence operator's: each product with one
+ * accumulator, k increasing from +0, then pre = (xw + rec) + B.
+ * X [batch, I], H [batch, hidden], W [hidden, I], R [hidden, hidden],
+ * B [hidden], Ho [batch, hidden]; f is relu, sigmoid or tanh (any case,
+ * NULL = tanh); clip must be positive (NaN, 0 and negative values are
+ * invalid).  Every NaN written to Ho is 0x7FC00000.  All arrays are
+ * required.  Returns 0, or 1 for an invalid argument. */
+int oracle_rnn_cell(long hidden_size, long input_size, const char* activation, float clip,
+                    long batch, const float* X, const float* Hprev, const float* W,
+                    const float* R, const float* B, float* Ho)
+{
+    if (hidden_size <= 0 || input_size < 0 || batch < 0) return 1;
+    int fn = activation ? o_name_to_fn(activation) : OA_TANH;
+    if (fn != OA_RELU && fn != OA_SIGMOID && fn != OA_TANH) return 1;
+    if (!(clip > 0.0f)) return 1;
+    if (batch > 0 && (!Hprev || !W || !R || !B || !Ho || (input_size > 0 && !X))) return 1;
+    const long H = hidden_size, I = input_size;
+    for (long n = 0; n < batch; ++n) {
+        for (long j = 0; j < H; ++j) {
+            float xw = o_dot(X + n * I, W + j * I, I);
+            float rec = o_dot(Hprev + n * H, R + j * H, H);
+            float pre = (xw + rec) + B[j];
+            if (pre > clip) pre = clip;
+            else if (pre < -clip) pre = -clip;
+            Ho[n * H + j] = o_canon(oracle_activation(fn, 0.0f, 0.0f, pre));
+        }
+    }
+    return 0;
 }
 
 /* XW = X . W[d]^T for all rows of X viewed as [rows, I] (the input

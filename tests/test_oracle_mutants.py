@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 import test_oracle_brute as tb
+import test_oracle_cell as tcell
 import test_oracle_closed_form as tc
 import test_oracle_hand as th
 import test_oracle_invariants as ti
@@ -60,6 +61,17 @@ MUTANTS = [
      "case OA_RELU:            return !(x >= 0.0f) ? 0.0f : x;"),
     ("NaN not canonical", "return o_isnan(x) ? o_from_bits(0x7FC00000u) : x;", "return x;"),
     ("leakyrelu default alpha", "case OA_LEAKYRELU: return 0.01f;", "case OA_LEAKYRELU: return 0.1f;"),
+    ("cell drops B", "float pre = (xw + rec) + B[j];", "float pre = xw + rec;"),
+    ("cell B added to rec first", "float pre = (xw + rec) + B[j];", "float pre = xw + (rec + B[j]);"),
+    ("cell R transposed", "float rec = o_dot(Hprev + n * H, R + j * H, H);",
+     "float rec = 0.0f; for (long k = 0; k < H; ++k) rec = rec + Hprev[n * H + k] * R[k * H + j];"),
+    ("cell W and R exchanged", "float xw = o_dot(X + n * I, W + j * I, I);",
+     "float xw = o_dot(X + n * I, R + j * I, I);"),
+    ("cell clip lower bound sign", "else if (pre < -clip) pre = -clip;", "else if (pre < -clip) pre = clip;"),
+    ("cell default sigmoid", "int fn = activation ? o_name_to_fn(activation) : OA_TANH;",
+     "int fn = activation ? o_name_to_fn(activation) : OA_SIGMOID;"),
+    ("cell accepts affine", "if (fn != OA_RELU && fn != OA_SIGMOID && fn != OA_TANH) return 1;",
+     "if (fn < 0) return 1;"),
 ]
 
 
@@ -84,6 +96,19 @@ def _battery():
     checks.append(("resolve defaults", ti.test_resolve_defaults_and_case_and_single_set))
     checks.append(("rnncell3", lambda: ti.test_rnncell3_one_step("tanh")))
     checks.append(("bnns gru", ti.test_bnns_gru_reset_after_matmul))
+    for p in tcell.FILES:
+        checks.append((f"cell golden {os.path.basename(p)}", lambda p=p: tcell.test_cell_golden(p)))
+    for s in range(6):
+        checks.append((f"cell float64 {s}", lambda s=s: tcell.test_cell_matches_float64(s)))
+    checks.append(("cell defaults", tcell.test_cell_default_activation_is_tanh_and_default_clip_clamps_nothing))
+    for act in tcell.ACTS:
+        for clip in (None, 0.25):
+            checks.append((f"cell sequence {act} {clip}",
+                           lambda a=act, c=clip: tcell.test_cell_is_the_sequence_operator_at_one_step(a, c)))
+    checks.append(("cell clip", tcell.test_cell_clip_saturates_exactly))
+    checks.append(("cell nan", tcell.test_cell_nan_is_canonical))
+    checks.append(("cell rejects affine", lambda: tcell.test_cell_rejects_what_the_page_excludes(
+        dict(activation="Affine"))))
     for fn in (tm.test_exp_special_values, tm.test_log_special_values, tm.test_tanh_special_values,
                tm.test_relu_points, tm.test_leaky_thresholded_points,
                tm.test_hardsigmoid_affine_softsign_points, tm.test_softplus_points,
@@ -96,7 +121,7 @@ def _battery():
     for name, fn in checks:
         try:
             fn()
-        except Exception:
+        except (Exception, pytest.fail.Exception):     # pytest.raises reports through the latter
             failed.append(name)
     return failed
 
