@@ -148,10 +148,20 @@ def algorithmic(case):
     return rec, proj, proj_bytes
 
 
-def source_digest():
+KERNEL_SOURCES = {
+    "recurrence": ["k_recur.cuh", "k_recur2.cuh", "k_recur_rnn.cu", "k_recur_gru.cu", "k_recur_lstm.cu",
+                   "k_recur_tc.cu", "tma.cuh", "exact_math.cuh", "rnn_internal.h"],
+    "projection": ["k_proj.cu", "k_proj_tc.cu", "tma.cuh", "rnn_internal.h"],
+    "cell": ["k_cell.cu", "exact_math.cuh", "rnn_internal.h"],
+}
+
+
+def source_digest(kernel):
+    """Digest of the sources a kernel is built from: a committed ncu traffic
+    figure applies only while they are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "onnx_recurrent_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES.get(kernel, sorted(os.listdir(csrc))):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -176,12 +186,80 @@ def profiled_traffic(kernel, workload, mode, digest):
 
 # ------------------------------------------------------------ our arm
 
+class SequenceJob:
+    """One rnn_run of a sequence-operator workload per step."""
+
+    def __init__(self, args, orc, torch):
+        from onnx_recurrent_gb300.synth import WORKLOADS, workload
+        self.case = c = workload(args.workload, lbr=args.lbr)
+        self.host = {k: v for k, v in c.tensors().items() if v is not None}
+        self.plan = orc.rnn_plan_create(c.op, c.direction, c.hidden_size, c.input_size,
+                                        activations=c.activations, alpha=c.alpha, beta=c.beta,
+                                        clip=c.clip, layout=c.layout,
+                                        linear_before_reset=c.linear_before_reset,
+                                        input_forget=c.input_forget)
+        self.out_shapes = [c.y_shape(), c.state_shape()] + ([c.state_shape()] if c.op == "LSTM" else [])
+        self.cells = c.cell_steps()
+        self.rec_flops, self.proj_flops, _ = algorithmic(c)
+        self.config = {"workload": args.workload, "description": WORKLOADS.get(args.workload, ""),
+                       "op": c.op, "direction": c.direction, "seq": c.seq, "batch": c.batch,
+                       "input": c.input_size, "hidden": c.hidden_size,
+                       "valid_cell_steps_per_step": c.valid_cell_steps()}
+        self.orc = orc
+
+    def run(self, dv, outs, stream):
+        Yc = outs[2] if len(outs) > 2 else None
+        self.orc.rnn_run(self.plan, dv["X"], dv["W"], dv["R"], dv.get("B"), dv.get("sequence_lens"),
+                         dv.get("initial_h"), dv.get("initial_c"), dv.get("P"), outs[0], outs[1], Yc, stream)
+
+    def cpu_baseline(self):
+        return cpu_baseline(self.case)
+
+
+class CellJob:
+    """One rnn_cell_run (RNNCell-3, a single step of batch rows) per step."""
+
+    def __init__(self, args, orc, torch):
+        from onnx_recurrent_gb300.synth import CELL_WORKLOADS, cell_workload
+        self.case = c = cell_workload(args.workload)
+        self.host = c.tensors()
+        self.plan = orc.rnn_cell_plan_create(c.hidden_size, c.input_size, activation=c.activation, clip=c.clip)
+        self.out_shapes = [(c.batch, c.hidden_size)]
+        self.cells = c.batch
+        self.rec_flops = 2.0 * c.batch * c.hidden_size * c.hidden_size
+        self.proj_flops = 2.0 * c.batch * c.hidden_size * c.input_size
+        self.config = {"workload": args.workload, "description": CELL_WORKLOADS[args.workload],
+                       "op": "RNNCell", "batch": c.batch, "input": c.input_size, "hidden": c.hidden_size,
+                       "activation": c.activation}
+        self.orc = orc
+
+    def run(self, dv, outs, stream):
+        self.orc.rnn_cell_run(self.plan, dv["X"], dv["H"], dv["W"], dv["R"], dv["B"], outs[0], stream)
+
+    def cpu_baseline(self, budget_s=12.0):
+        """The oracle's cell, single-threaded, whole batch per call, repeated
+        while the time spent stays under about `budget_s`."""
+        import oracle
+        c = self.case
+        oracle.build()
+        calls = 0
+        t0 = time.perf_counter()
+        while True:
+            oracle.rnn_cell(c.hidden_size, c.input_size, c.X, c.H, c.W, c.R, c.B, activation=c.activation,
+                            clip=float("inf") if c.clip is None else c.clip)
+            calls += 1
+            dt = time.perf_counter() - t0
+            if dt + dt / calls > budget_s:
+                break
+        return {"value": round(calls * c.batch / dt, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{calls} calls over all {c.batch} batch rows, {dt:.1f} s"}
+
+
 def run_ours(args, ws, rank, local):
-    import numpy as np
     import torch
 
     import onnx_recurrent_gb300 as orc
-    from onnx_recurrent_gb300.synth import WORKLOADS, workload
+    from onnx_recurrent_gb300.synth import CELL_WORKLOADS
 
     torch.cuda.set_device(local)
     dist = None
@@ -195,23 +273,16 @@ def run_ours(args, ws, rank, local):
     orc.build()
     orc.load()
 
-    case = workload(args.workload, lbr=args.lbr)
-    dev = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in case.tensors().items()}
-    plan = orc.rnn_plan_create(case.op, case.direction, case.hidden_size, case.input_size,
-                               activations=case.activations, alpha=case.alpha, beta=case.beta,
-                               clip=case.clip, layout=case.layout,
-                               linear_before_reset=case.linear_before_reset,
-                               input_forget=case.input_forget)
+    job = (CellJob if args.workload in CELL_WORKLOADS else SequenceJob)(args, orc, torch)
+    plan = job.plan
     orc.rnn_plan_set_mode(plan, args.mode)
-    Y = torch.empty(case.y_shape(), device="cuda")
-    Yh = torch.empty(case.state_shape(), device="cuda")
-    Yc = torch.empty(case.state_shape(), device="cuda") if case.op == "LSTM" else None
+    dev = {k: torch.from_numpy(v).cuda() for k, v in job.host.items()}
+    outs = [torch.empty(sh, device="cuda") for sh in job.out_shapes]
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step():
-        orc.rnn_run(plan, dev["X"], dev["W"], dev["R"], dev["B"], dev["sequence_lens"],
-                    dev["initial_h"], dev["initial_c"], dev["P"], Y, Yh, Yc, stream)
+        job.run(dev, outs, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -256,13 +327,12 @@ def run_ours(args, ws, rank, local):
     # stream, downloads on another copy stream, with two sets of device
     # buffers, so batch i+1's upload and batch i-1's download ride the copy
     # engines while batch i computes
-    host_in = {k: (None if v is None else torch.from_numpy(v).pin_memory()) for k, v in case.tensors().items()}
+    host_in = {k: torch.from_numpy(v).pin_memory() for k, v in job.host.items()}
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    devs = [dev, {k: (None if v is None else torch.empty_like(v)) for k, v in dev.items()}]
-    outs = [[t for t in (Y, Yh, Yc) if t is not None]]
-    outs.append([torch.empty_like(t) for t in outs[0]])
-    host_outs = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[0]] for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values() if t is not None)
+    devs = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
+    bufs = [outs, [torch.empty_like(t) for t in outs]]
+    host_outs = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_outs[0])
     E = K
     ev = lambda: torch.cuda.Event()
@@ -274,19 +344,16 @@ def run_ours(args, ws, rank, local):
     s_out.wait_event(e_start)
     for i in range(E):
         j = i % 2
-        dv, ov = devs[j], outs[j]
+        dv, ov = devs[j], bufs[j]
         if i >= 2:
             s_in.wait_event(run_done[j])       # the run of batch i-2 has read these inputs
             stream.wait_event(out_done[j])     # batch i-2's outputs have left these buffers
         with torch.cuda.stream(s_in):
             for k, v in host_in.items():
-                if v is not None:
-                    dv[k].copy_(v, non_blocking=True)
+                dv[k].copy_(v, non_blocking=True)
         in_done[j].record(s_in)
         stream.wait_event(in_done[j])
-        Ys = ov + [None] * (3 - len(ov))
-        orc.rnn_run(plan, dv["X"], dv["W"], dv["R"], dv["B"], dv["sequence_lens"], dv["initial_h"],
-                    dv["initial_c"], dv["P"], Ys[0], Ys[1], Ys[2], stream)
+        job.run(dv, ov, stream)
         run_done[j].record(stream)
         s_out.wait_event(run_done[j])
         with torch.cuda.stream(s_out):
@@ -309,7 +376,7 @@ def run_ours(args, ws, rank, local):
             dist.destroy_process_group()
         return
 
-    cells = case.cell_steps()
+    cells = job.cells
     value = cells * K * ws / (total_ms / 1e3)
     e2e_value = cells * E * ws / (e2e_ms / 1e3)
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
@@ -318,13 +385,23 @@ def run_ours(args, ws, rank, local):
     clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
     exact = args.mode == "exact"
     alu_peak = sms * 128 * (1 if exact else 2) * clock_mhz * 1e6          # FLOP/s
-    rec_flops, proj_flops, proj_bytes = algorithmic(case)
+    rec_flops, proj_flops = job.rec_flops, job.proj_flops
     avg = {k: (v / runs if runs else 0.0) for k, v in kern_ms.items()}
+    if isinstance(job, CellJob):
+        avg = {"cell": avg["recurrence"]}      # one kernel, timed in the recurrence slot
     dominant = max(avg, key=avg.get)
-    digest = source_digest()
 
     def roof(kernel):
         ms = avg[kernel]
+        if kernel == "cell":
+            flops = rec_flops + proj_flops
+            ach = flops / (ms / 1e3) / 1e12 if ms else 0.0
+            return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
+                    "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
+                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
+                    "kernel": "rnn_cell_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": flops,
+                    "peak_note": f"{'no' if exact else 'fused'} multiply-add: {sms} SMs x 128 FP32 "
+                                 f"lanes x {'1' if exact else '2'} FLOP x {clock_mhz:.0f} MHz (derived)"}
         if kernel == "recurrence" and geometry.get("kernel") == 3:
             # fp16 tensor-core products (tcgen05 kind::f16): the measured bf16
             # burst peak, fp16 and bf16 having the same nominal dense rate
@@ -332,14 +409,14 @@ def run_ours(args, ws, rank, local):
             ach = rec_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
                     "frac": round(ach / peak, 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, digest),
+                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
                     "kernel": "rnn_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": rec_flops,
                     "peak_note": "of measured bf16 burst (fp16 operands, same nominal rate)"}
         if kernel == "recurrence":
             ach = rec_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
                     "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, digest),
+                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
                     "kernel": "rnn_dataflow_kernel" if geometry.get("kernel") == 2 else "rnn_recurrent_kernel",
                     "avg_ms": round(ms, 5),
                     "algorithmic_flops_per_launch": rec_flops,
@@ -353,14 +430,14 @@ def run_ours(args, ws, rank, local):
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
                     "frac": round(ach / peak, 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, digest),
+                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
                     "kernel": "proj_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": proj_flops,
                     "peak_note": "of measured bf16 burst" + ("" if args.mode == "bf16" else " x 1.1/2.25 (TF32)")}
         if kernel == "projection":
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
                     "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, digest),
+                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
                     "kernel": "proj_tma_kernel", "avg_ms": round(ms, 5),
                     "algorithmic_flops_per_launch": proj_flops}
         return {"kernel": kernel, "avg_ms": round(ms, 5)}
@@ -373,12 +450,8 @@ def run_ours(args, ws, rank, local):
         "dtype": {"exact": "f32", "fast": "f32", "tf32": "f32 (tf32 projection)",
                   "bf16": "f32 (bf16 projection)"}[args.mode],
         "data": "synthetic (seeded, see synth.py)",
-        "config": {"workload": args.workload, "description": WORKLOADS.get(args.workload, ""),
-                   "op": case.op, "direction": case.direction, "seq": case.seq,
-                   "batch": case.batch, "input": case.input_size, "hidden": case.hidden_size,
-                   "mode": args.mode, "l2": "flushed between timed steps (256 MiB write)",
-                   "parallelism": f"replicas x{ws}", "geometry": geometry,
-                   "valid_cell_steps_per_step": case.valid_cell_steps()},
+        "config": dict(job.config, mode=args.mode, l2="flushed between timed steps (256 MiB write)",
+                       parallelism=f"replicas x{ws}", geometry=geometry),
         "roofline": roof(dominant),
         "kernels": {k: roof(k) for k in avg if avg[k] > 0},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -389,7 +462,7 @@ def run_ours(args, ws, rank, local):
         "impl": "ours",
     }
     if not args.no_cpu_baseline and ws == 1:
-        result["cpu_baseline"] = cpu_baseline(case)
+        result["cpu_baseline"] = job.cpu_baseline()
     emit(result, args.out)
     if dist:
         dist.destroy_process_group()
@@ -466,7 +539,9 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return
     import oracle
-    from onnx_recurrent_gb300.synth import WORKLOADS, workload
+    from onnx_recurrent_gb300.synth import CELL_WORKLOADS, WORKLOADS, cell_workload, workload
+    if args.workload in CELL_WORKLOADS:
+        return run_reference_cell(args, ws)
     case = workload(args.workload, lbr=args.lbr)
     a = case.attrs()
     t = case.tensors()
@@ -498,6 +573,37 @@ def run_reference(args, ws, rank):
                            "sample": f"one batch row ({case.seq} steps) of the workload per step"},
           "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
                   "d2h_bytes_per_step": 0},
+          "gpu_launches": 0}, args.out)
+
+
+def run_reference_cell(args, ws):
+    """The oracle's cell on one batch row of the cell workload per step."""
+    import oracle
+    from onnx_recurrent_gb300.synth import CELL_WORKLOADS, cell_workload
+    c = cell_workload(args.workload)
+    oracle.build()
+    clip = float("inf") if c.clip is None else c.clip
+
+    def one_row(r):
+        oracle.rnn_cell(c.hidden_size, c.input_size, c.X[r:r + 1], c.H[r:r + 1], c.W, c.R, c.B,
+                        activation=c.activation, clip=clip)
+    for i in range(args.warmup):
+        one_row(i % c.batch)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one_row(i % c.batch)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    emit({"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+          "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+          "data": "synthetic (seeded, see synth.py)",
+          "config": {"workload": args.workload, "description": CELL_WORKLOADS[args.workload],
+                     "mode": "exact", "sample": "one batch row per step"},
+          "impl": "reference",
+          "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                           "sample": "one batch row of the cell workload per step"},
+          "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
           "gpu_launches": 0}, args.out)
 
 

@@ -244,6 +244,42 @@ rnn_status rnn_run_static_scratch(rnn_plan_t plan, int64_t seq_length, int64_t b
                                   const float* P, float* Y, float* Y_h, float* Y_c,
                                   void* stream);
 
+/* Single RNN cell (page "RNNCell", RNNCell-3: Detailed description,
+ * Attributes, Inputs, Outputs):  Ho = f(clip(X.W^T + H.R^T + B)), where B is
+ * the sum of the input and recurrence biases, given once.
+ *
+ * rnn_cell_plan_create: `activation` is "Relu", "Sigmoid" or "Tanh" (any
+ * case; NULL = Tanh, the page's default; any other name is
+ * RNN_ERR_INVALID_ARGUMENT, as are hidden_size <= 0 and input_size < 0).
+ * `clip` clamps f's input to [-clip, clip]; it must be positive, and
+ * +INFINITY (the page's default) clamps nothing; NaN, 0 or a negative value
+ * is RNN_ERR_INVALID_ARGUMENT.  The result is an RNN plan (forward, layout 0,
+ * one activation) marked as a cell: rnn_plan_set_mode, rnn_plan_set_weights,
+ * rnn_plan_sync, the timing calls and rnn_plan_destroy apply to it, and
+ * rnn_run works on it as on any forward RNN plan.
+ *
+ * rnn_cell_run: device pointers, row-major fp32:
+ *     X  [batch_size, input_size]       H  [batch_size, hidden_size]
+ *     W  [hidden_size, input_size]      R  [hidden_size, hidden_size]
+ *     B  [hidden_size]                  Ho [batch_size, hidden_size] (out)
+ * X, H, W, R and B are read only and stay the caller's; Ho must not overlap
+ * them.  H, B and Ho are required (W and R may be NULL once constant
+ * weights are set with rnn_plan_set_weights, shapes [1, hidden, input] and
+ * [1, hidden, hidden]; X may be NULL when input_size is 0).  One kernel
+ * computes every cell: xw and rec each with one accumulator from +0, k
+ * increasing, then pre = (xw + rec) + B, clip, f, canonical NaN.  Exact
+ * mode rounds every product and sum separately and uses the library's own
+ * tanh and sigmoid, bit-identical to the sequence operator run for one
+ * step with bias [B | -0]; every other mode (FAST, FAST_TF32, FAST_BF16)
+ * runs the FAST arithmetic (fused multiply-add, CUDA's tanhf / expf), within
+ * FAST's 1e-5.  batch_size 0 returns RNN_OK with nothing queued and no
+ * pointer read.  Stream-ordered and asynchronous; with timing on, the
+ * kernel is reported as the recurrence.  One call at a time per plan. */
+rnn_status rnn_cell_plan_create(rnn_plan_t* out, int64_t hidden_size, int64_t input_size,
+                                const char* activation, float clip);
+rnn_status rnn_cell_run(rnn_plan_t plan, int64_t batch_size, const float* X, const float* H,
+                        const float* W, const float* R, const float* B, float* Ho, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 const char* rnn_last_error(void);
 

@@ -158,6 +158,8 @@ struct rnn_plan {
 
     long long spin_limit_ns = kDefaultSpinNs;
     int skip_cta = -1;
+
+    bool cell = false;   // made by rnn_cell_plan_create
 };
 
 namespace {
@@ -1067,6 +1069,7 @@ rnn_status rnn_plan_sync(rnn_plan_t pl)
     if (!pl->ran) return RNN_OK;
     cudaError_t e = pl->done_ready ? cudaEventSynchronize(pl->done) : cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "waiting for the run");
+    if (!pl->ctrl) return RNN_OK;      // only cell runs so far: no device-side waits, no status word
     int st = 0;
     e = cudaMemcpy(&st, pl->ctrl + kCtrlStatusOffset, sizeof st, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
@@ -1180,6 +1183,70 @@ rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const fl
     cudaEventRecord(pl->done, a.st);
     pl->ran = true;
     pl->last_launches = launches;
+    return RNN_OK;
+}
+
+rnn_status rnn_cell_plan_create(rnn_plan_t* out, int64_t hidden_size, int64_t input_size, const char* activation,
+                                float clip)
+{
+    g_error.clear();
+    if (!out) return fail(RNN_ERR_INVALID_ARGUMENT, "out is NULL");
+    *out = nullptr;
+    const char* name = activation ? activation : "Tanh";
+    const int id = act_id(name);
+    if (id != act_id("Relu") && id != act_id("Sigmoid") && id != act_id("Tanh"))
+        return fail(RNN_ERR_INVALID_ARGUMENT, "a cell takes Relu, Sigmoid or Tanh, not '%s'", name);
+    if (!(clip > 0.0f)) return fail(RNN_ERR_INVALID_ARGUMENT, "clip must be positive (+infinity: no clip)");
+    const char* acts[1] = {name};
+    const float no_clip = std::nanf("");
+    rnn_status rs = rnn_plan_create(out, RNN_OP_RNN, RNN_DIR_FORWARD, hidden_size, input_size, acts, 1, nullptr, 0,
+                                    nullptr, 0, std::isinf(clip) ? no_clip : clip, 0, 0, 0);
+    if (rs != RNN_OK) return rs;
+    (*out)->cell = true;
+    return RNN_OK;
+}
+
+rnn_status rnn_cell_run(rnn_plan_t pl, int64_t batch_size, const float* X, const float* H, const float* W,
+                        const float* R, const float* B, float* Ho, void* stream)
+{
+    g_error.clear();
+    if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
+    if (!pl->cell) return fail(RNN_ERR_INVALID_ARGUMENT, "not a cell plan (rnn_cell_plan_create)");
+    if (batch_size < 0) return fail(RNN_ERR_INVALID_ARGUMENT, "batch_size must be >= 0");
+    pl->last_launches = 0;
+    if (batch_size == 0) return RNN_OK;     // nothing to read or write (the arrays may be empty, NULL)
+    if (!H || !B || !Ho) return fail(RNN_ERR_INVALID_ARGUMENT, "H, B and Ho are required");
+    if (pl->I > 0 && !X) return fail(RNN_ERR_INVALID_ARGUMENT, "X is required when input_size > 0");
+    const float* Wc = pl->const_weights ? pl->wk_const : W;     // K-major pack of a 1-gate W is W itself
+    const float* Rc = pl->const_weights ? pl->r_orig_const : R;
+    if (!Rc || (pl->I > 0 && !Wc)) return fail(RNN_ERR_INVALID_ARGUMENT, "W and R are required");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (pl->timing && !pl->events_ready) {
+        rnn_status rs = rnn_plan_set_timing(pl, 1);
+        if (rs != RNN_OK) return rs;
+    }
+    if (!pl->done_ready) {
+        cudaError_t e = cudaEventCreateWithFlags(&pl->done, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+        pl->done_ready = true;
+    }
+    if (pl->timing) {
+        pl->slot = (pl->slot + 1) % rnn_plan::kRing;
+        cudaError_t eh = harvest(pl, pl->slot);
+        if (eh != cudaSuccess) return cuda_fail(eh, "reading timing events");
+        for (bool& u : pl->ev_used[pl->slot]) u = false;
+        record(pl, 3, st);      // the cell kernel is timed as the recurrence (the one event pair)
+    }
+    cudaError_t e = launch_cell(X, H, Wc, Rc, B, Ho, batch_size, pl->I, pl->H, pl->act[0][0].fn, pl->has_clip,
+                                pl->clip, pl->mode == RNN_MODE_EXACT, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cell launch");
+    if (pl->timing) {
+        record(pl, 4, st);
+        pl->slot_pending[pl->slot] = true;
+    }
+    cudaEventRecord(pl->done, st);
+    pl->ran = true;
+    pl->last_launches = 1;
     return RNN_OK;
 }
 

@@ -176,6 +176,11 @@ cudaError_t launch_tc_state_init(const RecParams& p, cudaStream_t stream);
 // perm[rank] = n, rank = the number of rows longer than n or as long and
 // before it: the rows sorted by length, longest first (stable).
 cudaError_t launch_rank_rows(const int32_t* lens, int32_t* perm, int N, cudaStream_t stream);
+// Single RNN cell: Ho = f(clip((X.W^T + Hp.R^T) + B)); fn 0 Relu, 1 Tanh, 2
+// Sigmoid; X [N, I], Hp and Ho [N, H], W [H, I], R [H, H], B [H].
+cudaError_t launch_cell(const float* X, const float* Hp, const float* W, const float* R, const float* B, float* Ho,
+                        int64_t N, int64_t I, int64_t H, int fn, int has_clip, float clip, bool exact,
+                        cudaStream_t stream);
 
 // Exchange buffer 0 = initial_h (or 0), everything else 0; bar, flags = 0.
 cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream);

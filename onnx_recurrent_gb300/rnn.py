@@ -66,13 +66,15 @@ def load(path: str | None = None):
     lib.rnn_plan_debug_barrier.argtypes = [vp, i64, i32]
     lib.rnn_plan_last_launch_count.argtypes = [vp]
     lib.rnn_plan_last_launch_count.restype = i32
+    lib.rnn_cell_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, ctypes.c_char_p, f32]
+    lib.rnn_cell_run.argtypes = [vp, i64] + [vp] * 6 + [vp]
     lib.rnn_last_error.argtypes = []
     lib.rnn_last_error.restype = ctypes.c_char_p
     for name in ("rnn_plan_create", "rnn_run", "rnn_run_static_scratch", "rnn_plan_set_mode", "rnn_plan_set_weights",
                  "rnn_plan_sync", "rnn_plan_get_activation", "rnn_plan_set_launch",
                  "rnn_plan_get_launch", "rnn_plan_set_timing", "rnn_plan_last_timing",
                  "rnn_plan_timing_totals",
-                 "rnn_plan_debug_barrier"):
+                 "rnn_plan_debug_barrier", "rnn_cell_plan_create", "rnn_cell_run"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -289,6 +291,32 @@ def rnn_run_static_scratch(plan: Plan, X, W, R, B=None, sequence_lens=None, init
                                        _ptr(initial_c), _ptr(P), _ptr(Y), _ptr(Y_h), _ptr(Y_c),
                                        _stream(stream))
     _check(st)
+
+
+def rnn_cell_plan_create(hidden_size, input_size, activation="Tanh", clip=None) -> Plan:
+    """Single RNN cell (RNNCell-3); clip None = +infinity (no clipping)."""
+    h = ctypes.c_void_p()
+    c = float("inf") if clip is None else float(clip)
+    _check(load().rnn_cell_plan_create(ctypes.byref(h), int(hidden_size), int(input_size),
+                                       None if activation is None else activation.encode(), c))
+    plan = Plan(h, "RNN", "forward", int(hidden_size), int(input_size), 0)
+    plan.cell = True
+    return plan
+
+
+def rnn_cell_run(plan: Plan, X, H, W, R, B, Ho, stream=None):
+    """Ho = f(clip(X.W^T + H.R^T + B)) on CUDA tensors: X [batch, input],
+    H and Ho [batch, hidden], W [hidden, input], R [hidden, hidden], B [hidden]."""
+    batch = H.shape[0]
+    hs, inp = plan.hidden_size, plan.input_size
+    _need(X, (batch, inp), "X")
+    _need(H, (batch, hs), "H")
+    _need(W, (hs, inp), "W")
+    _need(R, (hs, hs), "R")
+    _need(B, (hs,), "B")
+    _need(Ho, (batch, hs), "Ho")
+    _check(load().rnn_cell_run(plan.handle, int(batch), _ptr(X), _ptr(H), _ptr(W), _ptr(R), _ptr(B),
+                               _ptr(Ho), _stream(stream)))
 
 
 def run(plan: Plan, X, W, R, B=None, sequence_lens=None, initial_h=None, initial_c=None, P=None,

@@ -186,6 +186,57 @@ def workload(name: str, *, lbr: int = 0, initial_h_zero: bool = False) -> RNNCas
     raise KeyError(name)
 
 
+@dataclass
+class CellCase:
+    """One call of the single RNN cell (RNNCell-3): attributes plus host inputs
+    X [batch, input], H [batch, hidden], W [hidden, input], R [hidden, hidden],
+    B [hidden] (the summed bias)."""
+    batch: int
+    input_size: int
+    hidden_size: int
+    activation: str = "Tanh"
+    clip: Optional[float] = None
+    X: np.ndarray = None
+    H: np.ndarray = None
+    W: np.ndarray = None
+    R: np.ndarray = None
+    B: np.ndarray = None
+    name: str = ""
+
+    def tensors(self) -> dict:
+        return dict(X=self.X, H=self.H, W=self.W, R=self.R, B=self.B)
+
+
+def make_cell_case(batch, input_size, hidden_size, *, seed=0, activation="Tanh", clip=None,
+                   w_scale=None, name="") -> CellCase:
+    """Draw order X, H, W, R, B: X ~ U(-1, 1), H ~ U(-0.5, 0.5), W and R ~ U(-s, s)
+    (default s = 1/sqrt(hidden)), B ~ U(-0.1, 0.1)."""
+    d = _Draw(seed)
+    N, I, Hs = batch, input_size, hidden_size
+    s = (1.0 / np.sqrt(Hs)) if w_scale is None else w_scale
+    X = d.uniform((N, I), -1.0, 1.0)
+    H = d.uniform((N, Hs), -0.5, 0.5)
+    W = d.uniform((Hs, I), -s, s)
+    R = d.uniform((Hs, Hs), -s, s)
+    B = d.uniform((Hs,), -0.1, 0.1)
+    return CellCase(N, I, Hs, activation, clip, X, H, W, R, B, name)
+
+
+CELL_WORKLOADS = {
+    "rnncell_b1_i16_h128": "RNNCell-3 single step, batch 1, input 16, hidden 128, Tanh (the page's example shapes)",
+    "rnncell_b256_i1024_h1024": "RNNCell-3 single step, batch 256, input 1024, hidden 1024, Tanh",
+}
+
+
+def cell_workload(name: str) -> CellCase:
+    """Seeded inputs (seed 0) of a named single-cell workload."""
+    if name == "rnncell_b1_i16_h128":
+        return make_cell_case(1, 16, 128, name=name)
+    if name == "rnncell_b256_i1024_h1024":
+        return make_cell_case(256, 1024, 1024, name=name)
+    raise KeyError(name)
+
+
 ACTIVATIONS = ["Relu", "Tanh", "Sigmoid", "Affine", "LeakyRelu", "ThresholdedRelu",
                "ScaledTanh", "HardSigmoid", "Elu", "Softsign", "Softplus"]
 

@@ -108,3 +108,39 @@ def test_product_does_not_import_or_link_the_oracle():
                     text = fh.read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "rnn_oracle" not in text and "liboracle" not in text, f
+
+
+# ------------------------------------------------------------ single cell
+
+@pytest.mark.parametrize("act", ["Relu", "sigmoid", "TANH", None])
+def test_cell_plan_create_resolves_the_page_activations(lib, act):
+    p = orc.rnn_cell_plan_create(16, 8, activation=act, clip=2.0)
+    name, _, _ = orc.rnn_plan_get_activation(p, 0, 0)
+    assert name == ("tanh" if act is None else act.lower())
+    orc.rnn_plan_destroy(p)
+
+
+@pytest.mark.parametrize("kw", [dict(activation="Affine"), dict(activation="LeakyRelu"),
+                                dict(activation="NoSuch"), dict(clip=0.0), dict(clip=-2.0),
+                                dict(clip=float("nan")), dict(hidden_size=0), dict(input_size=-1)])
+def test_cell_plan_create_rejects(lib, kw):
+    args = dict(hidden_size=4, input_size=3, activation="Tanh", clip=None)
+    args.update(kw)
+    with pytest.raises(rb.RNNError) as e:
+        orc.rnn_cell_plan_create(**args)
+    assert e.value.status == 1
+
+
+def test_cell_run_checks_before_device_work(lib):
+    seq_plan = orc.rnn_plan_create("RNN", "forward", 4, 3)
+    cell = orc.rnn_cell_plan_create(4, 3)
+    nul = ctypes.c_void_p()
+    st = lib.rnn_cell_run(seq_plan.handle, 2, nul, nul, nul, nul, nul, nul, nul)
+    assert st == 1 and "cell" in orc.rnn_last_error()
+    st = lib.rnn_cell_run(cell.handle, 2, nul, nul, nul, nul, nul, nul, nul)
+    assert st == 1
+    st = lib.rnn_cell_run(cell.handle, -1, nul, nul, nul, nul, nul, nul, nul)
+    assert st == 1
+    assert lib.rnn_cell_run(cell.handle, 0, nul, nul, nul, nul, nul, nul, nul) == 0   # batch 0: nothing read
+    orc.rnn_plan_destroy(seq_plan)
+    orc.rnn_plan_destroy(cell)
