@@ -192,6 +192,18 @@ __global__ void rank_rows_kernel(const int32_t* __restrict__ lens, int32_t* __re
     }
 }
 
+__global__ void pack_r_split_kernel(const float* __restrict__ R, __half* __restrict__ Rp, int64_t H, int64_t rows)
+{
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const int64_t d = r / (3 * H), rem = r - d * 3 * H;
+        const int64_t u = rem < 2 * H ? rem / 2 : rem - 2 * H;
+        const int64_t g = rem < 2 * H ? rem % 2 : 2;
+        const float* src = R + (d * 3 * H + g * H + u) * H;
+        __half* dst = Rp + r * H;
+        for (int64_t k = threadIdx.x; k < H; k += blockDim.x) dst[k] = __float2half_rn(src[k]);
+    }
+}
+
 // Tensor-core kernel: hx[b][d][r][u] (fp16, 128 rows) = initial_h for b = 0
 // and r < N, else 0; step counters 0.
 __global__ void tc_state_init_kernel(const RecParams p)
@@ -208,11 +220,24 @@ __global__ void tc_state_init_kernel(const RecParams p)
             v = p.h0[si];
         }
         hx[i] = __float2half_rn(v);
+        if (p.rhbuf) reinterpret_cast<__half*>(p.rhbuf)[i] = __float2half_rn(0.0f);   // GRU lbr = 0: r (.) h
     }
-    if (blockIdx.x == 0 && threadIdx.x < p.D) p.bar[threadIdx.x] = 0u;
+    if (blockIdx.x == 0 && threadIdx.x < p.D) {
+        p.bar[threadIdx.x] = 0u;
+        if (p.flags) p.flags[threadIdx.x] = 0u;
+    }
 }
 
 }  // namespace
+
+cudaError_t launch_pack_r_split(const float* R, void* Rp, int D, int64_t H, cudaStream_t stream)
+{
+    const int64_t rows = (int64_t)D * 3 * H;
+    if (rows <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::min<int64_t>(rows, 152 * 8);
+    pack_r_split_kernel<<<blocks, 128, 0, stream>>>(R, (__half*)Rp, H, rows);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_rank_rows(const int32_t* lens, int32_t* perm, int N, cudaStream_t stream)
 {

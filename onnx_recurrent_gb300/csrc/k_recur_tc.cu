@@ -181,13 +181,17 @@ __device__ __forceinline__ void tc_act_array(const ActSpec& a, float (&v)[K], co
     }
 }
 
-template <int OP>
+// TWO (GRU with linear_before_reset = 0): two products per step, z and r
+// over h, then the candidate over r (.) h once every CTA has published its
+// units' r (.) h; R's rows are packed z/r first, candidate rows after.
+template <int OP, bool TWO>
 __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_constant__ RecParams p)
 {
     constexpr int G = OP == 0 ? 1 : (OP == 1 ? 3 : 4);
     constexpr int UMAX = G == 1 ? 32 : TR_NPMAX / G;   // most units per CTA (register arrays)
     extern __shared__ __align__(1024) unsigned char tr_smem[];
     __shared__ __align__(8) uint64_t full[TR_STMAX], empty[TR_STMAX], r_ready, acc_ready, acc_free, mma_done;
+    __shared__ __align__(8) uint64_t acc2_ready, acc2_free;   // TWO: the candidate product's accumulators
     __shared__ uint32_t tmem_slot;
     __shared__ int s_abort;
     __shared__ float s_wb[TR_NPMAX], s_rb[TR_NPMAX], s_p[3][UMAX];
@@ -200,19 +204,23 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
     const int u0 = (int)(((long long)c * H) / C);
     const int U = (int)(((long long)(c + 1) * H) / C) - u0;
     const int NP = p.npad;                                  // padded gate columns (MMA N)
+    const int NP2 = TWO ? p.npad2 : 0;                      // TWO: padded candidate columns
     const int nkb = (H + TR_KB - 1) / TR_KB;
     unsigned char* rsm = base;                              // R slice: nkb blocks of [NP rows][128 B]
+    unsigned char* rsm2 = base + (size_t)nkb * NP * 128;    // TWO: nkb blocks of [NP2 rows][128 B]
     const int nst = p.slots;                                // h ring stages
-    unsigned char* hring = base + (size_t)nkb * NP * 128;   // nst blocks of [128 rows][128 B]
+    unsigned char* hring = rsm2 + (size_t)nkb * NP2 * 128;  // nst blocks of [128 rows][128 B]
     // per-step staging of the CTA's output tiles: Y [128][umax] fp32, h [128][umax] fp16, t per row
     float* s_y = reinterpret_cast<float*>(hring + (size_t)nst * kTrHStage);
     __half* s_h = reinterpret_cast<__half*>(s_y + (size_t)TR_M * p.umax);
     int* s_t = reinterpret_cast<int*>(s_h + (size_t)TR_M * ((p.umax + 1) & ~1));
     const bool rev = p.dir_reverse[d] != 0;
     unsigned* counter = p.bar + d;
+    unsigned* counter2 = p.flags + d;                       // TWO: r (.) h publications
     const uint32_t idesc = (1u << 4) | ((uint32_t)(NP >> 3) << 17) | ((uint32_t)(TR_M >> 4) << 24);
+    const uint32_t idesc2 = (1u << 4) | ((uint32_t)(NP2 >> 3) << 17) | ((uint32_t)(TR_M >> 4) << 24);
     int tmem_cols = 32;
-    while (tmem_cols < NP) tmem_cols *= 2;
+    while (tmem_cols < NP + NP2) tmem_cols *= 2;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nst; ++i) {
@@ -222,6 +230,8 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
         mbar_init(&r_ready, 1);
         mbar_init(&acc_ready, 1);
         mbar_init(&acc_free, 4);   // one arrival per epilogue warp
+        mbar_init(&acc2_ready, 1);
+        mbar_init(&acc2_free, 4);
         mbar_init(&mma_done, 1);
         s_abort = 0;
         mbar_fence_init();
@@ -251,9 +261,16 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
     if (warp == 4) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(&r_ready, (unsigned)(nkb * NP * 128));
-            for (int kb = 0; kb < nkb; ++kb)
-                tma_load_2d(rsm + (size_t)kb * NP * 128, &p.rmap, kb * TR_KB, d * GH + u0 * G, &r_ready);
+            mbar_arrive_expect_tx(&r_ready, (unsigned)(nkb * (NP + NP2) * 128));
+            for (int kb = 0; kb < nkb; ++kb) {
+                if constexpr (TWO) {
+                    tma_load_2d(rsm + (size_t)kb * NP * 128, &p.rmap, kb * TR_KB, d * GH + u0 * 2, &r_ready);
+                    tma_load_2d(rsm2 + (size_t)kb * NP2 * 128, &p.rmap2, kb * TR_KB, d * GH + 2 * H + u0,
+                                &r_ready);
+                } else {
+                    tma_load_2d(rsm + (size_t)kb * NP * 128, &p.rmap, kb * TR_KB, d * GH + u0 * G, &r_ready);
+                }
+            }
             unsigned q = 0;
             bool ok = true;
             for (int s = 0; s < p.max_len && ok; ++s) {
@@ -275,15 +292,36 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                     fence_proxy_async_global();
                 }
                 const int z = (s & 1) * p.D + d;
-                for (int kb = 0; kb < nkb; ++kb, ++q) {
-                    const int slot = (int)(q % nst);
-                    if (q >= (unsigned)nst && !tr_wait(&empty[slot], ((q / nst) - 1u) & 1u, p, &s_abort)) {
-                        tr_fail(p, &s_abort);
-                        ok = false;
-                        break;
+                for (int part = 0; part < (TWO ? 2 : 1) && ok; ++part) {
+                    if (part == 1) {
+                        // every CTA of the direction has published r (.) h of this step
+                        const unsigned need = (unsigned)(s + 1) * (unsigned)C;
+                        const unsigned long long t0 = globaltimer_ns();
+                        unsigned it = 0;
+                        while (ld_acquire_u32(counter2) < need) {
+                            if ((++it & 63u) == 0u) {
+                                if (s_abort || ld_relaxed_s32(p.status) != 0) { ok = false; break; }
+                                if ((long long)(globaltimer_ns() - t0) > p.spin_limit_ns) {
+                                    tr_fail(p, &s_abort);
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                        }
+                        if (!ok) break;
+                        fence_proxy_async_global();
                     }
-                    mbar_arrive_expect_tx(&full[slot], kTrHStage);
-                    tma_load_3d(hring + (size_t)slot * kTrHStage, &p.hmap, kb * TR_KB, 0, z, &full[slot]);
+                    const CUtensorMap* src = part == 0 ? &p.hmap : &p.rhmap;
+                    for (int kb = 0; kb < nkb; ++kb, ++q) {
+                        const int slot = (int)(q % nst);
+                        if (q >= (unsigned)nst && !tr_wait(&empty[slot], ((q / nst) - 1u) & 1u, p, &s_abort)) {
+                            tr_fail(p, &s_abort);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[slot], kTrHStage);
+                        tma_load_3d(hring + (size_t)slot * kTrHStage, src, kb * TR_KB, 0, z, &full[slot]);
+                    }
                 }
             }
             // copies still in flight land before the CTA can leave
@@ -304,24 +342,40 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                     break;
                 }
                 tr_fence_after();
-                for (int kb = 0; kb < nkb; ++kb, ++q) {
-                    const int slot = (int)(q % nst);
-                    if (!tr_wait(&full[slot], (q / nst) & 1u, p, &s_abort)) {
-                        tr_fail(p, &s_abort);
-                        ok = false;
-                        break;
+                for (int part = 0; part < (TWO ? 2 : 1) && ok; ++part) {
+                    if (part == 1) {
+                        // the candidate accumulators of the previous step have been read
+                        if (s > 0 && !tr_wait(&acc2_free, (unsigned)(s - 1) & 1u, p, &s_abort)) {
+                            tr_fail(p, &s_abort);
+                            ok = false;
+                            break;
+                        }
+                        tr_fence_after();
                     }
-                    tr_fence_after();
-                    const unsigned sa = smem_addr(hring + (size_t)slot * kTrHStage);
-                    const unsigned sb = smem_addr(rsm + (size_t)kb * NP * 128);
+                    unsigned char* rb = part == 0 ? rsm : rsm2;
+                    const int np = part == 0 ? NP : NP2;
+                    const uint32_t id = part == 0 ? idesc : idesc2;
+                    const uint32_t td = tmem + (part == 0 ? 0u : (uint32_t)NP);
+                    for (int kb = 0; kb < nkb; ++kb, ++q) {
+                        const int slot = (int)(q % nst);
+                        if (!tr_wait(&full[slot], (q / nst) & 1u, p, &s_abort)) {
+                            tr_fail(p, &s_abort);
+                            ok = false;
+                            break;
+                        }
+                        tr_fence_after();
+                        const unsigned sa = smem_addr(hring + (size_t)slot * kTrHStage);
+                        const unsigned sb = smem_addr(rb + (size_t)kb * np * 128);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)   // K 16 per MMA = 32 bytes along the swizzled rows
-                        tr_mma_f16(tmem, tr_sdesc(sa + 32u * j), tr_sdesc(sb + 32u * j), idesc,
-                                   (kb > 0 || j > 0) ? 1u : 0u);
-                    tr_commit(&empty[slot]);
+                        for (int j = 0; j < 4; ++j)   // K 16 per MMA = 32 bytes along the swizzled rows
+                            tr_mma_f16(td, tr_sdesc(sa + 32u * j), tr_sdesc(sb + 32u * j), id,
+                                       (kb > 0 || j > 0) ? 1u : 0u);
+                        tr_commit(&empty[slot]);
+                    }
+                    if (!ok) break;
+                    tr_commit(part == 0 ? &acc_ready : &acc2_ready);
                 }
                 if (!ok) break;
-                tr_commit(&acc_ready);
             }
             // completes once every MMA issued above has: waited for before the
             // tensor memory is freed
@@ -350,155 +404,289 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
         __half* hx = reinterpret_cast<__half*>(p.hbuf);
         const bool skip_first = p.debug_skip_cta == (int)blockIdx.x;
         bool alive = true;
-        for (int s = 0; s < p.max_len; ++s) {
-            // this step's XW row (independent of the product: loaded first)
-            float xw[TR_NPMAX];
-            const bool live = row && s < len;
-            const int t = live ? (rev ? len - 1 - s : s) : 0;
-            if (live) {
-                const size_t xrow = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
-                const float* src = p.XW + xrow * xw_ld + xw_col;
+        if constexpr (TWO) {
+            __half* rx = reinterpret_cast<__half*>(p.rhbuf);
+            for (int s = 0; s < p.max_len; ++s) {
+                float xw[TR_NPMAX];
+                const bool live = row && s < len;
+                const int t = live ? (rev ? len - 1 - s : s) : 0;
+                if (live) {
+                    const size_t xrow = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
+                    const float* src = p.XW + xrow * xw_ld + xw_col;
 #pragma unroll
-                for (int j = 0; j < TR_NPMAX; ++j) xw[j] = j < U * G ? __ldg(src + j) : 0.f;
-            }
-            // accumulators (warp-collective loads: the decision is warp-uniform)
-            const bool got = __all_sync(0xffffffffu, alive && tr_wait(&acc_ready, (unsigned)s & 1u, p, &s_abort));
-            float acc[TR_NPMAX];
-            if (got) {
-                tr_fence_after();
+                    for (int j = 0; j < TR_NPMAX; ++j) xw[j] = j < U * G ? __ldg(src + j) : 0.f;
+                }
+                // ---- z and r: accumulators j = 2 ul + g in columns 0 .. NP-1
                 const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-                tr_ld16<0>(taddr, acc);
-                if (NP > 16) tr_ld16<16>(taddr + 16u, acc);
-                if (NP > 32) tr_ld16<32>(taddr + 32u, acc);
-                if (NP > 48) tr_ld16<48>(taddr + 48u, acc);
-                tr_ld_wait();
-                tr_fence_before();
-            } else if (alive && lane == 0) {
-                tr_fail(p, &s_abort);
-            }
-            __syncwarp();
-            if (lane == 0 && got) mbar_arrive(&acc_free);
-            // pre-activations in place: acc = ((xw + rec) + Wb) + Rb, except the
-            // GRU candidate's column, whose xw is kept apart (it is added after
-            // r (.) (rec + Rb))
-            float xh[OP == 1 ? UMAX : 1];
-            if (got && live) {
+                const bool got = __all_sync(0xffffffffu, alive && tr_wait(&acc_ready, (unsigned)s & 1u, p, &s_abort));
+                float acc[TR_NPMAX];
+                if (got) {
+                    tr_fence_after();
+                    tr_ld16<0>(taddr, acc);
+                    if (NP > 16) tr_ld16<16>(taddr + 16u, acc);
+                    if (NP > 32) tr_ld16<32>(taddr + 32u, acc);
+                    if (NP > 48) tr_ld16<48>(taddr + 48u, acc);
+                    tr_ld_wait();
+                    tr_fence_before();
+                } else if (alive && lane == 0) {
+                    tr_fail(p, &s_abort);
+                }
+                __syncwarp();
+                if (lane == 0 && got) mbar_arrive(&acc_free);
+                float z[UMAX], rr[UMAX];
+                if (got && live) {
 #pragma unroll
-                for (int j = 0; j < TR_NPMAX; ++j) {
-                    if (OP == 1 && j % 3 == 2) {
-                        if (j / 3 < UMAX) xh[j / 3] = xw[j];
+                    for (int ul = 0; ul < UMAX; ++ul) {
+                        const int j = 3 * ul;
+                        z[ul] = (xw[j] + acc[2 * ul]) + s_wb[j] + s_rb[j];
+                        rr[ul] = (xw[j + 1] + acc[2 * ul + 1]) + s_wb[j + 1] + s_rb[j + 1];
+                    }
+                    if (fixed_acts) {
+                        tc_act_array<1, UMAX>(fA, z, p, true);
+                        tc_act_array<1, UMAX>(fA, rr, p, true);
                     } else {
-                        acc[j] = (xw[j] + acc[j]) + s_wb[j] + s_rb[j];
+                        tc_act_array<0, UMAX>(fA, z, p, true);
+                        tc_act_array<0, UMAX>(fA, rr, p, true);
                     }
                 }
-            }
-            if (got && live) {
-                // gate arithmetic gate-by-gate over the CTA's units: each
-                // activation is applied to a whole array, so its dispatch is
-                // paid once per gate and the units' chains run side by side
-                auto cells = [&](auto fx) {
-                    constexpr int KIND_F = decltype(fx)::value ? (OP == 0 ? 2 : 1) : 0;   // 1 sigmoid, 2 tanh
-                    constexpr int KIND_T = decltype(fx)::value ? 2 : 0;
-                    (void)KIND_T;
-                    if constexpr (OP == 0) {
-                        float a[UMAX];
-#pragma unroll
-                        for (int ul = 0; ul < UMAX; ++ul) a[ul] = acc[ul];
-                        tc_act_array<KIND_F, UMAX>(fA, a, p, true);
-#pragma unroll
-                        for (int ul = 0; ul < UMAX; ++ul) hown[ul] = ul < U ? a[ul] : hown[ul];
-                    } else if constexpr (OP == 1) {
-                        float z[UMAX], r[UMAX];
-#pragma unroll
-                        for (int ul = 0; ul < UMAX; ++ul) {
-                            z[ul] = acc[3 * ul];
-                            r[ul] = acc[3 * ul + 1];
-                        }
-                        tc_act_array<KIND_F, UMAX>(fA, z, p, true);
-                        tc_act_array<KIND_F, UMAX>(fA, r, p, true);
-#pragma unroll
-                        for (int ul = 0; ul < UMAX; ++ul) {
-                            const int j = 3 * ul + 2;
-                            r[ul] = p.has_B ? (xh[ul] + r[ul] * (acc[j] + s_rb[j])) + s_wb[j] : xh[ul] + r[ul] * acc[j];
-                        }
-                        tc_act_array<KIND_T, UMAX>(gA, r, p, true);   // r now holds the candidate
-#pragma unroll
-                        for (int ul = 0; ul < UMAX; ++ul)
-                            if (ul < U) hown[ul] = (1.0f - z[ul]) * r[ul] + z[ul] * hown[ul];
-                    } else {
-                        float gi[UMAX], gf[UMAX], gc[UMAX], go[UMAX];
-#pragma unroll
-                        for (int ul = 0; ul < UMAX; ++ul) {
-                            const int j = 4 * ul;
-                            gi[ul] = acc[j];
-                            go[ul] = acc[j + 1];
-                            gf[ul] = acc[j + 2];
-                            gc[ul] = acc[j + 3];
-                            if (p.has_P) {
-                                gi[ul] += s_p[0][ul] * cown[ul];
-                                gf[ul] += s_p[2][ul] * cown[ul];
-                            }
-                        }
-                        tc_act_array<KIND_F, UMAX>(fA, gi, p, true);
-                        if (p.input_forget) {
-#pragma unroll
-                            for (int ul = 0; ul < UMAX; ++ul) gf[ul] = 1.0f - gi[ul];
-                        } else {
-                            tc_act_array<KIND_F, UMAX>(fA, gf, p, true);
-                        }
-                        tc_act_array<KIND_T, UMAX>(gA, gc, p, true);
-#pragma unroll
-                        for (int ul = 0; ul < UMAX; ++ul) {
-                            const float cn = gf[ul] * cown[ul] + gi[ul] * gc[ul];
-                            if (ul < U) cown[ul] = cn;
-                            gc[ul] = cn;
-                            if (p.has_P) go[ul] += s_p[1][ul] * cn;
-                        }
-                        tc_act_array<KIND_F, UMAX>(fA, go, p, true);
-                        tc_act_array<KIND_T, UMAX>(hA, gc, p, false);   // the cell state is not clipped
-#pragma unroll
-                        for (int ul = 0; ul < UMAX; ++ul)
-                            if (ul < U) hown[ul] = go[ul] * gc[ul];
-                    }
+                // r (.) h of the CTA's units, staged and written units-fastest
+                if (got && row) {
 #pragma unroll
                     for (int ul = 0; ul < UMAX; ++ul)
-                        if (ul < U) s_y[n * p.umax + ul] = canon_nan(hown[ul]);
-                };
-                if (fixed_acts) cells(std::true_type{});
-                else cells(std::false_type{});
-            } else if (got && row) {
+                        if (ul < U) s_h[n * p.umax + ul] = __float2half_rn(live ? rr[ul] * hown[ul] : 0.f);
+                }
+                tr_bar(1, 128);
+                bool abort_now = s_abort != 0 || !got;
+                if (!abort_now) {
+                    __half* rdst = rx + ((size_t)(s & 1) * p.D + d) * TR_M * H + u0;
+                    const int tot = p.N * U;
+                    for (int i = threadIdx.x; i < tot; i += 128) {
+                        const int rn = i / U, ul = i - rn * U;
+                        rdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
+                    }
+                }
+                tr_bar(1, 128);
+                if (abort_now) {
+                    alive = false;
+                    break;
+                }
+                if (threadIdx.x == 0) {
+                    fence_proxy_async_global();
+                    red_release_add_u32(counter2, 1u);
+                }
+                // ---- candidate: accumulators j = ul in columns NP .. NP+NP2-1
+                const bool got2 =
+                    __all_sync(0xffffffffu, alive && tr_wait(&acc2_ready, (unsigned)s & 1u, p, &s_abort));
+                if (got2) {
+                    tr_fence_after();
+                    tr_ld16<0>(taddr + (uint32_t)NP, acc);
+                    if (NP2 > 16) tr_ld16<16>(taddr + (uint32_t)NP + 16u, acc);
+                    tr_ld_wait();
+                    tr_fence_before();
+                } else if (alive && lane == 0) {
+                    tr_fail(p, &s_abort);
+                }
+                __syncwarp();
+                if (lane == 0 && got2) mbar_arrive(&acc2_free);
+                if (got2 && live) {
+                    float hc[UMAX];
 #pragma unroll
-                for (int ul = 0; ul < UMAX; ++ul)
-                    if (ul < U) s_y[n * p.umax + ul] = 0.f;   // Y is +0 past the row's length
-            }
-            if (got && row) {
-                s_t[n] = live ? t : s;
+                    for (int ul = 0; ul < UMAX; ++ul) {
+                        const int j = 3 * ul + 2;
+                        hc[ul] = p.has_B ? ((xw[j] + acc[ul]) + s_wb[j]) + s_rb[j] : xw[j] + acc[ul];
+                    }
+                    if (fixed_acts) tc_act_array<2, UMAX>(gA, hc, p, true);
+                    else tc_act_array<0, UMAX>(gA, hc, p, true);
 #pragma unroll
-                for (int ul = 0; ul < UMAX; ++ul)
-                    if (ul < U) s_h[n * p.umax + ul] = __float2half_rn(hown[ul]);
-            }
-            tr_bar(1, 128);
-            const bool abort_now = s_abort != 0 || !got;
-            if (!abort_now) {
-                // the staged tiles, units fastest: a warp's stores cover a few
-                // contiguous row segments
-                __half* hdst = hx + ((size_t)((s + 1) & 1) * p.D + d) * TR_M * H + u0;
-                const int tot = p.N * U;
-                for (int i = threadIdx.x; i < tot; i += 128) {
-                    const int rn = i / U, ul = i - rn * U;
-                    if (p.Y) p.Y[y_index(p, s_t[rn], d, rn, u0 + ul)] = s_y[rn * p.umax + ul];
-                    hdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
+                    for (int ul = 0; ul < UMAX; ++ul) {
+                        if (ul < U) {
+                            hown[ul] = (1.0f - z[ul]) * hc[ul] + z[ul] * hown[ul];
+                            s_y[n * p.umax + ul] = canon_nan(hown[ul]);
+                        }
+                    }
+                } else if (got2 && row) {
+#pragma unroll
+                    for (int ul = 0; ul < UMAX; ++ul)
+                        if (ul < U) s_y[n * p.umax + ul] = 0.f;   // Y is +0 past the row's length
+                }
+                if (got2 && row) {
+                    s_t[n] = live ? t : s;
+#pragma unroll
+                    for (int ul = 0; ul < UMAX; ++ul)
+                        if (ul < U) s_h[n * p.umax + ul] = __float2half_rn(hown[ul]);
+                }
+                tr_bar(1, 128);
+                abort_now = s_abort != 0 || !got2;
+                if (!abort_now) {
+                    __half* hdst = hx + ((size_t)((s + 1) & 1) * p.D + d) * TR_M * H + u0;
+                    const int tot = p.N * U;
+                    for (int i = threadIdx.x; i < tot; i += 128) {
+                        const int rn = i / U, ul = i - rn * U;
+                        if (p.Y) p.Y[y_index(p, s_t[rn], d, rn, u0 + ul)] = s_y[rn * p.umax + ul];
+                        hdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
+                    }
+                }
+                tr_bar(1, 128);
+                if (abort_now) {
+                    alive = false;
+                    break;
+                }
+                if (threadIdx.x == 0 && !(skip_first && s == 0)) {
+                    fence_proxy_async_global();
+                    red_release_add_u32(counter, 1u);
                 }
             }
-            // publish: every epilogue thread's writes are done; leave together on a failure
-            tr_bar(1, 128);
-            if (abort_now) {
-                alive = false;
-                break;
-            }
-            if (threadIdx.x == 0 && !(skip_first && s == 0)) {
-                fence_proxy_async_global();
-                red_release_add_u32(counter, 1u);
+        } else {
+            for (int s = 0; s < p.max_len; ++s) {
+                // this step's XW row (independent of the product: loaded first)
+                float xw[TR_NPMAX];
+                const bool live = row && s < len;
+                const int t = live ? (rev ? len - 1 - s : s) : 0;
+                if (live) {
+                    const size_t xrow = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
+                    const float* src = p.XW + xrow * xw_ld + xw_col;
+    #pragma unroll
+                    for (int j = 0; j < TR_NPMAX; ++j) xw[j] = j < U * G ? __ldg(src + j) : 0.f;
+                }
+                // accumulators (warp-collective loads: the decision is warp-uniform)
+                const bool got = __all_sync(0xffffffffu, alive && tr_wait(&acc_ready, (unsigned)s & 1u, p, &s_abort));
+                float acc[TR_NPMAX];
+                if (got) {
+                    tr_fence_after();
+                    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+                    tr_ld16<0>(taddr, acc);
+                    if (NP > 16) tr_ld16<16>(taddr + 16u, acc);
+                    if (NP > 32) tr_ld16<32>(taddr + 32u, acc);
+                    if (NP > 48) tr_ld16<48>(taddr + 48u, acc);
+                    tr_ld_wait();
+                    tr_fence_before();
+                } else if (alive && lane == 0) {
+                    tr_fail(p, &s_abort);
+                }
+                __syncwarp();
+                if (lane == 0 && got) mbar_arrive(&acc_free);
+                // pre-activations in place: acc = ((xw + rec) + Wb) + Rb, except the
+                // GRU candidate's column, whose xw is kept apart (it is added after
+                // r (.) (rec + Rb))
+                float xh[OP == 1 ? UMAX : 1];
+                if (got && live) {
+    #pragma unroll
+                    for (int j = 0; j < TR_NPMAX; ++j) {
+                        if (OP == 1 && j % 3 == 2) {
+                            if (j / 3 < UMAX) xh[j / 3] = xw[j];
+                        } else {
+                            acc[j] = (xw[j] + acc[j]) + s_wb[j] + s_rb[j];
+                        }
+                    }
+                }
+                if (got && live) {
+                    // gate arithmetic gate-by-gate over the CTA's units: each
+                    // activation is applied to a whole array, so its dispatch is
+                    // paid once per gate and the units' chains run side by side
+                    auto cells = [&](auto fx) {
+                        constexpr int KIND_F = decltype(fx)::value ? (OP == 0 ? 2 : 1) : 0;   // 1 sigmoid, 2 tanh
+                        constexpr int KIND_T = decltype(fx)::value ? 2 : 0;
+                        (void)KIND_T;
+                        if constexpr (OP == 0) {
+                            float a[UMAX];
+    #pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul) a[ul] = acc[ul];
+                            tc_act_array<KIND_F, UMAX>(fA, a, p, true);
+    #pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul) hown[ul] = ul < U ? a[ul] : hown[ul];
+                        } else if constexpr (OP == 1) {
+                            float z[UMAX], r[UMAX];
+    #pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul) {
+                                z[ul] = acc[3 * ul];
+                                r[ul] = acc[3 * ul + 1];
+                            }
+                            tc_act_array<KIND_F, UMAX>(fA, z, p, true);
+                            tc_act_array<KIND_F, UMAX>(fA, r, p, true);
+    #pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul) {
+                                const int j = 3 * ul + 2;
+                                r[ul] = p.has_B ? (xh[ul] + r[ul] * (acc[j] + s_rb[j])) + s_wb[j] : xh[ul] + r[ul] * acc[j];
+                            }
+                            tc_act_array<KIND_T, UMAX>(gA, r, p, true);   // r now holds the candidate
+    #pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul)
+                                if (ul < U) hown[ul] = (1.0f - z[ul]) * r[ul] + z[ul] * hown[ul];
+                        } else {
+                            float gi[UMAX], gf[UMAX], gc[UMAX], go[UMAX];
+    #pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul) {
+                                const int j = 4 * ul;
+                                gi[ul] = acc[j];
+                                go[ul] = acc[j + 1];
+                                gf[ul] = acc[j + 2];
+                                gc[ul] = acc[j + 3];
+                                if (p.has_P) {
+                                    gi[ul] += s_p[0][ul] * cown[ul];
+                                    gf[ul] += s_p[2][ul] * cown[ul];
+                                }
+                            }
+                            tc_act_array<KIND_F, UMAX>(fA, gi, p, true);
+                            if (p.input_forget) {
+    #pragma unroll
+                                for (int ul = 0; ul < UMAX; ++ul) gf[ul] = 1.0f - gi[ul];
+                            } else {
+                                tc_act_array<KIND_F, UMAX>(fA, gf, p, true);
+                            }
+                            tc_act_array<KIND_T, UMAX>(gA, gc, p, true);
+    #pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul) {
+                                const float cn = gf[ul] * cown[ul] + gi[ul] * gc[ul];
+                                if (ul < U) cown[ul] = cn;
+                                gc[ul] = cn;
+                                if (p.has_P) go[ul] += s_p[1][ul] * cn;
+                            }
+                            tc_act_array<KIND_F, UMAX>(fA, go, p, true);
+                            tc_act_array<KIND_T, UMAX>(hA, gc, p, false);   // the cell state is not clipped
+    #pragma unroll
+                            for (int ul = 0; ul < UMAX; ++ul)
+                                if (ul < U) hown[ul] = go[ul] * gc[ul];
+                        }
+    #pragma unroll
+                        for (int ul = 0; ul < UMAX; ++ul)
+                            if (ul < U) s_y[n * p.umax + ul] = canon_nan(hown[ul]);
+                    };
+                    if (fixed_acts) cells(std::true_type{});
+                    else cells(std::false_type{});
+                } else if (got && row) {
+    #pragma unroll
+                    for (int ul = 0; ul < UMAX; ++ul)
+                        if (ul < U) s_y[n * p.umax + ul] = 0.f;   // Y is +0 past the row's length
+                }
+                if (got && row) {
+                    s_t[n] = live ? t : s;
+    #pragma unroll
+                    for (int ul = 0; ul < UMAX; ++ul)
+                        if (ul < U) s_h[n * p.umax + ul] = __float2half_rn(hown[ul]);
+                }
+                tr_bar(1, 128);
+                const bool abort_now = s_abort != 0 || !got;
+                if (!abort_now) {
+                    // the staged tiles, units fastest: a warp's stores cover a few
+                    // contiguous row segments
+                    __half* hdst = hx + ((size_t)((s + 1) & 1) * p.D + d) * TR_M * H + u0;
+                    const int tot = p.N * U;
+                    for (int i = threadIdx.x; i < tot; i += 128) {
+                        const int rn = i / U, ul = i - rn * U;
+                        if (p.Y) p.Y[y_index(p, s_t[rn], d, rn, u0 + ul)] = s_y[rn * p.umax + ul];
+                        hdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
+                    }
+                }
+                // publish: every epilogue thread's writes are done; leave together on a failure
+                tr_bar(1, 128);
+                if (abort_now) {
+                    alive = false;
+                    break;
+                }
+                if (threadIdx.x == 0 && !(skip_first && s == 0)) {
+                    fence_proxy_async_global();
+                    red_release_add_u32(counter, 1u);
+                }
             }
         }
         if (alive && row) {
@@ -520,15 +708,22 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
     }
 }
 
-template <int OP>
+template <int OP, bool TWO>
 const void* tc_kernel_ptr()
 {
-    return (const void*)rnn_tc_kernel<OP>;
+    return (const void*)rnn_tc_kernel<OP, TWO>;
+}
+
+const void* tc_kernel_for(int op, bool two)
+{
+    if (op == 0) return tc_kernel_ptr<0, false>();
+    if (op == 1) return two ? tc_kernel_ptr<1, true>() : tc_kernel_ptr<1, false>();
+    return tc_kernel_ptr<2, false>();
 }
 
 }  // namespace
 
-size_t tc_recurrent_smem(int H, int npad, int umax, int stages)
+size_t tc_recurrent_smem(int H, int npad, int umax, int stages)   // npad: R rows per CTA (both products)
 {
     return 1024 + (size_t)((H + TR_KB - 1) / TR_KB) * npad * 128 + (size_t)stages * kTrHStage +
            (size_t)TR_M * umax * 4 + (size_t)TR_M * ((umax + 1) & ~1) * 2 + (size_t)TR_M * 4;
@@ -542,9 +737,9 @@ int tc_recurrent_max_columns() { return TR_NPMAX; }
 
 int tc_recurrent_max_units(int op) { return op == 0 ? 32 : TR_NPMAX / (op == 1 ? 3 : 4); }
 
-cudaError_t tc_recurrent_occupancy(int op, size_t smem, int* blocks)
+cudaError_t tc_recurrent_occupancy(int op, bool two, size_t smem, int* blocks)
 {
-    const void* fn = op == 0 ? tc_kernel_ptr<0>() : (op == 1 ? tc_kernel_ptr<1>() : tc_kernel_ptr<2>());
+    const void* fn = tc_kernel_for(op, two);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, TR_THREADS, smem);
@@ -552,7 +747,7 @@ cudaError_t tc_recurrent_occupancy(int op, size_t smem, int* blocks)
 
 cudaError_t launch_tc_recurrent(const RecParams& p, size_t smem, cudaStream_t stream)
 {
-    const void* fn = p.op == 0 ? tc_kernel_ptr<0>() : (p.op == 1 ? tc_kernel_ptr<1>() : tc_kernel_ptr<2>());
+    const void* fn = tc_kernel_for(p.op, p.op == 1 && p.lbr == 0);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     void* args[] = {(void*)&p};

@@ -124,7 +124,7 @@ struct rnn_plan {
     float* wt_const = nullptr;   // [I][D*G*H]
     float* wk_const = nullptr;   // [D*G*H][I] (the tensor-core projection's operand)
     void* wkb_const = nullptr;   // the same rounded to bf16
-    void* rp16_const = nullptr;  // R [D*G*H][H] in the projection's column order, fp16 (tensor-core recurrence)
+    void* rp16_const = nullptr;  // R [D*G*H][H] fp16 (tensor-core recurrence): the projection's column order, GRU lbr = 0 the split order
     float* rt_const = nullptr;   // [D][H][G*H]
     float* r_orig_const = nullptr;   // R as given, [D][G*H][H] (the dataflow kernel reads this layout)
 
@@ -194,7 +194,8 @@ struct Geometry {
     int slots;        // dataflow ring slots
     int umax, tn, threads, rres;
     size_t smem;
-    int npad;         // rows per row group (padded)
+    int npad;         // rows per row group (padded); tensor-core kernel: gate columns per CTA
+    int npad2;        // tensor-core kernel, GRU lbr = 0: candidate columns per CTA
     int hpad;         // dataflow: exchange-buffer row length
     int cpb;          // dataflow: chunks per tensor copy
     int ustride;      // dataflow: floats per unit of the resident R slice
@@ -385,26 +386,26 @@ rnn_status plan_tc(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out)
     const int G = pl->G, D = pl->D;
     if (N > 128) return fail(RNN_ERR_UNSUPPORTED, "the tensor-core kernel takes at most 128 batch rows");
     if (H % 8 != 0) return fail(RNN_ERR_UNSUPPORTED, "the tensor-core kernel needs hidden_size a multiple of 8");
-    if (pl->op == RNN_OP_GRU && pl->lbr == 0)
-        return fail(RNN_ERR_UNSUPPORTED, "the tensor-core kernel has no linear_before_reset = 0 path");
+    const bool two = pl->op == RNN_OP_GRU && pl->lbr == 0;   // z, r product, then the candidate's
     if (!tc_bounded_h(pl)) return fail(RNN_ERR_UNSUPPORTED, "the tensor-core kernel needs bounded h activations");
     int64_t C = std::min<int64_t>(di.sms / D, H);
     if (pl->ov_units > 0) C = std::min<int64_t>(pl->ov_units, H);
     if (C < 1) return fail(RNN_ERR_UNSUPPORTED, "no SM for the tensor-core kernel");
     const int64_t U = ceil_div(H, C);
     C = ceil_div(H, U);
-    const int NP = (int)round_up(U * G, 16);
+    const int NP = (int)round_up(U * (two ? 2 : G), 16);
+    const int NP2 = two ? (int)round_up(U, 16) : 0;
     if (NP > tc_recurrent_max_columns() || U > tc_recurrent_max_units(pl->op))
         return fail(RNN_ERR_UNSUPPORTED, "hidden_size %lld is too large for the tensor-core kernel", (long long)H);
     // h ring: as many 16 KB stages as fit (at least 2)
     const size_t cap = (size_t)di.smem_optin - 2048;
-    const size_t fixed = tc_recurrent_smem((int)H, NP, (int)U, 0);
-    const size_t per_stage = tc_recurrent_smem((int)H, NP, (int)U, 1) - fixed;
+    const size_t fixed = tc_recurrent_smem((int)H, NP + NP2, (int)U, 0);
+    const size_t per_stage = tc_recurrent_smem((int)H, NP + NP2, (int)U, 1) - fixed;
     if (fixed + 2 * per_stage > cap) return fail(RNN_ERR_UNSUPPORTED, "tensor-core kernel: shared memory");
     const int stages = (int)std::min<size_t>((size_t)tc_recurrent_max_stages(), (cap - fixed) / per_stage);
-    const size_t smem = tc_recurrent_smem((int)H, NP, (int)U, stages);
+    const size_t smem = tc_recurrent_smem((int)H, NP + NP2, (int)U, stages);
     int blocks = 0;
-    cudaError_t e = tc_recurrent_occupancy(pl->op, smem, &blocks);
+    cudaError_t e = tc_recurrent_occupancy(pl->op, two, smem, &blocks);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
     if (blocks < 1 || (int64_t)D * C > (int64_t)blocks * di.sms)
         return fail(RNN_ERR_UNSUPPORTED, "tensor-core kernel: the grid does not fit");
@@ -420,6 +421,7 @@ rnn_status plan_tc(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out)
     out->rres = 1;
     out->smem = smem;
     out->npad = NP;
+    out->npad2 = NP2;
     out->slots = stages;
     return RNN_OK;
 }
@@ -732,7 +734,8 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         }
     }
     if (geo.kernel == 3 && !pl->const_weights) {
-        e = launch_pack_kmajor(a.R, scratch + L.rp, (int)D, (int)G, H, H, 2, a.st);
+        e = (pl->op == RNN_OP_GRU && pl->lbr == 0) ? launch_pack_r_split(a.R, scratch + L.rp, (int)D, H, a.st)
+                                                    : launch_pack_kmajor(a.R, scratch + L.rp, (int)D, (int)G, H, H, 2, a.st);
         if (e != cudaSuccess) return cuda_fail(e, "pack launch");
         launches += 1;
     }
@@ -765,6 +768,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     p.ctas_per_dir = geo.ctas; p.unit_groups = geo.units; p.row_groups = geo.rows; p.unit_quant = geo.quant;
     p.slots = geo.slots; p.umax = geo.umax; p.rows_per_thread = geo.tn; p.r_resident = geo.rres;
     p.npad = geo.npad;
+    p.npad2 = geo.npad2;
     p.hpad = geo.hpad;
     p.chunks_per_piece = geo.cpb;
     p.unit_stride = geo.ustride;
@@ -790,7 +794,15 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         if (!encode_tensor_map(&p.hmap, p.hbuf, 3, hdims, hstrides, hbox, true, 2) ||
             !encode_tensor_map(&p.rmap, rp, 2, rdims, rstrides, rbox, true, 2))
             return fail(RNN_ERR_CUDA, "tensor map for the tensor-core kernel");
-        p.rhmap = p.hmap;   // unused
+        p.rhmap = p.hmap;   // GRU lbr = 0 only
+        p.rmap2 = p.rmap;
+        if (geo.npad2 > 0) {
+            // GRU lbr = 0: the r (.) h exchange buffer (as h) and R's candidate rows (box npad2 rows)
+            const cuuint32_t rbox2[2] = {64, (cuuint32_t)geo.npad2};
+            if (!p.rhbuf || !encode_tensor_map(&p.rhmap, p.rhbuf, 3, hdims, hstrides, hbox, true, 2) ||
+                !encode_tensor_map(&p.rmap2, rp, 2, rdims, rstrides, rbox2, true, 2))
+                return fail(RNN_ERR_CUDA, "tensor map for the tensor-core kernel");
+        }
     }
     if (geo.kernel == 2) {
         // h / r (.) h exchange buffers [D*2*CR blocks][hpad/32 chunks][npad rows][36],
@@ -1113,7 +1125,9 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
     e = launch_pack(W, R, pl->wt_const, pl->rt_const, pl->D, pl->G, pl->H, pl->I, s);
     if (e == cudaSuccess && pl->wk_const) e = launch_pack_kmajor(W, pl->wk_const, pl->D, pl->G, pl->H, pl->I, false, s);
     if (e == cudaSuccess && pl->wkb_const) e = launch_pack_kmajor(W, pl->wkb_const, pl->D, pl->G, pl->H, pl->I, true, s);
-    if (e == cudaSuccess && pl->rp16_const) e = launch_pack_kmajor(R, pl->rp16_const, pl->D, pl->G, pl->H, pl->H, 2, s);
+    if (e == cudaSuccess && pl->rp16_const)
+        e = (pl->op == RNN_OP_GRU && pl->lbr == 0) ? launch_pack_r_split(R, pl->rp16_const, pl->D, pl->H, s)
+                                                    : launch_pack_kmajor(R, pl->rp16_const, pl->D, pl->G, pl->H, pl->H, 2, s);
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
     pl->const_weights = true;
     return RNN_OK;

@@ -20,6 +20,8 @@ struct RecParams {
     // ([blocks][hpad/32 chunks][rows][36], box 36 x rows x cpb x 1) and of R
     // as given ([D][G][H units][H], box 36 x units x G x 1), no swizzle
     CUtensorMap hmap, rhmap, rmap;
+    // tensor-core kernel, GRU lbr = 0: R's candidate rows (box npad2 rows)
+    CUtensorMap rmap2;
     int op, G, D, N, H, S, layout;
     int lbr, input_forget;
     int has_B, has_P, has_h0, has_c0, has_lens, has_clip;
@@ -39,7 +41,9 @@ struct RecParams {
     int umax;                    // most units in one group
     int rows_per_thread;         // TN (template parameter mirrored here)
     int r_resident;              // 1: R slice lives in shared memory
-    int npad;                    // rows per row group, padded (staged kernel: N padded to 8)
+    int npad;                    // rows per row group, padded (staged kernel: N padded to 8);
+                                 // tensor-core kernel: gate columns per CTA (GRU lbr = 0: z and r only)
+    int npad2;                   // tensor-core kernel, GRU lbr = 0: candidate columns per CTA
     int hpad;                    // dataflow kernel: H rounded up to 32 (chunks x 32)
     int unit_stride;             // dataflow kernel: floats per unit of the resident R slice
 
@@ -169,13 +173,17 @@ int tc_recurrent_max_stages();
 int tc_recurrent_threads();
 int tc_recurrent_max_columns();
 int tc_recurrent_max_units(int op);
-cudaError_t tc_recurrent_occupancy(int op, size_t smem, int* blocks_per_sm);
+cudaError_t tc_recurrent_occupancy(int op, bool two, size_t smem, int* blocks_per_sm);   // two: GRU lbr = 0
 cudaError_t launch_tc_recurrent(const RecParams& p, size_t smem, cudaStream_t stream);
 cudaError_t launch_tc_state_init(const RecParams& p, cudaStream_t stream);
 
 // perm[rank] = n, rank = the number of rows longer than n or as long and
 // before it: the rows sorted by length, longest first (stable).
 cudaError_t launch_rank_rows(const int32_t* lens, int32_t* perm, int N, cudaStream_t stream);
+// GRU R [D][3H][H] to fp16 K-major rows in the tensor-core kernel's split
+// order for linear_before_reset = 0: per direction the z and r rows of every
+// unit interleaved (row 2u + g), then the candidate rows (row 2H + u).
+cudaError_t launch_pack_r_split(const float* R, void* Rp, int D, int64_t H, cudaStream_t stream);
 // Single RNN cell: Ho = f(clip((X.W^T + Hp.R^T) + B)); fn 0 Relu, 1 Tanh, 2
 // Sigmoid; X [N, I], Hp and Ho [N, H], W [H, I], R [H, H], B [H].
 cudaError_t launch_cell(const float* X, const float* Hp, const float* W, const float* R, const float* B, float* Ho,

@@ -376,8 +376,7 @@ def test_tensor_core_modes_differ_from_fp32_only_by_the_projection(mode):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
-@pytest.mark.parametrize("name,lbr,k", [WORKLOAD_CASES[1], WORKLOAD_CASES[3], WORKLOAD_CASES[4]],
-                         ids=[f"{w[0]}-lbr{w[1]}" for w in (WORKLOAD_CASES[1], WORKLOAD_CASES[3], WORKLOAD_CASES[4])])
+@pytest.mark.parametrize("name,lbr,k", WORKLOAD_CASES[1:5], ids=[f"{w[0]}-lbr{w[1]}" for w in WORKLOAD_CASES[1:5]])
 def test_workload_full_size_tensor_core_modes(name, lbr, k, mode):
     c = workload(name, lbr=lbr)
     rows = _sample_rows(c, min(k, 3))
@@ -399,6 +398,11 @@ TC_REC_SHAPES = [
     ("RNN", "bidirectional", 10, 77, 8, 96, 0, 0, ("uniform", 0, 10), None, None),
     ("LSTM", "reverse", 5, 9, 16, 64, 0, 0, None, None, (0, 0, -1, 0, 3)),
     ("GRU", "forward", 4, 1, 8, 32, 1, 1, None, None, (3, 0, -1, 0, 3)),
+    # GRU linear_before_reset = 0: the z, r product, then r (.) h exchanged and the candidate's product
+    ("GRU", "bidirectional", 8, 100, 16, 136, 1, 0, ("uniform", 1, 8), None, None),
+    ("GRU", "forward", 6, 64, 32, 512, 0, 0, None, 2.0, None),
+    ("GRU", "reverse", 5, 48, 8, 64, 0, 0, None, None, (4, 0, -1, 0, 3)),
+    ("GRU", "forward", 4, 32, 8, 168, 0, 0, ("uniform", 0, 4), None, (8, 0, -1, 0, 3)),
 ]
 
 
@@ -415,11 +419,11 @@ def test_tensor_core_recurrence_within_tolerance(shape, mode):
     _compare_fast((Y, Yh, Yc), oracle_case(c), TC_TOL)
 
 
-@pytest.mark.parametrize("what", ["gru_lbr0", "relu", "too_many_rows"])
+@pytest.mark.parametrize("what", ["hidden_not_multiple_of_8", "relu", "too_many_rows"])
 def test_tensor_core_recurrence_falls_back(what):
     # cases the fp16 tensor-core kernel does not take run on the FP32 kernels
-    if what == "gru_lbr0":
-        c = make_case("GRU", "forward", 4, 64, 16, 64, seed=5, linear_before_reset=0)
+    if what == "hidden_not_multiple_of_8":
+        c = make_case("GRU", "forward", 4, 64, 16, 60, seed=5, linear_before_reset=0)
     elif what == "relu":
         c = make_case("RNN", "forward", 4, 64, 16, 64, seed=5, activations=["Relu"], w_scale=0.05)
     else:
@@ -430,11 +434,12 @@ def test_tensor_core_recurrence_falls_back(what):
     _compare_fast((Y, Yh, Yc), oracle_case(c), TC_TOL)
 
 
-def test_tensor_core_recurrence_timeout_is_reported_and_the_device_stays_usable():
+@pytest.mark.parametrize("op,lbr", [("LSTM", 0), ("GRU", 0)])
+def test_tensor_core_recurrence_timeout_is_reported_and_the_device_stays_usable(op, lbr):
     # one CTA withholds its first publication: the others' bounded waits
     # (50 ms) expire, the status says TIMEOUT, and the next run is correct
-    c = make_case("LSTM", "forward", 5, 64, 8, 64, seed=9, h0_scale=0.5)
-    plan = orc.rnn_plan_create("LSTM", "forward", 64, 8)
+    c = make_case(op, "forward", 5, 64, 8, 64, seed=9, h0_scale=0.5, linear_before_reset=lbr)
+    plan = orc.rnn_plan_create(op, "forward", 64, 8, linear_before_reset=lbr)
     orc.rnn_plan_set_mode(plan, "tf32")
     orc.rnn_plan_set_launch(plan, 4, 0, -1, 0, 3)
     orc.rnn_plan_debug_barrier(plan, 50_000_000, 1)
