@@ -314,3 +314,49 @@ def rnn_cell(hidden_size, input_size, X, H, W, R, B, activation="Tanh", clip=flo
     if st != 0:
         raise OracleError(st)
     return Ho
+
+
+# ------------------------------------------------------------ fp16 / bf16 I/O
+#
+# The operator with 2-byte activation tensors (the fp16/bf16 variants of the
+# type T on the Apple BNNS page): the fp32 operator applied to the inputs
+# widened exactly, each output rounded to nearest even once, a NaN output
+# written as the type's canonical quiet NaN.  bf16 arrays are carried as
+# their uint16 bit patterns (numpy has no bf16 type).
+
+def widen(a, io):
+    """fp16 (numpy float16) or bf16 (uint16 bits) to float32, exactly."""
+    if a is None or io == "f32":
+        return a
+    if io == "f16":
+        return np.asarray(a, np.float16).astype(np.float32)
+    bits = np.asarray(a, np.uint16).astype(np.uint32) << 16
+    return bits.view(np.float32)
+
+
+def narrow(a, io):
+    """float32 to fp16 (numpy float16) or bf16 (uint16 bits), round to nearest even."""
+    if a is None or io == "f32":
+        return a
+    a = np.ascontiguousarray(a, np.float32)
+    nan = np.isnan(a)
+    if io == "f16":
+        with np.errstate(over="ignore"):
+            out = a.astype(np.float16)
+        out.view(np.uint16)[nan] = 0x7E00
+        return out
+    u = a.view(np.uint32).astype(np.uint64)
+    # add half an ulp of the kept part, plus one if the kept part is odd (ties to even)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    r[nan] = 0x7FC0
+    return r
+
+
+def rnn_io(io, op, direction, hidden_size, input_size, X, W, R, B=None, sequence_lens=None,
+           initial_h=None, initial_c=None, P=None, **kw):
+    """rnn() with X, initial_h, initial_c given in `io` ("f16": float16, "bf16":
+    uint16 bits) and Y, Y_h, Y_c returned in it; W, R, B, P stay float32."""
+    Y, Yh, Yc = rnn(op, direction, hidden_size, input_size, widen(X, io), W, R, B=B,
+                    sequence_lens=sequence_lens, initial_h=widen(initial_h, io),
+                    initial_c=widen(initial_c, io), P=P, **kw)
+    return narrow(Y, io), narrow(Yh, io), narrow(Yc, io)
