@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--lbr", type=int, default=0)
     ap.add_argument("--mode", default="exact", choices=["exact", "fast", "tf32", "bf16"])
+    ap.add_argument("--io", default="f32", choices=["f32", "f16", "bf16"],
+                    help="element type of X, initial states and outputs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     return ap.parse_args()
@@ -276,8 +278,12 @@ def run_ours(args, ws, rank, local):
     job = (CellJob if args.workload in CELL_WORKLOADS else SequenceJob)(args, orc, torch)
     plan = job.plan
     orc.rnn_plan_set_mode(plan, args.mode)
-    dev = {k: torch.from_numpy(v).cuda() for k, v in job.host.items()}
-    outs = [torch.empty(sh, device="cuda") for sh in job.out_shapes]
+    orc.rnn_plan_set_io_type(plan, args.io)
+    act = orc.rnn.io_dtype(plan)
+    io_in = ("X", "initial_h", "initial_c")       # the tensors in the I/O type (weights stay fp32)
+    dev = {k: (torch.from_numpy(v).to(act) if k in io_in else torch.from_numpy(v)).cuda()
+           for k, v in job.host.items()}
+    outs = [torch.empty(sh, device="cuda", dtype=act) for sh in job.out_shapes]
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -327,7 +333,7 @@ def run_ours(args, ws, rank, local):
     # stream, downloads on another copy stream, with two sets of device
     # buffers, so batch i+1's upload and batch i-1's download ride the copy
     # engines while batch i computes
-    host_in = {k: torch.from_numpy(v).pin_memory() for k, v in job.host.items()}
+    host_in = {k: v.cpu().pin_memory() for k, v in dev.items()}
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     devs = [dev, {k: torch.empty_like(v) for k, v in dev.items()}]
     bufs = [outs, [torch.empty_like(t) for t in outs]]
@@ -448,9 +454,9 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"exact": "f32", "fast": "f32", "tf32": "f32 (tf32 projection)",
-                  "bf16": "f32 (bf16 projection)"}[args.mode],
+                  "bf16": "f32 (bf16 projection)"}[args.mode] + ("" if args.io == "f32" else f", {args.io} I/O"),
         "data": "synthetic (seeded, see synth.py)",
-        "config": dict(job.config, mode=args.mode, l2="flushed between timed steps (256 MiB write)",
+        "config": dict(job.config, mode=args.mode, io=args.io, l2="flushed between timed steps (256 MiB write)",
                        parallelism=f"replicas x{ws}", geometry=geometry),
         "roofline": roof(dominant),
         "kernels": {k: roof(k) for k in avg if avg[k] > 0},

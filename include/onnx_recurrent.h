@@ -69,6 +69,9 @@ enum { RNN_DIR_FORWARD = 0, RNN_DIR_REVERSE = 1, RNN_DIR_BIDIRECTIONAL = 2 };
  *          arithmetic stays unfused. */
 enum { RNN_MODE_EXACT = 0, RNN_MODE_FAST = 1, RNN_MODE_FAST_TF32 = 2, RNN_MODE_FAST_BF16 = 3 };
 
+/* Element types of the activation tensors (rnn_plan_set_io_type). */
+enum { RNN_IO_F32 = 0, RNN_IO_F16 = 1, RNN_IO_BF16 = 2 };
+
 /* Activation function ids (page "Recurrent operators", Activations). */
 enum {
     RNN_ACT_RELU = 0, RNN_ACT_TANH = 1, RNN_ACT_SIGMOID = 2, RNN_ACT_AFFINE = 3,
@@ -154,6 +157,23 @@ void rnn_plan_destroy(rnn_plan_t plan);
  *              FAST projection).  Scratch grows by 2 bytes per element of X.
  * An unknown mode returns RNN_ERR_INVALID_ARGUMENT. */
 rnn_status rnn_plan_set_mode(rnn_plan_t plan, int mode);
+
+/* Element type of the activation tensors of the plan's runs: RNN_IO_F32
+ * (default), RNN_IO_F16 or RNN_IO_BF16 (the fp16/bf16 variants of the
+ * operator's type T, Apple BNNS page; the WebGPU page's kernels take fp32
+ * only).  It applies to X, initial_h, initial_c (read) and Y, Y_h, Y_c
+ * (written); their pointers in rnn_run / rnn_run_static_scratch then point
+ * to 2-byte elements (cast to float*), in the same shapes and layouts.  W, R,
+ * B and P stay fp32.  The arithmetic is the mode's, in fp32: an input is
+ * widened exactly, every output is the fp32 result rounded to nearest even
+ * once, and a NaN output is the type's canonical quiet NaN (0x7E00 fp16,
+ * 0x7FC0 bf16).  So EXACT mode gives the oracle's fp32 outputs rounded.
+ * The recurrent kernels write the 2-byte outputs directly; X is widened to
+ * fp32 in scratch for the FP32 and TF32 projections (4 bytes per element of
+ * X), while in RNN_MODE_FAST_BF16 a bf16 X feeds the tensor-core projection
+ * as it stands.  An unknown type is RNN_ERR_INVALID_ARGUMENT; a cell plan
+ * (rnn_cell_plan_create) takes RNN_IO_F32 only (RNN_ERR_UNSUPPORTED). */
+rnn_status rnn_plan_set_io_type(rnn_plan_t plan, int io);
 
 /* Declare W and R constant (page "Recurrent operators", Computation: weights
  * are transposed once per plan when they are constants).  Packs them now on

@@ -8,11 +8,11 @@ from .rnn import (Plan, RNNError, load, rnn_cell_plan_create, rnn_cell_run, rnn_
                   rnn_plan_destroy, rnn_plan_get_activation, rnn_plan_get_launch,
                   rnn_plan_last_launch_count, rnn_plan_last_timing, rnn_plan_set_launch,
                   rnn_plan_timing_totals,
-                  rnn_plan_set_mode, rnn_plan_set_timing, rnn_plan_set_weights, rnn_plan_sync,
+                  rnn_plan_set_io_type, rnn_plan_set_mode, rnn_plan_set_timing, rnn_plan_set_weights, rnn_plan_sync,
                   rnn_run, run)
 
 __all__ = ["build", "load", "Plan", "RNNError", "rnn_plan_create", "rnn_run", "rnn_plan_destroy",
            "rnn_plan_set_mode", "rnn_plan_set_weights", "rnn_plan_sync", "rnn_plan_get_activation",
            "rnn_plan_set_launch", "rnn_plan_get_launch", "rnn_plan_set_timing",
            "rnn_plan_last_timing", "rnn_plan_timing_totals", "rnn_plan_debug_barrier", "rnn_plan_last_launch_count",
-           "rnn_last_error", "rnn_cell_plan_create", "rnn_cell_run", "run"]
+           "rnn_last_error", "rnn_cell_plan_create", "rnn_cell_run", "rnn_plan_set_io_type", "run"]

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "io_types.cuh"
 #include "rnn_internal.h"
 
 namespace rnngb {
@@ -73,7 +74,7 @@ __global__ void state_init_kernel(const RecParams p)
         if (n < p.N && u < p.H && p.h0) {
             const int64_t nr = p.perm ? p.perm[n] : n;    // the caller's row behind internal row n
             const int64_t si = p.layout == 0 ? (d * p.N + nr) * p.H + u : (nr * p.D + d) * p.H + u;
-            v = p.h0[si];
+            v = io_load(p.h0, si, p.io);
         }
         const int64_t off = i - d * CR * blk;             // offset inside direction d
         p.hbuf[(d * 2) * CR * blk + off] = v;
@@ -91,21 +92,21 @@ __global__ void state_init_kernel(const RecParams p)
 }
 
 __global__ void mask_tail_kernel(float* __restrict__ Y, int layout, int64_t S, int64_t D, int64_t N,
-                                 int64_t H, int64_t t0)
+                                 int64_t H, int64_t t0, int io)
 {
     const int64_t DH = D * H;
     if (layout == 0) {
         const int64_t begin = t0 * D * N * H, end = S * D * N * H;
         for (int64_t i = begin + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < end;
              i += (int64_t)gridDim.x * blockDim.x)
-            Y[i] = 0.0f;
+            io_store(Y, (size_t)i, 0.0f, io);
     } else {
         const int64_t per_row = (S - t0) * DH;
         const int64_t total = N * per_row;
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
              i += (int64_t)gridDim.x * blockDim.x) {
             const int64_t n = i / per_row, r = i - n * per_row;
-            Y[(n * S + t0) * DH + r] = 0.0f;
+            io_store(Y, (size_t)((n * S + t0) * DH + r), 0.0f, io);
         }
     }
 }
@@ -129,6 +130,18 @@ __global__ void pack_kmajor_kernel(const float* __restrict__ W, T* __restrict__ 
     }
 }
 
+// dst[i] = src[i] between fp32 (0), fp16 (1) and bf16 (2); widening is exact,
+// narrowing rounds to nearest even.
+__global__ void convert_kernel(const void* __restrict__ src, int st, void* __restrict__ dst, int dt, int64_t n)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = io_load(reinterpret_cast<const float*>(src), (size_t)i, st);
+        if (dt == 2) reinterpret_cast<__nv_bfloat16*>(dst)[i] = __float2bfloat16_rn(v);
+        else if (dt == 1) reinterpret_cast<__half*>(dst)[i] = __float2half_rn(v);
+        else reinterpret_cast<float*>(dst)[i] = v;
+    }
+}
+
 __global__ void to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t n)
 {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
@@ -146,6 +159,14 @@ cudaError_t launch_pack_kmajor(const float* W, void* Wk, int D, int G, int64_t H
     if (dtype == 1) pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (__nv_bfloat16*)Wk, G, H, I, rows);
     else if (dtype == 2) pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (__half*)Wk, G, H, I, rows);
     else pack_kmajor_kernel<<<blocks, 128, 0, stream>>>(W, (float*)Wk, G, H, I, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const void* src, int src_type, void* dst, int dst_type, int64_t n, cudaStream_t stream)
+{
+    if (n <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 16);
+    convert_kernel<<<blocks, 256, 0, stream>>>(src, src_type, dst, dst_type, n);
     return cudaGetLastError();
 }
 
@@ -217,7 +238,7 @@ __global__ void tc_state_init_kernel(const RecParams p)
         float v = 0.0f;
         if (b == 0 && r < p.N && p.h0) {
             const int64_t si = p.layout == 0 ? (d * p.N + r) * p.H + u : (r * p.D + d) * p.H + u;
-            v = p.h0[si];
+            v = io_load(p.h0, si, p.io);
         }
         hx[i] = __float2half_rn(v);
         if (p.rhbuf) reinterpret_cast<__half*>(p.rhbuf)[i] = __float2half_rn(0.0f);   // GRU lbr = 0: r (.) h
@@ -263,14 +284,14 @@ cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-cudaError_t launch_mask_tail(float* Y, int layout, int64_t S, int64_t D, int64_t N, int64_t H, int64_t t0,
+cudaError_t launch_mask_tail(float* Y, int layout, int64_t S, int64_t D, int64_t N, int64_t H, int64_t t0, int io,
                              cudaStream_t stream)
 {
     if (!Y || t0 >= S) return cudaSuccess;
     const int64_t total = (S - t0) * D * N * H;
     int blocks = (int)std::min<int64_t>((total + 255) / 256, 8192);
     if (blocks < 1) blocks = 1;
-    mask_tail_kernel<<<blocks, 256, 0, stream>>>(Y, layout, S, D, N, H, t0);
+    mask_tail_kernel<<<blocks, 256, 0, stream>>>(Y, layout, S, D, N, H, t0, io);
     return cudaGetLastError();
 }
 

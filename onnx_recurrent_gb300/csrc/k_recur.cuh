@@ -30,6 +30,7 @@
 #pragma once
 
 #include "exact_math.cuh"
+#include "io_types.cuh"
 #include "rnn_internal.h"
 #include "tma.cuh"
 
@@ -356,8 +357,8 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
         rown[i] = ok ? (p.perm ? p.perm[r] : r) : 0;
         len[i] = ok ? (p.has_lens ? p.lens[rown[i]] : p.S) : 0;
         tile_len = len[i] > tile_len ? len[i] : tile_len;
-        hown[i] = (ok && p.has_h0) ? p.h0[s_index(p, d, rown[i], u)] : 0.f;
-        cown[i] = (ok && OP == 2 && p.has_c0) ? p.c0[s_index(p, d, rown[i], u)] : 0.f;
+        hown[i] = (ok && p.has_h0) ? io_load(p.h0, s_index(p, d, rown[i], u), p.io) : 0.f;
+        cown[i] = (ok && OP == 2 && p.has_c0) ? io_load(p.c0, s_index(p, d, rown[i], u), p.io) : 0.f;
     }
 
     const size_t xw_ld = (size_t)p.D * x.GH;
@@ -440,9 +441,9 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
                         const float ht = act<EXACT>(gA, clipv(p, ph));
                         const float hn = fadd(fmul(fsub(1.0f, zg[i]), ht), fmul(zg[i], hown[i]));
                         hown[i] = hn;
-                        if (p.Y) p.Y[y_index(p, t, d, nr, u)] = canon_nan(hn);
+                        if (p.Y) io_store(p.Y, y_index(p, t, d, nr, u), canon_nan(hn), p.io);
                     } else if (p.Y) {
-                        p.Y[y_index(p, s, d, nr, u)] = 0.f;
+                        io_store(p.Y, y_index(p, s, d, nr, u), 0.f, p.io);
                     }
                     hdst[(size_t)u * x.npad + n] = hown[i];
                 }
@@ -503,9 +504,9 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
                     cown[i] = cn;
                 }
                 hown[i] = hn;
-                if (p.Y) p.Y[y_index(p, t, d, nr, u)] = canon_nan(hn);
+                if (p.Y) io_store(p.Y, y_index(p, t, d, nr, u), canon_nan(hn), p.io);
             } else if (p.Y) {
-                p.Y[y_index(p, s, d, nr, u)] = 0.f;
+                io_store(p.Y, y_index(p, s, d, nr, u), 0.f, p.io);
             }
             hdst[(size_t)u * x.npad + n] = hown[i];
         }
@@ -520,8 +521,8 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
         const int n = x.rb * TN + i;
         if (!(x.active && n < N)) continue;
         const size_t si = s_index(p, d, rown[i], u);
-        if (p.Yh) p.Yh[si] = len[i] > 0 ? canon_nan(hown[i]) : 0.f;
-        if (OP == 2 && p.Yc) p.Yc[si] = len[i] > 0 ? canon_nan(cown[i]) : 0.f;
+        if (p.Yh) io_store(p.Yh, si, len[i] > 0 ? canon_nan(hown[i]) : 0.f, p.io);
+        if (OP == 2 && p.Yc) io_store(p.Yc, si, len[i] > 0 ? canon_nan(cown[i]) : 0.f, p.io);
     }
 }
 

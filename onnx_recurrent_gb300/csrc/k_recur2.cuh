@@ -481,8 +481,8 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         const int n = x.cr * x.NRP + rl;
         const bool ok = x.active && rl < x.NR;
         len[i] = ok ? (p.has_lens ? p.lens[n] : p.S) : 0;
-        hown[i] = (ok && p.has_h0) ? p.h0[s_index(p, d, n, u)] : 0.f;
-        cown[i] = (ok && OP == 2 && p.has_c0) ? p.c0[s_index(p, d, n, u)] : 0.f;
+        hown[i] = (ok && p.has_h0) ? io_load(p.h0, s_index(p, d, n, u), p.io) : 0.f;
+        cown[i] = (ok && OP == 2 && p.has_c0) ? io_load(p.c0, s_index(p, d, n, u), p.io) : 0.f;
     }
     const size_t xw_ld = (size_t)p.D * x.GH;
     const size_t xw_col = (size_t)d * x.GH + (size_t)u * G;
@@ -572,9 +572,9 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                             const float ht = A.Gf(clipv(p, ph));
                             const float hn = fadd(fmul(fsub(1.0f, zg[i]), ht), fmul(zg[i], hown[i]));
                             hown[i] = hn;
-                            if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
+                            if (p.Y) io_store(p.Y, y_index(p, t, d, n, u), canon_nan(hn), p.io);
                         } else if (p.Y) {
-                            p.Y[y_index(p, s, d, n, u)] = 0.f;
+                            io_store(p.Y, y_index(p, s, d, n, u), 0.f, p.io);
                         }
                         hdst[xoff(rl, u)] = hown[i];
                     }
@@ -636,9 +636,9 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                             cown[i] = cn;
                         }
                         hown[i] = hn;
-                        if (p.Y) p.Y[y_index(p, t, d, n, u)] = canon_nan(hn);
+                        if (p.Y) io_store(p.Y, y_index(p, t, d, n, u), canon_nan(hn), p.io);
                     } else if (p.Y) {
-                        p.Y[y_index(p, s, d, n, u)] = 0.f;
+                        io_store(p.Y, y_index(p, s, d, n, u), 0.f, p.io);
                     }
                     hdst[xoff(rl, u)] = hown[i];
                 }
@@ -655,8 +655,8 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         const int n = x.cr * x.NRP + rl;
         if (!(x.active && rl < x.NR)) continue;
         const size_t si = s_index(p, d, n, u);
-        if (p.Yh) p.Yh[si] = len[i] > 0 ? canon_nan(hown[i]) : 0.f;
-        if (OP == 2 && p.Yc) p.Yc[si] = len[i] > 0 ? canon_nan(cown[i]) : 0.f;
+        if (p.Yh) io_store(p.Yh, si, len[i] > 0 ? canon_nan(hown[i]) : 0.f, p.io);
+        if (OP == 2 && p.Yc) io_store(p.Yc, si, len[i] > 0 ? canon_nan(cown[i]) : 0.f, p.io);
     }
 }
 

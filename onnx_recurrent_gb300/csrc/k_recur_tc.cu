@@ -396,8 +396,8 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
         float hown[UMAX], cown[UMAX];
 #pragma unroll
         for (int ul = 0; ul < UMAX; ++ul) {
-            hown[ul] = (row && ul < U && p.has_h0) ? p.h0[s_index(p, d, n, u0 + ul)] : 0.f;
-            cown[ul] = (row && ul < U && OP == 2 && p.has_c0) ? p.c0[s_index(p, d, n, u0 + ul)] : 0.f;
+            hown[ul] = (row && ul < U && p.has_h0) ? io_load(p.h0, s_index(p, d, n, u0 + ul), p.io) : 0.f;
+            cown[ul] = (row && ul < U && OP == 2 && p.has_c0) ? io_load(p.c0, s_index(p, d, n, u0 + ul), p.io) : 0.f;
         }
         const size_t xw_ld = (size_t)p.D * GH;
         const size_t xw_col = (size_t)d * GH + (size_t)u0 * G;
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                     const int tot = p.N * U;
                     for (int i = threadIdx.x; i < tot; i += 128) {
                         const int rn = i / U, ul = i - rn * U;
-                        if (p.Y) p.Y[y_index(p, s_t[rn], d, rn, u0 + ul)] = s_y[rn * p.umax + ul];
+                        if (p.Y) io_store(p.Y, y_index(p, s_t[rn], d, rn, u0 + ul), s_y[rn * p.umax + ul], p.io);
                         hdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
                     }
                 }
@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                     const int tot = p.N * U;
                     for (int i = threadIdx.x; i < tot; i += 128) {
                         const int rn = i / U, ul = i - rn * U;
-                        if (p.Y) p.Y[y_index(p, s_t[rn], d, rn, u0 + ul)] = s_y[rn * p.umax + ul];
+                        if (p.Y) io_store(p.Y, y_index(p, s_t[rn], d, rn, u0 + ul), s_y[rn * p.umax + ul], p.io);
                         hdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
                     }
                 }
@@ -694,8 +694,8 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
             for (int ul = 0; ul < UMAX; ++ul) {
                 if (ul >= U) break;
                 const size_t si = s_index(p, d, n, u0 + ul);
-                if (p.Yh) p.Yh[si] = len > 0 ? canon_nan(hown[ul]) : 0.f;
-                if (OP == 2 && p.Yc) p.Yc[si] = len > 0 ? canon_nan(cown[ul]) : 0.f;
+                if (p.Yh) io_store(p.Yh, si, len > 0 ? canon_nan(hown[ul]) : 0.f, p.io);
+                if (OP == 2 && p.Yc) io_store(p.Yc, si, len > 0 ? canon_nan(cown[ul]) : 0.f, p.io);
             }
         }
     }

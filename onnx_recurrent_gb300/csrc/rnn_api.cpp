@@ -160,6 +160,7 @@ struct rnn_plan {
     int skip_cta = -1;
 
     bool cell = false;   // made by rnn_cell_plan_create
+    int io = 0;          // element type of X, initial states, Y, Y_h, Y_c (RNN_IO_*)
 };
 
 namespace {
@@ -599,7 +600,7 @@ rnn_status check_run(rnn_plan* pl, RunArgs& a, bool* done)
         return fail(RNN_ERR_UNSUPPORTED, "per-direction scratch of %.0f floats reaches the 2^30 limit", per_dir);
     // Zero-size: nothing runs; final states are the initial states or zeros.
     if (a.S == 0 || a.N == 0) {
-        const size_t sb = sizeof(float) * (size_t)D * a.N * H;
+        const size_t sb = (pl->io == 0 ? sizeof(float) : 2) * (size_t)D * a.N * H;
         cudaError_t e = cudaSuccess;
         if (a.Yh && sb)
             e = a.h0 ? cudaMemcpyAsync(a.Yh, a.h0, sb, cudaMemcpyDeviceToDevice, a.st) : cudaMemsetAsync(a.Yh, 0, sb, a.st);
@@ -629,7 +630,7 @@ rnn_status check_lengths(const int32_t* host, int64_t N, int64_t S, int64_t* max
 }
 
 struct Layout {
-    size_t wt, rt, rp, xw, xb, hb, rh, perm, total;
+    size_t wt, rt, rp, xw, xb, xf, hb, rh, perm, total;
     bool need_rh;
 };
 
@@ -644,6 +645,7 @@ Layout scratch_layout(const rnn_plan* pl, const Geometry& geo, int64_t S, int64_
     L.rp = off; off += (pl->const_weights || geo.kernel != 3) ? 0 : align256((size_t)2 * D * GH * H);   // R fp16
     L.xw = off; off += align256(sizeof(float) * (size_t)S * N * D * GH);
     L.xb = off; off += pl->mode == RNN_MODE_FAST_BF16 ? align256((size_t)2 * S * N * I) : 0;   // X as bf16
+    L.xf = off; off += pl->io != 0 ? align256(sizeof(float) * (size_t)S * N * I) : 0;          // fp16/bf16 X widened
     const size_t row = geo.kernel == 2 ? (size_t)geo.hpad / kRecKC * kDfPitch : (size_t)H;
     const size_t hbuf = geo.kernel == 3 ? (size_t)2 * 2 * D * 128 * H   // fp16 [2][D][128][H]
                                         : sizeof(float) * (size_t)D * 2 * geo.rows * geo.npad * row;
@@ -711,7 +713,11 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     // and W rounded to bf16
     const bool bf16 = pl->mode == RNN_MODE_FAST_BF16;
     void* wk = pl->const_weights ? (bf16 ? pl->wkb_const : (void*)pl->wk_const) : (void*)(scratch + L.wt);
-    const void* xin = bf16 ? (const void*)(scratch + L.xb) : (const void*)a.X;
+    // an fp16/bf16 X is widened to fp32 for the FP32 and TF32 projections; in
+    // BF16 mode a bf16 X is the tensor-core operand as it stands
+    const float* x32 = pl->io != 0 ? (const float*)(scratch + L.xf) : a.X;
+    const bool x_is_bf16 = bf16 && pl->io == 2;
+    const void* xin = bf16 ? (x_is_bf16 ? (const void*)a.X : (const void*)(scratch + L.xb)) : (const void*)x32;
     const bool use_tc = (pl->mode == RNN_MODE_FAST_TF32 || bf16) &&
                         projection_tc_supported(xin, wk ? wk : (const void*)scratch, (float*)(scratch + L.xw), M, I,
                                                 D * GH, bf16);
@@ -740,15 +746,22 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         launches += 1;
     }
     if (use_tc && bf16) {
-        e = launch_to_bf16(a.X, scratch + L.xb, M * I, a.st);
-        if (e != cudaSuccess) return cuda_fail(e, "bf16 conversion launch");
+        if (!x_is_bf16) {
+            e = pl->io == 0 ? launch_to_bf16(a.X, scratch + L.xb, M * I, a.st)
+                            : launch_convert(a.X, pl->io, scratch + L.xb, 2, M * I, a.st);
+            if (e != cudaSuccess) return cuda_fail(e, "bf16 conversion launch");
+            launches += 1;
+        }
+    } else if (pl->io != 0 && M * I > 0) {
+        e = launch_convert(a.X, pl->io, scratch + L.xf, 0, M * I, a.st);
+        if (e != cudaSuccess) return cuda_fail(e, "X conversion launch");
         launches += 1;
     }
     if (timed) record(pl, 1, a.st);
     if (use_tc)
         e = launch_projection_tc(xin, wk, xw, M, I, D * GH, bf16, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
     else
-        e = launch_projection(a.X, wt, xw, M, I, D * GH, exact, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
+        e = launch_projection(x32, wt, xw, M, I, D * GH, exact, (int*)(ctrl + kCtrlStatusOffset), spin_ns, a.st);
     if (e != cudaSuccess) return cuda_fail(e, "projection launch");
     launches += 1;
     if (timed) record(pl, 2, a.st);
@@ -759,6 +772,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     p.layout = pl->layout; p.lbr = pl->lbr; p.input_forget = pl->input_forget;
     p.has_B = a.B != nullptr; p.has_P = a.P != nullptr; p.has_h0 = a.h0 != nullptr; p.has_c0 = a.c0 != nullptr;
     p.has_lens = a.lens != nullptr; p.has_clip = pl->has_clip; p.clip = pl->clip;
+    p.io = pl->io;
     for (int d = 0; d < 2; ++d)
         for (int s = 0; s < 3; ++s) p.act[d][s] = pl->act[d][s];
     p.max_len = (int)max_len;
@@ -845,7 +859,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     launches += 1;
     if (timed) record(pl, 4, a.st);
     if (a.Y && max_len < a.S) {
-        e = launch_mask_tail(a.Y, pl->layout, a.S, D, a.N, H, max_len, a.st);
+        e = launch_mask_tail(a.Y, pl->layout, a.S, D, a.N, H, max_len, pl->io, a.st);
         if (e != cudaSuccess) return cuda_fail(e, "mask launch");
         launches += 1;
     }
@@ -1197,6 +1211,16 @@ rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const fl
     cudaEventRecord(pl->done, a.st);
     pl->ran = true;
     pl->last_launches = launches;
+    return RNN_OK;
+}
+
+rnn_status rnn_plan_set_io_type(rnn_plan_t pl, int io)
+{
+    g_error.clear();
+    if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
+    if (io < RNN_IO_F32 || io > RNN_IO_BF16) return fail(RNN_ERR_INVALID_ARGUMENT, "unknown io type %d", io);
+    if (pl->cell && io != RNN_IO_F32) return fail(RNN_ERR_UNSUPPORTED, "a cell plan takes fp32 tensors only");
+    pl->io = io;
     return RNN_OK;
 }
 

@@ -26,6 +26,7 @@ struct RecParams {
     int lbr, input_forget;
     int has_B, has_P, has_h0, has_c0, has_lens, has_clip;
     float clip;
+    int io;                      // element type of X, initial states and outputs: 0 fp32, 1 fp16, 2 bf16
     ActSpec act[2][3];           // per direction: f, g, h
     int max_len;                 // steps to run: max over rows of the length
     int dir_reverse[2];          // per direction: 1 if it walks time backwards
@@ -157,6 +158,8 @@ cudaError_t launch_pack_kmajor(const float* W, void* Wk, int D, int G, int64_t H
 
 // dst[i] = src[i] rounded to bf16 (nearest even), n elements.
 cudaError_t launch_to_bf16(const float* src, void* dst, int64_t n, cudaStream_t stream);
+// dst = src between element types 0 fp32, 1 fp16, 2 bf16 (n elements).
+cudaError_t launch_convert(const void* src, int src_type, void* dst, int dst_type, int64_t n, cudaStream_t stream);
 
 // Pack: Wt[k][d*GH + u*G + g] = W[d][g*H + u][k]  (ld = D*GH),
 //       Rt[d][k][u*G + g]    = R[d][g*H + u][k].
@@ -195,8 +198,8 @@ cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream);
 
 // Y = +0 at t >= t0 for every row (rows that ended earlier are written by
 // the recurrent kernel).
-cudaError_t launch_mask_tail(float* Y, int layout, int64_t S, int64_t D, int64_t N, int64_t H,
-                             int64_t t0, cudaStream_t stream);
+cudaError_t launch_mask_tail(float* Y, int layout, int64_t S, int64_t D, int64_t N, int64_t H, int64_t t0, int io,
+                             cudaStream_t stream);
 
 // Device address and size of the fixed scratch array used by
 // rnn_run_static_scratch (looked up once per device; see rnn_static.cu).

@@ -15,6 +15,7 @@ from . import _build
 OPS = {"RNN": 0, "GRU": 1, "LSTM": 2}
 DIRECTIONS = {"forward": 0, "reverse": 1, "bidirectional": 2}
 MODES = {"exact": 0, "fast": 1, "tf32": 2, "bf16": 3}
+IO_TYPES = {"f32": 0, "f16": 1, "bf16": 2}
 ACT_NAMES = ["relu", "tanh", "sigmoid", "affine", "leakyrelu", "thresholdedrelu",
              "scaledtanh", "hardsigmoid", "elu", "softsign", "softplus"]
 STATUS = {0: "RNN_OK", 1: "RNN_ERR_INVALID_ARGUMENT", 2: "RNN_ERR_INVALID_INPUT",
@@ -66,6 +67,7 @@ def load(path: str | None = None):
     lib.rnn_plan_debug_barrier.argtypes = [vp, i64, i32]
     lib.rnn_plan_last_launch_count.argtypes = [vp]
     lib.rnn_plan_last_launch_count.restype = i32
+    lib.rnn_plan_set_io_type.argtypes = [vp, i32]
     lib.rnn_cell_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, ctypes.c_char_p, f32]
     lib.rnn_cell_run.argtypes = [vp, i64] + [vp] * 6 + [vp]
     lib.rnn_last_error.argtypes = []
@@ -74,7 +76,7 @@ def load(path: str | None = None):
                  "rnn_plan_sync", "rnn_plan_get_activation", "rnn_plan_set_launch",
                  "rnn_plan_get_launch", "rnn_plan_set_timing", "rnn_plan_last_timing",
                  "rnn_plan_timing_totals",
-                 "rnn_plan_debug_barrier", "rnn_cell_plan_create", "rnn_cell_run"):
+                 "rnn_plan_debug_barrier", "rnn_cell_plan_create", "rnn_cell_run", "rnn_plan_set_io_type"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -123,6 +125,7 @@ class Plan:
         self.hidden_size = hidden_size
         self.input_size = input_size
         self.layout = layout
+        self.io = "f32"          # element type of X, initial states and outputs
 
     @property
     def dirs(self):
@@ -169,6 +172,17 @@ def rnn_plan_destroy(plan: Plan):
 
 def rnn_plan_set_mode(plan: Plan, mode):
     _check(load().rnn_plan_set_mode(plan.handle, MODES[mode] if isinstance(mode, str) else int(mode)))
+
+
+def rnn_plan_set_io_type(plan: Plan, io):
+    """Element type of X, initial_h, initial_c, Y, Y_h, Y_c: "f32", "f16" or "bf16"."""
+    _check(load().rnn_plan_set_io_type(plan.handle, IO_TYPES[io] if isinstance(io, str) else int(io)))
+    plan.io = io if isinstance(io, str) else {v: k for k, v in IO_TYPES.items()}[int(io)]
+
+
+def io_dtype(plan: Plan):
+    import torch
+    return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[plan.io]
 
 
 def rnn_plan_set_weights(plan: Plan, W, R, stream=None):
@@ -231,7 +245,7 @@ def _need(t, shape, name, dtype="float32"):
     import torch
     if t is None:
         return
-    want = torch.float32 if dtype == "float32" else torch.int32
+    want = {"float32": torch.float32, "int32": torch.int32}.get(dtype, dtype)
     if t.dtype != want:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda:
@@ -259,17 +273,18 @@ def rnn_run(plan: Plan, X, W, R, B=None, sequence_lens=None, initial_h=None, ini
     """Run on CUDA tensors; outputs are written into Y, Y_h, Y_c (each optional)."""
     seq, batch = (X.shape[0], X.shape[1]) if plan.layout == 0 else (X.shape[1], X.shape[0])
     sh = shapes(plan, seq, batch)
-    _need(X, sh["X"], "X")
+    act = io_dtype(plan)
+    _need(X, sh["X"], "X", act)
     _need(W, sh["W"], "W")
     _need(R, sh["R"], "R")
     _need(B, sh["B"], "B")
     _need(P, sh["P"], "P")
-    _need(initial_h, sh["state"], "initial_h")
-    _need(initial_c, sh["state"], "initial_c")
+    _need(initial_h, sh["state"], "initial_h", act)
+    _need(initial_c, sh["state"], "initial_c", act)
     _need(sequence_lens, sh["lens"], "sequence_lens", "int32")
-    _need(Y, sh["Y"], "Y")
-    _need(Y_h, sh["state"], "Y_h")
-    _need(Y_c, sh["state"], "Y_c")
+    _need(Y, sh["Y"], "Y", act)
+    _need(Y_h, sh["state"], "Y_h", act)
+    _need(Y_c, sh["state"], "Y_c", act)
     st = load().rnn_run(plan.handle, int(seq), int(batch), _ptr(X), _ptr(W), _ptr(R), _ptr(B),
                         _ptr(sequence_lens), _ptr(initial_h), _ptr(initial_c), _ptr(P), _ptr(Y),
                         _ptr(Y_h), _ptr(Y_c), _stream(stream))
@@ -281,10 +296,12 @@ def rnn_run_static_scratch(plan: Plan, X, W, R, B=None, sequence_lens=None, init
     """rnn_run that allocates no device memory (the library's fixed scratch array)."""
     seq, batch = (X.shape[0], X.shape[1]) if plan.layout == 0 else (X.shape[1], X.shape[0])
     sh = shapes(plan, seq, batch)
-    for t, k, n in ((X, "X", "X"), (W, "W", "W"), (R, "R", "R"), (B, "B", "B"), (P, "P", "P"),
-                    (initial_h, "state", "initial_h"), (initial_c, "state", "initial_c"),
-                    (Y, "Y", "Y"), (Y_h, "state", "Y_h"), (Y_c, "state", "Y_c")):
-        _need(t, sh[k], n)
+    act = io_dtype(plan)
+    for t, k, n, dt in ((X, "X", "X", act), (W, "W", "W", "float32"), (R, "R", "R", "float32"),
+                        (B, "B", "B", "float32"), (P, "P", "P", "float32"),
+                        (initial_h, "state", "initial_h", act), (initial_c, "state", "initial_c", act),
+                        (Y, "Y", "Y", act), (Y_h, "state", "Y_h", act), (Y_c, "state", "Y_c", act)):
+        _need(t, sh[k], n, dt)
     _need(sequence_lens, sh["lens"], "sequence_lens", "int32")
     st = load().rnn_run_static_scratch(plan.handle, int(seq), int(batch), _ptr(X), _ptr(W), _ptr(R),
                                        _ptr(B), _ptr(sequence_lens), _ptr(initial_h),
@@ -325,9 +342,10 @@ def run(plan: Plan, X, W, R, B=None, sequence_lens=None, initial_h=None, initial
     import torch
     seq, batch = (X.shape[0], X.shape[1]) if plan.layout == 0 else (X.shape[1], X.shape[0])
     sh = shapes(plan, seq, batch)
-    Y = torch.empty(sh["Y"], dtype=torch.float32, device=X.device) if want_y else None
-    Yh = torch.empty(sh["state"], dtype=torch.float32, device=X.device)
+    act = io_dtype(plan)
+    Y = torch.empty(sh["Y"], dtype=act, device=X.device) if want_y else None
+    Yh = torch.empty(sh["state"], dtype=act, device=X.device)
     is_lstm = plan.op in ("LSTM", 2)
-    Yc = torch.empty(sh["state"], dtype=torch.float32, device=X.device) if is_lstm else None
+    Yc = torch.empty(sh["state"], dtype=act, device=X.device) if is_lstm else None
     rnn_run(plan, X, W, R, B, sequence_lens, initial_h, initial_c, P, Y, Yh, Yc, stream)
     return Y, Yh, Yc

@@ -144,3 +144,21 @@ def test_cell_run_checks_before_device_work(lib):
     assert lib.rnn_cell_run(cell.handle, 0, nul, nul, nul, nul, nul, nul, nul) == 0   # batch 0: nothing read
     orc.rnn_plan_destroy(seq_plan)
     orc.rnn_plan_destroy(cell)
+
+
+# ------------------------------------------------------------ fp16 / bf16 I/O
+
+def test_io_type_validation(lib):
+    p = orc.rnn_plan_create("GRU", "forward", 8, 4)
+    for io in ("f16", "bf16", "f32"):
+        orc.rnn_plan_set_io_type(p, io)
+    with pytest.raises(rb.RNNError) as e:
+        orc.rnn_plan_set_io_type(p, 7)
+    assert e.value.status == 1
+    orc.rnn_plan_destroy(p)
+    cell = orc.rnn_cell_plan_create(8, 4)
+    with pytest.raises(rb.RNNError) as e:
+        orc.rnn_plan_set_io_type(cell, "f16")
+    assert e.value.status == 3
+    orc.rnn_plan_set_io_type(cell, "f32")
+    orc.rnn_plan_destroy(cell)
