@@ -360,3 +360,48 @@ def rnn_io(io, op, direction, hidden_size, input_size, X, W, R, B=None, sequence
                     sequence_lens=sequence_lens, initial_h=widen(initial_h, io),
                     initial_c=widen(initial_c, io), P=P, **kw)
     return narrow(Y, io), narrow(Yh, io), narrow(Yc, io)
+
+
+# ------------------------------------------------------------ stacked layers
+#
+# Layers chained by their output sequence: layer l+1 reads layer l's Y with
+# the directions side by side per step (input_size of layer l+1 = dirs_l *
+# hidden_l), forward units first:  layout 0  X'[t, n, d*H + u] = Y[t, d, n, u];
+# layout 1  X'[n, t, d*H + u] = Y[n, t, d, u].  sequence_lens is shared.
+
+def stack_input(Y, layout):
+    """The next layer's X from a layer's Y (the rule above)."""
+    Y = np.asarray(Y, np.float32)
+    if layout == 0:
+        S, D, N, H = Y.shape
+        X = np.empty((S, N, D * H), np.float32)
+        for t in range(S):
+            for n in range(N):
+                for d in range(D):
+                    X[t, n, d * H:(d + 1) * H] = Y[t, d, n, :]
+        return X
+    N, S, D, H = Y.shape
+    X = np.empty((N, S, D * H), np.float32)
+    for n in range(N):
+        for t in range(S):
+            for d in range(D):
+                X[n, t, d * H:(d + 1) * H] = Y[n, t, d, :]
+    return X
+
+
+def rnn_stack(layers, X, sequence_lens=None):
+    """Run layers (dicts of rnn() keyword arguments without X and
+    sequence_lens) one after another; returns (Y of the last layer, [Y_h per
+    layer], [Y_c per layer])."""
+    x = X
+    yh, yc = [], []
+    Y = None
+    for L in layers:
+        L = dict(L)
+        args = [L.pop(k) for k in ("op", "direction", "hidden_size", "input_size")]
+        W, R = L.pop("W"), L.pop("R")
+        Y, h, c = rnn(*args, x, W, R, sequence_lens=sequence_lens, **L)
+        yh.append(h)
+        yc.append(c)
+        x = stack_input(Y, L.get("layout", 0))
+    return Y, yh, yc
