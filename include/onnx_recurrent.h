@@ -46,6 +46,7 @@ extern "C" {
 #endif
 
 typedef struct rnn_plan* rnn_plan_t;
+typedef struct rnn_stack* rnn_stack_t;
 
 typedef enum {
     RNN_OK = 0,
@@ -263,6 +264,42 @@ rnn_status rnn_run_static_scratch(rnn_plan_t plan, int64_t seq_length, int64_t b
                                   const float* initial_h, const float* initial_c,
                                   const float* P, float* Y, float* Y_h, float* Y_c,
                                   void* stream);
+
+/* Stacked layers.  The pages define single layers; a stack chains them by
+ * the output sequence (this library's reading): layer l+1's X is layer l's
+ * Y with the directions side by side per step, forward units first,
+ *     layout 0:  X[t, n, d*H + u] = Y[t, d, n, u]
+ *     layout 1:  X[n, t, d*H + u] = Y[n, t, d, u]   (Y's memory as it stands)
+ * so layer l+1's input_size must be dirs(l) * hidden(l); sequence_lens is
+ * shared by every layer.
+ *
+ * rnn_stack_create: `layers` is a host array of n_layers >= 1 plans, which
+ * stay the caller's (borrowed: they must outlive the stack, and their modes,
+ * weights and timing apply per layer); all share one layout and one io type
+ * (rnn_plan_set_io_type); cell plans are refused.  Any mismatch is
+ * RNN_ERR_INVALID_ARGUMENT.
+ *
+ * rnn_stack_run: W, R (required) and B, initial_h, initial_c, P, Y_h, Y_c
+ * (each optional: NULL, or entries that may be NULL) are HOST arrays of
+ * n_layers device pointers, each with rnn_run's meaning for its layer; X
+ * feeds layer 0 and Y (may be NULL) receives the last layer's output
+ * sequence.  sequence_lens is checked once (RNN_ERR_INVALID_INPUT before any
+ * write).  The layers run one after another on `stream`; the intermediate
+ * sequences live in two stack-owned device buffers (grown with cudaMalloc
+ * when a run needs more, which synchronises the device), and a layout-0
+ * bidirectional layer's Y is rearranged into the next X by one kernel (any
+ * other layer's Y is the next X as it stands).  Errors are rnn_run's, for
+ * the first failing layer. */
+rnn_status rnn_stack_create(rnn_stack_t* out, const rnn_plan_t* layers, int n_layers);
+rnn_status rnn_stack_run(rnn_stack_t stack, int64_t seq_length, int64_t batch_size,
+                         const float* X, const float* const* W, const float* const* R,
+                         const float* const* B, const int32_t* sequence_lens,
+                         const float* const* initial_h, const float* const* initial_c,
+                         const float* const* P, float* Y, float* const* Y_h, float* const* Y_c,
+                         void* stream);
+void rnn_stack_destroy(rnn_stack_t stack);
+/* Kernels the last rnn_stack_run queued (all layers). */
+int rnn_stack_last_launch_count(rnn_stack_t stack);
 
 /* Single RNN cell (page "RNNCell", RNNCell-3: Detailed description,
  * Attributes, Inputs, Outputs):  Ho = f(clip(X.W^T + H.R^T + B)), where B is

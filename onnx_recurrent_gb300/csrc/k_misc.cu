@@ -225,6 +225,19 @@ __global__ void pack_r_split_kernel(const float* __restrict__ R, __half* __restr
     }
 }
 
+// Stacked layers, layout 0, bidirectional layer below: x[t][n][d*H + u] =
+// y[t][d][n][u] (element size 4 or 2 bytes; moved as bits).
+template <typename T>
+__global__ void stack_permute_kernel(const T* __restrict__ y, T* __restrict__ x, int64_t S, int64_t N, int64_t H)
+{
+    const int64_t total = S * 2 * N * H;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t u = i % H, r = i / H;        // r = (t*2 + d)*N + n over y
+        const int64_t n = r % N, td = r / N, d = td % 2, t = td / 2;
+        x[(t * N + n) * 2 * H + d * H + u] = y[i];
+    }
+}
+
 // Tensor-core kernel: hx[b][d][r][u] (fp16, 128 rows) = initial_h for b = 0
 // and r < N, else 0; step counters 0.
 __global__ void tc_state_init_kernel(const RecParams p)
@@ -257,6 +270,19 @@ cudaError_t launch_pack_r_split(const float* R, void* Rp, int D, int64_t H, cuda
     if (rows <= 0) return cudaSuccess;
     const unsigned blocks = (unsigned)std::min<int64_t>(rows, 152 * 8);
     pack_r_split_kernel<<<blocks, 128, 0, stream>>>(R, (__half*)Rp, H, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stack_permute(const void* y, void* x, int64_t S, int64_t N, int64_t H, int elem,
+                                 cudaStream_t stream)
+{
+    const int64_t total = S * 2 * N * H;
+    if (total <= 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::min<int64_t>((total + 255) / 256, 152 * 16);
+    if (elem == 2)
+        stack_permute_kernel<<<blocks, 256, 0, stream>>>((const unsigned short*)y, (unsigned short*)x, S, N, H);
+    else
+        stack_permute_kernel<<<blocks, 256, 0, stream>>>((const float*)y, (float*)x, S, N, H);
     return cudaGetLastError();
 }
 

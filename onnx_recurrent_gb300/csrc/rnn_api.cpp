@@ -12,6 +12,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "rnn_internal.h"
 
@@ -872,6 +873,36 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
 
 }  // namespace
 
+struct rnn_stack {
+    std::vector<rnn_plan*> layers;   // the caller's plans, borrowed
+    void* buf[2] = {nullptr, nullptr};
+    size_t cap[2] = {0, 0};
+    int last_launches = 0;
+};
+
+namespace {
+
+// Layers chain by the output sequence: layer l+1's input_size is layer l's
+// dirs * hidden; one layout and one activation element type throughout.
+rnn_status stack_check(const rnn_stack* st)
+{
+    for (size_t l = 0; l < st->layers.size(); ++l) {
+        const rnn_plan* pl = st->layers[l];
+        if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "layer %zu: plan is NULL", l);
+        if (pl->cell) return fail(RNN_ERR_INVALID_ARGUMENT, "layer %zu: a cell plan cannot be stacked", l);
+        if (l == 0) continue;
+        const rnn_plan* prev = st->layers[l - 1];
+        if (pl->layout != prev->layout) return fail(RNN_ERR_INVALID_ARGUMENT, "layer %zu: layout differs", l);
+        if (pl->io != prev->io) return fail(RNN_ERR_INVALID_ARGUMENT, "layer %zu: io type differs", l);
+        if (pl->I != (int64_t)prev->D * prev->H)
+            return fail(RNN_ERR_INVALID_ARGUMENT, "layer %zu: input_size %lld, the layer below gives %lld", l,
+                        (long long)pl->I, (long long)prev->D * prev->H);
+    }
+    return RNN_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* rnn_last_error(void) { return g_error.c_str(); }
@@ -1147,16 +1178,18 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
     return RNN_OK;
 }
 
-rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const float* W, const float* R,
-                   const float* B, const int32_t* lens, const float* h0, const float* c0, const float* P,
-                   float* Y, float* Yh, float* Yc, void* stream)
+// One run of a plan.  known_max_len >= 0: sequence_lens was already checked
+// (by a stack's first layer) and its maximum is known.
+static rnn_status run_plan(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const float* W, const float* R,
+                    const float* B, const int32_t* lens, const float* h0, const float* c0, const float* P,
+                    float* Y, float* Yh, float* Yc, void* stream, int64_t known_max_len, int64_t* max_len_out)
 {
-    g_error.clear();
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
     pl->last_launches = 0;
     RunArgs a{S, N, X, W, R, B, lens, h0, c0, P, Y, Yh, Yc, (cudaStream_t)stream};
     bool done = false;
     rnn_status rs = check_run(pl, a, &done);
+    if (max_len_out) *max_len_out = 0;
     if (rs != RNN_OK || done) return rs;
 
     DeviceInfo di;
@@ -1165,8 +1198,8 @@ rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const fl
     if (!di.coop) return fail(RNN_ERR_UNSUPPORTED, "device lacks cooperative launch");
 
     // sequence_lens: check on the host before anything is written.
-    int64_t max_len = S;
-    if (lens) {
+    int64_t max_len = known_max_len >= 0 ? known_max_len : S;
+    if (lens && known_max_len < 0) {
         if (N > pl->lens_cap) {
             if (pl->lens_host) cudaFreeHost(pl->lens_host);
             pl->lens_host = nullptr;
@@ -1211,8 +1244,112 @@ rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const fl
     cudaEventRecord(pl->done, a.st);
     pl->ran = true;
     pl->last_launches = launches;
+    if (max_len_out) *max_len_out = max_len;
     return RNN_OK;
 }
+
+rnn_status rnn_run(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const float* W, const float* R,
+                   const float* B, const int32_t* lens, const float* h0, const float* c0, const float* P,
+                   float* Y, float* Yh, float* Yc, void* stream)
+{
+    g_error.clear();
+    return run_plan(pl, S, N, X, W, R, B, lens, h0, c0, P, Y, Yh, Yc, stream, -1, nullptr);
+}
+
+// ------------------------------------------------------------ stacked layers
+
+rnn_status rnn_stack_create(rnn_stack_t* out, const rnn_plan_t* layers, int n_layers)
+{
+    g_error.clear();
+    if (!out) return fail(RNN_ERR_INVALID_ARGUMENT, "out is NULL");
+    *out = nullptr;
+    if (n_layers < 1 || !layers) return fail(RNN_ERR_INVALID_ARGUMENT, "a stack needs at least one layer");
+    rnn_stack* st = new (std::nothrow) rnn_stack();
+    if (!st) return fail(RNN_ERR_OOM, "out of host memory");
+    st->layers.assign(layers, layers + n_layers);
+    rnn_status rs = stack_check(st);
+    if (rs != RNN_OK) {
+        delete st;
+        return rs;
+    }
+    *out = st;
+    return RNN_OK;
+}
+
+rnn_status rnn_stack_run(rnn_stack_t st, int64_t S, int64_t N, const float* X, const float* const* W,
+                         const float* const* R, const float* const* B, const int32_t* lens,
+                         const float* const* h0, const float* const* c0, const float* const* P, float* Y,
+                         float* const* Yh, float* const* Yc, void* stream)
+{
+    g_error.clear();
+    if (!st) return fail(RNN_ERR_INVALID_ARGUMENT, "stack is NULL");
+    rnn_status rs = stack_check(st);
+    if (rs != RNN_OK) return rs;
+    const int L = (int)st->layers.size();
+    if (!W || !R) return fail(RNN_ERR_INVALID_ARGUMENT, "W and R are per-layer arrays");
+    const size_t elem = st->layers[0]->io == 0 ? 4 : 2;
+    size_t need = 0;
+    for (int l = 0; l + 1 < L; ++l)
+        need = std::max(need, elem * (size_t)S * N * st->layers[l]->D * st->layers[l]->H);
+    for (int b = 0; b < 2; ++b) {
+        if (need > st->cap[b]) {
+            if (st->buf[b]) cudaFree(st->buf[b]);   // synchronises with outstanding work
+            st->buf[b] = nullptr;
+            st->cap[b] = 0;
+            cudaError_t e = cudaMalloc(&st->buf[b], need);
+            if (e != cudaSuccess) {
+                st->buf[b] = nullptr;
+                return cuda_fail(e, "cudaMalloc(stack buffer)");
+            }
+            st->cap[b] = need;
+        }
+    }
+    const float* x = X;
+    int cur = -1;                 // which stack buffer holds x (-1: the caller's X)
+    int64_t max_len = -1;         // sequence_lens is checked by the first layer only
+    st->last_launches = 0;
+    for (int l = 0; l < L; ++l) {
+        rnn_plan* pl = st->layers[l];
+        const bool last = l + 1 == L;
+        const int yb = cur == 0 ? 1 : 0;
+        float* y = last ? Y : (float*)st->buf[yb];
+        int64_t ml = 0;
+        rs = run_plan(pl, S, N, x, W[l], R[l], B ? B[l] : nullptr, lens, h0 ? h0[l] : nullptr,
+                      c0 ? c0[l] : nullptr, P ? P[l] : nullptr, y, Yh ? Yh[l] : nullptr, Yc ? Yc[l] : nullptr,
+                      stream, max_len, &ml);
+        if (rs != RNN_OK) return rs;
+        if (max_len < 0) max_len = ml;
+        st->last_launches += pl->last_launches;
+        if (last) break;
+        if (pl->layout == 0 && pl->D == 2 && S > 0 && N > 0) {
+            // [S][2][N][H] -> [S][N][2H]: forward units, then reverse, per (t, n)
+            const int pb = 1 - yb;
+            cudaError_t e = launch_stack_permute(st->buf[yb], st->buf[pb], S, N, pl->H, (int)elem,
+                                                 (cudaStream_t)stream);
+            if (e != cudaSuccess) return cuda_fail(e, "stack permute launch");
+            st->last_launches += 1;
+            x = (const float*)st->buf[pb];
+            cur = pb;
+        } else {
+            x = y;                // [S][1][N][H] is [S][N][H]; layout 1 [N][S][D][H] is [N][S][D*H]
+            cur = yb;
+        }
+    }
+    return RNN_OK;
+}
+
+void rnn_stack_destroy(rnn_stack_t st)
+{
+    if (!st) return;
+    bool ran = false;
+    for (rnn_plan* pl : st->layers) ran = ran || (pl && pl->ran);
+    if (ran) cudaDeviceSynchronize();
+    for (void* b : st->buf)
+        if (b) cudaFree(b);
+    delete st;
+}
+
+int rnn_stack_last_launch_count(rnn_stack_t st) { return st ? st->last_launches : 0; }
 
 rnn_status rnn_plan_set_io_type(rnn_plan_t pl, int io)
 {

@@ -186,6 +186,10 @@ cudaError_t launch_rank_rows(const int32_t* lens, int32_t* perm, int N, cudaStre
 // GRU R [D][3H][H] to fp16 K-major rows in the tensor-core kernel's split
 // order for linear_before_reset = 0: per direction the z and r rows of every
 // unit interleaved (row 2u + g), then the candidate rows (row 2H + u).
+// Stacked layers, layout 0: a bidirectional layer's Y [S][2][N][H] as the
+// next layer's X [S][N][2H] (elem: 4 or 2 bytes).
+cudaError_t launch_stack_permute(const void* y, void* x, int64_t S, int64_t N, int64_t H, int elem,
+                                 cudaStream_t stream);
 cudaError_t launch_pack_r_split(const float* R, void* Rp, int D, int64_t H, cudaStream_t stream);
 // Single RNN cell: Ho = f(clip((X.W^T + Hp.R^T) + B)); fn 0 Relu, 1 Tanh, 2
 // Sigmoid; X [N, I], Hp and Ho [N, H], W [H, I], R [H, H], B [H].

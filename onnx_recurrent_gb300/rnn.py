@@ -68,6 +68,14 @@ def load(path: str | None = None):
     lib.rnn_plan_last_launch_count.argtypes = [vp]
     lib.rnn_plan_last_launch_count.restype = i32
     lib.rnn_plan_set_io_type.argtypes = [vp, i32]
+    lib.rnn_stack_create.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32]
+    lib.rnn_stack_run.argtypes = [vp, i64, i64, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), vp,
+                                  ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(vp), vp,
+                                  ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
+    lib.rnn_stack_destroy.argtypes = [vp]
+    lib.rnn_stack_destroy.restype = None
+    lib.rnn_stack_last_launch_count.argtypes = [vp]
+    lib.rnn_stack_last_launch_count.restype = i32
     lib.rnn_cell_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, ctypes.c_char_p, f32]
     lib.rnn_cell_run.argtypes = [vp, i64] + [vp] * 6 + [vp]
     lib.rnn_last_error.argtypes = []
@@ -76,7 +84,8 @@ def load(path: str | None = None):
                  "rnn_plan_sync", "rnn_plan_get_activation", "rnn_plan_set_launch",
                  "rnn_plan_get_launch", "rnn_plan_set_timing", "rnn_plan_last_timing",
                  "rnn_plan_timing_totals",
-                 "rnn_plan_debug_barrier", "rnn_cell_plan_create", "rnn_cell_run", "rnn_plan_set_io_type"):
+                 "rnn_plan_debug_barrier", "rnn_cell_plan_create", "rnn_cell_run", "rnn_plan_set_io_type",
+                 "rnn_stack_create", "rnn_stack_run"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -334,6 +343,69 @@ def rnn_cell_run(plan: Plan, X, H, W, R, B, Ho, stream=None):
     _need(Ho, (batch, hs), "Ho")
     _check(load().rnn_cell_run(plan.handle, int(batch), _ptr(X), _ptr(H), _ptr(W), _ptr(R), _ptr(B),
                                _ptr(Ho), _stream(stream)))
+
+
+class Stack:
+    """A stack handle plus its layers' plans (kept alive with it)."""
+
+    def __init__(self, handle, plans):
+        self.handle = handle
+        self.plans = list(plans)
+
+    def __del__(self):
+        try:
+            if self.handle:
+                rnn_stack_destroy(self)
+        except Exception:
+            pass
+
+
+def rnn_stack_create(plans) -> Stack:
+    h = ctypes.c_void_p()
+    arr = (ctypes.c_void_p * len(plans))(*[p.handle for p in plans])
+    _check(load().rnn_stack_create(ctypes.byref(h), arr, len(plans)))
+    return Stack(h, plans)
+
+
+def rnn_stack_destroy(stack: Stack):
+    if stack.handle:
+        load().rnn_stack_destroy(stack.handle)
+        stack.handle = None
+
+
+def rnn_stack_last_launch_count(stack: Stack) -> int:
+    return int(load().rnn_stack_last_launch_count(stack.handle))
+
+
+def rnn_stack_run(stack: Stack, X, W, R, B=None, sequence_lens=None, initial_h=None, initial_c=None, P=None,
+                  Y=None, Y_h=None, Y_c=None, stream=None):
+    """Per-layer arguments are lists (one entry per layer, entries may be None)."""
+    plans = stack.plans
+    L = len(plans)
+    first = plans[0]
+    seq, batch = (X.shape[0], X.shape[1]) if first.layout == 0 else (X.shape[1], X.shape[0])
+    act = io_dtype(first)
+    _need(X, shapes(first, seq, batch)["X"], "X", act)
+    _need(sequence_lens, (batch,), "sequence_lens", "int32")
+
+    def per_layer(v, key, name, dt):
+        if v is None:
+            return None
+        if len(v) != L:
+            raise ValueError(f"{name}: one entry per layer ({L})")
+        for pl, t in zip(plans, v):
+            _need(t, shapes(pl, seq, batch)[key], name, dt)
+        return (ctypes.c_void_p * L)(*[None if t is None else t.data_ptr() for t in v])
+    args = [per_layer(W, "W", "W", "float32"), per_layer(R, "R", "R", "float32"),
+            per_layer(B, "B", "B", "float32")]
+    h0 = per_layer(initial_h, "state", "initial_h", act)
+    c0 = per_layer(initial_c, "state", "initial_c", act)
+    Pa = per_layer(P, "P", "P", "float32")
+    _need(Y, shapes(plans[-1], seq, batch)["Y"], "Y", act)
+    yh = per_layer(Y_h, "state", "Y_h", act)
+    yc = per_layer(Y_c, "state", "Y_c", act)
+    _check(load().rnn_stack_run(stack.handle, int(seq), int(batch), _ptr(X), args[0], args[1], args[2],
+                                _ptr(sequence_lens), h0, c0, Pa, _ptr(Y), yh, yc, _stream(stream)))
 
 
 def run(plan: Plan, X, W, R, B=None, sequence_lens=None, initial_h=None, initial_c=None, P=None,

@@ -162,3 +162,24 @@ def test_io_type_validation(lib):
     assert e.value.status == 3
     orc.rnn_plan_set_io_type(cell, "f32")
     orc.rnn_plan_destroy(cell)
+
+
+# ------------------------------------------------------------ stacked layers
+
+def test_stack_create_validation(lib):
+    a = orc.rnn_plan_create("LSTM", "bidirectional", 8, 4)
+    b = orc.rnn_plan_create("GRU", "forward", 5, 16)       # 2 * 8 inputs: chains
+    c = orc.rnn_plan_create("GRU", "forward", 5, 15)       # does not
+    d = orc.rnn_plan_create("GRU", "forward", 5, 16, layout=1)
+    st = orc.rnn_stack_create([a, b])
+    orc.rnn_stack_destroy(st)
+    for bad in ([a, c], [a, d], [a, orc.rnn_cell_plan_create(5, 16)]):
+        with pytest.raises(rb.RNNError) as e:
+            orc.rnn_stack_create(bad)
+        assert e.value.status == 1
+    orc.rnn_plan_set_io_type(b, "f16")
+    with pytest.raises(rb.RNNError) as e:
+        orc.rnn_stack_create([a, b])
+    assert e.value.status == 1 and "io" in orc.rnn_last_error()
+    with pytest.raises(rb.RNNError):
+        orc.rnn_stack_create([])
