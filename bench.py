@@ -257,11 +257,72 @@ class CellJob:
                 "sample": f"{calls} calls over all {c.batch} batch rows, {dt:.1f} s"}
 
 
+class StackJob:
+    """One rnn_stack_run of a stack workload per step; the metric counts every
+    layer's cell-steps."""
+
+    def __init__(self, args, orc, torch):
+        from onnx_recurrent_gb300.synth import STACK_WORKLOADS, stack_workload
+        self.cases = cs = stack_workload(args.workload)
+        self.case = cs[0]
+        self.host = {"X": cs[0].X}
+        if cs[0].sequence_lens is not None:
+            self.host["sequence_lens"] = cs[0].sequence_lens
+        for i, c in enumerate(cs):
+            for k in ("W", "R", "B", "P", "initial_h", "initial_c"):
+                v = getattr(c, k)
+                if v is not None:
+                    self.host[f"{k}{i}"] = v
+        self.layer_plans = [orc.rnn_plan_create(c.op, c.direction, c.hidden_size, c.input_size, clip=c.clip,
+                                                layout=c.layout, linear_before_reset=c.linear_before_reset)
+                            for c in cs]
+        self.plan = self.layer_plans[-1]
+        self.stack = None
+        last = cs[-1]
+        self.out_shapes = [last.y_shape()] + [c.state_shape() for c in cs] + \
+                          [c.state_shape() for c in cs if c.op == "LSTM"]
+        self.cells = sum(c.cell_steps() for c in cs)
+        rows_steps = cs[0].valid_cell_steps() // cs[0].dirs      # the shared lengths, summed
+        self.rec_flops = sum(2.0 * rows_steps * c.dirs * c.gates * c.hidden_size ** 2 for c in cs)
+        self.proj_flops = sum(algorithmic(c)[1] for c in cs)
+        self.config = {"workload": args.workload, "description": STACK_WORKLOADS[args.workload],
+                       "layers": [{"op": c.op, "direction": c.direction, "input": c.input_size,
+                                   "hidden": c.hidden_size} for c in cs],
+                       "seq": cs[0].seq, "batch": cs[0].batch,
+                       "valid_cell_steps_per_step": sum(rows_steps * c.dirs for c in cs)}
+        self.orc = orc
+
+    def set_mode(self, mode, io):
+        for p in self.layer_plans:
+            self.orc.rnn_plan_set_mode(p, mode)
+            self.orc.rnn_plan_set_io_type(p, io)
+        self.stack = self.orc.rnn_stack_create(self.layer_plans)
+
+    def run(self, dv, outs, stream):
+        cs = self.cases
+        L = len(cs)
+        g = lambda k: [dv.get(f"{k}{i}") for i in range(L)]
+        yh = outs[1:1 + L]
+        lstm = [i for i, c in enumerate(cs) if c.op == "LSTM"]
+        yc = [None] * L
+        for j, i in enumerate(lstm):
+            yc[i] = outs[1 + L + j]
+        self.orc.rnn_stack_run(self.stack, dv["X"], g("W"), g("R"), g("B"), dv.get("sequence_lens"),
+                               g("initial_h"), g("initial_c"), g("P"), outs[0], yh, yc, stream)
+
+    def launches(self):
+        return self.orc.rnn_stack_last_launch_count(self.stack)
+
+    def cpu_baseline(self):
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "not run for stacks (the single-layer workloads carry the oracle baseline)"}
+
+
 def run_ours(args, ws, rank, local):
     import torch
 
     import onnx_recurrent_gb300 as orc
-    from onnx_recurrent_gb300.synth import CELL_WORKLOADS
+    from onnx_recurrent_gb300.synth import CELL_WORKLOADS, STACK_WORKLOADS
 
     torch.cuda.set_device(local)
     dist = None
@@ -275,13 +336,17 @@ def run_ours(args, ws, rank, local):
     orc.build()
     orc.load()
 
-    job = (CellJob if args.workload in CELL_WORKLOADS else SequenceJob)(args, orc, torch)
+    job = (CellJob if args.workload in CELL_WORKLOADS else
+           StackJob if args.workload in STACK_WORKLOADS else SequenceJob)(args, orc, torch)
     plan = job.plan
-    orc.rnn_plan_set_mode(plan, args.mode)
-    orc.rnn_plan_set_io_type(plan, args.io)
+    if isinstance(job, StackJob):
+        job.set_mode(args.mode, args.io)
+    else:
+        orc.rnn_plan_set_mode(plan, args.mode)
+        orc.rnn_plan_set_io_type(plan, args.io)
     act = orc.rnn.io_dtype(plan)
-    io_in = ("X", "initial_h", "initial_c")       # the tensors in the I/O type (weights stay fp32)
-    dev = {k: (torch.from_numpy(v).to(act) if k in io_in else torch.from_numpy(v)).cuda()
+    is_io = lambda k: k == "X" or k.startswith("initial_")   # the tensors in the I/O type (weights stay fp32)
+    dev = {k: (torch.from_numpy(v).to(act) if is_io(k) else torch.from_numpy(v)).cuda()
            for k, v in job.host.items()}
     outs = [torch.empty(sh, device="cuda", dtype=act) for sh in job.out_shapes]
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
@@ -295,11 +360,13 @@ def run_ours(args, ws, rank, local):
         step()
     torch.cuda.synchronize()
     orc.rnn_plan_sync(plan)
-    launches_per_step = orc.rnn_plan_last_launch_count(plan)
+    launches_per_step = job.launches() if isinstance(job, StackJob) else orc.rnn_plan_last_launch_count(plan)
     geometry = orc.rnn_plan_get_launch(plan)
 
     # ---- timed region: inputs resident, L2 flushed between steps
-    orc.rnn_plan_set_timing(plan, True)
+    timed = job.layer_plans if isinstance(job, StackJob) else [plan]
+    for p_ in timed:
+        orc.rnn_plan_set_timing(p_, True)
     K = args.steps
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -324,8 +391,13 @@ def run_ours(args, ws, rank, local):
         sampler.stop()
     orc.rnn_plan_sync(plan)
     total_ms = sum(a.elapsed_time(b) for a, b in evs)
-    kern_ms, runs = orc.rnn_plan_timing_totals(plan)
-    orc.rnn_plan_set_timing(plan, False)
+    kern_ms, runs = {}, 0
+    for p_ in timed:                       # a stack: each kernel kind summed over the layers
+        orc.rnn_plan_sync(p_)
+        km, runs = orc.rnn_plan_timing_totals(p_)
+        for k_, v_ in km.items():
+            kern_ms[k_] = kern_ms.get(k_, 0.0) + v_
+        orc.rnn_plan_set_timing(p_, False)
 
     # ---- end to end: pinned host inputs -> device -> run -> host outputs,
     # every input (weights included) uploaded afresh each step, pipelined the

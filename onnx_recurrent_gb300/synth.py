@@ -237,6 +237,29 @@ def cell_workload(name: str) -> CellCase:
     raise KeyError(name)
 
 
+STACK_WORKLOADS = {
+    "lstm2_fwd_s64_b32_i256_h512": "two stacked LSTM forward layers, seq 64, batch 32, input 256, hidden 512, "
+                                   "peepholes (the LSTM forward workload with a second layer on top)",
+    "gru2_bidi_s128_b64_i512_h1024": "two stacked GRU bidirectional layers, seq 128, batch 64, input 512, hidden "
+                                     "1024, lbr 1, layout 0, sequence_lens",
+}
+
+
+def stack_workload(name: str):
+    """Seeded per-layer cases (seed 0, then 1) of a named stack workload."""
+    if name == "lstm2_fwd_s64_b32_i256_h512":
+        a = make_case("LSTM", "forward", 64, 32, 256, 512, with_P=True, h0_scale=0.5, c0_scale=0.5, name=name)
+        b = make_case("LSTM", "forward", 64, 32, 512, 512, seed=1, with_P=True, h0_scale=0.5, c0_scale=0.5)
+        return [a, b]
+    if name == "gru2_bidi_s128_b64_i512_h1024":
+        a = make_case("GRU", "bidirectional", 128, 64, 512, 1024, w_scale=1.0 / 32, lens=("uniform", 0, 128),
+                      linear_before_reset=1, name=name)
+        b = make_case("GRU", "bidirectional", 128, 64, 2048, 1024, seed=1, w_scale=1.0 / 32,
+                      linear_before_reset=1)
+        return [a, b]
+    raise KeyError(name)
+
+
 ACTIVATIONS = ["Relu", "Tanh", "Sigmoid", "Affine", "LeakyRelu", "ThresholdedRelu",
                "ScaledTanh", "HardSigmoid", "Elu", "Softsign", "Softplus"]
 
