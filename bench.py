@@ -152,7 +152,7 @@ def algorithmic(case):
 
 KERNEL_SOURCES = {
     "recurrence": ["k_recur.cuh", "k_recur2.cuh", "k_recur_rnn.cu", "k_recur_gru.cu", "k_recur_lstm.cu",
-                   "k_recur_tc.cu", "tma.cuh", "exact_math.cuh", "rnn_internal.h"],
+                   "k_recur_tc.cu", "tma.cuh", "exact_math.cuh", "io_types.cuh", "rnn_internal.h"],
     "projection": ["k_proj.cu", "k_proj_tc.cu", "tma.cuh", "rnn_internal.h"],
     "cell": ["k_cell.cu", "exact_math.cuh", "rnn_internal.h"],
 }
