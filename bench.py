@@ -469,6 +469,8 @@ def run_ours(args, ws, rank, local):
         avg = {"cell": avg["recurrence"]}      # one kernel, timed in the recurrence slot
     dominant = max(avg, key=avg.get)
 
+    traffic_name = args.workload + (f"-lbr{args.lbr}" if args.lbr else "")   # the workload as profiles name it
+
     def roof(kernel):
         ms = avg[kernel]
         if kernel == "cell":
@@ -476,7 +478,7 @@ def run_ours(args, ws, rank, local):
             ach = flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
                     "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
+                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
                     "kernel": "rnn_cell_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": flops,
                     "peak_note": f"{'no' if exact else 'fused'} multiply-add: {sms} SMs x 128 FP32 "
                                  f"lanes x {'1' if exact else '2'} FLOP x {clock_mhz:.0f} MHz (derived)"}
@@ -487,14 +489,14 @@ def run_ours(args, ws, rank, local):
             ach = rec_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
                     "frac": round(ach / peak, 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
+                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
                     "kernel": "rnn_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": rec_flops,
                     "peak_note": "of measured bf16 burst (fp16 operands, same nominal rate)"}
         if kernel == "recurrence":
             ach = rec_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
                     "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
+                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
                     "kernel": "rnn_dataflow_kernel" if geometry.get("kernel") == 2 else "rnn_recurrent_kernel",
                     "avg_ms": round(ms, 5),
                     "algorithmic_flops_per_launch": rec_flops,
@@ -508,14 +510,14 @@ def run_ours(args, ws, rank, local):
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
                     "frac": round(ach / peak, 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
+                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
                     "kernel": "proj_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": proj_flops,
                     "peak_note": "of measured bf16 burst" + ("" if args.mode == "bf16" else " x 1.1/2.25 (TF32)")}
         if kernel == "projection":
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
                     "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, args.workload, args.mode, source_digest(kernel)),
+                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
                     "kernel": "proj_tma_kernel", "avg_ms": round(ms, 5),
                     "algorithmic_flops_per_launch": proj_flops}
         return {"kernel": kernel, "avg_ms": round(ms, 5)}
