@@ -60,6 +60,20 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, dist, device):
+    """Each value's maximum over the ranks (the slowest replica sets the
+    job's time); `dist` is torch.distributed with a process group up."""
+    import torch
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_value(units_per_rank, steps, world_size, total_ms):
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank * steps * world_size / (total_ms / 1e3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -446,17 +460,15 @@ def run_ours(args, ws, rank, local):
     e2e_ms = e_start.elapsed_time(e_end)
 
     if dist:
-        t = torch.tensor([total_ms, e2e_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+        total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, "cuda")
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
     cells = job.cells
-    value = cells * K * ws / (total_ms / 1e3)
-    e2e_value = cells * E * ws / (e2e_ms / 1e3)
+    value = job_value(cells, K, ws, total_ms)
+    e2e_value = job_value(cells, E, ws, e2e_ms)
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     sms = props.multi_processor_count
     peaks = measured_peaks()
