@@ -89,7 +89,7 @@ struct DfCtx {
     bool active;
     float* Rs;        // resident R: [umax][ugs] floats (unit-major, gate rows of H)
     char* Rring;      // streamed R: slots x rslot bytes, each cpb chunks of [G][umax][36]
-    char* Hring;      // slots x hslot bytes, each [cpb][NRP][36]
+    char* Hring;      // slots x hslot bytes, each [cpb][NRP][36] (padded to 128 bytes)
     int rslot, rsub, hslot; // bytes per slot (one piece: cpb chunks of 32 k), per R chunk
     uint64_t* full;
     uint64_t* empty;
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     x.cpb = p.chunks_per_piece;
     x.npieces = (x.nchunks + x.cpb - 1) / x.cpb;
     x.slots = p.slots;
-    x.hslot = x.NRP * x.cpb * kDfPitch * 4;
+    x.hslot = (int)df_hslot_bytes(x.NRP, x.cpb);   // 128-byte aligned slot starts
     x.rsub = (int)df_rsub_bytes(x.umax, G);
     x.rslot = p.r_resident ? 0 : x.cpb * x.rsub;
     x.ncompute = blockDim.x - 32;

@@ -287,7 +287,11 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
     const int ncr = pl->ov_rows > 0 ? 1 : 6;
     for (int cri = 0; cri < ncr; ++cri) {
         const int CRc = pl->ov_rows > 0 ? pl->ov_rows : cr_auto[cri];
-        const int64_t NRP = round_up(ceil_div(N, CRc), 8);
+        // rows per group padded to 8; a single group of a small batch to 4
+        // (padding rows skip their products but still take lanes: a batch of
+        // 4 in an 8-row group left half of every warp idle).  Measured: 4-row
+        // groups elsewhere (LSTM batch 32 as 8 groups) were slower than 8.
+        const int64_t NRP = round_up(ceil_div(N, CRc), CRc == 1 ? 4 : 8);
         const int CR = (int)ceil_div(N, NRP);
         if (CR != CRc) continue;                                   // would leave an empty row group
         if (NRP > 256) continue;                                   // a tensor-copy box spans at most 256 rows

@@ -104,6 +104,15 @@ constexpr int kDfPitch = 36;
 // Bytes of one chunk of streamed R: G x umax rows of 144 bytes, 128-aligned.
 __host__ __device__ inline size_t df_rsub_bytes(int umax, int G) { return (((size_t)G * umax * kDfPitch * 4 + 127) / 128) * 128; }
 
+// Dataflow kernel: bytes between h ring slots.  A slot holds one piece (cpb
+// chunks of npad rows of 36 floats) and is a tensor-copy destination, so its
+// start must be 128-byte aligned: the pitch is rounded up to 128 bytes (npad
+// need not be a multiple of 8).
+__host__ __device__ inline size_t df_hslot_bytes(int npad, int cpb)
+{
+    return (((size_t)npad * cpb * kDfPitch * 4 + 127) / 128) * 128;
+}
+
 // Dataflow kernel: dynamic shared memory (128-byte alignment slack + R
 // resident or ring of R pieces + ring of h pieces; a slot holds one piece of
 // cpb chunks).
@@ -112,7 +121,7 @@ inline size_t df_smem_bytes(int H, int umax, int G, int npad, int r_resident, in
     const size_t rres = (((size_t)umax * df_unit_stride(H, G) * 4 + 127) / 128) * 128;
     const size_t rslot = (size_t)cpb * df_rsub_bytes(umax, G);
     const size_t rbytes = r_resident ? rres : (size_t)slots * rslot;
-    return 128 + rbytes + (size_t)slots * npad * cpb * kDfPitch * 4;
+    return 128 + rbytes + (size_t)slots * df_hslot_bytes(npad, cpb);
 }
 
 // The control block: barrier counters, status word, publication flags.
