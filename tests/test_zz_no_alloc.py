@@ -80,3 +80,35 @@ def test_static_scratch_refuses_runs_that_do_not_fit(lib):
     assert st == 3
     assert "static scratch" in orc.rnn_last_error()
     orc.rnn_plan_destroy(plan)
+
+
+def test_static_scratch_runs_inside_a_cuda_graph(lib):
+    # captured once (after one call outside the capture, which looks up the
+    # static array), then replayed with new inputs: the same bits as rnn_run
+    c = make_case("LSTM", "forward", 6, 8, 16, 64, seed=11, with_P=True, h0_scale=0.5, c0_scale=0.5)
+    plan = orc.rnn_plan_create(c.op, c.direction, c.hidden_size, c.input_size, layout=c.layout)
+    dev = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in c.tensors().items()}
+    outs = [torch.empty(c.y_shape(), device="cuda"), torch.empty(c.state_shape(), device="cuda"),
+            torch.empty(c.state_shape(), device="cuda")]
+    _static_run(lib, plan, c, dev, outs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            _static_run(lib, plan, c, dev, outs)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(2)
+    for rep in range(2):
+        X = g.normal(size=c.X.shape).astype(np.float32)
+        dev["X"].copy_(torch.from_numpy(X))
+        for o in outs:
+            o.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = gpu_case(c.with_(X=X), "exact")
+        for nm, got, r in zip(("Y", "Y_h", "Y_c"), outs, ref):
+            assert_bits_equal(got.cpu().numpy(), r, f"replay {rep} {nm}")
+    del graph
+    orc.rnn_plan_destroy(plan)
