@@ -194,7 +194,6 @@ struct RecCtx {
     int d, H, npad, G, GH, u0, UG, ugp, tid, nthreads, ul, rb;
     bool active;
     bool live;   // this step: some row of the thread's tile has not finished
-    bool local;  // one CTA per direction, R resident, h fits the ring: h stays in shared memory
     float* Rs;   // resident [H][ugp] or ring [stages][KC][ugp]
     float* Hs;   // ring [stages][KC][npad]
 };
@@ -229,24 +228,6 @@ __device__ __forceinline__ void accumulate(const RecParams& p, const RecCtx& x, 
                                            int col_off, float (&acc)[TN][NC])
 {
     const int nchunks = (x.H + kRecKC - 1) / kRecKC;
-    if (x.local) {
-        // the operand is already in the ring, chunk c in slot c ([H][npad]
-        // contiguous), written by this CTA before the barrier that ended the
-        // last phase
-        __syncthreads();
-        if (x.active && x.live) {
-            for (int c = 0; c < nchunks; ++c) {
-                const int k0 = c * kRecKC;
-                const int kc = min(kRecKC, x.H - k0);
-                const float* hk = x.Hs + (size_t)k0 * x.npad + x.rb * TN;
-                const float* rk = x.Rs + (size_t)k0 * x.ugp + x.ul * x.G + col_off;
-                if (kc == kRecKC) chunk_full<TN, NC, EXACT>(hk, x.npad, rk, x.ugp, acc);
-                else chunk_part<TN, NC, EXACT>(hk, x.npad, rk, x.ugp, kc, acc);
-            }
-        }
-        __syncthreads();   // every read done before the operand is overwritten
-        return;
-    }
 #pragma unroll
     for (int c = 0; c < kRecStages - 1; ++c) {
         if (c < nchunks) issue_chunk(p, x, src, c, c);
@@ -324,9 +305,6 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
     x.live = true;
     x.Rs = smem;
     x.Hs = smem + (p.r_resident ? (size_t)p.H * x.ugp : (size_t)kRecStages * kRecKC * x.ugp);
-    // One CTA per direction: h never needs to leave the SM.  The ring holds
-    // kRecStages chunks of [32][npad], so an H of at most 128 fits whole.
-    x.local = C == 1 && p.r_resident && p.H <= kRecStages * kRecKC;
 
     const int d = x.d;
     const int u = x.u0 + x.ul;
@@ -404,14 +382,9 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
 
     unsigned episode = 0;
     load_xw(0);
-    if (x.local) {
-        // h(0) from the exchange buffer the set-up kernel filled
-        const float* h0b = p.hbuf + (size_t)(d * 2) * p.H * x.npad;
-        for (int i = x.tid; i < p.H * x.npad; i += x.nthreads) x.Hs[i] = h0b[i];
-    }
     for (int s = 0; s < p.max_len; ++s) {
         const float* hsrc = p.hbuf + ((size_t)(d * 2 + (s & 1)) * p.H) * x.npad;
-        float* hdst = x.local ? x.Hs : p.hbuf + ((size_t)(d * 2 + ((s + 1) & 1)) * p.H) * x.npad;
+        float* hdst = p.hbuf + ((size_t)(d * 2 + ((s + 1) & 1)) * p.H) * x.npad;
         float xc[TN][G];
 #pragma unroll
         for (int i = 0; i < TN; ++i)
@@ -428,7 +401,7 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
                 accumulate<TN, 2, EXACT>(p, x, hsrc, 0, az);
                 if (s + 1 < p.max_len) load_xw(s + 1);
                 float zg[TN];
-                float* rh = x.local ? x.Hs : p.rhbuf + (size_t)d * 2 * p.H * x.npad;
+                float* rh = p.rhbuf + (size_t)d * 2 * p.H * x.npad;
 #pragma unroll
                 for (int i = 0; i < TN; ++i) {
                     const int n = x.rb * TN + i;   // internal row (exchange buffers)
