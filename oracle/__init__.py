@@ -72,8 +72,6 @@ def _configure(lib):
         getattr(lib, name).restype = None
     lib.oracle_activation_n.argtypes = [ctypes.c_int, ctypes.c_float, ctypes.c_float, fp, fp, L]
     lib.oracle_activation_n.restype = None
-    lib.oracle_projection.argtypes = [L, L, L, fp, fp, fp]
-    lib.oracle_projection.restype = None
     lib.oracle_rnn_cell.argtypes = [L, L, ctypes.c_char_p, ctypes.c_float, L, fp, fp, fp, fp, fp, fp]
     lib.oracle_rnn_cell.restype = ctypes.c_int
     return lib
@@ -286,18 +284,6 @@ def activation(name, x, alpha=0.0, beta=0.0):
     lib.oracle_activation_n(ACT_NAMES.index(name.lower()), float(alpha), float(beta),
                             _fptr(x), _fptr(y), x.size)
     return y
-
-
-def projection(X2, Wd):
-    """XW = X2 . Wd^T, X2 [rows, I], Wd [cols, I], one accumulator per output."""
-    lib = _load()
-    X2 = _f32(X2)
-    Wd = _f32(Wd)
-    rows, I = X2.shape
-    cols = Wd.shape[0]
-    out = np.empty((rows, cols), np.float32)
-    lib.oracle_projection(rows, I, cols, _fptr(X2), _fptr(Wd), _fptr(out))
-    return out
 
 
 def rnn_cell(hidden_size, input_size, X, H, W, R, B, activation="Tanh", clip=float("inf")):

@@ -630,16 +630,6 @@ int oracle_rnn_cell(long hidden_size, long input_size, const char* activation, f
     return 0;
 }
 
-/* XW = X . W[d]^T for all rows of X viewed as [rows, I] (the input
- * projection of the Computation section), written as [rows, G*H]. */
-void oracle_projection(long rows, long input_size, long cols,
-                       const float* X, const float* Wd, float* XW)
-{
-    for (long m = 0; m < rows; ++m)
-        for (long j = 0; j < cols; ++j)
-            XW[m * cols + j] = o_dot(X + m * input_size, Wd + j * input_size, input_size);
-}
-
 /* Array forms of the transcendental and activation functions, for tests. */
 void oracle_exp_n(const float* x, float* y, long n) { for (long i = 0; i < n; ++i) y[i] = oracle_exp(x[i]); }
 void oracle_log_n(const float* x, float* y, long n) { for (long i = 0; i < n; ++i) y[i] = oracle_log(x[i]); }
