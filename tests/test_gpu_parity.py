@@ -297,13 +297,25 @@ def _sample_rows(c, k):
     return sorted(rows)
 
 
+_ORACLE_ROWS = {}
+
+
+def _oracle_rows(c, rows):
+    """The oracle's outputs on the listed rows of a workload (row slices only),
+    computed once per (workload, lbr, rows) for the exact and the fast checks."""
+    key = (c.name, c.linear_before_reset, tuple(rows))
+    if key not in _ORACLE_ROWS:
+        ref = oracle_case(c, rows=rows, threaded=True)
+        _ORACLE_ROWS[key] = (row_slice(c, rows, ref[0], "Y"), row_slice(c, rows, ref[1], "state"),
+                             row_slice(c, rows, ref[2], "state"))
+    return _ORACLE_ROWS[key]
+
+
 def _workload_check(c, rows, mode="exact"):
     got = gpu_case(c, mode)
-    ref = oracle_case(c, rows=rows, threaded=True)
+    rs = _oracle_rows(c, rows)
     gs = (row_slice(c, rows, got[0], "Y"), row_slice(c, rows, got[1], "state"),
           row_slice(c, rows, got[2], "state"))
-    rs = (row_slice(c, rows, ref[0], "Y"), row_slice(c, rows, ref[1], "state"),
-          row_slice(c, rows, ref[2], "state"))
     if mode == "exact":
         _compare_exact(c, gs, rs, c.name)
     else:
@@ -319,7 +331,7 @@ def _workload_check(c, rows, mode="exact"):
 
 WORKLOAD_CASES = [("rnn_fwd_s8_b1_i16_h128", 0, 1), ("lstm_fwd_s64_b32_i256_h512", 0, 8),
                   ("gru_bidi_s128_b64_i512_h1024", 0, 6), ("gru_bidi_s128_b64_i512_h1024", 1, 6),
-                  ("lstm_bidi_s512_b128_i1024_h1024", 0, 3), ("gru_rev_s4096_b4_i256_h2048", 1, 1)]
+                  ("lstm_bidi_s512_b128_i1024_h1024", 0, 3), ("gru_rev_s4096_b4_i256_h2048", 1, 4)]
 
 
 @pytest.mark.slow
@@ -330,10 +342,13 @@ def test_workload_full_size_exact(name, lbr, k):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,lbr,k", WORKLOAD_CASES[:5], ids=[f"{w[0]}-lbr{w[1]}" for w in WORKLOAD_CASES[:5]])
+@pytest.mark.parametrize("name,lbr,k", WORKLOAD_CASES, ids=[f"{w[0]}-lbr{w[1]}" for w in WORKLOAD_CASES])
 def test_workload_full_size_fast(name, lbr, k):
+    # the same rows as the exact check (the oracle's rows are computed once);
+    # the 4096-step GRU reverse workload checks all four of its rows, where
+    # the fused products' rounding compounds over the most steps
     c = workload(name, lbr=lbr)
-    _workload_check(c, _sample_rows(c, min(k, 3)), "fast")
+    _workload_check(c, _sample_rows(c, k), "fast")
 
 
 # TF32 and BF16 modes: the input projection on the tensor cores (tcgen05),
@@ -379,11 +394,10 @@ def test_tensor_core_modes_differ_from_fp32_only_by_the_projection(mode):
 @pytest.mark.parametrize("name,lbr,k", WORKLOAD_CASES[1:5], ids=[f"{w[0]}-lbr{w[1]}" for w in WORKLOAD_CASES[1:5]])
 def test_workload_full_size_tensor_core_modes(name, lbr, k, mode):
     c = workload(name, lbr=lbr)
-    rows = _sample_rows(c, min(k, 3))
+    rows = _sample_rows(c, k)
     got = gpu_case(c, mode)
-    ref = oracle_case(c, rows=rows, threaded=True)
     _compare_fast(tuple(row_slice(c, rows, g, kind) for g, kind in zip(got, ("Y", "state", "state"))),
-                  tuple(row_slice(c, rows, r, kind) for r, kind in zip(ref, ("Y", "state", "state"))), TC_TOL)
+                  _oracle_rows(c, rows), TC_TOL)
 
 
 # The tensor-core recurrent kernel (kernel 3: fp16 operands, FP32 sums),
