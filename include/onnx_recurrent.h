@@ -186,7 +186,10 @@ rnn_status rnn_plan_set_weights(rnn_plan_t plan, const float* W, const float* R,
 
 /* Wait for the plan's last run and report its device status: RNN_OK, or
  * RNN_ERR_TIMEOUT if the step barrier gave up (the outputs are then
- * incomplete).  Clears the status. */
+ * incomplete).  Clears the status.  After rnn_run_static_scratch it waits for
+ * the whole device and reads the status word of the fixed scratch array,
+ * which every static-scratch run on that device shares (the latest such run's
+ * status). */
 rnn_status rnn_plan_sync(rnn_plan_t plan);
 
 /* The resolved activation of slot `slot` (0 = f, 1 = g, 2 = h) of direction
@@ -251,13 +254,18 @@ int rnn_plan_last_launch_count(rnn_plan_t plan);
  * they are constant, seq*batch*D*G*H floats of projection and the h exchange
  * buffers) does not fit returns RNN_ERR_UNSUPPORTED before any device work.
  * The first call on a device looks up the array's device address (once per
- * device); make that first call before any stream capture.  Every call
- * shares the one array and leaves its contents behind; what must start at
- * zero is cleared by each call, so calls that overlap on the GPU (another
- * stream, another thread or another plan) race and must be serialised by the
- * caller.  Barrier waits are bounded as in rnn_run, but a timed-out run is
- * not reported by rnn_plan_sync (its outputs are then incomplete), and
- * rnn_plan_debug_barrier and timing do not apply. */
+ * device, cached for the life of the process: a device reset with
+ * cudaDeviceReset makes the cached address stale, so do not call this entry
+ * point on a device after resetting it); make that first call before any
+ * stream capture.  Every call shares the one array and leaves its contents
+ * behind; what must start at zero (barrier counters, the status word) is
+ * cleared by each call, so calls that overlap on the GPU (another stream,
+ * another thread or another plan) race and must be serialised by the
+ * caller.  Outside a stream capture the recurrent launch is ordered behind
+ * the device's other recurrent launches, as in rnn_run.  Barrier waits are
+ * bounded as in rnn_run (rnn_plan_debug_barrier applies): rnn_plan_sync
+ * reports a timed-out run as RNN_ERR_TIMEOUT (its outputs are then
+ * incomplete).  Timing (rnn_plan_set_timing) does not apply. */
 rnn_status rnn_run_static_scratch(rnn_plan_t plan, int64_t seq_length, int64_t batch_size,
                                   const float* X, const float* W, const float* R,
                                   const float* B, const int32_t* sequence_lens,

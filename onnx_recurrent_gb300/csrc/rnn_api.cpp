@@ -162,6 +162,11 @@ struct rnn_plan {
 
     bool cell = false;   // made by rnn_cell_plan_create
     int io = 0;          // element type of X, initial states, Y, Y_h, Y_c (RNN_IO_*)
+
+    // the last run came from rnn_run_static_scratch: its status word lives in
+    // the fixed array (shared by every static run on that device)
+    bool last_static = false;
+    int* static_status = nullptr;
 };
 
 namespace {
@@ -1128,6 +1133,23 @@ rnn_status rnn_plan_sync(rnn_plan_t pl)
 {
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
     if (!pl->ran) return RNN_OK;
+    if (pl->last_static) {
+        // a static-scratch run records no event of its own: wait for the
+        // device, then read (and clear) the status word of the fixed array
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "waiting for the run");
+        int st = 0;
+        e = cudaMemcpy(&st, pl->static_status, sizeof st, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+        if (st != 0) {
+            const int zero = 0;
+            cudaMemcpy(pl->static_status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+            if (st == RNN_ERR_TIMEOUT)
+                return fail(RNN_ERR_TIMEOUT, "a device-side wait (step barrier or copy) timed out; outputs are incomplete");
+            return fail((rnn_status)st, "device reported status %d", st);
+        }
+        return RNN_OK;
+    }
     cudaError_t e = pl->done_ready ? cudaEventSynchronize(pl->done) : cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "waiting for the run");
     if (!pl->ctrl) return RNN_OK;      // only cell runs so far: no device-side waits, no status word
@@ -1241,6 +1263,7 @@ static rnn_status run_plan(rnn_plan_t pl, int64_t S, int64_t N, const float* X, 
         for (bool& u : pl->ev_used[pl->slot]) u = false;
     }
     int launches = 0;
+    pl->last_static = false;
     rs = enqueue(pl, a, geo, max_len, pl->scratch, L, pl->ctrl, pl->timing, pl->spin_limit_ns, pl->skip_cta,
                  &launches);
     if (rs != RNN_OK) return rs;
@@ -1441,12 +1464,12 @@ rnn_status rnn_run_static_scratch(rnn_plan_t pl, int64_t S, int64_t N, const flo
     g_error.clear();
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
     pl->last_launches = 0;
-    if (N > kMaxBatch)
-        return fail(RNN_ERR_UNSUPPORTED, "static-scratch runs take at most %lld batch rows", (long long)kMaxBatch);
     RunArgs a{S, N, X, W, R, B, lens, h0, c0, P, Y, Yh, Yc, (cudaStream_t)stream};
     bool done = false;
     rnn_status rs = check_run(pl, a, &done);
-    if (rs != RNN_OK || done) return rs;
+    if (rs != RNN_OK || done) return rs;      // zero-size runs need no scratch: any batch size
+    if (N > kMaxBatch)
+        return fail(RNN_ERR_UNSUPPORTED, "static-scratch runs take at most %lld batch rows", (long long)kMaxBatch);
 
     DeviceInfo di;
     rs = device_info(&di);
@@ -1478,9 +1501,12 @@ rnn_status rnn_run_static_scratch(rnn_plan_t pl, int64_t S, int64_t N, const flo
     e = cudaMemsetAsync(sb + kCtrlStatusOffset, 0, sizeof(int), a.st);   // status starts at 0 on every call
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
     int launches = 0;
-    rs = enqueue(pl, a, geo, max_len, sb, L, sb, false, kDefaultSpinNs, -1, &launches);
+    rs = enqueue(pl, a, geo, max_len, sb, L, sb, false, pl->spin_limit_ns, pl->skip_cta, &launches);
     if (rs != RNN_OK) return rs;
     pl->last_launches = launches;
+    pl->last_static = true;          // rnn_plan_sync reads the fixed array's status word
+    pl->static_status = (int*)(sb + kCtrlStatusOffset);
+    pl->ran = true;
     return RNN_OK;
 }
 

@@ -7,7 +7,10 @@
 // memory, so its device address is looked up here with cudaGetSymbolAddress,
 // once per device with that device current, and cached; that address is what
 // the kernels receive.  The first call on a device performs this look-up, so
-// it should come before any stream capture.
+// it should come before any stream capture.  The cache lives as long as the
+// process: after cudaDeviceReset the module is loaded again in a new context
+// and the cached address would be stale, so the entry point is not for use on
+// a device that has been reset.
 #include <mutex>
 
 #include "rnn_internal.h"

@@ -8,7 +8,6 @@ This file is collected last so that a failure here, under -x, comes after
 every other test has run; it also passes alone in a fresh process."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -82,33 +81,47 @@ def test_static_scratch_refuses_runs_that_do_not_fit(lib):
     orc.rnn_plan_destroy(plan)
 
 
-def test_static_scratch_runs_inside_a_cuda_graph(lib):
-    # captured once (after one call outside the capture, which looks up the
-    # static array), then replayed with new inputs: the same bits as rnn_run
-    c = make_case("LSTM", "forward", 6, 8, 16, 64, seed=11, with_P=True, h0_scale=0.5, c0_scale=0.5)
-    plan = orc.rnn_plan_create(c.op, c.direction, c.hidden_size, c.input_size, layout=c.layout)
+def test_static_scratch_timeout_is_reported(lib):
+    # one CTA withholds its first arrival and every wait gives up after 50 ms:
+    # rnn_plan_sync reads the fixed array's status word and reports TIMEOUT;
+    # the next call clears the word and gives rnn_run's bits
+    c = make_case("LSTM", "forward", 5, 4, 8, 64, seed=9, h0_scale=0.5, c0_scale=0.5)
+    plan = orc.rnn_plan_create(c.op, c.direction, c.hidden_size, c.input_size)
+    orc.rnn_plan_set_launch(plan, 4, 1, 1, 0, 1)
+    orc.rnn_plan_debug_barrier(plan, 50_000_000, 1)
     dev = {k: (None if v is None else torch.from_numpy(v).cuda()) for k, v in c.tensors().items()}
     outs = [torch.empty(c.y_shape(), device="cuda"), torch.empty(c.state_shape(), device="cuda"),
             torch.empty(c.state_shape(), device="cuda")]
     _static_run(lib, plan, c, dev, outs)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(graph, stream=side):
-            _static_run(lib, plan, c, dev, outs)
-    torch.cuda.synchronize()
-    g = np.random.default_rng(2)
-    for rep in range(2):
-        X = g.normal(size=c.X.shape).astype(np.float32)
-        dev["X"].copy_(torch.from_numpy(X))
+    with pytest.raises(orc.RNNError) as e:
+        orc.rnn_plan_sync(plan)
+    assert e.value.status == 6
+    orc.rnn_plan_debug_barrier(plan, 0, -1)
+    ref = gpu_case(c, "exact")
+    for call in range(2):
         for o in outs:
             o.fill_(float("nan"))
-        graph.replay()
-        torch.cuda.synchronize()
-        ref = gpu_case(c.with_(X=X), "exact")
-        for nm, got, r in zip(("Y", "Y_h", "Y_c"), outs, ref):
-            assert_bits_equal(got.cpu().numpy(), r, f"replay {rep} {nm}")
-    del graph
+        _static_run(lib, plan, c, dev, outs)
+        orc.rnn_plan_sync(plan)
+        for nm, g, r in zip(("Y", "Y_h", "Y_c"), outs, ref):
+            assert_bits_equal(g.cpu().numpy(), r, f"after timeout, call {call} {nm}")
+    orc.rnn_plan_destroy(plan)
+
+
+def test_static_scratch_zero_size_takes_any_batch(lib):
+    # seq 0 needs no scratch: a batch past the static limit (4096 rows) is
+    # served like rnn_run (Y_h = initial_h)
+    N, H = 5000, 8
+    plan = orc.rnn_plan_create("GRU", "forward", H, 3)
+    h0 = torch.randn(1, N, H, device="cuda")
+    Yh = torch.full((1, N, H), float("nan"), device="cuda")
+    X = torch.empty(0, N, 3, device="cuda")
+    W = torch.zeros(1, 3 * H, 3, device="cuda")
+    R = torch.zeros(1, 3 * H, H, device="cuda")
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    st = lib.rnn_run_static_scratch(plan.handle, 0, N, p(X), p(W), p(R), None, None, p(h0), None, None,
+                                    None, p(Yh), None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, orc.rnn_last_error()
+    torch.cuda.synchronize()
+    assert torch.equal(Yh, h0)
     orc.rnn_plan_destroy(plan)
