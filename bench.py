@@ -3,10 +3,14 @@
 
 One step = one rnn_run (weight pack, input projection, state set-up,
 persistent recurrence, mask epilogue) over one batch of the workload, inputs
-resident in HBM.  The default workload is the LSTM forward layer (seq 64,
-batch 32, input 256, hidden 512, peepholes).  The metric is cell-steps per
-second (seq * batch * dirs per step), aggregated over ranks; each rank runs
-an independent replica (the operator has no exchange between GPUs).
+resident in HBM.  The default workload is the largest one that fits one GPU:
+the LSTM bidirectional layer (seq 512, batch 128, input 1024, hidden 1024,
+clip 3, HardSigmoid / LeakyRelu / ScaledTanh forward, sequence_lens), in
+fast mode (fp32: fused multiply-adds, within 1e-5 of the exact arithmetic).
+The metric is cell-steps per second (seq * batch * dirs per step),
+aggregated over ranks; each rank runs an independent replica (the operator
+has no exchange between GPUs).  The value comes from the median step time
+over the K timed steps (the mean is reported beside it).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--mode exact|fast|tf32|bf16]
                   [--workload NAME] [--impl ours|reference]
@@ -14,6 +18,10 @@ an independent replica (the operator has no exchange between GPUs).
 The L2 (129 MB) is flushed between timed steps by writing a 256 MiB buffer
 outside the timed events.  Per-kernel times come from CUDA events the library
 records on its own stream around each kernel during the timed steps.  The
+recurrent kernel's roofline is the per-step one: each step is bounded below by
+the largest of its FP32 work over the ALU peak, its resident R bytes over the
+shared-memory bandwidth, and the R bytes that cannot stay in shared memory
+over the L2 bandwidth (measured here with a copy that fits in L2).  The
 reference arm (--impl reference) times the CPU oracle on the host, one batch
 row of the workload per step.
 """
@@ -33,19 +41,20 @@ sys.path.insert(0, ROOT)
 
 METRIC = "cell-steps/sec (seq*batch*dirs per s) at 1 GB300; % of roofline per kernel"
 UNIT = "cell-steps/s"
-DEFAULT_WORKLOAD = "lstm_fwd_s64_b32_i256_h512"
+DEFAULT_WORKLOAD = "lstm_bidi_s512_b128_i1024_h1024"
+DEFAULT_MODE = "fast"
 FLUSH_BYTES = 256 << 20
 
 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--lbr", type=int, default=0)
-    ap.add_argument("--mode", default="exact", choices=["exact", "fast", "tf32", "bf16"])
+    ap.add_argument("--mode", default=DEFAULT_MODE, choices=["exact", "fast", "tf32", "bf16"])
     ap.add_argument("--io", default="f32", choices=["f32", "f16", "bf16"],
                     help="element type of X, initial states and outputs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -164,6 +173,76 @@ def algorithmic(case):
     return rec, proj, proj_bytes
 
 
+def live_rows_per_step(case):
+    """Rows still running at each step the recurrent kernel takes (it runs
+    max(len) steps; a row of length L is live in steps 0..L-1)."""
+    import numpy as np
+    if case.sequence_lens is None:
+        return [case.batch] * case.seq
+    L = np.asarray(case.sequence_lens, np.int64)
+    steps = int(L.max(initial=0))
+    return [int((L > s).sum()) for s in range(steps)]
+
+
+def step_roofline(case, mode, rec_ms, sms, clock_mhz, l2_gbs, smem_per_sm):
+    """The recurrent kernel's per-step roofline (per launch): every step takes
+    at least the largest of
+      alu   2 * live rows * D * G * H^2 FLOP over the FP32 peak (fused
+            multiply-add in the fast modes, separate multiply and add in exact);
+      smem  the R slices read once from shared memory, D * 4 * G * H^2 bytes,
+            over SMs * 128 bytes per clock;
+      l2    the part of R that cannot stay resident in the SMs' shared memory
+            (D * 4 * G * H^2 - SMs * smem_per_sm, if positive), streamed from L2
+            every step, over the measured L2 copy bandwidth.
+    Returns the terms per step (microseconds, averaged over the steps), the
+    binding term, the roofline time of the launch and its fraction of the
+    measured time."""
+    G, H, D = case.gates, case.hidden_size, case.dirs
+    live = live_rows_per_step(case)
+    clock = clock_mhz * 1e6
+    alu_peak = sms * 128 * (1 if mode == "exact" else 2) * clock
+    smem_bw = sms * 128 * clock
+    r_bytes = 4.0 * D * G * H * H
+    streamed = max(0.0, r_bytes - float(sms) * smem_per_sm)
+    t_smem = r_bytes / smem_bw
+    t_l2 = streamed / (l2_gbs * 1e9) if l2_gbs else 0.0
+    roof, terms = 0.0, {"alu": 0.0, "smem": 0.0, "l2": 0.0}
+    for n in live:
+        t_alu = 2.0 * n * D * G * H * H / alu_peak
+        roof += max(t_alu, t_smem, t_l2)
+        terms["alu"] += t_alu
+        terms["smem"] += t_smem
+        terms["l2"] += t_l2
+    steps = max(1, len(live))
+    binding = max(terms, key=terms.get)
+    return {"terms_us_per_step": {k: round(v / steps * 1e6, 4) for k, v in terms.items()},
+            "binding": binding, "steps": len(live), "roof_ms": round(roof * 1e3, 5),
+            "measured_ms": round(rec_ms, 5), "frac": round(roof * 1e3 / rec_ms, 4) if rec_ms else 0.0,
+            "peaks": {"alu_tflops": round(alu_peak / 1e12, 3), "smem_tbs": round(smem_bw / 1e12, 3),
+                      "l2_gbs": round(l2_gbs, 1) if l2_gbs else None,
+                      "note": "alu and smem derived (SMs x 128 lanes or bytes per clock x max SM clock); "
+                              "l2 measured by a device copy that fits in L2"},
+            "r_bytes_per_step": r_bytes, "r_streamed_bytes_per_step": streamed}
+
+
+def measure_l2_gbs(torch, nbytes=32 << 20, reps=50):
+    """Copy bandwidth (read + write bytes per second) of a buffer pair that
+    fits in the L2, timed with CUDA events after warm-up copies."""
+    a = torch.empty(nbytes // 4, device="cuda")
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    for _ in range(5):
+        b.copy_(a)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        b.copy_(a)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return 2.0 * nbytes * reps / (ms / 1e3) / 1e9
+
+
 KERNEL_SOURCES = {
     "recurrence": ["k_recur.cuh", "k_recur2.cuh", "k_recur_rnn.cu", "k_recur_gru.cu", "k_recur_lstm.cu",
                    "k_recur_tc.cu", "tma.cuh", "exact_math.cuh", "io_types.cuh", "rnn_internal.h"],
@@ -206,7 +285,7 @@ class SequenceJob:
     """One rnn_run of a sequence-operator workload per step."""
 
     def __init__(self, args, orc, torch):
-        from onnx_recurrent_gb300.synth import WORKLOADS, workload
+        from onnx_recurrent_gb300.synth import PROFILE_WORKLOADS, WORKLOADS, workload
         self.case = c = workload(args.workload, lbr=args.lbr)
         self.host = {k: v for k, v in c.tensors().items() if v is not None}
         self.plan = orc.rnn_plan_create(c.op, c.direction, c.hidden_size, c.input_size,
@@ -217,7 +296,8 @@ class SequenceJob:
         self.out_shapes = [c.y_shape(), c.state_shape()] + ([c.state_shape()] if c.op == "LSTM" else [])
         self.cells = c.cell_steps()
         self.rec_flops, self.proj_flops, _ = algorithmic(c)
-        self.config = {"workload": args.workload, "description": WORKLOADS.get(args.workload, ""),
+        desc = WORKLOADS.get(args.workload, PROFILE_WORKLOADS.get(args.workload, ""))
+        self.config = {"workload": args.workload, "description": desc,
                        "op": c.op, "direction": c.direction, "seq": c.seq, "batch": c.batch,
                        "input": c.input_size, "hidden": c.hidden_size,
                        "valid_cell_steps_per_step": c.valid_cell_steps()}
@@ -365,6 +445,7 @@ def run_ours(args, ws, rank, local):
     outs = [torch.empty(sh, device="cuda", dtype=act) for sh in job.out_shapes]
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
     stream = torch.cuda.current_stream()
+    l2_gbs = measure_l2_gbs(torch)
 
     def step():
         job.run(dev, outs, stream)
@@ -404,7 +485,9 @@ def run_ours(args, ws, rank, local):
         time.sleep(0.25)
         sampler.stop()
     orc.rnn_plan_sync(plan)
-    total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(step_ms)
+    median_ms = statistics.median(step_ms)
     kern_ms, runs = {}, 0
     for p_ in timed:                       # a stack: each kernel kind summed over the layers
         orc.rnn_plan_sync(p_)
@@ -460,17 +543,18 @@ def run_ours(args, ws, rank, local):
     e2e_ms = e_start.elapsed_time(e_end)
 
     if dist:
-        total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, "cuda")
+        total_ms, median_ms, e2e_ms = max_over_ranks([total_ms, median_ms, e2e_ms], dist, "cuda")
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
     cells = job.cells
-    value = job_value(cells, K, ws, total_ms)
+    value = job_value(cells, 1, ws, median_ms)
     e2e_value = job_value(cells, E, ws, e2e_ms)
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     sms = props.multi_processor_count
+    smem_per_sm = int(getattr(props, "shared_memory_per_block_optin", 232448))
     peaks = measured_peaks()
     clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
     exact = args.mode == "exact"
@@ -505,18 +589,33 @@ def run_ours(args, ws, rank, local):
                     "kernel": "rnn_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": rec_flops,
                     "peak_note": "of measured bf16 burst (fp16 operands, same nominal rate)"}
         if kernel == "recurrence":
+            name = "rnn_dataflow_kernel" if geometry.get("kernel") == 2 else "rnn_recurrent_kernel"
+            traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel))
+            sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm)
+                  if isinstance(job, SequenceJob) else None)
+            if sr and sr["binding"] == "l2":
+                # R does not fit in the SMs' shared memory and its streamed part
+                # bounds the step: bytes from L2 against the measured L2 copy rate
+                nbytes = sr["r_streamed_bytes_per_step"] * sr["steps"]
+                ach = nbytes / (ms / 1e3) / 1e9 if ms else 0.0
+                return {"bound": "l2", "achieved": round(ach, 1), "peak": round(l2_gbs, 1), "unit": "GB/s",
+                        "frac": sr["frac"], "traffic": traffic, "kernel": name, "avg_ms": round(ms, 5),
+                        "algorithmic_bytes_per_launch": nbytes, "step_roofline": sr,
+                        "peak_note": "of measured L2 copy bandwidth (read + write, a 32 MiB pair)"}
             ach = rec_flops / (ms / 1e3) / 1e12 if ms else 0.0
-            return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
-                    "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
-                    "kernel": "rnn_dataflow_kernel" if geometry.get("kernel") == 2 else "rnn_recurrent_kernel",
-                    "avg_ms": round(ms, 5),
-                    "algorithmic_flops_per_launch": rec_flops,
-                    "peak_note": f"{'no' if exact else 'fused'} multiply-add: {sms} SMs x 128 FP32 "
-                                 f"lanes x {'1' if exact else '2'} FLOP x {clock_mhz:.0f} MHz (derived)"}
+            out = {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
+                   "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
+                   "traffic": traffic, "kernel": name, "avg_ms": round(ms, 5),
+                   "algorithmic_flops_per_launch": rec_flops,
+                   "peak_note": f"{'no' if exact else 'fused'} multiply-add: {sms} SMs x 128 FP32 "
+                                f"lanes x {'1' if exact else '2'} FLOP x {clock_mhz:.0f} MHz (derived)"}
+            if sr:
+                out["step_roofline"] = sr
+            return out
         if kernel == "projection" and args.mode in ("tf32", "bf16"):
             # tensor cores: the measured bf16 burst peak, scaled by the nominal
-            # TF32 : bf16 ratio (1.1 : 2.25 PFLOP/s dense) for TF32
+            # TF32 : bf16 ratio (1.1 : 2.25 PFLOP/s dense) for TF32: the TF32
+            # peak is derived from the bf16 measurement, not measured itself
             bf16 = float(peaks.get("bf16_tflops", 1900.0))
             peak = bf16 if args.mode == "bf16" else bf16 * 1.1 / 2.25
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
@@ -524,7 +623,9 @@ def run_ours(args, ws, rank, local):
                     "frac": round(ach / peak, 4) if ms else 0.0,
                     "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
                     "kernel": "proj_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": proj_flops,
-                    "peak_note": "of measured bf16 burst" + ("" if args.mode == "bf16" else " x 1.1/2.25 (TF32)")}
+                    "peak_note": "of measured bf16 burst" + ("" if args.mode == "bf16" else
+                                                             " x 1.1/2.25 (TF32: derived from the bf16 "
+                                                             "measurement by the nominal dense-rate ratio)")}
         if kernel == "projection":
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
@@ -537,7 +638,9 @@ def run_ours(args, ws, rank, local):
     clocks = sampler.summary(t0, t1) if sampler else None
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(median_ms, 5),
+        "ms_per_step_mean": round(total_ms / K, 5), "value_from": "median step time over the timed steps",
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"exact": "f32", "fast": "f32", "tf32": "f32 (tf32 projection)",
                   "bf16": "f32 (bf16 projection)"}[args.mode] + ("" if args.io == "f32" else f", {args.io} I/O"),

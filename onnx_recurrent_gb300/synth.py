@@ -155,6 +155,16 @@ WORKLOADS = {
         "GRU reverse, seq 4096, batch 4, input 256, hidden 2048, linear_before_reset 1",
 }
 
+# Shorter sequences of the same per-step shapes, for profiler captures (a few
+# hundred MB on the device instead of gigabytes; every step is the same work).
+PROFILE_WORKLOADS = {
+    "lstm_bidi_s64_b128_i1024_h1024":
+        "the LSTM bidirectional workload (batch 128, input 1024, hidden 1024, clip 3, same activations) "
+        "cut to 64 steps, sequence_lens U{1..64}",
+    "gru_rev_s256_b4_i256_h2048":
+        "the GRU reverse workload (batch 4, input 256, hidden 2048, linear_before_reset 1) cut to 256 steps",
+}
+
 
 def workload(name: str, *, lbr: int = 0, initial_h_zero: bool = False) -> RNNCase:
     """Seeded inputs (seed 0) of a named workload."""
@@ -182,6 +192,15 @@ def workload(name: str, *, lbr: int = 0, initial_h_zero: bool = False) -> RNNCas
                          alpha=[0.25, 0.05, 1.5], beta=[0.45, 0.8], name=name)
     if name == "gru_rev_s4096_b4_i256_h2048":
         return make_case("GRU", "reverse", 4096, 4, 256, 2048, linear_before_reset=1,
+                         h0_scale=0.5, name=name)
+    if name == "lstm_bidi_s64_b128_i1024_h1024":
+        return make_case("LSTM", "bidirectional", 64, 128, 1024, 1024, w_scale=1.0 / 32,
+                         with_B=False, with_P=True, lens=("uniform", 1, 64), clip=3.0,
+                         activations=["HardSigmoid", "LeakyRelu", "ScaledTanh",
+                                      "Sigmoid", "Tanh", "Tanh"],
+                         alpha=[0.25, 0.05, 1.5], beta=[0.45, 0.8], name=name)
+    if name == "gru_rev_s256_b4_i256_h2048":
+        return make_case("GRU", "reverse", 256, 4, 256, 2048, linear_before_reset=1,
                          h0_scale=0.5, name=name)
     raise KeyError(name)
 

@@ -72,3 +72,42 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["unit"] == bench.UNIT and d["steps"] == 3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["value"] == pytest.approx(d["e2e"]["value"])
+
+
+def test_live_rows_follow_the_lengths():
+    c = workload("lstm_bidi_s512_b128_i1024_h1024")
+    live = bench.live_rows_per_step(c)
+    assert len(live) == int(c.sequence_lens.max())
+    assert live[0] == c.batch and live[-1] >= 1
+    assert sum(live) == int(c.sequence_lens.sum())          # sum over steps = sum of lengths
+    assert all(a >= b for a, b in zip(live, live[1:]))
+
+
+def test_step_roofline_terms():
+    # LSTM forward, fast mode: 2 * 32 * 4 * 512^2 FLOP per step against
+    # 152 SMs x 128 lanes x 2 FLOP x 2070 MHz; R (4 MiB) fits in shared memory
+    c = workload("lstm_fwd_s64_b32_i256_h512")
+    sr = bench.step_roofline(c, "fast", 1.0, 152, 2070.0, 20000.0, 232448)
+    alu_us = 2.0 * 32 * 4 * 512 * 512 / (152 * 128 * 2 * 2070e6) * 1e6
+    smem_us = 4.0 * 4 * 512 * 512 / (152 * 128 * 2070e6) * 1e6
+    assert sr["terms_us_per_step"]["alu"] == pytest.approx(alu_us, rel=1e-3)
+    assert sr["terms_us_per_step"]["smem"] == pytest.approx(smem_us, rel=1e-3)
+    assert sr["terms_us_per_step"]["l2"] == 0.0 and sr["r_streamed_bytes_per_step"] == 0.0
+    assert sr["binding"] == "alu"
+    assert sr["roof_ms"] == pytest.approx(64 * max(alu_us, smem_us) / 1e3, rel=1e-3)
+    assert sr["frac"] == pytest.approx(sr["roof_ms"] / 1.0, rel=1e-3)
+    # exact mode halves the ALU peak (no fused multiply-add)
+    ex = bench.step_roofline(c, "exact", 1.0, 152, 2070.0, 20000.0, 232448)
+    assert ex["terms_us_per_step"]["alu"] == pytest.approx(2 * alu_us, rel=1e-3)
+
+
+def test_step_roofline_streams_what_does_not_fit():
+    # GRU reverse, hidden 2048: R is 3 * 2048^2 * 4 bytes = 48 MiB, more than
+    # 152 SMs x 227 KiB of shared memory; the rest streams from L2 every step
+    c = workload("gru_rev_s4096_b4_i256_h2048")
+    sr = bench.step_roofline(c, "fast", 10.0, 152, 2070.0, 10000.0, 232448)
+    r = 4.0 * 3 * 2048 * 2048
+    assert sr["r_bytes_per_step"] == r
+    assert sr["r_streamed_bytes_per_step"] == r - 152 * 232448
+    assert sr["terms_us_per_step"]["l2"] == pytest.approx((r - 152 * 232448) / 10000e9 * 1e6, rel=1e-3)
+    assert sr["steps"] == 4096
