@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--mode", default=DEFAULT_MODE, choices=["exact", "fast", "tf32", "bf16"])
     ap.add_argument("--io", default="f32", choices=["f32", "f16", "bf16"],
                     help="element type of X, initial states and outputs")
+    ap.add_argument("--launch", default=None,
+                    help="recurrent launch override unit_groups,rows_per_thread,r_resident,row_groups,kernel "
+                         "(rnn_plan_set_launch; 0 / -1 = the planner's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     return ap.parse_args()
@@ -438,6 +441,8 @@ def run_ours(args, ws, rank, local):
     else:
         orc.rnn_plan_set_mode(plan, args.mode)
         orc.rnn_plan_set_io_type(plan, args.io)
+        if args.launch:
+            orc.rnn_plan_set_launch(plan, *[int(v) for v in args.launch.split(",")])
     act = orc.rnn.io_dtype(plan)
     is_io = lambda k: k == "X" or k.startswith("initial_")   # the tensors in the I/O type (weights stay fp32)
     dev = {k: (torch.from_numpy(v).to(act) if is_io(k) else torch.from_numpy(v)).cuda()

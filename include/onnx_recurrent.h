@@ -206,7 +206,7 @@ rnn_status rnn_plan_get_activation(rnn_plan_t plan, int dir, int slot, int* fn,
  * fetches h with TMA tensor copies once every CTA of its row group has
  * published the step on the row group's counter).  unit_groups: CTAs per direction along
  * hidden units; row_groups: along batch rows (dataflow kernel only);
- * rows_per_thread: 1, 2, 4 (or 8, staged kernel only); r_resident: R slice
+ * rows_per_thread: 1, 2, 4 or 8; r_resident: R slice
  * kept in shared memory (1) or streamed through it (0).  Every geometry gives
  * the same results.  rnn_plan_get_launch reports the geometry of the last
  * run; a shape the override cannot serve makes the run return

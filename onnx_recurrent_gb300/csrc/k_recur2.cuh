@@ -233,14 +233,14 @@ __device__ __forceinline__ void df_piece(const char* const (&hp)[TN], int hstep,
 template <int TN, int NC, bool EXACT>
 __device__ __forceinline__ bool consume_product(const RecParams& p, const DfCtx& x, int col_off,
                                                 float (&acc)[TN][NC], unsigned& q, volatile int* abort_flag,
-                                                int lane)
+                                                int lane, bool live)
 {
     bool ok = true;
     for (int pc = 0; pc < x.npieces; ++pc, ++q) {
         const int slot = (int)(q % (unsigned)x.slots);
         const unsigned round = q / (unsigned)x.slots;
         if (ok) ok = mbar_wait(&x.full[slot], round & 1u, p.status, abort_flag, p.spin_limit_ns);
-        if (ok && x.active) {
+        if (ok && x.active && live) {
             const int k0 = pc * x.cpb * kRecKC;
             const int ngroups = (min(x.cpb * kRecKC, x.H - k0) + 3) / 4;
             const char* hbox = x.Hring + (size_t)slot * x.hslot;
@@ -317,10 +317,11 @@ __device__ __forceinline__ bool publish(const DfCtx& x, unsigned* counter, volat
 
 // Threads per CTA: one row per thread keeps three groups of operands in
 // flight (up to 255 registers, 256 threads); wider tiles keep one group in
-// flight and more accumulators (up to 168 registers, 384 threads).
+// flight and more accumulators (up to 168 registers, 384 threads); eight rows
+// per thread (32 LSTM accumulators) take up to 255 registers, 256 threads.
 template <int TN>
 struct DfBounds {
-    static constexpr int threads = TN == 1 ? 256 : 384;
+    static constexpr int threads = (TN == 1 || TN == 8) ? 256 : 384;
 };
 
 // TWO: GRU with linear_before_reset = 0 (two products per step, the second
@@ -363,9 +364,16 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     x.ncompute = blockDim.x - 32;
     x.ctid = (int)threadIdx.x - 32;
     const int RB = x.NRP / TN;
-    x.rb = x.ctid >= 0 ? x.ctid % RB : 0;
-    x.ul = x.ctid >= 0 ? x.ctid / RB : 0;
-    x.active = x.ctid >= 0 && x.ul < x.U && x.rb * TN < x.NR;
+    if (p.unit_fastest) {
+        // the lanes of a quarter warp share a row tile (their h loads are
+        // broadcasts) and take distinct units (R rows 144 bytes apart)
+        x.ul = x.ctid >= 0 ? x.ctid % x.umax : 0;
+        x.rb = x.ctid >= 0 ? x.ctid / x.umax : 0;
+    } else {
+        x.rb = x.ctid >= 0 ? x.ctid % RB : 0;
+        x.ul = x.ctid >= 0 ? x.ctid / RB : 0;
+    }
+    x.active = x.ctid >= 0 && x.ul < x.U && x.rb < RB && x.rb * TN < x.NR;
     // tensor-copy destinations are 128-byte aligned
     unsigned char* base = df_smem + ((128u - (smem_addr(df_smem) & 127u)) & 127u);
     const size_t rbytes = p.r_resident ? (((size_t)x.umax * x.ugs * 4 + 127) / 128) * 128
@@ -459,6 +467,12 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     float pI = 0.f, pO = 0.f, pF = 0.f;
     float hown[TN], cown[TN], xw[TN][G];
     int len[TN];
+    // rows: the exchange buffers use the internal row rl of the row group;
+    // with sequence_lens the rows are ranked by length (longest first, so a
+    // row tile whose first row has finished has finished altogether) and
+    // rown[i] is the caller's row behind internal row cr * NRP + rl
+    int rown[TN];
+    int tile_len = 0;
 #pragma unroll
     for (int g = 0; g < G; ++g) { wb[g] = 0.f; rbv[g] = 0.f; }
     if (x.active) {
@@ -478,23 +492,29 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
 #pragma unroll
     for (int i = 0; i < TN; ++i) {
         const int rl = x.rb * TN + i;
-        const int n = x.cr * x.NRP + rl;
         const bool ok = x.active && rl < x.NR;
+        const int ni = x.cr * x.NRP + rl;
+        const int n = ok ? (p.perm ? p.perm[ni] : ni) : 0;
+        rown[i] = n;
         len[i] = ok ? (p.has_lens ? p.lens[n] : p.S) : 0;
+        tile_len = len[i] > tile_len ? len[i] : tile_len;
         hown[i] = (ok && p.has_h0) ? io_load(p.h0, s_index(p, d, n, u), p.io) : 0.f;
         cown[i] = (ok && OP == 2 && p.has_c0) ? io_load(p.c0, s_index(p, d, n, u), p.io) : 0.f;
     }
     const size_t xw_ld = (size_t)p.D * x.GH;
     const size_t xw_col = (size_t)d * x.GH + (size_t)u * G;
+    auto xw_row = [&](int s, int i) {
+        const int n = rown[i];
+        const int t = rev ? len[i] - 1 - s : s;
+        const size_t row = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
+        return p.XW + row * xw_ld + xw_col;
+    };
     auto load_xw = [&](int s) {
 #pragma unroll
         for (int i = 0; i < TN; ++i) {
             const int rl = x.rb * TN + i;
-            const int n = x.cr * x.NRP + rl;
             if (x.active && rl < x.NR && s < len[i]) {
-                const int t = rev ? len[i] - 1 - s : s;
-                const size_t row = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
-                const float* q = p.XW + row * xw_ld + xw_col;
+                const float* q = xw_row(s, i);
 #pragma unroll
                 for (int g = 0; g < G; ++g) xw[i][g] = __ldg(q + g);
             } else {
@@ -503,28 +523,54 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
             }
         }
     };
+    // Wide row tiles (4 or 8 rows per thread) have no registers to spare for
+    // the next step's XW during a product: they ask L2 for this step's XW
+    // before the product and load it into registers after it.
+    constexpr bool XW_LATE = TN >= 4;
+    auto prefetch_xw = [&](int s) {
+#pragma unroll
+        for (int i = 0; i < TN; ++i) {
+            const int rl = x.rb * TN + i;
+            if (x.active && rl < x.NR && s < len[i]) prefetch_l2(xw_row(s, i));
+        }
+    };
 
     unsigned q = 0;
     const bool skip_first = p.debug_skip_cta == (int)blockIdx.x;
     // the resident R slice must have landed (a failure here sets the abort
     // flag, and the warps leave together at the first publication)
     if (p.r_resident) mbar_wait(&s_rfill, 0u, p.status, &s_abort, p.spin_limit_ns);
-    load_xw(0);
+    if (!XW_LATE) load_xw(0);
     for (int s = 0; s < p.max_len; ++s) {
         float xc[TN][G];
+        // the step's XW: prefetched into registers during the previous step,
+        // or (wide tiles) requested from L2 now and loaded after the product
+        auto take_xw = [&]() {
 #pragma unroll
-        for (int i = 0; i < TN; ++i)
+            for (int i = 0; i < TN; ++i)
 #pragma unroll
-            for (int g = 0; g < G; ++g) xc[i][g] = xw[i][g];
+                for (int g = 0; g < G; ++g) xc[i][g] = xw[i][g];
+        };
+        auto next_xw = [&]() {
+            if constexpr (XW_LATE) {
+                load_xw(s);
+                take_xw();
+            } else if (s + 1 < p.max_len) {
+                load_xw(s + 1);
+            }
+        };
+        if constexpr (XW_LATE) prefetch_xw(s);
+        else take_xw();
         float* hdst = hblock((s + 1) & 1);
+        const bool live = s < tile_len;   // a finished row tile skips its products (its rows stay frozen)
 
         if constexpr (TWO) {
             {
                 float az[TN][2];
 #pragma unroll
                 for (int i = 0; i < TN; ++i) { az[i][0] = 0.f; az[i][1] = 0.f; }
-                consume_product<TN, 2, EXACT>(p, x, 0, az, q, &s_abort, lane);
-                if (s + 1 < p.max_len) load_xw(s + 1);
+                consume_product<TN, 2, EXACT>(p, x, 0, az, q, &s_abort, lane, live);
+                next_xw();
                 float zg[TN];
                 float* rh = rhblock(s & 1);
                 auto epi_r = [&](auto fx) {
@@ -556,14 +602,14 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 float ah[TN][1];
 #pragma unroll
                 for (int i = 0; i < TN; ++i) ah[i][0] = 0.f;
-                consume_product<TN, 1, EXACT>(p, x, 2, ah, q, &s_abort, lane);
+                consume_product<TN, 1, EXACT>(p, x, 2, ah, q, &s_abort, lane, live);
                 auto epi = [&](auto fx) {
                     constexpr bool FX = decltype(fx)::value;
                     const Acts<OP, EXACT, FX> A{fA, gA, hA};
 #pragma unroll
                     for (int i = 0; i < TN; ++i) {
                         const int rl = x.rb * TN + i;
-                        const int n = x.cr * x.NRP + rl;
+                        const int n = rown[i];
                         if (!(x.active && rl < x.NR)) continue;
                         if (s < len[i]) {
                             const int t = rev ? len[i] - 1 - s : s;
@@ -589,8 +635,8 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
             for (int i = 0; i < TN; ++i)
 #pragma unroll
                 for (int g = 0; g < G; ++g) acc[i][g] = 0.f;
-            consume_product<TN, G, EXACT>(p, x, 0, acc, q, &s_abort, lane);
-            if (s + 1 < p.max_len) load_xw(s + 1);
+            consume_product<TN, G, EXACT>(p, x, 0, acc, q, &s_abort, lane, live);
+            next_xw();
 
             auto epi = [&](auto fx) {
                 constexpr bool FX = decltype(fx)::value;
@@ -598,7 +644,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
 #pragma unroll
                 for (int i = 0; i < TN; ++i) {
                     const int rl = x.rb * TN + i;
-                    const int n = x.cr * x.NRP + rl;
+                    const int n = rown[i];
                     if (!(x.active && rl < x.NR)) continue;
                     if (s < len[i]) {
                         const int t = rev ? len[i] - 1 - s : s;
@@ -652,7 +698,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
 #pragma unroll
     for (int i = 0; i < TN; ++i) {
         const int rl = x.rb * TN + i;
-        const int n = x.cr * x.NRP + rl;
+        const int n = rown[i];
         if (!(x.active && rl < x.NR)) continue;
         const size_t si = s_index(p, d, n, u);
         if (p.Yh) io_store(p.Yh, si, len[i] > 0 ? canon_nan(hown[i]) : 0.f, p.io);
@@ -670,6 +716,8 @@ const void* dataflow_kernel_ptr(int tn, bool exact)
     case 5: return (const void*)rnn_dataflow_kernel<OP, 2, true, TWO>;
     case 8: return (const void*)rnn_dataflow_kernel<OP, 4, false, TWO>;
     case 9: return (const void*)rnn_dataflow_kernel<OP, 4, true, TWO>;
+    case 16: return (const void*)rnn_dataflow_kernel<OP, 8, false, TWO>;
+    case 17: return (const void*)rnn_dataflow_kernel<OP, 8, true, TWO>;
     default: return nullptr;
     }
 }

@@ -206,6 +206,7 @@ struct Geometry {
     int hpad;         // dataflow: exchange-buffer row length
     int cpb;          // dataflow: chunks per tensor copy
     int ustride;      // dataflow: floats per unit of the resident R slice
+    int ufast;        // dataflow: compute threads take units fastest (wide row tiles)
 };
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -292,11 +293,11 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
     const int ncr = pl->ov_rows > 0 ? 1 : 6;
     for (int cri = 0; cri < ncr; ++cri) {
         const int CRc = pl->ov_rows > 0 ? pl->ov_rows : cr_auto[cri];
-        // rows per group padded to 8; a single group of a small batch to 4
+        // rows per group padded to 8; a single group of at most 4 rows to 4
         // (padding rows skip their products but still take lanes: a batch of
         // 4 in an 8-row group left half of every warp idle).  Measured: 4-row
         // groups elsewhere (LSTM batch 32 as 8 groups) were slower than 8.
-        const int64_t NRP = round_up(ceil_div(N, CRc), CRc == 1 ? 4 : 8);
+        const int64_t NRP = round_up(ceil_div(N, CRc), (CRc == 1 && N <= 4) ? 4 : 8);
         const int CR = (int)ceil_div(N, NRP);
         if (CR != CRc) continue;                                   // would leave an empty row group
         if (NRP > 256) continue;                                   // a tensor-copy box spans at most 256 rows
@@ -312,11 +313,11 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
             const int umax = (int)(qmax * quant);
             if ((int64_t)D * CR > kMaxFlags) continue;
             int tn = 0;
-            const int tlist[3] = {1, 2, 4};
+            const int tlist[4] = {1, 2, 4, 8};
             for (int t : tlist) {
                 if (pl->ov_tn > 0 && t != pl->ov_tn) continue;
                 if (NRP % t) continue;
-                const int cap = t == 1 ? 224 : 352;   // the kernel's launch bound, less the loader
+                const int cap = (t == 1 || t == 8) ? 224 : 352;   // the kernel's launch bound, less the loader
                 if ((int64_t)umax * (NRP / t) <= cap) { tn = t; break; }
             }
             if (!tn) continue;
@@ -366,6 +367,7 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
                 out->hpad = (int)round_up(H, kRecKC);
                 out->cpb = cpb;
                 out->ustride = df_unit_stride((int)H, G);
+                out->ufast = tn >= 4 ? 1 : 0;
             }
         }
     }
@@ -662,7 +664,7 @@ Layout scratch_layout(const rnn_plan* pl, const Geometry& geo, int64_t S, int64_
     L.hb = off; off += align256(hbuf);
     L.need_rh = pl->op == RNN_OP_GRU && pl->lbr == 0;
     L.rh = off; off += L.need_rh ? align256(hbuf) : 0;
-    L.perm = off; off += geo.kernel == 1 ? align256(sizeof(int32_t) * (size_t)N) : 0;   // rows by length
+    L.perm = off; off += (geo.kernel == 1 || geo.kernel == 2) ? align256(sizeof(int32_t) * (size_t)N) : 0;   // rows by length
     L.total = off;
     return L;
 }
@@ -796,6 +798,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     p.hpad = geo.hpad;
     p.chunks_per_piece = geo.cpb;
     p.unit_stride = geo.ustride;
+    p.unit_fastest = geo.ufast;
     p.XW = xw; p.Rt = rt; p.Rorig = pl->const_weights ? pl->r_orig_const : a.R; p.B = a.B; p.P = a.P; p.h0 = a.h0; p.c0 = a.c0; p.lens = a.lens;
     p.Y = a.Y; p.Yh = a.Yh; p.Yc = a.Yc;
     p.hbuf = (float*)(scratch + L.hb);
@@ -852,9 +855,10 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         }
     }
 
-    if (geo.kernel == 1 && a.lens) {
-        // the staged kernel takes the rows longest first, so that finished
-        // row tiles drop out of the products
+    if ((geo.kernel == 1 || geo.kernel == 2) && a.lens) {
+        // the FP32 kernels take the rows longest first, so that finished row
+        // tiles (and, with several per warp, whole warps) drop out of the
+        // products
         p.perm = (const int32_t*)(scratch + L.perm);
         e = launch_rank_rows(a.lens, (int32_t*)(scratch + L.perm), (int)a.N, a.st);
         if (e != cudaSuccess) return cuda_fail(e, "row ranking launch");
@@ -1048,8 +1052,6 @@ rnn_status rnn_plan_set_launch(rnn_plan_t pl, int unit_groups, int rows_per_thre
         rows_per_thread != 8)
         return fail(RNN_ERR_INVALID_ARGUMENT, "rows_per_thread must be 0, 1, 2, 4 or 8");
     if (kernel == 1 && row_groups > 1) return fail(RNN_ERR_INVALID_ARGUMENT, "the staged kernel has one row group");
-    if (kernel == 2 && rows_per_thread == 8)
-        return fail(RNN_ERR_INVALID_ARGUMENT, "the dataflow kernel takes 1, 2 or 4 rows per thread");
     pl->ov_units = unit_groups;
     pl->ov_tn = rows_per_thread;
     pl->ov_rres = r_resident;

@@ -47,6 +47,8 @@ struct RecParams {
     int npad2;                   // tensor-core kernel, GRU lbr = 0: candidate columns per CTA
     int hpad;                    // dataflow kernel: H rounded up to 32 (chunks x 32)
     int unit_stride;             // dataflow kernel: floats per unit of the resident R slice
+    int unit_fastest;            // dataflow kernel: compute thread t takes unit t % umax and row tile t / umax
+                                 // (else row tile t % tiles, unit t / tiles)
 
     // tensors
     const float* XW;             // [S*N rows][D*G*H], columns u*G + g per direction
@@ -57,8 +59,8 @@ struct RecParams {
     const float* h0;             // layout-dependent [D,N,H] / [N,D,H] (may be null)
     const float* c0;
     const int32_t* lens;         // [N] device (may be null)
-    const int32_t* perm;         // staged kernel with lens: internal row r is the caller's row perm[r]
-                                 // (rows by length, longest first; null = identity)
+    const int32_t* perm;         // staged and dataflow kernels with lens: internal row r is the caller's
+                                 // row perm[r] (rows by length, longest first; null = identity)
     float* Y;                    // may be null
     float* Yh;
     float* Yc;

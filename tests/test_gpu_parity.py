@@ -90,6 +90,7 @@ GEOMETRIES = [
     (13, 1, 0, 0, 1), (72, 2, 1, 0, 1), (4, 8, 1, 0, 1),
     (0, 0, -1, 0, 2), (8, 1, 1, 1, 2), (9, 2, 1, 2, 2), (5, 1, 0, 2, 2), (18, 4, 1, 1, 2),
     (3, 1, 0, 2, 2), (36, 1, 1, 2, 2), (1, 4, 0, 1, 2), (3, 2, 0, 1, 2),
+    (9, 8, 0, 1, 2), (4, 8, 1, 1, 2), (6, 4, 1, 1, 2),
 ]
 
 

@@ -62,14 +62,16 @@ FINITE_EDGES = np.where(np.isfinite(EDGES) & (np.abs(EDGES) < 1e3), EDGES, F(0.7
 
 # (unit_groups, rows_per_thread, r_resident, row_groups, kernel): the planner's
 # choice, the staged kernel with one and with several CTAs, streamed R, and the
-# dataflow kernel with resident and streamed R.
+# dataflow kernel with resident and streamed R, one row per thread or a tile
+# of four rows (units fastest across the lanes, rows ranked by length).
 KERNELS = {
     "planner": None,
     "staged-1cta": (1, 1, 1, 0, 1),
     "staged-3cta": (3, 2, 1, 0, 1),
     "staged-streamed": (2, 1, 0, 0, 1),
     "dataflow": (4, 1, 1, 1, 2),
-    "dataflow-streamed": (3, 1, 0, 2, 2),
+    "dataflow-streamed": (3, 1, 0, 1, 2),
+    "dataflow-wide": (3, 4, 0, 1, 2),
 }
 
 # (op, direction, activations, alpha, beta, lbr, input_forget)
