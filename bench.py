@@ -60,6 +60,11 @@ def parse_args():
     ap.add_argument("--launch", default=None,
                     help="recurrent launch override unit_groups,rows_per_thread,r_resident,row_groups,kernel "
                          "(rnn_plan_set_launch; 0 / -1 = the planner's choice)")
+    ap.add_argument("--layer-by-layer", action="store_true",
+                    help="stack workloads: run the layers one after another")
+    ap.add_argument("--wavefront", action="store_true",
+                    help="stack workloads: one wavefront launch whenever the stack qualifies "
+                         "(default: where the library measures it faster)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     return ap.parse_args()
@@ -373,7 +378,8 @@ class StackJob:
         self.layer_plans = [orc.rnn_plan_create(c.op, c.direction, c.hidden_size, c.input_size, clip=c.clip,
                                                 layout=c.layout, linear_before_reset=c.linear_before_reset)
                             for c in cs]
-        self.plan = self.layer_plans[-1]
+        # the first layer's plan carries a wavefront run's timing, geometry and status
+        self.plan = self.layer_plans[0]
         self.stack = None
         last = cs[-1]
         self.out_shapes = [last.y_shape()] + [c.state_shape() for c in cs] + \
@@ -382,6 +388,11 @@ class StackJob:
         rows_steps = cs[0].valid_cell_steps() // cs[0].dirs      # the shared lengths, summed
         self.rec_flops = sum(2.0 * rows_steps * c.dirs * c.gates * c.hidden_size ** 2 for c in cs)
         self.proj_flops = sum(algorithmic(c)[1] for c in cs)
+        # a wavefront run forms every layer's input product but the first inside
+        # the recurrent launch (the valid steps only, as for the recurrent product)
+        self.wave_rec_flops = self.rec_flops + sum(2.0 * rows_steps * c.dirs * c.gates * c.hidden_size * c.input_size
+                                                   for c in cs[1:])
+        self.wave_proj_flops = algorithmic(cs[0])[1]
         self.config = {"workload": args.workload, "description": STACK_WORKLOADS[args.workload],
                        "layers": [{"op": c.op, "direction": c.direction, "input": c.input_size,
                                    "hidden": c.hidden_size} for c in cs],
@@ -409,6 +420,9 @@ class StackJob:
 
     def launches(self):
         return self.orc.rnn_stack_last_launch_count(self.stack)
+
+    def wavefront(self):
+        return self.orc.rnn_stack_last_wavefront(self.stack)
 
     def cpu_baseline(self):
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -438,6 +452,9 @@ def run_ours(args, ws, rank, local):
     plan = job.plan
     if isinstance(job, StackJob):
         job.set_mode(args.mode, args.io)
+        orc.rnn_stack_set_wavefront(job.stack, 0 if args.layer_by_layer else (2 if args.wavefront else 1))
+        if args.launch:        # the first plan's override: its unit_groups cap the CTAs per wavefront layer
+            orc.rnn_plan_set_launch(job.layer_plans[0], *[int(v) for v in args.launch.split(",")])
     else:
         orc.rnn_plan_set_mode(plan, args.mode)
         orc.rnn_plan_set_io_type(plan, args.io)
@@ -462,6 +479,10 @@ def run_ours(args, ws, rank, local):
     orc.rnn_plan_sync(plan)
     launches_per_step = job.launches() if isinstance(job, StackJob) else orc.rnn_plan_last_launch_count(plan)
     geometry = orc.rnn_plan_get_launch(plan)
+    if isinstance(job, StackJob):
+        job.config["wavefront"] = job.wavefront()
+        if job.config["wavefront"]:
+            job.rec_flops, job.proj_flops = job.wave_rec_flops, job.wave_proj_flops
 
     # ---- timed region: inputs resident, L2 flushed between steps
     timed = job.layer_plans if isinstance(job, StackJob) else [plan]
@@ -496,7 +517,8 @@ def run_ours(args, ws, rank, local):
     kern_ms, runs = {}, 0
     for p_ in timed:                       # a stack: each kernel kind summed over the layers
         orc.rnn_plan_sync(p_)
-        km, runs = orc.rnn_plan_timing_totals(p_)
+        km, r_ = orc.rnn_plan_timing_totals(p_)
+        runs = max(runs, r_)               # (a wavefront run is timed on the first layer's plan alone)
         for k_, v_ in km.items():
             kern_ms[k_] = kern_ms.get(k_, 0.0) + v_
         orc.rnn_plan_set_timing(p_, False)
@@ -594,7 +616,8 @@ def run_ours(args, ws, rank, local):
                     "kernel": "rnn_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": rec_flops,
                     "peak_note": "of measured bf16 burst (fp16 operands, same nominal rate)"}
         if kernel == "recurrence":
-            name = "rnn_dataflow_kernel" if geometry.get("kernel") == 2 else "rnn_recurrent_kernel"
+            name = {2: "rnn_dataflow_kernel", 4: "rnn_wavefront_kernel"}.get(geometry.get("kernel"),
+                                                                            "rnn_recurrent_kernel")
             traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel))
             sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm)
                   if isinstance(job, SequenceJob) else None)

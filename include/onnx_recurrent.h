@@ -209,8 +209,9 @@ rnn_status rnn_plan_get_activation(rnn_plan_t plan, int dir, int slot, int* fn,
  * rows_per_thread: 1, 2, 4 or 8; r_resident: R slice
  * kept in shared memory (1) or streamed through it (0).  Every geometry gives
  * the same results.  rnn_plan_get_launch reports the geometry of the last
- * run; a shape the override cannot serve makes the run return
- * RNN_ERR_UNSUPPORTED. */
+ * run (kernel 4 on a stack's first plan: the run was the stack's wavefront
+ * launch, unit_groups its first layer's CTAs); a shape the override cannot
+ * serve makes the run return RNN_ERR_UNSUPPORTED. */
 rnn_status rnn_plan_set_launch(rnn_plan_t plan, int unit_groups, int rows_per_thread,
                                int r_resident, int row_groups, int kernel);
 rnn_status rnn_plan_get_launch(rnn_plan_t plan, int* unit_groups, int* rows_per_thread,
@@ -292,12 +293,30 @@ rnn_status rnn_run_static_scratch(rnn_plan_t plan, int64_t seq_length, int64_t b
  * n_layers device pointers, each with rnn_run's meaning for its layer; X
  * feeds layer 0 and Y (may be NULL) receives the last layer's output
  * sequence.  sequence_lens is checked once (RNN_ERR_INVALID_INPUT before any
- * write).  The layers run one after another on `stream`; the intermediate
- * sequences live in two stack-owned device buffers (grown with cudaMalloc
- * when a run needs more, which synchronises the device), and a layout-0
- * bidirectional layer's Y is rearranged into the next X by one kernel (any
- * other layer's Y is the next X as it stands).  Errors are rnn_run's, for
- * the first failing layer. */
+ * write).  Errors are rnn_run's, for the first failing layer.
+ *
+ * Two ways to run a stack, both giving rnn_run's results layer by layer
+ * (bit for bit in RNN_MODE_EXACT):
+ *   - the wavefront: when every layer is unidirectional, with one operator,
+ *     one hidden size, one direction and one mode (RNN_MODE_EXACT or
+ *     RNN_MODE_FAST), fp32 I/O, 2 to 8 layers, and the layers' slices of R
+ *     and W fit in shared memory (and rnn_stack_set_wavefront allows it),
+ *     the stack runs as one persistent launch
+ *     (after layer 0's input projection) in which the SMs are split between
+ *     the layers and layer l+1 takes step t while layer l takes step t+1;
+ *     layer l+1 forms its input product from layer l's h in that launch, so
+ *     no intermediate sequence is stored.  Its scratch (layer 0's
+ *     projection, the packed weights, h ring buffers) is stack-owned and
+ *     grown with cudaMalloc when a run needs more (which synchronises the
+ *     device); the device status (a bounded wait that gave up) is reported
+ *     by rnn_plan_sync on the first layer's plan, and the first layer's plan
+ *     also carries the run's timing (rnn_plan_set_timing) and its
+ *     rnn_plan_debug_barrier settings.
+ *   - otherwise the layers run one after another on `stream`; the
+ *     intermediate sequences live in two stack-owned device buffers (grown
+ *     with cudaMalloc when a run needs more), and a layout-0 bidirectional
+ *     layer's Y is rearranged into the next X by one kernel (any other
+ *     layer's Y is the next X as it stands). */
 rnn_status rnn_stack_create(rnn_stack_t* out, const rnn_plan_t* layers, int n_layers);
 rnn_status rnn_stack_run(rnn_stack_t stack, int64_t seq_length, int64_t batch_size,
                          const float* X, const float* const* W, const float* const* R,
@@ -308,6 +327,19 @@ rnn_status rnn_stack_run(rnn_stack_t stack, int64_t seq_length, int64_t batch_si
 void rnn_stack_destroy(rnn_stack_t stack);
 /* Kernels the last rnn_stack_run queued (all layers). */
 int rnn_stack_last_launch_count(rnn_stack_t stack);
+/* rnn_stack_set_wavefront: 0 runs the layers one after another; 1 (the
+ * default) runs a qualifying stack as one wavefront launch when its layers
+ * are small enough for that to be faster (batch * G * hidden * (hidden +
+ * input) products per step at most 8e6 in every layer after the first: the
+ * step is then mostly exchange latency, which the layers overlap; larger
+ * layers run faster one after another, their input products in the
+ * projection GEMM); 2 runs every qualifying stack as a wavefront launch.
+ * Other values: RNN_ERR_INVALID_ARGUMENT.  The first layer's plan's
+ * unit_groups override (rnn_plan_set_launch) caps the CTAs per layer of a
+ * wavefront launch.  rnn_stack_last_wavefront: 1 if the last rnn_stack_run
+ * used the wavefront launch, else 0. */
+rnn_status rnn_stack_set_wavefront(rnn_stack_t stack, int enable);
+int rnn_stack_last_wavefront(rnn_stack_t stack);
 
 /* Single RNN cell (page "RNNCell", RNNCell-3: Detailed description,
  * Attributes, Inputs, Outputs):  Ho = f(clip(X.W^T + H.R^T + B)), where B is

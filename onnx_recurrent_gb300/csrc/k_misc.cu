@@ -91,6 +91,32 @@ __global__ void state_init_kernel(const RecParams p)
     }
 }
 
+// Wavefront kernel: every layer's ring buffer 0 = initial_h (rows through
+// perm) or 0, the other ring buffers and r (.) h 0; the arrival counters 0.
+__global__ void wave_state_init_kernel(const WaveParams p)
+{
+    const int64_t blk = (int64_t)p.H * p.npad;           // one [H][npad] buffer
+    const int64_t per_layer = (int64_t)kWaveRing * blk;
+    const int64_t total = (int64_t)p.L * per_layer;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int l = (int)(i / per_layer);
+        const int64_t off = i - (int64_t)l * per_layer;
+        const int64_t buf = off / blk;
+        const int64_t e = off - buf * blk;
+        const int64_t u = e / p.npad, n = e % p.npad;
+        const WaveLayer& ly = p.layer[l];
+        float v = 0.0f;
+        if (buf == 0 && n < p.N && ly.h0) {
+            const int64_t nr = p.perm ? p.perm[n] : n;
+            v = ly.h0[nr * p.H + u];
+        }
+        ly.hbuf[off] = v;
+        if (buf == 0 && ly.rhbuf) ly.rhbuf[e] = 0.0f;
+    }
+    if (blockIdx.x == 0 && threadIdx.x < p.L) p.bar[threadIdx.x] = 0u;
+}
+
 __global__ void mask_tail_kernel(float* __restrict__ Y, int layout, int64_t S, int64_t D, int64_t N,
                                  int64_t H, int64_t t0, int io)
 {
@@ -298,6 +324,15 @@ cudaError_t launch_tc_state_init(const RecParams& p, cudaStream_t stream)
     const int64_t total = (int64_t)2 * p.D * 128 * p.H;
     const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, 4096));
     tc_state_init_kernel<<<blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wave_state_init(const WaveParams& p, cudaStream_t stream)
+{
+    const int64_t total = (int64_t)p.L * kWaveRing * p.H * p.npad;
+    const int threads = 256;
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((total + threads - 1) / threads, 4096));
+    wave_state_init_kernel<<<blocks, threads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,18 @@
+// Instances of the stacked-layer wavefront kernel for one operator
+// (page "Recurrent operators: RNN, GRU, LSTM", Computation).
+#include "k_wave.cuh"
+
+namespace rnngb {
+
+cudaError_t launch_wavefront_rnn(const WaveParams& p, bool exact, int tn, int ctas, int threads, size_t smem,
+                                   cudaStream_t stream)
+{
+    return launch_wavefront_op<0>(p, exact, tn, ctas, threads, smem, stream);
+}
+
+cudaError_t wavefront_occupancy_rnn(int tn, bool exact, int threads, size_t smem, int* blocks)
+{
+    return wavefront_occupancy_op<0>(tn, exact, threads, smem, blocks);
+}
+
+}  // namespace rnngb

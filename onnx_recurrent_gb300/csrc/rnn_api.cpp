@@ -33,6 +33,32 @@ cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t
     }
 }
 
+cudaError_t launch_wavefront_rnn(const WaveParams&, bool, int, int, int, size_t, cudaStream_t);
+cudaError_t launch_wavefront_gru(const WaveParams&, bool, int, int, int, size_t, cudaStream_t);
+cudaError_t launch_wavefront_lstm(const WaveParams&, bool, int, int, int, size_t, cudaStream_t);
+cudaError_t wavefront_occupancy_rnn(int, bool, int, size_t, int*);
+cudaError_t wavefront_occupancy_gru(int, bool, int, size_t, int*);
+cudaError_t wavefront_occupancy_lstm(int, bool, int, size_t, int*);
+
+cudaError_t launch_wavefront(int op, const WaveParams& p, bool exact, int tn, int ctas, int threads, size_t smem,
+                             cudaStream_t s)
+{
+    switch (op) {
+    case 0: return launch_wavefront_rnn(p, exact, tn, ctas, threads, smem, s);
+    case 1: return launch_wavefront_gru(p, exact, tn, ctas, threads, smem, s);
+    default: return launch_wavefront_lstm(p, exact, tn, ctas, threads, smem, s);
+    }
+}
+
+cudaError_t wavefront_occupancy(int op, int tn, bool exact, int threads, size_t smem, int* blocks)
+{
+    switch (op) {
+    case 0: return wavefront_occupancy_rnn(tn, exact, threads, smem, blocks);
+    case 1: return wavefront_occupancy_gru(tn, exact, threads, smem, blocks);
+    default: return wavefront_occupancy_lstm(tn, exact, threads, smem, blocks);
+    }
+}
+
 cudaError_t recurrent_occupancy(int op, int lbr, int kernel, int tn, bool exact, int threads, size_t smem, int* blocks)
 {
     switch (op) {
@@ -200,6 +226,7 @@ struct Geometry {
     int quant;        // unit quantum
     int slots;        // dataflow ring slots
     int umax, tn, threads, rres;
+    int res_chunks;   // staged: resident 32-k chunks of the R slice (all of them when rres)
     size_t smem;
     int npad;         // rows per row group (padded); tensor-core kernel: gate columns per CTA
     int npad2;        // tensor-core kernel, GRU lbr = 0: candidate columns per CTA
@@ -254,12 +281,19 @@ rnn_status plan_staged(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* 
         return fail(RNN_ERR_UNSUPPORTED, "recurrent launch needs %lld threads per CTA (max %d)",
                     (long long)thr, kMaxThreads);
     g->threads = (int)round_up(thr, 32);
-    const size_t sres = rec_smem_bytes((int)H, g->umax, G, g->npad, 1);
-    const size_t sstr = rec_smem_bytes((int)H, g->umax, G, g->npad, 0);
+    // R slice: all resident when it fits; else as many leading 32-k chunks as
+    // fit beside the two rings, the rest streamed (override 0: all streamed)
+    const int nch = (int)ceil_div(H, kRecKC);
+    const size_t cap = (size_t)di.smem_optin - 1024;
+    const size_t sres = rec_smem_bytes((int)H, g->umax, G, g->npad, nch);
     if (pl->ov_rres == 1) g->rres = 1;
     else if (pl->ov_rres == 0) g->rres = 0;
-    else g->rres = sres <= (size_t)di.smem_optin ? 1 : 0;
-    g->smem = g->rres ? sres : sstr;
+    else g->rres = sres <= cap ? 1 : 0;
+    g->res_chunks = g->rres ? nch : 0;
+    if (!g->rres && pl->ov_rres != 0)
+        while (g->res_chunks + 1 < nch && rec_smem_bytes((int)H, g->umax, G, g->npad, g->res_chunks + 1) <= cap)
+            ++g->res_chunks;
+    g->smem = rec_smem_bytes((int)H, g->umax, G, g->npad, g->res_chunks);
     if (g->smem > (size_t)di.smem_optin)
         return fail(RNN_ERR_UNSUPPORTED, "recurrent kernel needs %zu bytes of shared memory (max %d)",
                     g->smem, di.smem_optin);
@@ -681,7 +715,8 @@ struct RecurrentGate {
     cudaEvent_t last = nullptr;
 };
 
-cudaError_t launch_recurrent_ordered(const RecParams& p, const Geometry& geo, bool exact, cudaStream_t st)
+template <class F>
+cudaError_t launch_ordered(cudaStream_t st, F launch)
 {
     static RecurrentGate gates[64];
     int dev = 0;
@@ -690,10 +725,6 @@ cudaError_t launch_recurrent_ordered(const RecParams& p, const Geometry& geo, bo
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     e = cudaStreamIsCapturing(st, &cs);
     if (e != cudaSuccess) return e;
-    auto launch = [&]() {
-        return geo.kernel == 3 ? launch_tc_recurrent(p, geo.smem, st)
-                               : launch_recurrent(p, exact, geo.threads, geo.smem, st);
-    };
     if (cs != cudaStreamCaptureStatusNone || dev < 0 || dev >= 64) return launch();
     RecurrentGate& g = gates[dev];
     std::lock_guard<std::mutex> lock(g.m);
@@ -710,6 +741,14 @@ cudaError_t launch_recurrent_ordered(const RecParams& p, const Geometry& geo, bo
     e = launch();
     if (e != cudaSuccess) return e;
     return cudaEventRecord(g.last, st);
+}
+
+cudaError_t launch_recurrent_ordered(const RecParams& p, const Geometry& geo, bool exact, cudaStream_t st)
+{
+    return launch_ordered(st, [&]() {
+        return geo.kernel == 3 ? launch_tc_recurrent(p, geo.smem, st)
+                               : launch_recurrent(p, exact, geo.threads, geo.smem, st);
+    });
 }
 
 // Queue the kernels of one run.  `scratch` holds the layout, `ctrl` the
@@ -793,6 +832,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     p.kernel = geo.kernel;
     p.ctas_per_dir = geo.ctas; p.unit_groups = geo.units; p.row_groups = geo.rows; p.unit_quant = geo.quant;
     p.slots = geo.slots; p.umax = geo.umax; p.rows_per_thread = geo.tn; p.r_resident = geo.rres;
+    p.res_chunks = geo.res_chunks;
     p.npad = geo.npad;
     p.npad2 = geo.npad2;
     p.hpad = geo.hpad;
@@ -891,6 +931,11 @@ struct rnn_stack {
     void* buf[2] = {nullptr, nullptr};
     size_t cap[2] = {0, 0};
     int last_launches = 0;
+    int wave_mode = 1;               // 0: layer by layer; 1: the wavefront where it is measured faster;
+                                     // 2: the wavefront whenever the stack qualifies
+    bool last_wave = false;          // the last run used the wavefront kernel
+    void* wbuf = nullptr;            // the wavefront run's scratch
+    size_t wcap = 0;
 };
 
 namespace {
@@ -1206,6 +1251,24 @@ rnn_status rnn_plan_set_weights(rnn_plan_t pl, const float* W, const float* R, v
     return RNN_OK;
 }
 
+// sequence_lens (device) to the plan's pinned host buffer, every length
+// checked against [0, S], the longest in *max_len.
+static rnn_status read_lengths(rnn_plan_t pl, const int32_t* lens, int64_t N, int64_t S, cudaStream_t st,
+                               int64_t* max_len)
+{
+    if (N > pl->lens_cap) {
+        if (pl->lens_host) cudaFreeHost(pl->lens_host);
+        pl->lens_host = nullptr;
+        cudaError_t e = cudaMallocHost((void**)&pl->lens_host, sizeof(int32_t) * (size_t)N);
+        if (e != cudaSuccess) { pl->lens_cap = 0; return cuda_fail(e, "cudaMallocHost(lens)"); }
+        pl->lens_cap = N;
+    }
+    cudaError_t e = cudaMemcpyAsync(pl->lens_host, lens, sizeof(int32_t) * (size_t)N, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "copying sequence_lens");
+    return check_lengths(pl->lens_host, N, S, max_len);
+}
+
 // One run of a plan.  known_max_len >= 0: sequence_lens was already checked
 // (by a stack's first layer) and its maximum is known.
 static rnn_status run_plan(rnn_plan_t pl, int64_t S, int64_t N, const float* X, const float* W, const float* R,
@@ -1228,17 +1291,7 @@ static rnn_status run_plan(rnn_plan_t pl, int64_t S, int64_t N, const float* X, 
     // sequence_lens: check on the host before anything is written.
     int64_t max_len = known_max_len >= 0 ? known_max_len : S;
     if (lens && known_max_len < 0) {
-        if (N > pl->lens_cap) {
-            if (pl->lens_host) cudaFreeHost(pl->lens_host);
-            pl->lens_host = nullptr;
-            cudaError_t e = cudaMallocHost((void**)&pl->lens_host, sizeof(int32_t) * (size_t)N);
-            if (e != cudaSuccess) { pl->lens_cap = 0; return cuda_fail(e, "cudaMallocHost(lens)"); }
-            pl->lens_cap = N;
-        }
-        cudaError_t e = cudaMemcpyAsync(pl->lens_host, lens, sizeof(int32_t) * (size_t)N, cudaMemcpyDeviceToHost, a.st);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(a.st);
-        if (e != cudaSuccess) return cuda_fail(e, "copying sequence_lens");
-        rs = check_lengths(pl->lens_host, N, S, &max_len);
+        rs = read_lengths(pl, lens, N, S, a.st, &max_len);
         if (rs != RNN_OK) return rs;
     }
 
@@ -1305,6 +1358,287 @@ rnn_status rnn_stack_create(rnn_stack_t* out, const rnn_plan_t* layers, int n_la
     return RNN_OK;
 }
 
+namespace {
+
+// Launch geometry of the wavefront kernel: CTAs per layer in proportion to
+// the layer's products per step (layer 0: the recurrent one; the others: the
+// recurrent and the input one), all slices of R and W resident.
+struct WaveGeometry {
+    int tn = 0, threads = 0, ctas = 0, npad = 0;
+    size_t smem = 0;
+    int C[kWaveMaxLayers] = {}, umax[kWaveMaxLayers] = {}, ugp[kWaveMaxLayers] = {}, cta0[kWaveMaxLayers] = {};
+};
+
+// Products per step of a layer (batch x gate columns x k of both products)
+// up to which the wavefront launch was measured faster than running the
+// layers one after another: such layers leave most of a step to exchange
+// latency, which the wavefront overlaps across the layers.  Larger layers
+// keep the SMs busy on their own, and layer by layer their input products
+// run in the projection GEMM, which is faster than the recurrent k-loop.
+constexpr double kWaveMaxProducts = 8.0e6;
+
+// Whether a stack can run as one wavefront launch; the reason if not.
+bool wave_eligible(const rnn_stack* st, int64_t S, int64_t N, std::string* why)
+{
+    const int L = (int)st->layers.size();
+    const rnn_plan* p0 = st->layers[0];
+    auto no = [&](const char* r) { *why = r; return false; };
+    if (st->wave_mode == 0) return no("disabled");
+    if (L < 2 || L > kWaveMaxLayers) return no("layer count");
+    if (S <= 0 || N <= 0) return no("zero size");
+    if (p0->io != RNN_IO_F32) return no("fp16/bf16 I/O rounds each layer's output");
+    if (p0->mode != RNN_MODE_EXACT && p0->mode != RNN_MODE_FAST) return no("tensor-core modes");
+    for (const rnn_plan* pl : st->layers) {
+        if (pl->D != 1) return no("bidirectional layer");
+        if (pl->direction != p0->direction || pl->op != p0->op || pl->H != p0->H || pl->mode != p0->mode)
+            return no("layers differ in direction, operator, hidden size or mode");
+    }
+    if (st->wave_mode == 1) {
+        for (int l = 1; l < L; ++l) {
+            const rnn_plan* pl = st->layers[l];
+            if ((double)N * pl->G * pl->H * (double)(pl->H + pl->I) > kWaveMaxProducts)
+                return no("layers large enough to run faster one after another");
+        }
+    }
+    return true;
+}
+
+rnn_status plan_wave(const rnn_stack* st, int64_t N, const DeviceInfo& di, WaveGeometry* g)
+{
+    const int L = (int)st->layers.size();
+    const rnn_plan* p0 = st->layers[0];
+    const int64_t H = p0->H;
+    const int G = p0->G;
+    const bool exact = p0->mode == RNN_MODE_EXACT;
+    g->npad = (int)round_up(N, 8);
+    double total = 0.0;
+    for (int l = 0; l < L; ++l) total += (double)H + (l > 0 ? (double)st->layers[l]->I : 0.0);
+    // at most this many CTAs per layer (the first plan's unit_groups
+    // override, else the SMs' share); enough that the layer's resident
+    // slices of R and W fit in shared memory
+    const int64_t cap = p0->ov_units > 0 ? p0->ov_units : (int64_t)di.sms;
+    const size_t ring = (size_t)kRecStages * kRecKC * g->npad * 4;
+    int ctas = 0, umax_all = 0;
+    for (int l = 0; l < L; ++l) {
+        const double w = (double)H + (l > 0 ? (double)st->layers[l]->I : 0.0);
+        const size_t krows = (size_t)H + (l > 0 ? (size_t)st->layers[l]->I : 0);
+        int64_t C = std::max<int64_t>(1, (int64_t)std::floor(di.sms * w / total));
+        C = std::min<int64_t>(std::min<int64_t>(C, cap), H);
+        int64_t um = ceil_div(H, C);
+        while (um > 1 && krows * rec_ugp((int)um, G) * 4 + ring > (size_t)di.smem_optin) --um;
+        C = ceil_div(H, um);
+        g->C[l] = (int)C;
+        g->umax[l] = (int)um;
+        g->ugp[l] = rec_ugp((int)um, G);
+        g->cta0[l] = ctas;
+        ctas += (int)C;
+        umax_all = std::max(umax_all, (int)um);
+    }
+    g->ctas = ctas;
+    g->tn = 0;
+    const int tns[3] = {1, 2, 4};
+    for (int t : tns)
+        if ((int64_t)umax_all * ceil_div(N, t) <= kMaxThreads) { g->tn = t; break; }
+    if (!g->tn) return fail(RNN_ERR_UNSUPPORTED, "wavefront: batch %lld needs more threads per CTA", (long long)N);
+    g->threads = (int)round_up((int64_t)umax_all * ceil_div(N, g->tn), 32);
+    size_t smem = 0;
+    for (int l = 0; l < L; ++l) {
+        const size_t k = (size_t)H + (l > 0 ? (size_t)st->layers[l]->I : 0);
+        smem = std::max(smem, k * g->ugp[l] * 4);
+    }
+    smem += (size_t)kRecStages * kRecKC * g->npad * 4;
+    if (smem > (size_t)di.smem_optin) return fail(RNN_ERR_UNSUPPORTED, "wavefront: weight slices do not fit");
+    g->smem = smem;
+    int blocks = 0;
+    cudaError_t e = wavefront_occupancy(p0->op, g->tn, exact, g->threads, smem, &blocks);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (blocks < 1 || ctas > blocks * di.sms) return fail(RNN_ERR_UNSUPPORTED, "wavefront: the grid does not fit");
+    return RNN_OK;
+}
+
+// One stack run as a single wavefront launch (after the layer-0 projection).
+// Returns RNN_ERR_UNSUPPORTED, having queued nothing, when the geometry does
+// not fit (the caller then runs the layers one by one).
+rnn_status stack_run_wave(rnn_stack* st, int64_t S, int64_t N, const float* X, const float* const* W,
+                          const float* const* R, const float* const* B, const int32_t* lens,
+                          const float* const* h0, const float* const* c0, const float* const* P, float* Y,
+                          float* const* Yh, float* const* Yc, cudaStream_t stream, int* launches_out)
+{
+    const int L = (int)st->layers.size();
+    rnn_plan* p0 = st->layers[0];
+    const int64_t H = p0->H, G = p0->G, GH = G * H, I0 = p0->I;
+    const bool exact = p0->mode == RNN_MODE_EXACT;
+    // the checks rnn_run makes for each layer (pointers, sizes, the scratch limit)
+    if (S > (1 << 30) || N > (1 << 24)) return fail(RNN_ERR_UNSUPPORTED, "seq_length or batch_size too large");
+    if (!X && I0 > 0) return fail(RNN_ERR_INVALID_ARGUMENT, "X is NULL");
+    for (int l = 0; l < L; ++l) {
+        const rnn_plan* pl = st->layers[l];
+        if (!pl->const_weights && (!R[l] || (!W[l] && pl->I > 0)))
+            return fail(RNN_ERR_INVALID_ARGUMENT, "W and R are required (layer %d)", l);
+        const double per_dir = (double)S * N * GH + 4.0 * N * H + (pl->const_weights ? 0.0 : (double)GH * (pl->I + H));
+        if (per_dir >= 1073741824.0)
+            return fail(RNN_ERR_UNSUPPORTED, "per-direction scratch of %.0f floats reaches the 2^30 limit", per_dir);
+    }
+    DeviceInfo di;
+    rnn_status rs = device_info(&di);
+    if (rs != RNN_OK) return rs;
+    if (!di.coop) return fail(RNN_ERR_UNSUPPORTED, "device lacks cooperative launch");
+    WaveGeometry wg;
+    rs = plan_wave(st, N, di, &wg);
+    if (rs != RNN_OK) return rs;
+    int64_t max_len = S;
+    if (lens) {
+        rs = read_lengths(p0, lens, N, S, stream, &max_len);
+        if (rs != RNN_OK) return rs;
+    }
+
+    // scratch: XW of layer 0, packed weights, ring buffers, row ranking
+    size_t off = 0;
+    auto take = [&](size_t bytes) { const size_t o = off; off += align256(bytes); return o; };
+    const size_t o_xw = take(sizeof(float) * (size_t)S * N * GH);
+    const size_t o_wt0 = take(p0->const_weights ? 0 : sizeof(float) * (size_t)I0 * GH);
+    size_t o_rt[kWaveMaxLayers], o_wt[kWaveMaxLayers], o_hb[kWaveMaxLayers], o_rh[kWaveMaxLayers];
+    for (int l = 0; l < L; ++l) {
+        const rnn_plan* pl = st->layers[l];
+        const bool two = pl->op == RNN_OP_GRU && pl->lbr == 0;
+        o_rt[l] = take(pl->const_weights ? 0 : sizeof(float) * (size_t)H * GH);
+        o_wt[l] = take((l == 0 || pl->const_weights) ? 0 : sizeof(float) * (size_t)pl->I * GH);
+        o_hb[l] = take(sizeof(float) * (size_t)kWaveRing * H * wg.npad);
+        o_rh[l] = take(two ? sizeof(float) * (size_t)H * wg.npad : 0);
+    }
+    const size_t o_perm = take(sizeof(int32_t) * (size_t)N);
+    if (off > st->wcap) {
+        if (st->wbuf) cudaFree(st->wbuf);   // synchronises with outstanding work
+        st->wbuf = nullptr;
+        st->wcap = 0;
+        cudaError_t e = cudaMalloc(&st->wbuf, off);
+        if (e != cudaSuccess) {
+            st->wbuf = nullptr;
+            return cuda_fail(e, "cudaMalloc(wavefront scratch)");
+        }
+        st->wcap = off;
+    }
+    rs = ensure_scratch(p0, 0);        // the first layer's control block: counters and status
+    if (rs != RNN_OK) return rs;
+    char* sb = (char*)st->wbuf;
+    if (p0->device < 0) cudaGetDevice(&p0->device);
+    if (p0->timing && !p0->events_ready) {
+        rs = rnn_plan_set_timing(p0, 1);
+        if (rs != RNN_OK) return rs;
+    }
+    if (!p0->done_ready) {
+        cudaError_t e = cudaEventCreateWithFlags(&p0->done, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+        p0->done_ready = true;
+    }
+    if (p0->timing) {
+        p0->slot = (p0->slot + 1) % rnn_plan::kRing;
+        cudaError_t eh = harvest(p0, p0->slot);
+        if (eh != cudaSuccess) return cuda_fail(eh, "reading timing events");
+        for (bool& u : p0->ev_used[p0->slot]) u = false;
+    }
+    const bool timed = p0->timing;
+    int launches = 0;
+    cudaError_t e;
+    int* status = (int*)(p0->ctrl + kCtrlStatusOffset);
+
+    // pack every layer's weights k-major (layer 0's W for the projection)
+    if (timed) record(p0, 0, stream);
+    WaveParams wp;
+    std::memset(&wp, 0, sizeof wp);
+    float* wt0 = p0->const_weights ? p0->wt_const : (float*)(sb + o_wt0);
+    for (int l = 0; l < L; ++l) {
+        rnn_plan* pl = st->layers[l];
+        WaveLayer& ly = wp.layer[l];
+        float* rt = pl->const_weights ? pl->rt_const : (float*)(sb + o_rt[l]);
+        float* wt = l == 0 ? wt0 : (pl->const_weights ? pl->wt_const : (float*)(sb + o_wt[l]));
+        if (!pl->const_weights) {
+            e = launch_pack(pl->I > 0 ? W[l] : nullptr, R[l], wt, rt, 1, (int)G, H, pl->I, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+            launches += (pl->I > 0 ? 1 : 0) + 1;
+        }
+        ly.cta0 = wg.cta0[l]; ly.C = wg.C[l]; ly.umax = wg.umax[l]; ly.ugp = wg.ugp[l];
+        ly.I = l == 0 ? 0 : (int)pl->I;
+        ly.lbr = pl->lbr; ly.input_forget = pl->input_forget;
+        ly.has_B = B && B[l]; ly.has_P = P && P[l] && pl->op == RNN_OP_LSTM;
+        ly.has_h0 = h0 && h0[l]; ly.has_c0 = c0 && c0[l] && pl->op == RNN_OP_LSTM;
+        ly.has_clip = pl->has_clip; ly.clip = pl->clip;
+        for (int k = 0; k < 3; ++k) ly.act[k] = pl->act[0][k];
+        ly.XW = l == 0 ? (const float*)(sb + o_xw) : nullptr;
+        ly.Wt = l == 0 ? nullptr : wt;
+        ly.Rt = rt;
+        ly.B = ly.has_B ? B[l] : nullptr;
+        ly.P = ly.has_P ? P[l] : nullptr;
+        ly.h0 = ly.has_h0 ? h0[l] : nullptr;
+        ly.c0 = ly.has_c0 ? c0[l] : nullptr;
+        ly.Y = l + 1 == L ? Y : nullptr;
+        ly.Yh = Yh ? Yh[l] : nullptr;
+        ly.Yc = (Yc && pl->op == RNN_OP_LSTM) ? Yc[l] : nullptr;
+        ly.hbuf = (float*)(sb + o_hb[l]);
+        ly.rhbuf = (pl->op == RNN_OP_GRU && pl->lbr == 0) ? (float*)(sb + o_rh[l]) : nullptr;
+    }
+    if (timed) record(p0, 1, stream);
+    e = launch_projection(X, wt0, (float*)(sb + o_xw), S * N, I0, GH, exact, status, p0->spin_limit_ns, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    launches += 1;
+    if (timed) record(p0, 2, stream);
+
+    wp.L = L; wp.N = (int)N; wp.H = (int)H; wp.S = (int)S; wp.layout = p0->layout;
+    wp.reverse = p0->direction == RNN_DIR_REVERSE ? 1 : 0;
+    wp.npad = wg.npad; wp.max_len = (int)max_len;
+    wp.has_lens = lens != nullptr; wp.lens = lens;
+    wp.bar = (unsigned*)p0->ctrl;
+    wp.status = status;
+    wp.spin_limit_ns = p0->spin_limit_ns;
+    wp.debug_skip_cta = p0->skip_cta;
+    if (lens) {
+        wp.perm = (const int32_t*)(sb + o_perm);
+        e = launch_rank_rows(lens, (int32_t*)(sb + o_perm), (int)N, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "row ranking launch");
+        launches += 1;
+    }
+    e = launch_wave_state_init(wp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "state set-up launch");
+    launches += 1;
+    if (timed) record(p0, 3, stream);
+    e = launch_ordered(stream, [&]() {
+        return launch_wavefront(p0->op, wp, exact, wg.tn, wg.ctas, wg.threads, wg.smem, stream);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "wavefront launch");
+    launches += 1;
+    if (timed) record(p0, 4, stream);
+    if (Y && max_len < S) {
+        e = launch_mask_tail(Y, p0->layout, S, 1, N, H, max_len, 0, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "mask launch");
+        launches += 1;
+    }
+    if (timed) {
+        record(p0, 5, stream);
+        p0->slot_pending[p0->slot] = true;
+    }
+    cudaEventRecord(p0->done, stream);
+    p0->ran = true;
+    p0->last_static = false;
+    p0->last_launches = launches;
+    p0->g_units = wg.C[0]; p0->g_tn = wg.tn; p0->g_rres = 1; p0->g_rows = 1;
+    p0->g_kernel = 4; p0->g_threads = wg.threads; p0->g_smem = (int)wg.smem;
+    *launches_out = launches;
+    return RNN_OK;
+}
+
+}  // namespace
+
+rnn_status rnn_stack_set_wavefront(rnn_stack_t st, int enable)
+{
+    g_error.clear();
+    if (!st) return fail(RNN_ERR_INVALID_ARGUMENT, "stack is NULL");
+    if (enable < 0 || enable > 2) return fail(RNN_ERR_INVALID_ARGUMENT, "the wavefront mode must be 0, 1 or 2");
+    st->wave_mode = enable;
+    return RNN_OK;
+}
+
+int rnn_stack_last_wavefront(rnn_stack_t st) { return st && st->last_wave ? 1 : 0; }
+
 rnn_status rnn_stack_run(rnn_stack_t st, int64_t S, int64_t N, const float* X, const float* const* W,
                          const float* const* R, const float* const* B, const int32_t* lens,
                          const float* const* h0, const float* const* c0, const float* const* P, float* Y,
@@ -1316,6 +1650,20 @@ rnn_status rnn_stack_run(rnn_stack_t st, int64_t S, int64_t N, const float* X, c
     if (rs != RNN_OK) return rs;
     const int L = (int)st->layers.size();
     if (!W || !R) return fail(RNN_ERR_INVALID_ARGUMENT, "W and R are per-layer arrays");
+    st->last_wave = false;
+    std::string why;
+    if (wave_eligible(st, S, N, &why)) {
+        const std::string saved = g_error;
+        int launches = 0;
+        rs = stack_run_wave(st, S, N, X, W, R, B, lens, h0, c0, P, Y, Yh, Yc, (cudaStream_t)stream, &launches);
+        if (rs == RNN_OK) {
+            st->last_wave = true;
+            st->last_launches = launches;
+            return RNN_OK;
+        }
+        if (rs != RNN_ERR_UNSUPPORTED) return rs;
+        g_error = saved;   // no launch fits: run the layers one by one
+    }
     const size_t elem = st->layers[0]->io == 0 ? 4 : 2;
     size_t need = 0;
     for (int l = 0; l + 1 < L; ++l)
@@ -1375,6 +1723,7 @@ void rnn_stack_destroy(rnn_stack_t st)
     if (ran) cudaDeviceSynchronize();
     for (void* b : st->buf)
         if (b) cudaFree(b);
+    if (st->wbuf) cudaFree(st->wbuf);
     delete st;
 }
 

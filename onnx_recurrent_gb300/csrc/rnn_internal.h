@@ -42,6 +42,8 @@ struct RecParams {
     int umax;                    // most units in one group
     int rows_per_thread;         // TN (template parameter mirrored here)
     int r_resident;              // 1: R slice lives in shared memory
+    int res_chunks;              // staged kernel: the first res_chunks 32-k chunks of the R slice stay in
+                                 // shared memory, the rest stream through the ring (all: r_resident)
     int npad;                    // rows per row group, padded (staged kernel: N padded to 8);
                                  // tensor-core kernel: gate columns per CTA (GRU lbr = 0: z and r only)
     int npad2;                   // tensor-core kernel, GRU lbr = 0: candidate columns per CTA
@@ -73,6 +75,46 @@ struct RecParams {
     int debug_skip_cta;
 };
 
+// Stacked unidirectional layers in one launch (the wavefront kernel,
+// k_wave.cuh).  Every layer has the same operator, hidden size, direction and
+// layout; layer l's CTAs are [cta0, cta0 + C).
+constexpr int kWaveMaxLayers = 8;
+constexpr int kWaveRing = 4;     // h buffers per layer (the next layer may lag by up to 3 steps)
+
+struct WaveLayer {
+    int cta0, C;                 // this layer's CTAs
+    int umax, ugp;               // most units per CTA; floats per k-row of a resident slice (rec_ugp)
+    int I;                       // K of the in-kernel input product (layers >= 1: hidden size), 0 for layer 0
+    int lbr, input_forget;
+    int has_B, has_P, has_h0, has_c0, has_clip;
+    float clip;
+    ActSpec act[3];              // f, g, h
+    const float* XW;             // layer 0: [S*N][G*H] projection (columns u*G + g)
+    const float* Wt;             // layers >= 1: W k-major [I][G*H] (columns u*G + g)
+    const float* Rt;             // R k-major [H][G*H]
+    const float* B;              // [2*G*H] (may be null)
+    const float* P;              // [3*H]   (may be null)
+    const float* h0;             // [N][H]  (may be null)
+    const float* c0;
+    float* Y;                    // the last layer's output sequence (null for the others)
+    float* Yh;
+    float* Yc;
+    float* hbuf;                 // [kWaveRing][H][npad], k-major, internal rows
+    float* rhbuf;                // GRU lbr = 0: r (.) h [H][npad]
+};
+
+struct WaveParams {
+    int L, N, H, S, layout, reverse, npad, max_len;
+    int has_lens;
+    const int32_t* lens;         // [N] device (may be null)
+    const int32_t* perm;         // internal row r is the caller's row perm[r] (null = identity)
+    unsigned* bar;               // [L] arrival counters (zeroed per run)
+    int* status;
+    long long spin_limit_ns;
+    int debug_skip_cta;
+    WaveLayer layer[kWaveMaxLayers];
+};
+
 // Shared-memory layout of the recurrent kernels, computed on the host.
 constexpr int kRecKC = 32;       // k rows per chunk
 constexpr int kRecStages = 4;    // chunks in the cp.async ring (staged kernel)
@@ -80,12 +122,17 @@ constexpr int kMaxSlots = 32;    // ring slots of the dataflow kernel
 
 __host__ __device__ inline int rec_ugp(int umax, int G) { return ((umax * G) + 3) / 4 * 4; }
 
-inline size_t rec_smem_bytes(int H, int umax, int G, int npad, int r_resident)
+// Staged kernel: res_chunks resident 32-k chunks of the R slice, a ring of
+// streamed R chunks when some are not resident, the ring of h chunks.
+inline size_t rec_smem_bytes(int H, int umax, int G, int npad, int res_chunks)
 {
-    size_t ugp = (size_t)rec_ugp(umax, G);
-    size_t rbytes = r_resident ? (size_t)H * ugp * 4 : (size_t)kRecStages * kRecKC * ugp * 4;
-    size_t hbytes = (size_t)kRecStages * kRecKC * (size_t)npad * 4;
-    return rbytes + hbytes;
+    const int nchunks = (H + kRecKC - 1) / kRecKC;
+    const size_t ugp = (size_t)rec_ugp(umax, G);
+    const size_t chunk = (size_t)kRecKC * ugp * 4;
+    const size_t rres = res_chunks >= nchunks ? (size_t)H * ugp * 4 : (size_t)res_chunks * chunk;
+    const size_t rring = res_chunks >= nchunks ? 0 : (size_t)kRecStages * chunk;
+    const size_t hbytes = (size_t)kRecStages * kRecKC * (size_t)npad * 4;
+    return rres + rring + hbytes;
 }
 
 // Dataflow kernel: floats per unit of the resident R slice (G rows of H,
@@ -215,6 +262,14 @@ cudaError_t launch_state_init(const RecParams& p, cudaStream_t stream);
 // the recurrent kernel).
 cudaError_t launch_mask_tail(float* Y, int layout, int64_t S, int64_t D, int64_t N, int64_t H, int64_t t0, int io,
                              cudaStream_t stream);
+
+// Wavefront kernel launch (op 0 RNN, 1 GRU, 2 LSTM; tn rows per thread 1, 2
+// or 4), its occupancy, and its set-up: every layer's ring buffer 0 from its
+// initial_h (rows through perm), the other buffers, r (.) h and the counters 0.
+cudaError_t launch_wavefront(int op, const WaveParams& p, bool exact, int tn, int ctas, int threads, size_t smem,
+                             cudaStream_t stream);
+cudaError_t wavefront_occupancy(int op, int tn, bool exact, int threads, size_t smem, int* blocks_per_sm);
+cudaError_t launch_wave_state_init(const WaveParams& p, cudaStream_t stream);
 
 // Device address and size of the fixed scratch array used by
 // rnn_run_static_scratch (looked up once per device; see rnn_static.cu).

@@ -76,6 +76,9 @@ def load(path: str | None = None):
     lib.rnn_stack_destroy.restype = None
     lib.rnn_stack_last_launch_count.argtypes = [vp]
     lib.rnn_stack_last_launch_count.restype = i32
+    lib.rnn_stack_set_wavefront.argtypes = [vp, i32]
+    lib.rnn_stack_last_wavefront.argtypes = [vp]
+    lib.rnn_stack_last_wavefront.restype = i32
     lib.rnn_cell_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, ctypes.c_char_p, f32]
     lib.rnn_cell_run.argtypes = [vp, i64] + [vp] * 6 + [vp]
     lib.rnn_last_error.argtypes = []
@@ -85,7 +88,7 @@ def load(path: str | None = None):
                  "rnn_plan_get_launch", "rnn_plan_set_timing", "rnn_plan_last_timing",
                  "rnn_plan_timing_totals",
                  "rnn_plan_debug_barrier", "rnn_cell_plan_create", "rnn_cell_run", "rnn_plan_set_io_type",
-                 "rnn_stack_create", "rnn_stack_run"):
+                 "rnn_stack_create", "rnn_stack_run", "rnn_stack_set_wavefront"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
         _lib = lib
@@ -375,6 +378,16 @@ def rnn_stack_destroy(stack: Stack):
 
 def rnn_stack_last_launch_count(stack: Stack) -> int:
     return int(load().rnn_stack_last_launch_count(stack.handle))
+
+
+def rnn_stack_set_wavefront(stack: Stack, mode=1):
+    """0 (or False): layer by layer; 1 (or True): the wavefront where it is
+    faster; 2: the wavefront whenever the stack qualifies."""
+    _check(load().rnn_stack_set_wavefront(stack.handle, int(mode)))
+
+
+def rnn_stack_last_wavefront(stack: Stack) -> bool:
+    return bool(load().rnn_stack_last_wavefront(stack.handle))
 
 
 def rnn_stack_run(stack: Stack, X, W, R, B=None, sequence_lens=None, initial_h=None, initial_c=None, P=None,

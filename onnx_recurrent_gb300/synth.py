@@ -261,6 +261,10 @@ STACK_WORKLOADS = {
                                    "peepholes (the LSTM forward workload with a second layer on top)",
     "gru2_bidi_s128_b64_i512_h1024": "two stacked GRU bidirectional layers, seq 128, batch 64, input 512, hidden "
                                      "1024, lbr 1, layout 0, sequence_lens",
+    "lstm4_fwd_s256_b8_i128_h128": "four stacked LSTM forward layers, seq 256, batch 8, input 128, hidden 128, "
+                                   "peepholes (small latency-bound layers)",
+    "gru3_fwd_s256_b16_i256_h256": "three stacked GRU forward layers, seq 256, batch 16, input 256, hidden 256, "
+                                   "lbr 1, sequence_lens",
 }
 
 
@@ -276,6 +280,14 @@ def stack_workload(name: str):
         b = make_case("GRU", "bidirectional", 128, 64, 2048, 1024, seed=1, w_scale=1.0 / 32,
                       linear_before_reset=1)
         return [a, b]
+    if name == "lstm4_fwd_s256_b8_i128_h128":
+        return [make_case("LSTM", "forward", 256, 8, 128, 128, seed=i, with_P=True, h0_scale=0.5, c0_scale=0.5,
+                          name=name if i == 0 else "") for i in range(4)]
+    if name == "gru3_fwd_s256_b16_i256_h256":
+        a = make_case("GRU", "forward", 256, 16, 256, 256, lens=("uniform", 64, 256), linear_before_reset=1,
+                      name=name)
+        return [a] + [make_case("GRU", "forward", 256, 16, 256, 256, seed=i, linear_before_reset=1)
+                      for i in (1, 2)]
     raise KeyError(name)
 
 
