@@ -192,15 +192,18 @@ __device__ __forceinline__ void chunk_part(const float* hk, int hstride, const f
 // Shared per-CTA context of the kernel.
 struct RecCtx {
     int d, H, npad, G, GH, u0, UG, ugp, tid, nthreads, ul, rb;
+    int res;     // resident 32-k chunks of the R slice (the rest streams)
+    bool r16;    // the streamed R rows are whole 16-byte pieces (copied 16 bytes at a time)
     bool active;
     bool live;   // this step: some row of the thread's tile has not finished
-    float* Rs;   // resident [H][ugp] or ring [stages][KC][ugp]
+    float* Rs;   // resident [res * KC (or H)][ugp]
+    float* Rring;// streamed chunks: ring [stages][KC][ugp]
     float* Hs;   // ring [stages][KC][npad]
 };
 
 // Issue the cp.async copies of k-chunk `chunk` into ring slot `slot`:
-// src rows k0 .. k0+kc-1 of a [H][npad] matrix, and (if R is streamed) the
-// CTA's R columns for those rows.
+// src rows k0 .. k0+kc-1 of a [H][npad] matrix, and (if that chunk of R is
+// not resident) the CTA's R columns for those rows.
 __device__ __forceinline__ void issue_chunk(const RecParams& p, const RecCtx& x, const float* src,
                                             int chunk, int slot)
 {
@@ -210,13 +213,22 @@ __device__ __forceinline__ void issue_chunk(const RecParams& p, const RecCtx& x,
     float* dst = x.Hs + (size_t)slot * kRecKC * x.npad;
     const int n4 = kc * x.npad / 4;
     for (int i = x.tid; i < n4; i += x.nthreads) cp_async16_cg(dst + 4 * i, s + 4 * i);
-    if (!p.r_resident) {
+    if (chunk >= x.res) {
         const float* rs = p.Rt + ((size_t)x.d * x.H + k0) * x.GH + (size_t)x.u0 * x.G;
-        float* rd = x.Rs + (size_t)slot * kRecKC * x.ugp;
-        const int tot = kc * x.UG;
-        for (int i = x.tid; i < tot; i += x.nthreads) {
-            const int kk = i / x.UG, j = i - kk * x.UG;
-            cp_async4_ca(rd + (size_t)kk * x.ugp + j, rs + (size_t)kk * x.GH + j);
+        float* rd = x.Rring + (size_t)slot * kRecKC * x.ugp;
+        if (x.r16) {
+            const int q = x.UG / 4;                 // 16-byte pieces per k-row
+            const int tot = kc * q;
+            for (int i = x.tid; i < tot; i += x.nthreads) {
+                const int kk = i / q, j = i - kk * q;
+                cp_async16_cg(rd + (size_t)kk * x.ugp + 4 * j, rs + (size_t)kk * x.GH + 4 * j);
+            }
+        } else {
+            const int tot = kc * x.UG;
+            for (int i = x.tid; i < tot; i += x.nthreads) {
+                const int kk = i / x.UG, j = i - kk * x.UG;
+                cp_async4_ca(rd + (size_t)kk * x.ugp + j, rs + (size_t)kk * x.GH + j);
+            }
         }
     }
 }
@@ -244,8 +256,8 @@ __device__ __forceinline__ void accumulate(const RecParams& p, const RecCtx& x, 
         const int kc = min(kRecKC, x.H - k0);
         if (x.active && x.live) {
             const float* hk = x.Hs + (size_t)slot * kRecKC * x.npad + x.rb * TN;
-            const float* rk = (p.r_resident ? x.Rs + (size_t)k0 * x.ugp
-                                            : x.Rs + (size_t)slot * kRecKC * x.ugp) +
+            const float* rk = (c < x.res ? x.Rs + (size_t)k0 * x.ugp
+                                         : x.Rring + (size_t)slot * kRecKC * x.ugp) +
                               x.ul * x.G + col_off;
             if (kc == kRecKC) chunk_full<TN, NC, EXACT>(hk, x.npad, rk, x.ugp, acc);
             else chunk_part<TN, NC, EXACT>(hk, x.npad, rk, x.ugp, kc, acc);
@@ -303,8 +315,12 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
     x.rb = x.tid / p.umax;
     x.active = (x.ul < U) && (x.rb * TN < p.N);
     x.live = true;
+    const int nchunks = (p.H + kRecKC - 1) / kRecKC;
+    x.res = p.r_resident ? nchunks : min(p.res_chunks, nchunks);
+    x.r16 = ((x.u0 * G) % 4 == 0) && (x.UG % 4 == 0) && (x.GH % 4 == 0);
     x.Rs = smem;
-    x.Hs = smem + (p.r_resident ? (size_t)p.H * x.ugp : (size_t)kRecStages * kRecKC * x.ugp);
+    x.Rring = smem + (x.res >= nchunks ? (size_t)p.H * x.ugp : (size_t)x.res * kRecKC * x.ugp);
+    x.Hs = x.Rring + (x.res >= nchunks ? 0 : (size_t)kRecStages * kRecKC * x.ugp);
 
     const int d = x.d;
     const int u = x.u0 + x.ul;
@@ -312,9 +328,9 @@ __global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p
     const bool rev = p.dir_reverse[d] != 0;
     unsigned* bar = p.bar + d;
 
-    if (p.r_resident) {
+    if (x.res > 0) {
         const float* src = p.Rt + (size_t)d * p.H * x.GH + (size_t)x.u0 * G;
-        const int tot = p.H * x.UG;
+        const int tot = min(p.H, x.res * kRecKC) * x.UG;
         for (int i = x.tid; i < tot; i += x.nthreads) {
             const int k = i / x.UG, j = i - k * x.UG;
             x.Rs[(size_t)k * x.ugp + j] = src[(size_t)k * x.GH + j];

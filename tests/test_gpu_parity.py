@@ -144,6 +144,23 @@ def test_hidden_not_multiple_of_four(op):
     assert e.value.status == 3
 
 
+# Staged kernel with hidden 1024 and 16-52 units per CTA: the R slice (up to
+# 245 KB) does not fit beside the rings, so its leading 32-k chunks stay in
+# shared memory and the rest stream (16 bytes at a time where the slice's
+# rows are whole 16-byte pieces, else 4); every split gives the same bits.
+@pytest.mark.parametrize("op,lbr,launch", [("LSTM", 0, (64, 2, -1, 0, 1)), ("GRU", 0, (52, 2, -1, 0, 1)),
+                                           ("GRU", 1, (52, 2, -1, 0, 1)), ("RNN", 0, (17, 2, -1, 0, 1)),
+                                           ("LSTM", 0, (64, 2, 0, 0, 1))])
+def test_staged_kernel_partly_resident_r(op, lbr, launch):
+    c = make_case(op, "bidirectional", 5, 11, 40, 1024, seed=44, with_P=True, h0_scale=0.5, c0_scale=0.5,
+                  lens=("uniform", 0, 5), linear_before_reset=lbr, clip=2.0, w_scale=1.0 / 32)
+    Y, Yh, Yc, plan = gpu_case(c, "exact", launch=launch, keep_plan=True)
+    got = orc.rnn_plan_get_launch(plan)
+    orc.rnn_plan_destroy(plan)
+    assert got["kernel"] == 1 and got["r_resident"] == 0
+    _compare_exact(c, (Y, Yh, Yc), oracle_case(c), f"{op} lbr {lbr} {launch}")
+
+
 @pytest.mark.parametrize("g", [(2, 1, 0, 0, 1), (5, 2, 1, 0, 1), (4, 1, 1, 2, 2), (3, 2, 0, 1, 2)])
 def test_fast_mode_is_geometry_independent(g):
     c = make_case("LSTM", "bidirectional", 6, 9, 20, 36, seed=5, with_P=True, h0_scale=0.5)
