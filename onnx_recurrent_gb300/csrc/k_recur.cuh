@@ -290,8 +290,15 @@ __device__ __forceinline__ size_t s_index(const RecParams& p, int d, int n, int 
     return p.layout == 0 ? ((size_t)d * p.N + n) * p.H + u : ((size_t)n * p.D + d) * p.H + u;
 }
 
+// Eight rows per thread hold 32 LSTM accumulators plus two blocks of
+// operands: up to 255 registers, so at most 256 threads per CTA.
+template <int TN>
+struct StagedBounds {
+    static constexpr int threads = TN == 8 ? 256 : 512;
+};
+
 template <int OP, int TN, bool EXACT>
-__global__ void __launch_bounds__(512, 1) rnn_recurrent_kernel(const RecParams p)
+__global__ void __launch_bounds__(StagedBounds<TN>::threads, 1) rnn_recurrent_kernel(const RecParams p)
 {
     constexpr int G = OP == 0 ? 1 : (OP == 1 ? 3 : 4);
     extern __shared__ __align__(16) float smem[];

@@ -93,6 +93,15 @@ rnn_status cuda_fail(cudaError_t e, const char* what)
 }
 
 constexpr int kMaxThreads = 512;          // staged kernel
+// The staged kernel's threads per CTA for rows_per_thread tn (eight rows
+// per thread take up to 255 registers: at most 256 threads).
+int staged_thread_limit(int tn) { return tn == 8 ? 256 : kMaxThreads; }
+// Threads of a one-CTA staged launch over H units and N rows with the
+// widest row tile that fits, or 0 if none does.
+bool staged_single_cta_fits(int64_t H, int64_t N)
+{
+    return H * ((N + 3) / 4) <= kMaxThreads || H * ((N + 7) / 8) <= staged_thread_limit(8);
+}
 constexpr int kMaxComputeThreads = 480;   // dataflow kernel (plus one loader warp)
 constexpr long long kDefaultSpinNs = 2000000000LL;   // 2 s per barrier wait
 
@@ -253,8 +262,7 @@ rnn_status plan_staged(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* 
         C = (int)std::min<int64_t>(pl->ov_units, H);
     } else {
         const long long macs = (long long)N * G * H * H;
-        const int64_t single_threads = H * ((N + 7) / 8);
-        if (macs <= 262144 && single_threads <= kMaxThreads)
+        if (macs <= 262144 && staged_single_cta_fits(H, N))
             C = 1;   // tiny step: one CTA per direction, no device-wide barrier
         else
             C = (int)std::max<int64_t>(1, std::min<int64_t>(di.sms / D, H));
@@ -270,16 +278,16 @@ rnn_status plan_staged(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* 
         g->tn = pl->ov_tn;
     } else {
         for (int tn : tns)
-            if ((int64_t)g->umax * ((N + tn - 1) / tn) <= kMaxThreads) { g->tn = tn; break; }
+            if ((int64_t)g->umax * ((N + tn - 1) / tn) <= staged_thread_limit(tn)) { g->tn = tn; break; }
     }
     if (g->tn == 0)
         return fail(RNN_ERR_UNSUPPORTED,
                     "no recurrent launch for batch %lld with %d hidden units per CTA (threads > %d)",
                     (long long)N, g->umax, kMaxThreads);
     const int64_t thr = (int64_t)g->umax * ((N + g->tn - 1) / g->tn);
-    if (thr > kMaxThreads)
+    if (thr > staged_thread_limit(g->tn))
         return fail(RNN_ERR_UNSUPPORTED, "recurrent launch needs %lld threads per CTA (max %d)",
-                    (long long)thr, kMaxThreads);
+                    (long long)thr, staged_thread_limit(g->tn));
     g->threads = (int)round_up(thr, 32);
     // R slice: all resident when it fits; else as many leading 32-k chunks as
     // fit beside the two rings, the rest streamed (override 0: all streamed)
@@ -493,7 +501,7 @@ rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, const fl
     if (pl->ov_kernel == 2) return plan_dataflow(pl, N, di, g);
     const int64_t H = pl->H;
     const long long macs = (long long)N * pl->G * H * H;
-    if (macs <= 262144 && H * ((N + 7) / 8) <= kMaxThreads && pl->ov_units <= 0 && pl->ov_rows <= 0)
+    if (macs <= 262144 && staged_single_cta_fits(H, N) && pl->ov_units <= 0 && pl->ov_rows <= 0)
         return plan_staged(pl, N, di, g);                          // one CTA per direction
     const std::string saved = g_error;
     if (plan_dataflow(pl, N, di, g) == RNN_OK) {

@@ -117,7 +117,7 @@ struct WaveParams {
 
 // Shared-memory layout of the recurrent kernels, computed on the host.
 constexpr int kRecKC = 32;       // k rows per chunk
-constexpr int kRecStages = 4;    // chunks in the cp.async ring (staged kernel)
+constexpr int kRecStages = 3;    // chunks in the cp.async ring (staged kernel; measured: 2-4 within 2%)
 constexpr int kMaxSlots = 32;    // ring slots of the dataflow kernel
 
 __host__ __device__ inline int rec_ugp(int umax, int G) { return ((umax * G) + 3) / 4 * 4; }
