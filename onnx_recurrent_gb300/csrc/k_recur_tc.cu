@@ -253,6 +253,19 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // h blocks are copied for the batch's rows only (rounded up to 8): the
+    // MMA's other rows stay zero in every ring slot (whole 128-byte rows, so
+    // the swizzle does not matter); the tensor cores read them through the
+    // async proxy
+    const int hrows = (p.N + 7) & ~7;
+    const unsigned hbytes = (unsigned)hrows * 128u;
+    if (hrows < TR_M) {
+        for (int st = 0; st < nst; ++st) {
+            uint4* z = reinterpret_cast<uint4*>(hring + (size_t)st * kTrHStage + hbytes);
+            for (int i = threadIdx.x; i < (int)((kTrHStage - hbytes) / 16); i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     tr_fence_before();
     __syncthreads();
     tr_fence_after();
@@ -319,7 +332,7 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full[slot], kTrHStage);
+                        mbar_arrive_expect_tx(&full[slot], hbytes);
                         tma_load_3d(hring + (size_t)slot * kTrHStage, src, kb * TR_KB, 0, z, &full[slot]);
                     }
                 }

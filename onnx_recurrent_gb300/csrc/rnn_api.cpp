@@ -862,7 +862,9 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         const void* rp = pl->const_weights ? pl->rp16_const : (const void*)(scratch + L.rp);
         const cuuint64_t hdims[3] = {(cuuint64_t)H, 128, (cuuint64_t)(2 * D)};
         const cuuint64_t hstrides[2] = {(cuuint64_t)H * 2, (cuuint64_t)H * 2 * 128};
-        const cuuint32_t hbox[3] = {64, 128, 1};
+        // only the batch's rows (rounded up to an 8-row swizzle group) are
+        // copied; the kernel keeps the other rows of its ring at zero
+        const cuuint32_t hbox[3] = {64, (cuuint32_t)round_up(a.N, 8), 1};
         const cuuint64_t rdims[2] = {(cuuint64_t)H, (cuuint64_t)(D * GH)};
         const cuuint64_t rstrides[1] = {(cuuint64_t)H * 2};
         const cuuint32_t rbox[2] = {64, (cuuint32_t)geo.npad};
