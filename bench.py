@@ -283,10 +283,9 @@ def profiled_traffic(kernel, workload, mode, digest):
             continue
         with open(os.path.join(pdir, name)) as f:
             text = f.read()
-        m = re.search(r"traffic_key:\s*(\S+)\s+(\S+)\s+(\S+)\s+(\S+)\s+(\d+)", text)
-        if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == mode \
-                and m.group(4) == digest:
-            return int(m.group(5))
+        for m in re.finditer(r"traffic_key:\s*(\S+)\s+(\S+)\s+(\S+)\s+(\S+)\s+(\d+)", text):
+            if m.group(1) == kernel and m.group(2) == workload and m.group(3) == mode and m.group(4) == digest:
+                return int(m.group(5))
     return None
 
 

@@ -111,3 +111,16 @@ def test_step_roofline_streams_what_does_not_fit():
     assert sr["r_streamed_bytes_per_step"] == r - 152 * 232448
     assert sr["terms_us_per_step"]["l2"] == pytest.approx((r - 152 * 232448) / 10000e9 * 1e6, rel=1e-3)
     assert sr["steps"] == 4096
+
+
+def test_traffic_lookup_reads_every_key_of_a_summary(tmp_path, monkeypatch):
+    # a summary captured on a shorter sequence carries a key for that case
+    # and a scaled one for the bench workload
+    d = bench.source_digest("recurrence")
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "x.md").write_text(f"traffic_key: recurrence short fast {d} 10\\n"
+                                                f"traffic_key: recurrence long fast {d} 80\\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("recurrence", "short", "fast", d) == 10
+    assert bench.profiled_traffic("recurrence", "long", "fast", d) == 80
+
