@@ -1,4 +1,4 @@
-"""Pins for the oracle's stacked layers (this build's reading: layer l+1's X
+"""Pins for the oracle's stacked layers (the library's reading: layer l+1's X
 is layer l's Y with the directions side by side per step): hand-derived
 cases (tests/golden/stack), the layer handoff against an independent
 transpose/reshape formula, one layer = the single operator, layout 1 = the
