@@ -207,7 +207,10 @@ rnn_status rnn_plan_get_activation(rnn_plan_t plan, int dir, int slot, int* fn,
  * published the step on the row group's counter).  unit_groups: CTAs per direction along
  * hidden units; row_groups: along batch rows (dataflow kernel only);
  * rows_per_thread: 1, 2, 4 or 8; r_resident: R slice
- * kept in shared memory (1) or streamed through it (0).  Every geometry gives
+ * kept in shared memory (1) or streamed through it (0); 2 asks the dataflow
+ * kernel to keep the slice's leading pieces resident and stream the rest
+ * (the staged kernel does that by itself whenever the slice does not fit,
+ * and takes 2 as -1).  Every geometry gives
  * the same results.  rnn_plan_get_launch reports the geometry of the last
  * run (kernel 4 on a stack's first plan: the run was the stack's wavefront
  * launch, unit_groups its first layer's CTAs); a shape the override cannot

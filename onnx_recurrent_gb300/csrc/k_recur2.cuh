@@ -85,9 +85,13 @@ __device__ __forceinline__ int unit_begin(int cu, int CU, int H, int quant)
 
 struct DfCtx {
     int d, cu, cr, H, HP, G, GH, CU, CR, u0, U, umax, ugs, NR, NRP, nchunks, cpb, npieces, slots;
+    int KR;           // k of each gate row held resident: H, or the leading res_chunks * 32 (0: none)
+    int rpieces;      // pieces whose R is resident (the leading ones); the others stream
     int ctid, ncompute, ul, rb;
-    bool active;
-    float* Rs;        // resident R: [umax][ugs] floats (unit-major, gate rows of H)
+    int gi;           // gate split: this thread's share of the gate columns (0: all, or the first share)
+    bool active;      // takes part in the products
+    bool lead;        // owns the (unit, row tile): gate arithmetic, state, stores
+    float* Rs;        // resident R: [umax][ugs] floats (unit-major, gate rows of KR k)
     char* Rring;      // streamed R: slots x rslot bytes, each cpb chunks of [G][umax][36]
     char* Hring;      // slots x hslot bytes, each [cpb][NRP][36] (padded to 128 bytes)
     int rslot, rsub, hslot; // bytes per slot (one piece: cpb chunks of 32 k), per R chunk
@@ -99,13 +103,16 @@ struct DfCtx {
 // Loader: the pieces of one product (one accumulate pass of the compute
 // warps).  `map` describes the h (or r (.) h) exchange buffer, `z` the row
 // group's block in it; every producer of the row group must have published
-// `target` times before the block may be read.  Every lane polls the row
+// `target` times before the block may be read.  Streamed R pieces bring the
+// ng gate rows from gate g0 on that the product uses (`rmap` has a box of ng
+// gates); they land from the start of each chunk's sub-block.  Every lane polls the row
 // group's counter (acquire loads); a proxy fence then orders the
 // generic-proxy writes that the acquire made visible before the tensor
 // copies (async proxy) that read them.
 __device__ __forceinline__ bool load_product(const RecParams& p, const DfCtx& x, const CUtensorMap* map, int z,
                                              unsigned target, const unsigned* counter, unsigned& q,
-                                             volatile int* abort_flag, int lane)
+                                             volatile int* abort_flag, int lane, const CUtensorMap* rmap, int g0,
+                                             int ng)
 {
     if (target > 0) {
         // This CTA's own publication comes first (the counter cannot be
@@ -157,13 +164,14 @@ __device__ __forceinline__ bool load_product(const RecParams& p, const DfCtx& x,
             const int c0 = (base + lane) * x.cpb;           // first chunk of the piece
             const int nc = min(x.cpb, x.nchunks - c0);      // R chunks to copy (h: the whole box)
             const unsigned hbytes = (unsigned)x.NRP * x.cpb * (kDfPitch * 4u);
-            const unsigned rbytes = p.r_resident ? 0u : (unsigned)(nc * x.G * x.umax) * (kDfPitch * 4u);
+            const bool rstream = base + lane >= x.rpieces;
+            const unsigned rbytes = rstream ? (unsigned)(nc * ng * x.umax) * (kDfPitch * 4u) : 0u;
             mbar_arrive_expect_tx(&x.full[slot], hbytes + rbytes);
             tma_load_4d(x.Hring + (size_t)slot * x.hslot, map, 0, 0, c0, z, &x.full[slot]);
-            if (!p.r_resident)
+            if (rstream)
                 for (int cl = 0; cl < nc; ++cl)
-                    tma_load_4d(x.Rring + (size_t)slot * x.rslot + (size_t)cl * x.rsub, &p.rmap, (c0 + cl) * kRecKC,
-                                x.u0, 0, x.d, &x.full[slot]);
+                    tma_load_4d(x.Rring + (size_t)slot * x.rslot + (size_t)cl * x.rsub, rmap, (c0 + cl) * kRecKC,
+                                x.u0, g0, x.d, &x.full[slot]);
         }
         q += (unsigned)nmine;
     }
@@ -228,10 +236,11 @@ __device__ __forceinline__ void df_piece(const char* const (&hp)[TN], int hstep,
 }
 
 // Compute warps: acc[i][j] += sum_k src[row_i][k] * R[gate col_off + j][k]
-// over the product's pieces (k ascending).  Returns false once the CTA is
-// aborting (the remaining pieces are then skipped, not waited for).
+// over the product's pieces (k ascending).  Streamed pieces hold the gate
+// rows from ring_g0 on.  Returns false once the CTA is aborting (the
+// remaining pieces are then skipped, not waited for).
 template <int TN, int NC, bool EXACT>
-__device__ __forceinline__ bool consume_product(const RecParams& p, const DfCtx& x, int col_off,
+__device__ __forceinline__ bool consume_product(const RecParams& p, const DfCtx& x, int col_off, int ring_g0,
                                                 float (&acc)[TN][NC], unsigned& q, volatile int* abort_flag,
                                                 int lane, bool live)
 {
@@ -249,16 +258,16 @@ __device__ __forceinline__ bool consume_product(const RecParams& p, const DfCtx&
             for (int i = 0; i < TN; ++i) hp[i] = hbox + (size_t)(x.rb * TN + i) * (kDfPitch * 4);
             const int hstep = x.NRP * kDfPitch * 4;
             const char* rp[NC];
-            if (p.r_resident) {
-                const float* rbase = x.Rs + (size_t)x.ul * x.ugs + (size_t)col_off * x.H + k0;
+            if (pc < x.rpieces) {
+                const float* rbase = x.Rs + (size_t)x.ul * x.ugs + (size_t)col_off * x.KR + k0;
 #pragma unroll
-                for (int g = 0; g < NC; ++g) rp[g] = reinterpret_cast<const char*>(rbase + (size_t)g * x.H);
+                for (int g = 0; g < NC; ++g) rp[g] = reinterpret_cast<const char*>(rbase + (size_t)g * x.KR);
                 df_piece<TN, NC, EXACT, true>(hp, hstep, rp, kRecKC * 4, ngroups, acc);
             } else {
                 const char* rbox = x.Rring + (size_t)slot * x.rslot;
 #pragma unroll
                 for (int g = 0; g < NC; ++g)
-                    rp[g] = rbox + (size_t)((col_off + g) * x.umax + x.ul) * (kDfPitch * 4);
+                    rp[g] = rbox + (size_t)((col_off - ring_g0 + g) * x.umax + x.ul) * (kDfPitch * 4);
                 df_piece<TN, NC, EXACT, false>(hp, hstep, rp, x.rsub, ngroups, acc);
             }
         }
@@ -326,10 +335,18 @@ struct DfBounds {
 
 // TWO: GRU with linear_before_reset = 0 (two products per step, the second
 // over r (.) h); a separate instance keeps its register allocation apart.
-template <int OP, int TN, bool EXACT, bool TWO>
+// GS > 1 (one product per step): gate split, GS lanes side by side share a
+// (unit, row tile), each taking G / GS of the gate columns over all k in
+// ascending order (so every accumulator sees the same operations as
+// without the split); the first lane of the group gathers the others'
+// sums by shuffles and does the gate arithmetic.  A warp holds 32 / GS such
+// groups; with GS = 3 its last two lanes idle.
+template <int OP, int TN, bool EXACT, bool TWO, int GS>
 __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(const __grid_constant__ RecParams p)
 {
     constexpr int G = OP == 0 ? 1 : (OP == 1 ? 3 : 4);
+    static_assert(GS == 1 || (!TWO && G % GS == 0), "gate split: one product per step, whole gate shares");
+    constexpr int NCG = G / GS;       // gate columns per thread
     extern __shared__ __align__(128) unsigned char df_smem[];
     __shared__ __align__(8) uint64_t s_full[kMaxSlots];
     __shared__ __align__(8) uint64_t s_empty[kMaxSlots];
@@ -361,26 +378,38 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     x.hslot = (int)df_hslot_bytes(x.NRP, x.cpb);   // 128-byte aligned slot starts
     x.rsub = (int)df_rsub_bytes(x.umax, G);
     x.rslot = p.r_resident ? 0 : x.cpb * x.rsub;
+    // R resident in full, or its leading res_chunks 32-k chunks (whole pieces)
+    x.KR = p.r_resident ? p.H : p.res_chunks * kRecKC;
+    x.rpieces = p.r_resident ? x.npieces : p.res_chunks / x.cpb;
     x.ncompute = blockDim.x - 32;
     x.ctid = (int)threadIdx.x - 32;
     const int RB = x.NRP / TN;
+    // t: the thread's (unit, row tile) index; gate split: lane groups of GS
+    int t = x.ctid;
+    x.gi = 0;
+    if (GS > 1 && x.ctid >= 0) {
+        constexpr int NG = 32 / GS;
+        const int gq = (x.ctid & 31) / GS;
+        x.gi = (x.ctid & 31) - gq * GS;
+        t = gq < NG ? (x.ctid >> 5) * NG + gq : 1 << 30;
+    }
     if (p.unit_fastest) {
         // the lanes of a quarter warp share a row tile (their h loads are
         // broadcasts) and take distinct units (R rows 144 bytes apart)
-        x.ul = x.ctid >= 0 ? x.ctid % x.umax : 0;
-        x.rb = x.ctid >= 0 ? x.ctid / x.umax : 0;
+        x.ul = x.ctid >= 0 ? t % x.umax : 0;
+        x.rb = x.ctid >= 0 ? t / x.umax : 0;
     } else {
-        x.rb = x.ctid >= 0 ? x.ctid % RB : 0;
-        x.ul = x.ctid >= 0 ? x.ctid / RB : 0;
+        x.rb = x.ctid >= 0 ? t % RB : 0;
+        x.ul = x.ctid >= 0 ? t / RB : 0;
     }
     x.active = x.ctid >= 0 && x.ul < x.U && x.rb < RB && x.rb * TN < x.NR;
+    x.lead = x.active && x.gi == 0;
     // tensor-copy destinations are 128-byte aligned
     unsigned char* base = df_smem + ((128u - (smem_addr(df_smem) & 127u)) & 127u);
-    const size_t rbytes = p.r_resident ? (((size_t)x.umax * x.ugs * 4 + 127) / 128) * 128
-                                       : (size_t)x.slots * x.rslot;
+    const size_t rres = x.KR > 0 ? (((size_t)x.umax * x.ugs * 4 + 127) / 128) * 128 : 0;
     x.Rs = reinterpret_cast<float*>(base);
-    x.Rring = reinterpret_cast<char*>(base);
-    x.Hring = reinterpret_cast<char*>(base + rbytes);
+    x.Rring = reinterpret_cast<char*>(base + rres);
+    x.Hring = reinterpret_cast<char*>(base + rres + (size_t)x.slots * x.rslot);
     x.full = s_full;
     x.empty = s_empty;
     x.pub = &s_pub;
@@ -409,18 +438,18 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         mbar_fence_init();
     }
     __syncthreads();
-    if (p.r_resident && threadIdx.x < 32) {
-        // R[d][g*H + u][k] -> Rs[(u - u0) * ugs + g*H + k]: one bulk copy of
-        // a row of H floats per (unit, gate), all completing on s_rfill
+    if (x.KR > 0 && threadIdx.x < 32) {
+        // R[d][g*H + u][k] -> Rs[(u - u0) * ugs + g*KR + k], k < KR: one bulk copy of
+        // a row of KR floats per (unit, gate), all completing on s_rfill
         // (H is a multiple of 4 and ugs*4 of 16, so every copy is 16-byte
         // aligned at both ends)
         const float* src = p.Rorig + (size_t)d * G * p.H * p.H;
-        if (lane == 0) mbar_arrive_expect_tx(&s_rfill, (unsigned)(x.U * G * p.H) * 4u);
+        if (lane == 0) mbar_arrive_expect_tx(&s_rfill, (unsigned)(x.U * G * x.KR) * 4u);
         __syncwarp();
         for (int j = lane; j < x.U * G; j += 32) {
             const int ul = j / G, g = j - ul * G;
-            bulk_g2s(x.Rs + (size_t)ul * x.ugs + (size_t)g * p.H, src + ((size_t)g * p.H + x.u0 + ul) * p.H,
-                     (unsigned)p.H * 4u, &s_rfill);
+            bulk_g2s(x.Rs + (size_t)ul * x.ugs + (size_t)g * x.KR, src + ((size_t)g * p.H + x.u0 + ul) * p.H,
+                     (unsigned)x.KR * 4u, &s_rfill);
         }
     }
 
@@ -431,14 +460,16 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         for (int s = 0; s < p.max_len && ok; ++s) {
             const int zh = zh0 + (s & 1) * x.CR;
             if (two_phase) {
-                ok = load_product(p, x, &p.hmap, zh, 2u * s, counter, q, &s_abort, lane);
-                if (ok) ok = load_product(p, x, &p.rhmap, zh, 2u * s + 1u, counter, q, &s_abort, lane);
+                // z and r rows with h, the candidate's rows with r (.) h
+                ok = load_product(p, x, &p.hmap, zh, 2u * s, counter, q, &s_abort, lane, &p.rmap, 0, 2);
+                if (ok)
+                    ok = load_product(p, x, &p.rhmap, zh, 2u * s + 1u, counter, q, &s_abort, lane, &p.rmap2, 2, 1);
             } else {
-                ok = load_product(p, x, &p.hmap, zh, (unsigned)s, counter, q, &s_abort, lane);
+                ok = load_product(p, x, &p.hmap, zh, (unsigned)s, counter, q, &s_abort, lane, &p.rmap, 0, G);
             }
         }
         // wait (bounded) for this CTA's copies still in flight before leaving
-        if (lane == 0 && p.r_resident) {
+        if (lane == 0 && x.KR > 0) {
             const unsigned long long t0 = globaltimer_ns();
             while (!mbar_test(&s_rfill, 0u) && (long long)(globaltimer_ns() - t0) <= p.spin_limit_ns) {
             }
@@ -513,7 +544,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
 #pragma unroll
         for (int i = 0; i < TN; ++i) {
             const int rl = x.rb * TN + i;
-            if (x.active && rl < x.NR && s < len[i]) {
+            if (x.lead && rl < x.NR && s < len[i]) {
                 const float* q = xw_row(s, i);
 #pragma unroll
                 for (int g = 0; g < G; ++g) xw[i][g] = __ldg(q + g);
@@ -531,7 +562,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
 #pragma unroll
         for (int i = 0; i < TN; ++i) {
             const int rl = x.rb * TN + i;
-            if (x.active && rl < x.NR && s < len[i]) prefetch_l2(xw_row(s, i));
+            if (x.lead && rl < x.NR && s < len[i]) prefetch_l2(xw_row(s, i));
         }
     };
 
@@ -539,7 +570,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     const bool skip_first = p.debug_skip_cta == (int)blockIdx.x;
     // the resident R slice must have landed (a failure here sets the abort
     // flag, and the warps leave together at the first publication)
-    if (p.r_resident) mbar_wait(&s_rfill, 0u, p.status, &s_abort, p.spin_limit_ns);
+    if (x.KR > 0) mbar_wait(&s_rfill, 0u, p.status, &s_abort, p.spin_limit_ns);
     if (!XW_LATE) load_xw(0);
     for (int s = 0; s < p.max_len; ++s) {
         float xc[TN][G];
@@ -569,7 +600,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 float az[TN][2];
 #pragma unroll
                 for (int i = 0; i < TN; ++i) { az[i][0] = 0.f; az[i][1] = 0.f; }
-                consume_product<TN, 2, EXACT>(p, x, 0, az, q, &s_abort, lane, live);
+                consume_product<TN, 2, EXACT>(p, x, 0, 0, az, q, &s_abort, lane, live);
                 next_xw();
                 float zg[TN];
                 float* rh = rhblock(s & 1);
@@ -580,7 +611,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                     for (int i = 0; i < TN; ++i) {
                         const int rl = x.rb * TN + i;
                         zg[i] = 0.f;
-                        if (!(x.active && rl < x.NR)) continue;
+                        if (!(x.lead && rl < x.NR)) continue;
                         float rhv = 0.f;
                         if (s < len[i]) {
                             float pz = fadd(xc[i][0], az[i][0]);
@@ -602,7 +633,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 float ah[TN][1];
 #pragma unroll
                 for (int i = 0; i < TN; ++i) ah[i][0] = 0.f;
-                consume_product<TN, 1, EXACT>(p, x, 2, ah, q, &s_abort, lane, live);
+                consume_product<TN, 1, EXACT>(p, x, 2, 2, ah, q, &s_abort, lane, live);
                 auto epi = [&](auto fx) {
                     constexpr bool FX = decltype(fx)::value;
                     const Acts<OP, EXACT, FX> A{fA, gA, hA};
@@ -610,7 +641,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                     for (int i = 0; i < TN; ++i) {
                         const int rl = x.rb * TN + i;
                         const int n = rown[i];
-                        if (!(x.active && rl < x.NR)) continue;
+                        if (!(x.lead && rl < x.NR)) continue;
                         if (s < len[i]) {
                             const int t = rev ? len[i] - 1 - s : s;
                             float ph = fadd(xc[i][2], ah[i][0]);
@@ -631,11 +662,23 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
             }
         } else {
             float acc[TN][G];
+            {
+                float part[TN][NCG];
 #pragma unroll
-            for (int i = 0; i < TN; ++i)
+                for (int i = 0; i < TN; ++i)
 #pragma unroll
-                for (int g = 0; g < G; ++g) acc[i][g] = 0.f;
-            consume_product<TN, G, EXACT>(p, x, 0, acc, q, &s_abort, lane, live);
+                    for (int g = 0; g < NCG; ++g) part[i][g] = 0.f;
+                consume_product<TN, NCG, EXACT>(p, x, x.gi * NCG, 0, part, q, &s_abort, lane, live);
+                // gate split: lane gi of a group holds gates [gi * NCG, (gi + 1) * NCG)
+#pragma unroll
+                for (int i = 0; i < TN; ++i)
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        if constexpr (GS == 1) acc[i][g] = part[i][g];
+                        else if (g < NCG) acc[i][g] = part[i][g];
+                        else acc[i][g] = __shfl_down_sync(0xffffffffu, part[i][g % NCG], g / NCG);
+                    }
+            }
             next_xw();
 
             auto epi = [&](auto fx) {
@@ -645,7 +688,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 for (int i = 0; i < TN; ++i) {
                     const int rl = x.rb * TN + i;
                     const int n = rown[i];
-                    if (!(x.active && rl < x.NR)) continue;
+                    if (!(x.lead && rl < x.NR)) continue;
                     if (s < len[i]) {
                         const int t = rev ? len[i] - 1 - s : s;
                         float hn;
@@ -699,7 +742,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     for (int i = 0; i < TN; ++i) {
         const int rl = x.rb * TN + i;
         const int n = rown[i];
-        if (!(x.active && rl < x.NR)) continue;
+        if (!(x.lead && rl < x.NR)) continue;
         const size_t si = s_index(p, d, n, u);
         if (p.Yh) io_store(p.Yh, si, len[i] > 0 ? canon_nan(hown[i]) : 0.f, p.io);
         if (OP == 2 && p.Yc) io_store(p.Yc, si, len[i] > 0 ? canon_nan(cown[i]) : 0.f, p.io);
@@ -710,21 +753,31 @@ template <int OP, bool TWO>
 const void* dataflow_kernel_ptr(int tn, bool exact)
 {
     switch (tn * 2 + (exact ? 1 : 0)) {
-    case 2: return (const void*)rnn_dataflow_kernel<OP, 1, false, TWO>;
-    case 3: return (const void*)rnn_dataflow_kernel<OP, 1, true, TWO>;
-    case 4: return (const void*)rnn_dataflow_kernel<OP, 2, false, TWO>;
-    case 5: return (const void*)rnn_dataflow_kernel<OP, 2, true, TWO>;
-    case 8: return (const void*)rnn_dataflow_kernel<OP, 4, false, TWO>;
-    case 9: return (const void*)rnn_dataflow_kernel<OP, 4, true, TWO>;
-    case 16: return (const void*)rnn_dataflow_kernel<OP, 8, false, TWO>;
-    case 17: return (const void*)rnn_dataflow_kernel<OP, 8, true, TWO>;
+    case 2: return (const void*)rnn_dataflow_kernel<OP, 1, false, TWO, 1>;
+    case 3: return (const void*)rnn_dataflow_kernel<OP, 1, true, TWO, 1>;
+    case 4: return (const void*)rnn_dataflow_kernel<OP, 2, false, TWO, 1>;
+    case 5: return (const void*)rnn_dataflow_kernel<OP, 2, true, TWO, 1>;
+    case 8: return (const void*)rnn_dataflow_kernel<OP, 4, false, TWO, 1>;
+    case 9: return (const void*)rnn_dataflow_kernel<OP, 4, true, TWO, 1>;
+    case 16: return (const void*)rnn_dataflow_kernel<OP, 8, false, TWO, 1>;
+    case 17: return (const void*)rnn_dataflow_kernel<OP, 8, true, TWO, 1>;
     default: return nullptr;
     }
 }
 
+// gs > 1: the gate-split instance (GRU with linear_before_reset = 1, one
+// row per thread, a gate column per lane)
 template <int OP>
-const void* dataflow_kernel_ptr(int tn, bool exact, bool two)
+const void* dataflow_kernel_ptr(int tn, bool exact, bool two, int gs)
 {
+    if (gs != 1) {
+        if constexpr (OP == 1) {
+            if (gs != 3 || two || tn != 1) return nullptr;
+            return exact ? (const void*)rnn_dataflow_kernel<OP, 1, true, false, 3>
+                         : (const void*)rnn_dataflow_kernel<OP, 1, false, false, 3>;
+        }
+        return nullptr;
+    }
     if constexpr (OP == 1) {
         if (two) return dataflow_kernel_ptr<OP, true>(tn, exact);
     }
@@ -734,7 +787,7 @@ const void* dataflow_kernel_ptr(int tn, bool exact, bool two)
 template <int OP>
 cudaError_t launch_dataflow_op(const RecParams& p, bool exact, int threads, size_t smem, cudaStream_t stream)
 {
-    const void* fn = dataflow_kernel_ptr<OP>(p.rows_per_thread, exact, OP == 1 && p.lbr == 0);
+    const void* fn = dataflow_kernel_ptr<OP>(p.rows_per_thread, exact, OP == 1 && p.lbr == 0, p.gate_split);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -743,9 +796,9 @@ cudaError_t launch_dataflow_op(const RecParams& p, bool exact, int threads, size
 }
 
 template <int OP>
-cudaError_t dataflow_occupancy_op(int tn, bool exact, bool two, int threads, size_t smem, int* blocks)
+cudaError_t dataflow_occupancy_op(int tn, bool exact, bool two, int gs, int threads, size_t smem, int* blocks)
 {
-    const void* fn = dataflow_kernel_ptr<OP>(tn, exact, two);
+    const void* fn = dataflow_kernel_ptr<OP>(tn, exact, two, gs);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -12,10 +12,10 @@ cudaError_t launch_recurrent_gru(const RecParams& p, bool exact, int threads, si
     return launch_recurrent_op<1>(p, exact, threads, smem, stream);
 }
 
-cudaError_t recurrent_occupancy_gru(int kernel, int lbr, int rows_per_thread, bool exact, int threads,
+cudaError_t recurrent_occupancy_gru(int kernel, int lbr, int rows_per_thread, int gs, bool exact, int threads,
                                       size_t smem, int* blocks)
 {
-    if (kernel == 2) return dataflow_occupancy_op<1>(rows_per_thread, exact, lbr == 0, threads, smem, blocks);
+    if (kernel == 2) return dataflow_occupancy_op<1>(rows_per_thread, exact, lbr == 0, gs, threads, smem, blocks);
     return recurrent_occupancy_op<1>(rows_per_thread, exact, threads, smem, blocks);
 }
 

@@ -12,10 +12,10 @@ cudaError_t launch_recurrent_rnn(const RecParams& p, bool exact, int threads, si
     return launch_recurrent_op<0>(p, exact, threads, smem, stream);
 }
 
-cudaError_t recurrent_occupancy_rnn(int kernel, int lbr, int rows_per_thread, bool exact, int threads,
+cudaError_t recurrent_occupancy_rnn(int kernel, int lbr, int rows_per_thread, int gs, bool exact, int threads,
                                       size_t smem, int* blocks)
 {
-    if (kernel == 2) return dataflow_occupancy_op<0>(rows_per_thread, exact, false, threads, smem, blocks);
+    if (kernel == 2) return dataflow_occupancy_op<0>(rows_per_thread, exact, false, gs, threads, smem, blocks);
     return recurrent_occupancy_op<0>(rows_per_thread, exact, threads, smem, blocks);
 }
 

@@ -20,9 +20,9 @@ namespace rnngb {
 cudaError_t launch_recurrent_rnn(const RecParams&, bool, int, size_t, cudaStream_t);
 cudaError_t launch_recurrent_gru(const RecParams&, bool, int, size_t, cudaStream_t);
 cudaError_t launch_recurrent_lstm(const RecParams&, bool, int, size_t, cudaStream_t);
-cudaError_t recurrent_occupancy_rnn(int, int, int, bool, int, size_t, int*);
-cudaError_t recurrent_occupancy_gru(int, int, int, bool, int, size_t, int*);
-cudaError_t recurrent_occupancy_lstm(int, int, int, bool, int, size_t, int*);
+cudaError_t recurrent_occupancy_rnn(int, int, int, int, bool, int, size_t, int*);
+cudaError_t recurrent_occupancy_gru(int, int, int, int, bool, int, size_t, int*);
+cudaError_t recurrent_occupancy_lstm(int, int, int, int, bool, int, size_t, int*);
 
 cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t smem, cudaStream_t s)
 {
@@ -59,12 +59,13 @@ cudaError_t wavefront_occupancy(int op, int tn, bool exact, int threads, size_t 
     }
 }
 
-cudaError_t recurrent_occupancy(int op, int lbr, int kernel, int tn, bool exact, int threads, size_t smem, int* blocks)
+cudaError_t recurrent_occupancy(int op, int lbr, int kernel, int tn, bool exact, int threads, size_t smem, int* blocks,
+                                int gs)
 {
     switch (op) {
-    case 0: return recurrent_occupancy_rnn(kernel, lbr, tn, exact, threads, smem, blocks);
-    case 1: return recurrent_occupancy_gru(kernel, lbr, tn, exact, threads, smem, blocks);
-    default: return recurrent_occupancy_lstm(kernel, lbr, tn, exact, threads, smem, blocks);
+    case 0: return recurrent_occupancy_rnn(kernel, lbr, tn, gs, exact, threads, smem, blocks);
+    case 1: return recurrent_occupancy_gru(kernel, lbr, tn, gs, exact, threads, smem, blocks);
+    default: return recurrent_occupancy_lstm(kernel, lbr, tn, gs, exact, threads, smem, blocks);
     }
 }
 }  // namespace rnngb
@@ -243,6 +244,7 @@ struct Geometry {
     int cpb;          // dataflow: chunks per tensor copy
     int ustride;      // dataflow: floats per unit of the resident R slice
     int ufast;        // dataflow: compute threads take units fastest (wide row tiles)
+    int gs;           // dataflow: gate split (lanes per unit and row)
 };
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -319,6 +321,12 @@ rnn_status plan_staged(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* 
 // per-CTA flags.  Picks the cheapest feasible shape under a simple cost
 // model (cycles per step: k-loop issue + h/R bytes into the SM + epilogue +
 // a fixed latency for the flags and the first copy).
+// Dataflow planner: cycles charged per piece of a product (a ring slot's
+// wait, release and tensor copies).  Measured on GRU, hidden 2048, batch 4
+// with R streamed: each halving of the piece adds about half a microsecond a
+// step, more than the resident chunks it makes room for save.
+constexpr double kDfPieceCost = 1000.0;
+
 rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out)
 {
     const int64_t H = pl->H;
@@ -346,7 +354,7 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
         const int64_t cu_cap = pl->ov_units > 0 ? pl->ov_units : di.sms / ((int64_t)D * CR);
         if (cu_cap < 1) continue;
         for (int rr = 1; rr >= 0; --rr) {
-            if (pl->ov_rres >= 0 && rr != pl->ov_rres) continue;
+            if (pl->ov_rres >= 0 && rr != (pl->ov_rres == 2 ? 0 : pl->ov_rres)) continue;
             const int quant = 1;
             const int64_t Q = H;
             int64_t CU = std::min<int64_t>(cu_cap, Q);
@@ -364,32 +372,67 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
             }
             if (!tn) continue;
             if (rr == 0 && (H < kDfPitch || umax > 256)) continue;   // R boxes: 36 k wide, <= 256 units
-            const int compute = (int)round_up((int64_t)umax * (NRP / tn), 32);
+            // gate split (GRU, one row per thread, one product per step): three
+            // lanes share a (unit, row) and take a gate column each, when that
+            // fits the launch bound (a warp holds ten such groups).  Measured:
+            // 5-9% faster on GRU with batch 4, hidden 256-2048; LSTM with four
+            // lanes per (unit, row) (batch 8, hidden 1024) was 47% slower, its
+            // h loads quadrupled.
+            int gs = 1;
+            if (pl->op == RNN_OP_GRU && tn == 1 && phases == 1 && ceil_div((int64_t)umax * NRP, 32 / G) * 32 <= 224)
+                gs = G;
+            const int compute = gs == 1 ? (int)round_up((int64_t)umax * (NRP / tn), 32)
+                                        : (int)ceil_div((int64_t)umax * NRP, 32 / G) * 32;
             // pieces: the whole block in one tensor copy per product (measured:
             // every extra piece boundary costs more than the earlier start
             // it buys), halved until the ring holds two pieces
-            int cpb = 0, slots = 0;
+            int cpb0 = 0, slots0 = 0;
             for (int c = nchunks; c >= 1; c /= 2) {
                 const size_t fixed = df_smem_bytes((int)H, umax, G, (int)NRP, rr, c, 0);
                 const size_t per_slot = df_smem_bytes((int)H, umax, G, (int)NRP, rr, c, 1) - fixed;
                 if (fixed + 2 * per_slot > smem_cap) continue;
                 const int np = (int)ceil_div(nchunks, c);
-                cpb = c;
-                slots = (int)std::min<size_t>(std::min<size_t>((size_t)kMaxSlots, (size_t)2 * np * phases),
-                                              (smem_cap - fixed) / per_slot);
+                cpb0 = c;
+                slots0 = (int)std::min<size_t>(std::min<size_t>((size_t)kMaxSlots, (size_t)2 * np * phases),
+                                               (smem_cap - fixed) / per_slot);
                 break;
             }
-            if (cpb == 0 || slots < 2) continue;
-            const size_t smem = df_smem_bytes((int)H, umax, G, (int)NRP, rr, cpb, slots);
-            const double wps = (double)ceil_div(compute / 32, 4);
-            const double per_k = ((exact ? 2.0 : 1.0) * 4.0 * tn * G + tn + G) / 4.0;
-            const double kloop = (double)H * per_k * wps;
-            const double bytes = (double)NRP * H * 4 * phases + (rr ? 0.0 : (double)H * umax * G * 4 * phases);
-            const double fetch = bytes / 64.0 * (slots >= (int)ceil_div(nchunks, cpb) * phases ? 0.5 : 1.0);
-            const double cost = kloop + fetch + 600.0 * tn * phases + 2500.0 * phases;
-            if (cost < best_cost) {
+            if (cpb0 == 0 || slots0 < 2) continue;
+            // streamed R: besides the ring alone, smaller pieces in a ring of
+            // 2-4 slots with as many leading pieces of R resident as the rest
+            // of shared memory holds
+            struct Ring { int cpb, slots, res; };
+            Ring cands[48];
+            int ncand = 0;
+            if (pl->ov_rres != 2) cands[ncand++] = {cpb0, slots0, 0};   // 2: only partly resident
+            if (!rr && pl->ov_rres != 0)
+                for (int c = cpb0; c >= 1 && ncand + 3 <= 48; c /= 2) {
+                    const int np = (int)ceil_div(nchunks, c);
+                    for (int sl = 2; sl <= 4; ++sl) {
+                        int r = 0;
+                        while (r + 1 < np &&
+                               df_smem_bytes((int)H, umax, G, (int)NRP, 0, c, sl, (r + 1) * c) <= smem_cap)
+                            ++r;
+                        if (r > 0) cands[ncand++] = {c, sl, r * c};
+                    }
+                }
+            for (int ci = 0; ci < ncand; ++ci) {
+                const int cpb = cands[ci].cpb, slots = cands[ci].slots, res = cands[ci].res;
+                const int np = (int)ceil_div(nchunks, cpb);
+                const size_t smem = df_smem_bytes((int)H, umax, G, (int)NRP, rr, cpb, slots, res);
+                if (smem > smem_cap) continue;
+                const double wps = (double)ceil_div(compute / 32, 4);
+                const double per_k = ((exact ? 2.0 : 1.0) * 4.0 * tn * G + tn + G) / 4.0;
+                const double kloop = (double)H * per_k * wps;
+                // GRU with linear_before_reset = 0 streams each gate's rows once a
+                // step (z and r in the first product, the candidate's in the second)
+                const double bytes =
+                    (double)NRP * H * 4 * phases + (rr ? 0.0 : (double)(H - res * kRecKC) * umax * G * 4);
+                const double fetch = bytes / 64.0 * (slots >= np * phases ? 0.5 : 1.0);
+                const double cost = kloop + fetch + kDfPieceCost * np * phases + 600.0 * tn * phases + 2500.0 * phases;
+                if (cost >= best_cost) continue;
                 int blocks = 0;
-                cudaError_t e = recurrent_occupancy(pl->op, pl->lbr, 2, tn, exact, compute + 32, smem, &blocks);
+                cudaError_t e = recurrent_occupancy(pl->op, pl->lbr, 2, tn, exact, compute + 32, smem, &blocks, gs);
                 if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
                 if (blocks < 1 || (int64_t)D * CR * CU > (int64_t)blocks * di.sms) continue;
                 best_cost = cost;
@@ -408,8 +451,10 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
                 out->npad = (int)NRP;
                 out->hpad = (int)round_up(H, kRecKC);
                 out->cpb = cpb;
-                out->ustride = df_unit_stride((int)H, G);
+                out->res_chunks = res;
+                out->ustride = df_unit_stride(rr ? (int)H : res * kRecKC, G);
                 out->ufast = tn >= 4 ? 1 : 0;
+                out->gs = gs;
             }
         }
     }
@@ -847,6 +892,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     p.chunks_per_piece = geo.cpb;
     p.unit_stride = geo.ustride;
     p.unit_fastest = geo.ufast;
+    p.gate_split = geo.kernel == 2 && geo.gs > 1 ? geo.gs : 1;
     p.XW = xw; p.Rt = rt; p.Rorig = pl->const_weights ? pl->r_orig_const : a.R; p.B = a.B; p.P = a.P; p.h0 = a.h0; p.c0 = a.c0; p.lens = a.lens;
     p.Y = a.Y; p.Yh = a.Yh; p.Yc = a.Yc;
     p.hbuf = (float*)(scratch + L.hb);
@@ -894,14 +940,25 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
         rs = tmap_encode(&p.rhmap, p.rhbuf ? p.rhbuf : p.hbuf, 4, hdims, hstrides, hbox);
         if (rs != RNN_OK) return rs;
         if (!geo.rres) {
-            // R as given [D][G][H units][H k], box 36 x umax x G x 1 (one chunk; k past H reads 0)
+            // R as given [D][G][H units][H k], box 36 x umax x gates x 1 (one
+            // chunk; k past H reads 0): all G gates, or for GRU with
+            // linear_before_reset = 0 the z and r rows (first product of a
+            // step) and the candidate's rows (second product)
             const cuuint64_t rdims[4] = {(cuuint64_t)H, (cuuint64_t)H, (cuuint64_t)G, (cuuint64_t)D};
             const cuuint64_t rstrides[3] = {(cuuint64_t)H * 4, (cuuint64_t)H * H * 4, (cuuint64_t)G * H * H * 4};
-            const cuuint32_t rbox[4] = {(cuuint32_t)kDfPitch, (cuuint32_t)geo.umax, (cuuint32_t)G, 1};
+            const bool two = pl->op == RNN_OP_GRU && pl->lbr == 0;
+            const cuuint32_t rbox[4] = {(cuuint32_t)kDfPitch, (cuuint32_t)geo.umax, (cuuint32_t)(two ? 2 : G), 1};
             rs = tmap_encode(&p.rmap, p.Rorig, 4, rdims, rstrides, rbox);
             if (rs != RNN_OK) return rs;
+            p.rmap2 = p.rmap;
+            if (two) {
+                const cuuint32_t rbox2[4] = {(cuuint32_t)kDfPitch, (cuuint32_t)geo.umax, 1, 1};
+                rs = tmap_encode(&p.rmap2, p.Rorig, 4, rdims, rstrides, rbox2);
+                if (rs != RNN_OK) return rs;
+            }
         } else {
             p.rmap = p.hmap;   // unused
+            p.rmap2 = p.hmap;
         }
     }
 
@@ -1098,7 +1155,7 @@ rnn_status rnn_plan_set_launch(rnn_plan_t pl, int unit_groups, int rows_per_thre
                                int row_groups, int kernel)
 {
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
-    if (unit_groups < 0 || rows_per_thread < 0 || r_resident < -1 || r_resident > 1 || row_groups < 0 ||
+    if (unit_groups < 0 || rows_per_thread < 0 || r_resident < -1 || r_resident > 2 || row_groups < 0 ||
         kernel < 0 || kernel > 3)
         return fail(RNN_ERR_INVALID_ARGUMENT, "bad launch override");
     if (kernel == 3 && (row_groups > 1 || rows_per_thread > 1))

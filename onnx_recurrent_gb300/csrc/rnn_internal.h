@@ -20,7 +20,9 @@ struct RecParams {
     // ([blocks][hpad/32 chunks][rows][36], box 36 x rows x cpb x 1) and of R
     // as given ([D][G][H units][H], box 36 x units x G x 1), no swizzle
     CUtensorMap hmap, rhmap, rmap;
-    // tensor-core kernel, GRU lbr = 0: R's candidate rows (box npad2 rows)
+    // GRU lbr = 0, R's candidate rows: tensor-core kernel, box npad2 rows;
+    // dataflow kernel, box 36 x units x 1 x 1 (rmap then has a box of the
+    // z and r gates)
     CUtensorMap rmap2;
     int op, G, D, N, H, S, layout;
     int lbr, input_forget;
@@ -50,6 +52,7 @@ struct RecParams {
     int hpad;                    // dataflow kernel: H rounded up to 32 (chunks x 32)
     int unit_stride;             // dataflow kernel: floats per unit of the resident R slice
     int unit_fastest;            // dataflow kernel: compute thread t takes unit t % umax and row tile t / umax
+    int gate_split;              // dataflow kernel: lanes per (unit, row tile), each with G / gate_split gates
                                  // (else row tile t % tiles, unit t / tiles)
 
     // tensors
@@ -163,14 +166,17 @@ __host__ __device__ inline size_t df_hslot_bytes(int npad, int cpb)
 }
 
 // Dataflow kernel: dynamic shared memory (128-byte alignment slack + R
-// resident or ring of R pieces + ring of h pieces; a slot holds one piece of
-// cpb chunks).
-inline size_t df_smem_bytes(int H, int umax, int G, int npad, int r_resident, int cpb, int slots)
+// resident, in full or its leading res_chunks 32-k chunks + a ring of
+// streamed R pieces unless all of R is resident + a ring of h pieces; a slot
+// holds one piece of cpb chunks).
+inline size_t df_smem_bytes(int H, int umax, int G, int npad, int r_resident, int cpb, int slots,
+                            int res_chunks = 0)
 {
-    const size_t rres = (((size_t)umax * df_unit_stride(H, G) * 4 + 127) / 128) * 128;
+    const int kr = r_resident ? H : res_chunks * kRecKC;
+    const size_t rres = kr > 0 ? (((size_t)umax * df_unit_stride(kr, G) * 4 + 127) / 128) * 128 : 0;
     const size_t rslot = (size_t)cpb * df_rsub_bytes(umax, G);
-    const size_t rbytes = r_resident ? rres : (size_t)slots * rslot;
-    return 128 + rbytes + (size_t)slots * df_hslot_bytes(npad, cpb);
+    const size_t rring = r_resident ? 0 : (size_t)slots * rslot;
+    return 128 + rres + rring + (size_t)slots * df_hslot_bytes(npad, cpb);
 }
 
 // The control block: barrier counters, status word, publication flags.
@@ -184,7 +190,7 @@ constexpr int kMaxFlags = (int)((kCtrlBytes - kCtrlFlagsOffset) / 4);
 cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t smem,
                              cudaStream_t stream);
 cudaError_t recurrent_occupancy(int op, int lbr, int kernel, int rows_per_thread, bool exact, int threads,
-                                size_t smem, int* blocks_per_sm);
+                                size_t smem, int* blocks_per_sm, int gate_split = 1);
 
 // Input projection XW[M][ncols] = X[M][K] . Bt[K][ncols].  A wait of the
 // tensor-copy loader that gives up writes RNN_ERR_TIMEOUT to *status.

@@ -88,7 +88,10 @@ def test_set_launch_validation(lib):
     with pytest.raises(rb.RNNError):
         orc.rnn_plan_set_launch(p, 4, 3, -1)
     with pytest.raises(rb.RNNError):
-        orc.rnn_plan_set_launch(p, 4, 1, 2)
+        orc.rnn_plan_set_launch(p, 4, 1, 3)
+    with pytest.raises(rb.RNNError):
+        orc.rnn_plan_set_launch(p, 4, 1, -2)
+    orc.rnn_plan_set_launch(p, 4, 1, 2)      # partly resident (dataflow kernel)
     orc.rnn_plan_set_launch(p, 4, 2, 0)
     with pytest.raises(rb.RNNError):
         orc.rnn_plan_set_mode(p, 9)

@@ -161,6 +161,30 @@ def test_staged_kernel_partly_resident_r(op, lbr, launch):
     _compare_exact(c, (Y, Yh, Yc), oracle_case(c), f"{op} lbr {lbr} {launch}")
 
 
+# Dataflow kernel with hidden 1024 and 16-64 units per CTA: the R slice does
+# not fit; r_resident 2 keeps its leading pieces resident and streams the
+# rest by tensor copies (GRU with linear_before_reset 0 streams the z and r
+# rows for the first product of a step and the candidate's rows for the
+# second), r_resident 0 streams all of it, -1 lets the planner choose.
+# Every split gives the same bits.
+@pytest.mark.parametrize("op,lbr,launch", [("LSTM", 0, (64, 0, 2, 1, 2)), ("GRU", 0, (48, 0, 2, 1, 2)),
+                                           ("GRU", 1, (48, 0, 2, 1, 2)), ("RNN", 0, (16, 0, 2, 1, 2)),
+                                           ("LSTM", 0, (64, 0, 0, 1, 2)), ("GRU", 0, (48, 0, 0, 1, 2)),
+                                           ("GRU", 1, (48, 0, -1, 1, 2))])
+def test_dataflow_kernel_partly_resident_r(op, lbr, launch):
+    c = make_case(op, "bidirectional", 5, 11, 40, 1024, seed=45, with_P=True, h0_scale=0.5, c0_scale=0.5,
+                  lens=("uniform", 0, 5), linear_before_reset=lbr, clip=2.0, w_scale=1.0 / 32)
+    Y, Yh, Yc, plan = gpu_case(c, "exact", launch=launch, keep_plan=True)
+    got = orc.rnn_plan_get_launch(plan)
+    orc.rnn_plan_destroy(plan)
+    assert got["kernel"] == 2 and got["r_resident"] == 0
+    ref = oracle_case(c)
+    _compare_exact(c, (Y, Yh, Yc), ref, f"{op} lbr {lbr} {launch}")
+    for g, r in zip(gpu_case(c, "fast", launch=launch), ref):
+        if g is not None:
+            assert float(np.abs(g.astype(np.float64) - r.astype(np.float64)).max(initial=0.0)) <= 1e-5
+
+
 @pytest.mark.parametrize("g", [(2, 1, 0, 0, 1), (5, 2, 1, 0, 1), (4, 1, 1, 2, 2), (3, 2, 0, 1, 2)])
 def test_fast_mode_is_geometry_independent(g):
     c = make_case("LSTM", "bidirectional", 6, 9, 20, 36, seed=5, with_P=True, h0_scale=0.5)
