@@ -255,7 +255,8 @@ def measure_l2_gbs(torch, nbytes=32 << 20, reps=50):
 
 KERNEL_SOURCES = {
     "recurrence": ["k_recur.cuh", "k_recur2.cuh", "k_recur_rnn.cu", "k_recur_gru.cu", "k_recur_lstm.cu",
-                   "k_recur_tc.cu", "k_wave.cuh", "k_wave_rnn.cu", "k_wave_gru.cu", "k_wave_lstm.cu", "tma.cuh",
+                   "k_recur_tc.cu", "k_wave.cuh", "k_wave_rnn.cu", "k_wave_gru.cu", "k_wave_lstm.cu",
+                   "k_clus_rnn.cu", "k_clus_gru.cu", "k_clus_lstm.cu", "tma.cuh",
                    "exact_math.cuh", "io_types.cuh", "rnn_internal.h"],
     "projection": ["k_proj.cu", "k_proj_tc.cu", "tma.cuh", "rnn_internal.h"],
     "cell": ["k_cell.cu", "exact_math.cuh", "rnn_internal.h"],

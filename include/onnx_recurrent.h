@@ -204,17 +204,23 @@ rnn_status rnn_plan_get_activation(rnn_plan_t plan, int dir, int slot, int* fn,
  * through a shared-memory ring; one device-wide barrier per step), kernel 2
  * the dataflow kernel (CTAs tile unit groups x row groups; a loader warp
  * fetches h with TMA tensor copies once every CTA of its row group has
- * published the step on the row group's counter).  unit_groups: CTAs per direction along
- * hidden units; row_groups: along batch rows (dataflow kernel only);
+ * published the step on the row group's counter), kernel 5 the dataflow
+ * kernel with the exchange inside a thread-block cluster (each row group of
+ * a direction is one cluster of at most 16 CTAs that hold all of R and write
+ * h into each other's shared memory; 1 or 2 rows per thread; R must fit).
+ * unit_groups: CTAs per direction along
+ * hidden units; row_groups: along batch rows (dataflow kernels only);
  * rows_per_thread: 1, 2, 4 or 8; r_resident: R slice
  * kept in shared memory (1) or streamed through it (0); 2 asks the dataflow
  * kernel to keep the slice's leading pieces resident and stream the rest
  * (the staged kernel does that by itself whenever the slice does not fit,
  * and takes 2 as -1).  Every geometry gives
  * the same results.  rnn_plan_get_launch reports the geometry of the last
- * run (kernel 4 on a stack's first plan: the run was the stack's wavefront
- * launch, unit_groups its first layer's CTAs); a shape the override cannot
- * serve makes the run return RNN_ERR_UNSUPPORTED. */
+ * run (kernel 5: the in-cluster exchange, which the planner also picks by
+ * itself where it models it faster; kernel 4 on a stack's first plan: the
+ * run was the stack's wavefront launch, unit_groups its first layer's
+ * CTAs); a shape the override cannot serve makes the run return
+ * RNN_ERR_UNSUPPORTED. */
 rnn_status rnn_plan_set_launch(rnn_plan_t plan, int unit_groups, int rows_per_thread,
                                int r_resident, int row_groups, int kernel);
 rnn_status rnn_plan_get_launch(rnn_plan_t plan, int* unit_groups, int* rows_per_thread,

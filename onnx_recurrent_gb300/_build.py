@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libonnx_recurrent_gb300.so")
 SOURCES = ["rnn_api.cpp", "k_proj.cu", "k_proj_tc.cu", "k_misc.cu", "k_recur_rnn.cu", "k_recur_gru.cu",
            "k_recur_lstm.cu", "k_recur_tc.cu", "k_cell.cu", "rnn_static.cu", "k_wave_rnn.cu", "k_wave_gru.cu",
-           "k_wave_lstm.cu"]
+           "k_wave_lstm.cu", "k_clus_rnn.cu", "k_clus_gru.cu", "k_clus_lstm.cu"]
 HEADERS = ["rnn_internal.h", "exact_math.cuh", "io_types.cuh", "tma.cuh", "k_recur.cuh", "k_recur2.cuh",
            "k_wave.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

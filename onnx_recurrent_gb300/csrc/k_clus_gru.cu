@@ -1,0 +1,18 @@
+// Instances of the dataflow kernel with the in-cluster exchange of h for one
+// operator (page "Recurrent operators: RNN, GRU, LSTM", Computation).
+#include "k_recur2.cuh"
+
+namespace rnngb {
+
+cudaError_t launch_cluster_gru(const RecParams& p, bool exact, int threads, size_t smem, cudaStream_t stream)
+{
+    return launch_cluster_op<1>(p, exact, threads, smem, stream);
+}
+
+cudaError_t cluster_occupancy_gru(int tn, bool exact, bool two, int ctas, int cluster, int threads, size_t smem,
+                                  int* clusters)
+{
+    return cluster_occupancy_op<1>(tn, exact, two, ctas, cluster, threads, smem, clusters);
+}
+
+}  // namespace rnngb

@@ -324,6 +324,60 @@ __device__ __forceinline__ bool publish(const DfCtx& x, unsigned* counter, volat
     return true;
 }
 
+// ---- in-cluster exchange (CL): the CTAs of a row group form one thread-block
+// cluster; each keeps the whole h of its rows in its own shared memory (two
+// buffers by step parity, plus r (.) h for GRU with linear_before_reset = 0),
+// writes the h it computes into every peer's buffer (distributed shared
+// memory) and arrives on every peer's barrier for that buffer.
+
+// Bounded wait for the peers' arrivals on one of this CTA's exchange barriers.
+__device__ __forceinline__ bool cl_wait(uint64_t* bar, unsigned parity, int* status, volatile int* abort_flag,
+                                        long long limit_ns)
+{
+    if (mbar_test_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    const unsigned long long t0 = globaltimer_ns();
+    unsigned it = 0;
+    while (!mbar_test_cluster(bar, parity)) {
+        if ((++it & 15u) == 0u) {
+            if (*abort_flag) return false;
+            if ((long long)(globaltimer_ns() - t0) > limit_ns) {
+                atomicCAS(status, 0, 6 /* RNN_ERR_TIMEOUT */);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// This CTA's products from its own copy of h (all chunks, k ascending) and
+// its resident R slice.
+template <int TN, int NC, bool EXACT>
+__device__ __forceinline__ void cl_product(const DfCtx& x, const char* hbox, int col_off, float (&acc)[TN][NC])
+{
+    const char* hp[TN];
+#pragma unroll
+    for (int i = 0; i < TN; ++i) hp[i] = hbox + (size_t)(x.rb * TN + i) * (kDfPitch * 4);
+    const float* rbase = x.Rs + (size_t)x.ul * x.ugs + (size_t)col_off * x.KR;
+    const char* rp[NC];
+#pragma unroll
+    for (int g = 0; g < NC; ++g) rp[g] = reinterpret_cast<const char*>(rbase + (size_t)g * x.KR);
+    df_piece<TN, NC, EXACT, true>(hp, x.NRP * kDfPitch * 4, rp, kRecKC * 4, (x.H + 3) / 4, acc);
+}
+
+// Each compute thread fences its writes into the peers' buffers at cluster
+// scope; once all have met, compute thread r arrives (release, cluster
+// scope) on the barrier `bar` of the CTA of rank r.  Measured: one thread
+// arriving on all 16 peers in turn took about 2 us a step; spread over the
+// lanes the exchange costs about a third of the device-wide one.
+__device__ __forceinline__ void cl_publish(const DfCtx& x, uint64_t* bar, bool send)
+{
+    if (send) fence_acq_rel_cluster();
+    named_barrier(1, x.ncompute);
+    if (send && x.ctid < x.CU) mbar_arrive_cluster(cluster_map(smem_addr(bar), (unsigned)x.ctid));
+}
+
 // Threads per CTA: one row per thread keeps three groups of operands in
 // flight (up to 255 registers, 256 threads); wider tiles keep one group in
 // flight and more accumulators (up to 168 registers, 384 threads); eight rows
@@ -341,16 +395,22 @@ struct DfBounds {
 // without the split); the first lane of the group gathers the others'
 // sums by shuffles and does the gate arithmetic.  A warp holds 32 / GS such
 // groups; with GS = 3 its last two lanes idle.
-template <int OP, int TN, bool EXACT, bool TWO, int GS>
+// CL: in-cluster exchange (the launch makes each row group of a direction
+// one cluster of unit_groups CTAs; R is resident; no loader work, no
+// counters): no CTA leaves before the whole cluster has met at its end, so
+// no peer's shared memory is written after its CTA exits.
+template <int OP, int TN, bool EXACT, bool TWO, int GS, bool CL>
 __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(const __grid_constant__ RecParams p)
 {
     constexpr int G = OP == 0 ? 1 : (OP == 1 ? 3 : 4);
     static_assert(GS == 1 || (!TWO && G % GS == 0), "gate split: one product per step, whole gate shares");
+    static_assert(!CL || GS == 1, "in-cluster exchange without gate split");
     constexpr int NCG = G / GS;       // gate columns per thread
     extern __shared__ __align__(128) unsigned char df_smem[];
     __shared__ __align__(8) uint64_t s_full[kMaxSlots];
     __shared__ __align__(8) uint64_t s_empty[kMaxSlots];
     __shared__ __align__(8) uint64_t s_pub, s_rfill;
+    __shared__ __align__(8) uint64_t s_hready[2], s_rhready;   // CL: peers' h / r (.) h landed
     __shared__ int s_abort;
 
     DfCtx x;
@@ -410,6 +470,9 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     x.Rs = reinterpret_cast<float*>(base);
     x.Rring = reinterpret_cast<char*>(base + rres);
     x.Hring = reinterpret_cast<char*>(base + rres + (size_t)x.slots * x.rslot);
+    // CL: h buffers 0 and 1, then r (.) h, each one row group's block
+    const size_t clb = CL ? (((size_t)x.NRP * (x.HP / kRecKC) * kDfPitch * 4 + 127) / 128) * 128 : 0;
+    auto clbuf = [&](int i) { return reinterpret_cast<char*>(base + rres + (size_t)i * clb); };
     x.full = s_full;
     x.empty = s_empty;
     x.pub = &s_pub;
@@ -434,18 +497,29 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         }
         mbar_init(&s_pub, 1);
         mbar_init(&s_rfill, 1);
+        if (CL) {
+            mbar_init(&s_hready[0], (unsigned)x.CU);
+            mbar_init(&s_hready[1], (unsigned)x.CU);
+            mbar_init(&s_rhready, (unsigned)x.CU);
+        }
         s_abort = 0;
         mbar_fence_init();
     }
     __syncthreads();
+    // CL: every peer's barriers are initialised before any arrival on them
+    if constexpr (CL) cluster_sync_all();
     if (x.KR > 0 && threadIdx.x < 32) {
         // R[d][g*H + u][k] -> Rs[(u - u0) * ugs + g*KR + k], k < KR: one bulk copy of
         // a row of KR floats per (unit, gate), all completing on s_rfill
         // (H is a multiple of 4 and ugs*4 of 16, so every copy is 16-byte
         // aligned at both ends)
         const float* src = p.Rorig + (size_t)d * G * p.H * p.H;
-        if (lane == 0) mbar_arrive_expect_tx(&s_rfill, (unsigned)(x.U * G * x.KR) * 4u);
+        // CL: also the row group's block of the exchange buffer (h before
+        // the first step) into h buffer 0
+        const unsigned hb0 = CL ? (unsigned)(x.NRP * (x.HP / kRecKC) * kDfPitch) * 4u : 0u;
+        if (lane == 0) mbar_arrive_expect_tx(&s_rfill, (unsigned)(x.U * G * x.KR) * 4u + hb0);
         __syncwarp();
+        if (CL && lane == 0) bulk_g2s(clbuf(0), hblock(0), hb0, &s_rfill);
         for (int j = lane; j < x.U * G; j += 32) {
             const int ul = j / G, g = j - ul * G;
             bulk_g2s(x.Rs + (size_t)ul * x.ugs + (size_t)g * x.KR, src + ((size_t)g * p.H + x.u0 + ul) * p.H,
@@ -454,6 +528,18 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     }
 
     // ------------------------------------------------------------ loader
+    if (CL && threadIdx.x < 32) {
+        // nothing to stream: wait (bounded) for the fill, then meet the
+        // cluster at its end
+        if (lane == 0) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (!mbar_test(&s_rfill, 0u) && (long long)(globaltimer_ns() - t0) <= p.spin_limit_ns) {
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();
+        return;
+    }
     if (threadIdx.x < 32) {
         unsigned q = 0;
         bool ok = true;
@@ -593,6 +679,20 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         if constexpr (XW_LATE) prefetch_xw(s);
         else take_xw();
         float* hdst = hblock((s + 1) & 1);
+        // CL: no exchange of the last step's h (nothing reads it)
+        const bool cl_send = s + 1 < p.max_len;
+        const unsigned cl_h = CL ? smem_addr(clbuf((s + 1) & 1)) : 0u;
+        auto put_h = [&](size_t off, float v) {
+            if constexpr (CL) {
+                if (cl_send)
+                    for (int r = 0; r < x.CU; ++r) st_cluster_f32(cluster_map(cl_h + (unsigned)off * 4u, (unsigned)r), v);
+            } else {
+                hdst[off] = v;
+            }
+        };
+        if constexpr (CL) {
+            if (s > 0) cl_wait(&s_hready[s & 1], (unsigned)((s - 1) >> 1) & 1u, p.status, &s_abort, p.spin_limit_ns);
+        }
         const bool live = s < tile_len;   // a finished row tile skips its products (its rows stay frozen)
 
         if constexpr (TWO) {
@@ -600,7 +700,11 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 float az[TN][2];
 #pragma unroll
                 for (int i = 0; i < TN; ++i) { az[i][0] = 0.f; az[i][1] = 0.f; }
-                consume_product<TN, 2, EXACT>(p, x, 0, 0, az, q, &s_abort, lane, live);
+                if constexpr (CL) {
+                    if (x.active && live) cl_product<TN, 2, EXACT>(x, clbuf(s & 1), 0, az);
+                } else {
+                    consume_product<TN, 2, EXACT>(p, x, 0, 0, az, q, &s_abort, lane, live);
+                }
                 next_xw();
                 float zg[TN];
                 float* rh = rhblock(s & 1);
@@ -624,16 +728,30 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                             const float r = A.F(clipv(p, pr));
                             rhv = fmul(r, hown[i]);
                         }
-                        rh[xoff(rl, u)] = rhv;
+                        if constexpr (CL) {
+                            const unsigned a = smem_addr(clbuf(2)) + (unsigned)xoff(rl, u) * 4u;
+                            for (int r = 0; r < x.CU; ++r) st_cluster_f32(cluster_map(a, (unsigned)r), rhv);
+                        } else {
+                            rh[xoff(rl, u)] = rhv;
+                        }
                     }
                 };
                 if (fixed_acts) epi_r(std::true_type{});
                 else epi_r(std::false_type{});
-                if (!publish(x, counter, &s_abort, skip_first && s == 0)) return;
+                if constexpr (CL) {
+                    cl_publish(x, &s_rhready, true);
+                    cl_wait(&s_rhready, (unsigned)s & 1u, p.status, &s_abort, p.spin_limit_ns);
+                } else if (!publish(x, counter, &s_abort, skip_first && s == 0)) {
+                    return;
+                }
                 float ah[TN][1];
 #pragma unroll
                 for (int i = 0; i < TN; ++i) ah[i][0] = 0.f;
-                consume_product<TN, 1, EXACT>(p, x, 2, 2, ah, q, &s_abort, lane, live);
+                if constexpr (CL) {
+                    if (x.active && live) cl_product<TN, 1, EXACT>(x, clbuf(2), 2, ah);
+                } else {
+                    consume_product<TN, 1, EXACT>(p, x, 2, 2, ah, q, &s_abort, lane, live);
+                }
                 auto epi = [&](auto fx) {
                     constexpr bool FX = decltype(fx)::value;
                     const Acts<OP, EXACT, FX> A{fA, gA, hA};
@@ -653,12 +771,13 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                         } else if (p.Y) {
                             io_store(p.Y, y_index(p, s, d, n, u), 0.f, p.io);
                         }
-                        hdst[xoff(rl, u)] = hown[i];
+                        put_h(xoff(rl, u), hown[i]);
                     }
                 };
                 if (fixed_acts) epi(std::true_type{});
                 else epi(std::false_type{});
-                if (!publish(x, counter, &s_abort, false)) return;
+                if constexpr (CL) cl_publish(x, &s_hready[(s + 1) & 1], cl_send);
+                else if (!publish(x, counter, &s_abort, false)) return;
             }
         } else {
             float acc[TN][G];
@@ -668,7 +787,11 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 for (int i = 0; i < TN; ++i)
 #pragma unroll
                     for (int g = 0; g < NCG; ++g) part[i][g] = 0.f;
-                consume_product<TN, NCG, EXACT>(p, x, x.gi * NCG, 0, part, q, &s_abort, lane, live);
+                if constexpr (CL) {
+                    if (x.active && live) cl_product<TN, NCG, EXACT>(x, clbuf(s & 1), 0, part);
+                } else {
+                    consume_product<TN, NCG, EXACT>(p, x, x.gi * NCG, 0, part, q, &s_abort, lane, live);
+                }
                 // gate split: lane gi of a group holds gates [gi * NCG, (gi + 1) * NCG)
 #pragma unroll
                 for (int i = 0; i < TN; ++i)
@@ -729,12 +852,13 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                     } else if (p.Y) {
                         io_store(p.Y, y_index(p, s, d, n, u), 0.f, p.io);
                     }
-                    hdst[xoff(rl, u)] = hown[i];
+                    put_h(xoff(rl, u), hown[i]);
                 }
             };
             if (fixed_acts) epi(std::true_type{});
             else epi(std::false_type{});
-            if (!publish(x, counter, &s_abort, skip_first && s == 0)) return;
+            if constexpr (CL) cl_publish(x, &s_hready[(s + 1) & 1], cl_send);
+            else if (!publish(x, counter, &s_abort, skip_first && s == 0)) return;
         }
     }
 
@@ -747,20 +871,21 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         if (p.Yh) io_store(p.Yh, si, len[i] > 0 ? canon_nan(hown[i]) : 0.f, p.io);
         if (OP == 2 && p.Yc) io_store(p.Yc, si, len[i] > 0 ? canon_nan(cown[i]) : 0.f, p.io);
     }
+    if constexpr (CL) cluster_sync_all();
 }
 
 template <int OP, bool TWO>
 const void* dataflow_kernel_ptr(int tn, bool exact)
 {
     switch (tn * 2 + (exact ? 1 : 0)) {
-    case 2: return (const void*)rnn_dataflow_kernel<OP, 1, false, TWO, 1>;
-    case 3: return (const void*)rnn_dataflow_kernel<OP, 1, true, TWO, 1>;
-    case 4: return (const void*)rnn_dataflow_kernel<OP, 2, false, TWO, 1>;
-    case 5: return (const void*)rnn_dataflow_kernel<OP, 2, true, TWO, 1>;
-    case 8: return (const void*)rnn_dataflow_kernel<OP, 4, false, TWO, 1>;
-    case 9: return (const void*)rnn_dataflow_kernel<OP, 4, true, TWO, 1>;
-    case 16: return (const void*)rnn_dataflow_kernel<OP, 8, false, TWO, 1>;
-    case 17: return (const void*)rnn_dataflow_kernel<OP, 8, true, TWO, 1>;
+    case 2: return (const void*)rnn_dataflow_kernel<OP, 1, false, TWO, 1, false>;
+    case 3: return (const void*)rnn_dataflow_kernel<OP, 1, true, TWO, 1, false>;
+    case 4: return (const void*)rnn_dataflow_kernel<OP, 2, false, TWO, 1, false>;
+    case 5: return (const void*)rnn_dataflow_kernel<OP, 2, true, TWO, 1, false>;
+    case 8: return (const void*)rnn_dataflow_kernel<OP, 4, false, TWO, 1, false>;
+    case 9: return (const void*)rnn_dataflow_kernel<OP, 4, true, TWO, 1, false>;
+    case 16: return (const void*)rnn_dataflow_kernel<OP, 8, false, TWO, 1, false>;
+    case 17: return (const void*)rnn_dataflow_kernel<OP, 8, true, TWO, 1, false>;
     default: return nullptr;
     }
 }
@@ -773,8 +898,8 @@ const void* dataflow_kernel_ptr(int tn, bool exact, bool two, int gs)
     if (gs != 1) {
         if constexpr (OP == 1) {
             if (gs != 3 || two || tn != 1) return nullptr;
-            return exact ? (const void*)rnn_dataflow_kernel<OP, 1, true, false, 3>
-                         : (const void*)rnn_dataflow_kernel<OP, 1, false, false, 3>;
+            return exact ? (const void*)rnn_dataflow_kernel<OP, 1, true, false, 3, false>
+                         : (const void*)rnn_dataflow_kernel<OP, 1, false, false, 3, false>;
         }
         return nullptr;
     }
@@ -803,6 +928,80 @@ cudaError_t dataflow_occupancy_op(int tn, bool exact, bool two, int gs, int thre
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, fn, threads, smem);
+}
+
+// In-cluster exchange instances (one or two rows per thread), instantiated
+// only by the translation units that launch them.
+template <int OP>
+const void* cluster_kernel_ptr(int tn, bool exact, bool two)
+{
+    if constexpr (OP == 1) {
+        if (two) {
+            if (tn == 1) return exact ? (const void*)rnn_dataflow_kernel<OP, 1, true, true, 1, true>
+                                      : (const void*)rnn_dataflow_kernel<OP, 1, false, true, 1, true>;
+            if (tn == 2) return exact ? (const void*)rnn_dataflow_kernel<OP, 2, true, true, 1, true>
+                                      : (const void*)rnn_dataflow_kernel<OP, 2, false, true, 1, true>;
+            return nullptr;
+        }
+    }
+    if (tn == 1) return exact ? (const void*)rnn_dataflow_kernel<OP, 1, true, false, 1, true>
+                              : (const void*)rnn_dataflow_kernel<OP, 1, false, false, 1, true>;
+    if (tn == 2) return exact ? (const void*)rnn_dataflow_kernel<OP, 2, true, false, 1, true>
+                              : (const void*)rnn_dataflow_kernel<OP, 2, false, false, 1, true>;
+    return nullptr;
+}
+
+// Launch configuration of the in-cluster kernel: clusters of unit_groups CTAs
+// (above 8 the non-portable sizes, up to 16).
+template <int OP>
+cudaError_t cluster_config(const void* fn, int ctas, int cluster, int threads, size_t smem, cudaStream_t stream,
+                           cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr)
+{
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (cluster > 8) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3((unsigned)ctas);
+    cfg->blockDim = dim3((unsigned)threads);
+    cfg->dynamicSmemBytes = smem;
+    cfg->stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+    return cudaSuccess;
+}
+
+template <int OP>
+cudaError_t launch_cluster_op(const RecParams& p, bool exact, int threads, size_t smem, cudaStream_t stream)
+{
+    const void* fn = cluster_kernel_ptr<OP>(p.rows_per_thread, exact, OP == 1 && p.lbr == 0);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    cudaError_t e = cluster_config<OP>(fn, p.D * p.ctas_per_dir, p.unit_groups, threads, smem, stream, &cfg, attr);
+    if (e != cudaSuccess) return e;
+    void* args[] = {(void*)&p};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// Clusters of the launch that fit on the device at once (0: none fits).
+template <int OP>
+cudaError_t cluster_occupancy_op(int tn, bool exact, bool two, int ctas, int cluster, int threads, size_t smem,
+                                 int* clusters)
+{
+    const void* fn = cluster_kernel_ptr<OP>(tn, exact, two);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    cudaError_t e = cluster_config<OP>(fn, ctas, cluster, threads, smem, nullptr, &cfg, attr);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveClusters(clusters, fn, &cfg);
 }
 
 }  // namespace rnngb

@@ -24,8 +24,33 @@ cudaError_t recurrent_occupancy_rnn(int, int, int, int, bool, int, size_t, int*)
 cudaError_t recurrent_occupancy_gru(int, int, int, int, bool, int, size_t, int*);
 cudaError_t recurrent_occupancy_lstm(int, int, int, int, bool, int, size_t, int*);
 
+cudaError_t launch_cluster_rnn(const RecParams&, bool, int, size_t, cudaStream_t);
+cudaError_t launch_cluster_gru(const RecParams&, bool, int, size_t, cudaStream_t);
+cudaError_t launch_cluster_lstm(const RecParams&, bool, int, size_t, cudaStream_t);
+cudaError_t cluster_occupancy_rnn(int, bool, bool, int, int, int, size_t, int*);
+cudaError_t cluster_occupancy_gru(int, bool, bool, int, int, int, size_t, int*);
+cudaError_t cluster_occupancy_lstm(int, bool, bool, int, int, int, size_t, int*);
+
+cudaError_t cluster_occupancy(int op, int lbr, int tn, bool exact, int ctas, int cluster, int threads, size_t smem,
+                              int* clusters)
+{
+    const bool two = op == 1 && lbr == 0;
+    switch (op) {
+    case 0: return cluster_occupancy_rnn(tn, exact, two, ctas, cluster, threads, smem, clusters);
+    case 1: return cluster_occupancy_gru(tn, exact, two, ctas, cluster, threads, smem, clusters);
+    default: return cluster_occupancy_lstm(tn, exact, two, ctas, cluster, threads, smem, clusters);
+    }
+}
+
 cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t smem, cudaStream_t s)
 {
+    if (p.kernel == 2 && p.cluster) {
+        switch (p.op) {
+        case 0: return launch_cluster_rnn(p, exact, threads, smem, s);
+        case 1: return launch_cluster_gru(p, exact, threads, smem, s);
+        default: return launch_cluster_lstm(p, exact, threads, smem, s);
+        }
+    }
     switch (p.op) {
     case 0: return launch_recurrent_rnn(p, exact, threads, smem, s);
     case 1: return launch_recurrent_gru(p, exact, threads, smem, s);
@@ -245,6 +270,7 @@ struct Geometry {
     int ustride;      // dataflow: floats per unit of the resident R slice
     int ufast;        // dataflow: compute threads take units fastest (wide row tiles)
     int gs;           // dataflow: gate split (lanes per unit and row)
+    int cluster;      // dataflow: in-cluster exchange of h (each row group one cluster)
 };
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -321,6 +347,29 @@ rnn_status plan_staged(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* 
 // per-CTA flags.  Picks the cheapest feasible shape under a simple cost
 // model (cycles per step: k-loop issue + h/R bytes into the SM + epilogue +
 // a fixed latency for the flags and the first copy).
+// Cycles of one thread's k-loop over H (k ascending, groups of 4 k) with
+// `warps` warps of tn rows x nc gate columns a thread: per group the largest
+// of the busiest scheduler's issue, the shared-memory wavefronts of all
+// warps (about 2.75 per 16-byte warp load with these broadcast patterns,
+// measured) and one warp's dependent issue (about 1.7 cycles an instruction,
+// measured on one warp).
+double kloop_cycles(int64_t H, int warps, int tn, int nc, bool exact)
+{
+    const double instr = (exact ? 2.0 : 1.0) * 4.0 * tn * nc + tn + nc;
+    const double group = std::max({instr * (double)ceil_div(warps, 4), warps * (tn + nc) * 2.75, 1.7 * instr});
+    return (double)H / 4.0 * group;
+}
+
+// In-cluster exchange against the device-wide one, cycles a step beyond the
+// k-loop (fitted to per-step times of both on LSTM, GRU and RNN with hidden
+// 128-512 and batch 1-128): about 5000 in a cluster (fenced remote stores,
+// arrivals, the wait, the epilogue), about 8000 device-wide (publication,
+// counter, tensor copy of h); the cluster's longer per-CTA k-loops ran about
+// 1.3 times the model.
+constexpr double kClusterExchangeCost = 5000.0;
+constexpr double kDeviceExchangeCost = 8000.0;
+constexpr double kClusterKloopScale = 1.3;
+
 // Dataflow planner: cycles charged per piece of a product (a ring slot's
 // wait, release and tensor copies).  Measured on GRU, hidden 2048, batch 4
 // with R streamed: each halving of the piece adds about half a microsecond a
@@ -464,6 +513,96 @@ rnn_status plan_dataflow(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry
     return RNN_OK;
 }
 
+// Dataflow kernel with the in-cluster exchange: each row group of a direction
+// is one cluster of CU <= 16 CTAs that hold all of R between them (resident)
+// and pass h through each other's shared memory; no device-wide counters.
+// Cost (cycles a step): the k-loop as in plan_dataflow, the remote stores
+// of h (every value to every CTA of the cluster) and a fixed exchange.
+rnn_status plan_cluster(rnn_plan* pl, int64_t N, const DeviceInfo& di, Geometry* out, double* cost_out)
+{
+    const int64_t H = pl->H;
+    const int G = pl->G, D = pl->D;
+    const bool exact = pl->mode == RNN_MODE_EXACT;
+    const bool two = pl->op == RNN_OP_GRU && pl->lbr == 0;
+    const int phases = two ? 2 : 1;
+    const size_t smem_cap = (size_t)di.smem_optin - 1024;
+    if (H % 4 != 0 || H > (1 << 20))
+        return fail(RNN_ERR_UNSUPPORTED, "the in-cluster dataflow kernel needs hidden_size a multiple of 4");
+    if (pl->ov_rres == 0 || pl->ov_rres == 2)
+        return fail(RNN_ERR_UNSUPPORTED, "the in-cluster dataflow kernel keeps all of R resident");
+    double best = 1e300;
+    bool found = false;
+    const int cr_auto[6] = {1, 2, 4, 8, 16, 32};
+    const int ncr = pl->ov_rows > 0 ? 1 : 6;
+    for (int cri = 0; cri < ncr; ++cri) {
+        const int CRc = pl->ov_rows > 0 ? pl->ov_rows : cr_auto[cri];
+        const int64_t NRP = round_up(ceil_div(N, CRc), (CRc == 1 && N <= 4) ? 4 : 8);
+        const int CR = (int)ceil_div(N, NRP);
+        if (CR != CRc || NRP > 256) continue;
+        for (int CU = 16; CU >= 1; --CU) {
+            if (pl->ov_units > 0 && CU != pl->ov_units) continue;
+            if (CU > H) continue;
+            const int umax = (int)ceil_div(H, CU);
+            if (ceil_div(H, umax) != CU) continue;                      // a CTA without units
+            const size_t smem = df_cluster_smem_bytes((int)H, umax, G, (int)NRP, two);
+            if (smem > smem_cap) continue;
+            // two rows per thread only when asked for (kernel 5): measured
+            // slower (GRU hidden 256 batch 16: 5.5 vs 3.9 us a step)
+            for (int tn = 1; tn <= (pl->ov_kernel == 5 ? 2 : 1); ++tn) {
+                if (pl->ov_tn > 0 && tn != pl->ov_tn) continue;
+                if (NRP % tn) continue;
+                const int64_t thr = (int64_t)umax * (NRP / tn);
+                if (thr > (tn == 1 ? 224 : 352)) continue;
+                const int compute = (int)round_up(thr, 32);
+                const double kloop = kloop_cycles(H, compute / 32, tn, G, exact) * kClusterKloopScale;
+                const double stores = (double)tn * CU * phases * 8.0;
+                const double cost = kloop + stores + kClusterExchangeCost * phases;
+                if (cost >= best) continue;
+                int clusters = 0;
+                cudaError_t e = cluster_occupancy(pl->op, pl->lbr, tn, exact, D * CR * CU, CU, compute + 32, smem,
+                                                  &clusters);
+                if (e != cudaSuccess) {
+                    cudaGetLastError();
+                    continue;
+                }
+                if (clusters < 1) continue;
+                // clusters beyond those that fit at once run in later waves;
+                // more CTAs than SMs share them
+                const double waves = std::max(std::ceil((double)D * CR / clusters),
+                                              (double)D * CR * CU / di.sms);
+                if (cost * waves >= best) continue;
+                best = cost * waves;
+                found = true;
+                *out = Geometry{};
+                out->kernel = 2;
+                out->cluster = 1;
+                out->units = CU;
+                out->rows = CR;
+                out->ctas = CU * CR;
+                out->quant = 1;
+                out->slots = 1;
+                out->umax = umax;
+                out->tn = tn;
+                out->threads = compute + 32;
+                out->rres = 1;
+                out->smem = smem;
+                out->npad = (int)NRP;
+                out->hpad = (int)round_up(H, kRecKC);
+                out->cpb = (int)ceil_div(H, kRecKC);
+                out->res_chunks = 0;
+                out->ustride = df_unit_stride((int)H, G);
+                out->ufast = 0;
+                out->gs = 1;
+            }
+        }
+    }
+    if (!found)
+        return fail(RNN_ERR_UNSUPPORTED, "no in-cluster dataflow launch fits batch %lld, hidden %lld", (long long)N,
+                    (long long)H);
+    if (cost_out) *cost_out = best;
+    return RNN_OK;
+}
+
 // The tensor-core recurrent kernel keeps h in fp16: it is used only when
 // every h the operator produces is bounded, i.e. the activation that makes h
 // is one of Tanh, Sigmoid, ScaledTanh, HardSigmoid, Softsign (and, for GRU,
@@ -531,6 +670,8 @@ rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, const fl
 {
     if (pl->ov_kernel == 1) return plan_staged(pl, N, di, g);
     if (pl->ov_kernel == 3) return plan_tc(pl, N, di, g);
+    if (pl->ov_kernel == 5 && (uintptr_t)(pl->const_weights ? pl->r_orig_const : R) % 16 != 0)
+        return fail(RNN_ERR_UNSUPPORTED, "the dataflow kernel needs R 16-byte aligned");
     // tensor-core modes: the tensor-core kernel for batches of 32..128 rows
     if ((pl->mode == RNN_MODE_FAST_TF32 || pl->mode == RNN_MODE_FAST_BF16) && pl->ov_kernel == 0 && N >= 32) {
         const std::string saved = g_error;
@@ -544,12 +685,38 @@ rnn_status plan_geometry(rnn_plan* pl, int64_t N, const DeviceInfo& di, const fl
         return plan_staged(pl, N, di, g);
     }
     if (pl->ov_kernel == 2) return plan_dataflow(pl, N, di, g);
+    if (pl->ov_kernel == 5) return plan_cluster(pl, N, di, g, nullptr);
     const int64_t H = pl->H;
     const long long macs = (long long)N * pl->G * H * H;
     if (macs <= 262144 && staged_single_cta_fits(H, N) && pl->ov_units <= 0 && pl->ov_rows <= 0)
         return plan_staged(pl, N, di, g);                          // one CTA per direction
     const std::string saved = g_error;
+    // In-cluster exchange where all of R fits in the shared memory of at most
+    // 16 CTAs per row group, with one row per thread and one product a step,
+    // when the model above puts it below the device-wide exchange.  Measured
+    // (exact, per step): LSTM hidden 128 batch 8 3.0 vs 4.1 us, LSTM 256
+    // batch 4 4.1 vs 5.3, batch 32 4.4 vs 5.2, GRU 256 batch 16 3.8 vs 4.4,
+    // RNN 512 batch 4 4.6 vs 5.4; slower with long per-CTA k-loops (LSTM 384
+    // batch 16: 7.1 vs 6.6) or more clusters than fit at once (LSTM 256 batch
+    // 128); GRU with linear_before_reset = 0 (two exchanges a step) gained
+    // nothing.
+    Geometry cg{};
+    double ccost = 0.0;
+    bool have_cl = false;
+    if (!(pl->op == RNN_OP_GRU && pl->lbr == 0)) {
+        have_cl = plan_cluster(pl, N, di, &cg, &ccost) == RNN_OK;
+        g_error = saved;
+    }
     if (plan_dataflow(pl, N, di, g) == RNN_OK) {
+        if (have_cl) {
+            const int nc = g->gs > 1 ? 1 : pl->G;
+            const double dcost = kloop_cycles(H, (g->threads - 32) / 32, g->tn, nc, pl->mode == RNN_MODE_EXACT) +
+                                 kDeviceExchangeCost;
+            if (ccost < dcost) {
+                *g = cg;
+                return RNN_OK;
+            }
+        }
         // Measured on GB300: the dataflow kernel wins while a CTA's share of a
         // step is small (its per-step latency dominates: 512 to 2048 hidden,
         // a few rows); with more than about a million products per CTA and
@@ -893,6 +1060,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     p.unit_stride = geo.ustride;
     p.unit_fastest = geo.ufast;
     p.gate_split = geo.kernel == 2 && geo.gs > 1 ? geo.gs : 1;
+    p.cluster = geo.kernel == 2 && geo.cluster ? 1 : 0;
     p.XW = xw; p.Rt = rt; p.Rorig = pl->const_weights ? pl->r_orig_const : a.R; p.B = a.B; p.P = a.P; p.h0 = a.h0; p.c0 = a.c0; p.lens = a.lens;
     p.Y = a.Y; p.Yh = a.Yh; p.Yc = a.Yc;
     p.hbuf = (float*)(scratch + L.hb);
@@ -986,7 +1154,7 @@ rnn_status enqueue(rnn_plan* pl, const RunArgs& a, const Geometry& geo, int64_t 
     }
     if (timed) record(pl, 5, a.st);
     pl->g_units = geo.units; pl->g_tn = geo.tn; pl->g_rres = geo.rres; pl->g_rows = geo.rows;
-    pl->g_kernel = geo.kernel; pl->g_threads = geo.threads; pl->g_smem = (int)geo.smem;
+    pl->g_kernel = geo.kernel == 2 && geo.cluster ? 5 : geo.kernel; pl->g_threads = geo.threads; pl->g_smem = (int)geo.smem;
     *launches_out = launches;
     return RNN_OK;
 }
@@ -1156,7 +1324,7 @@ rnn_status rnn_plan_set_launch(rnn_plan_t pl, int unit_groups, int rows_per_thre
 {
     if (!pl) return fail(RNN_ERR_INVALID_ARGUMENT, "plan is NULL");
     if (unit_groups < 0 || rows_per_thread < 0 || r_resident < -1 || r_resident > 2 || row_groups < 0 ||
-        kernel < 0 || kernel > 3)
+        kernel < 0 || kernel > 5 || kernel == 4)
         return fail(RNN_ERR_INVALID_ARGUMENT, "bad launch override");
     if (kernel == 3 && (row_groups > 1 || rows_per_thread > 1))
         return fail(RNN_ERR_INVALID_ARGUMENT, "the tensor-core kernel has one row group and one row per thread");
@@ -1164,6 +1332,8 @@ rnn_status rnn_plan_set_launch(rnn_plan_t pl, int unit_groups, int rows_per_thre
         rows_per_thread != 8)
         return fail(RNN_ERR_INVALID_ARGUMENT, "rows_per_thread must be 0, 1, 2, 4 or 8");
     if (kernel == 1 && row_groups > 1) return fail(RNN_ERR_INVALID_ARGUMENT, "the staged kernel has one row group");
+    if (kernel == 5 && (rows_per_thread > 2 || unit_groups > 16))
+        return fail(RNN_ERR_INVALID_ARGUMENT, "the in-cluster kernel takes 1 or 2 rows per thread and <= 16 unit groups");
     pl->ov_units = unit_groups;
     pl->ov_tn = rows_per_thread;
     pl->ov_rres = r_resident;

@@ -53,6 +53,7 @@ struct RecParams {
     int unit_stride;             // dataflow kernel: floats per unit of the resident R slice
     int unit_fastest;            // dataflow kernel: compute thread t takes unit t % umax and row tile t / umax
     int gate_split;              // dataflow kernel: lanes per (unit, row tile), each with G / gate_split gates
+    int cluster;                 // dataflow kernel: each row group is one cluster exchanging h in shared memory
                                  // (else row tile t % tiles, unit t / tiles)
 
     // tensors
@@ -169,6 +170,15 @@ __host__ __device__ inline size_t df_hslot_bytes(int npad, int cpb)
 // resident, in full or its leading res_chunks 32-k chunks + a ring of
 // streamed R pieces unless all of R is resident + a ring of h pieces; a slot
 // holds one piece of cpb chunks).
+// Dataflow kernel with the in-cluster exchange: slack + resident R + two h
+// buffers (three with r (.) h), each one row group's exchange block.
+inline size_t df_cluster_smem_bytes(int H, int umax, int G, int npad, bool two)
+{
+    const size_t rres = (((size_t)umax * df_unit_stride(H, G) * 4 + 127) / 128) * 128;
+    const size_t blk = (((size_t)npad * ((H + kRecKC - 1) / kRecKC) * kDfPitch * 4 + 127) / 128) * 128;
+    return 128 + rres + (two ? 3 : 2) * blk;
+}
+
 inline size_t df_smem_bytes(int H, int umax, int G, int npad, int r_resident, int cpb, int slots,
                             int res_chunks = 0)
 {
@@ -191,6 +201,9 @@ cudaError_t launch_recurrent(const RecParams& p, bool exact, int threads, size_t
                              cudaStream_t stream);
 cudaError_t recurrent_occupancy(int op, int lbr, int kernel, int rows_per_thread, bool exact, int threads,
                                 size_t smem, int* blocks_per_sm, int gate_split = 1);
+// In-cluster dataflow launches: clusters of `cluster` CTAs that fit at once.
+cudaError_t cluster_occupancy(int op, int lbr, int rows_per_thread, bool exact, int ctas, int cluster, int threads,
+                              size_t smem, int* clusters);
 
 // Input projection XW[M][ncols] = X[M][K] . Bt[K][ncols].  A wait of the
 // tensor-copy loader that gives up writes RNN_ERR_TIMEOUT to *status.

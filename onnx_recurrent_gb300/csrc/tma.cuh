@@ -96,4 +96,52 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
 // async-proxy (tensor copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+// ---- thread-block clusters: distributed shared memory
+__device__ __forceinline__ unsigned cluster_rank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared variable in the CTA of cluster rank `rank`.
+__device__ __forceinline__ unsigned cluster_map(unsigned local_addr, unsigned rank)
+{
+    unsigned a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local_addr), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ void st_cluster_f32(unsigned addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// One arrival (release, cluster scope) on an mbarrier of a CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(unsigned remote_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+// One non-blocking test of an mbarrier phase, acquiring at cluster scope
+// (the writes that peers made before their arrivals become visible).
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, unsigned parity)
+{
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Every thread of every CTA of the cluster meets (release / acquire).
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 }  // namespace rnngb

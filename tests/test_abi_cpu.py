@@ -93,6 +93,10 @@ def test_set_launch_validation(lib):
         orc.rnn_plan_set_launch(p, 4, 1, -2)
     orc.rnn_plan_set_launch(p, 4, 1, 2)      # partly resident (dataflow kernel)
     orc.rnn_plan_set_launch(p, 4, 2, 0)
+    orc.rnn_plan_set_launch(p, 16, 2, -1, 2, 5)   # in-cluster exchange
+    for bad in [(4, 1, -1, 0, 4), (4, 4, -1, 0, 5), (17, 1, -1, 0, 5), (4, 1, -1, 0, 6)]:
+        with pytest.raises(rb.RNNError):
+            orc.rnn_plan_set_launch(p, *bad)
     with pytest.raises(rb.RNNError):
         orc.rnn_plan_set_mode(p, 9)
     orc.rnn_plan_set_mode(p, "fast")

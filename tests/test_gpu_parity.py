@@ -185,7 +185,36 @@ def test_dataflow_kernel_partly_resident_r(op, lbr, launch):
             assert float(np.abs(g.astype(np.float64) - r.astype(np.float64)).max(initial=0.0)) <= 1e-5
 
 
-@pytest.mark.parametrize("g", [(2, 1, 0, 0, 1), (5, 2, 1, 0, 1), (4, 1, 1, 2, 2), (3, 2, 0, 1, 2)])
+# Dataflow kernel with the in-cluster exchange (kernel 5): each row group of
+# a direction is one thread-block cluster of 1-16 CTAs holding all of R; h
+# (and r (.) h) passes through the CTAs' shared memory.  One or two rows per
+# thread, one or two row groups, ragged unit splits.
+@pytest.mark.parametrize("op,lbr,H,launch", [("LSTM", 0, 128, (8, 2, -1, 1, 5)), ("LSTM", 0, 256, (16, 1, -1, 2, 5)),
+                                             ("LSTM", 0, 256, (8, 2, -1, 1, 5)), ("GRU", 0, 256, (9, 2, -1, 2, 5)),
+                                             ("GRU", 1, 256, (16, 2, -1, 2, 5)), ("RNN", 0, 512, (12, 2, -1, 2, 5)),
+                                             ("GRU", 0, 64, (1, 2, -1, 2, 5))])
+def test_cluster_exchange(op, lbr, H, launch):
+    c = make_case(op, "bidirectional", 7, 11, 40, H, seed=46, with_P=True, h0_scale=0.5, c0_scale=0.5,
+                  lens=("uniform", 0, 7), linear_before_reset=lbr, clip=2.0)
+    Y, Yh, Yc, plan = gpu_case(c, "exact", launch=launch, keep_plan=True)
+    got = orc.rnn_plan_get_launch(plan)
+    orc.rnn_plan_destroy(plan)
+    assert got["kernel"] == 5 and got["unit_groups"] == launch[0]
+    ref = oracle_case(c)
+    _compare_exact(c, (Y, Yh, Yc), ref, f"{op} lbr {lbr} H {H} {launch}")
+    for g, r in zip(gpu_case(c, "fast", launch=launch), ref):
+        if g is not None:
+            assert float(np.abs(g.astype(np.float64) - r.astype(np.float64)).max(initial=0.0)) <= 1e-5
+
+
+def test_cluster_exchange_refuses_streamed_r():
+    c = make_case("LSTM", "forward", 3, 4, 8, 64, seed=3)
+    with pytest.raises(orc.RNNError) as e:
+        gpu_case(c, "exact", launch=(4, 1, 0, 1, 5))
+    assert e.value.status == 3
+
+
+@pytest.mark.parametrize("g", [(2, 1, 0, 0, 1), (5, 2, 1, 0, 1), (4, 1, 1, 2, 2), (3, 2, 0, 1, 2), (4, 1, -1, 1, 5)])
 def test_fast_mode_is_geometry_independent(g):
     c = make_case("LSTM", "bidirectional", 6, 9, 20, 36, seed=5, with_P=True, h0_scale=0.5)
     a = gpu_case(c, "fast", launch=(1, 1, 1, 0, 1))

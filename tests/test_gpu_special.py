@@ -63,7 +63,8 @@ FINITE_EDGES = np.where(np.isfinite(EDGES) & (np.abs(EDGES) < 1e3), EDGES, F(0.7
 # (unit_groups, rows_per_thread, r_resident, row_groups, kernel): the planner's
 # choice, the staged kernel with one and with several CTAs, streamed R, and the
 # dataflow kernel with resident and streamed R, one row per thread or a tile
-# of four rows (units fastest across the lanes, rows ranked by length).
+# of four rows (units fastest across the lanes, rows ranked by length), and
+# the dataflow kernel exchanging h inside a cluster of 4 or 7 CTAs.
 KERNELS = {
     "planner": None,
     "staged-1cta": (1, 1, 1, 0, 1),
@@ -72,6 +73,8 @@ KERNELS = {
     "dataflow": (4, 1, 1, 1, 2),
     "dataflow-streamed": (3, 1, 0, 1, 2),
     "dataflow-wide": (3, 4, 0, 1, 2),
+    "cluster": (4, 1, -1, 1, 5),
+    "cluster-2rows": (7, 2, -1, 0, 5),
 }
 
 # (op, direction, activations, alpha, beta, lbr, input_forget)
