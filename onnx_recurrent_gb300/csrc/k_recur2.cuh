@@ -86,12 +86,13 @@ __device__ __forceinline__ int unit_begin(int cu, int CU, int H, int quant)
 struct DfCtx {
     int d, cu, cr, H, HP, G, GH, CU, CR, u0, U, umax, ugs, NR, NRP, nchunks, cpb, npieces, slots;
     int KR;           // k of each gate row held resident: H, or the leading res_chunks * 32 (0: none)
+    int KRP;          // floats between a unit's resident gate rows
     int rpieces;      // pieces whose R is resident (the leading ones); the others stream
     int ctid, ncompute, ul, rb;
     int gi;           // gate split: this thread's share of the gate columns (0: all, or the first share)
     bool active;      // takes part in the products
     bool lead;        // owns the (unit, row tile): gate arithmetic, state, stores
-    float* Rs;        // resident R: [umax][ugs] floats (unit-major, gate rows of KR k)
+    float* Rs;        // resident R: [umax][ugs] floats (unit-major, gate rows of KR k, KRP apart)
     char* Rring;      // streamed R: slots x rslot bytes, each cpb chunks of [G][umax][36]
     char* Hring;      // slots x hslot bytes, each [cpb][NRP][36] (padded to 128 bytes)
     int rslot, rsub, hslot; // bytes per slot (one piece: cpb chunks of 32 k), per R chunk
@@ -105,19 +106,59 @@ struct DfCtx {
 // group's block in it; every producer of the row group must have published
 // `target` times before the block may be read.  Streamed R pieces bring the
 // ng gate rows from gate g0 on that the product uses (`rmap` has a box of ng
-// gates); they land from the start of each chunk's sub-block.  Every lane polls the row
-// group's counter (acquire loads); a proxy fence then orders the
-// generic-proxy writes that the acquire made visible before the tensor
-// copies (async proxy) that read them.
+// gates); they land from the start of each chunk's sub-block.
 __device__ __forceinline__ bool load_product(const RecParams& p, const DfCtx& x, const CUtensorMap* map, int z,
                                              unsigned target, const unsigned* counter, unsigned& q,
                                              volatile int* abort_flag, int lane, const CUtensorMap* rmap, int g0,
                                              int ng)
 {
+    // One tensor copy of h per piece of cpb chunks (a box of many small
+    // copies lands one after another, a few large boxes land together), and
+    // for a streamed piece one of R per chunk.  Pieces are issued by the
+    // lanes in parallel, lane j taking piece base + j, in groups no larger
+    // than the ring (so no two lanes share a slot).  R does not depend on h:
+    // the first group claims its slots and starts its R copies before the
+    // wait for the producers, so they run during the exchange.
+    const unsigned hbytes = (unsigned)x.NRP * x.cpb * (kDfPitch * 4u);
+    const int gsz = min(32, x.slots);
+    auto claim = [&](int base, int nmine) -> bool {   // wait for the slots, expect the bytes, copy R
+        const bool mine = lane < nmine;
+        const unsigned qq = q + (unsigned)lane;
+        const int slot = (int)(qq % (unsigned)x.slots);
+        const unsigned round = qq / (unsigned)x.slots;
+        bool ok = true;
+        if (mine) ok = mbar_wait(&x.empty[slot], (round & 1u) ^ 1u, p.status, abort_flag, p.spin_limit_ns);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        if (mine) {
+            const int c0 = (base + lane) * x.cpb;           // first chunk of the piece
+            const int nc = min(x.cpb, x.nchunks - c0);      // R chunks to copy (h: the whole box)
+            const bool rstream = base + lane >= x.rpieces;
+            const unsigned rbytes = rstream ? (unsigned)(nc * ng * x.umax) * (kDfPitch * 4u) : 0u;
+            mbar_arrive_expect_tx(&x.full[slot], hbytes + rbytes);
+            if (rstream)
+                for (int cl = 0; cl < nc; ++cl)
+                    tma_load_4d(x.Rring + (size_t)slot * x.rslot + (size_t)cl * x.rsub, rmap, (c0 + cl) * kRecKC,
+                                x.u0, g0, x.d, &x.full[slot]);
+        }
+        return true;
+    };
+    auto copy_h = [&](int base, int nmine) {
+        if (lane < nmine) {
+            const int slot = (int)((q + (unsigned)lane) % (unsigned)x.slots);
+            tma_load_4d(x.Hring + (size_t)slot * x.hslot, map, 0, 0, (base + lane) * x.cpb, z, &x.full[slot]);
+        }
+    };
+    const int pre = min(gsz, x.npieces);
+    if (!claim(0, pre)) return false;
     if (target > 0) {
         // This CTA's own publication comes first (the counter cannot be
         // complete before it); waiting for it on the mbarrier keeps the
-        // loader off the memory pipe while the compute warps work.
+        // loader off the memory pipe while the compute warps work.  Every
+        // lane then polls the row group's counter (acquire loads); a proxy
+        // fence orders the generic-proxy writes that the acquire made
+        // visible before the tensor copies (async proxy) that read them.
+        const unsigned qa = q;
+        q += (unsigned)pre;   // armed: the exit wait covers these slots
         if (!mbar_wait(x.pub, (target - 1u) & 1u, p.status, abort_flag, p.spin_limit_ns)) return false;
         const unsigned need = target * (unsigned)x.CU;
         bool ready = ld_acquire_u32(counter) >= need;
@@ -145,34 +186,14 @@ __device__ __forceinline__ bool load_product(const RecParams& p, const DfCtx& x,
         __syncwarp();
         fence_proxy_async_global();
         __syncwarp();
+        q = qa;
     }
-    // One tensor copy per piece of cpb chunks: a box of many small copies
-    // lands one after another, a few large boxes land together.  Pieces are
-    // issued by the lanes in parallel, lane j taking piece base + j, in
-    // groups no larger than the ring (so no two lanes share a slot).
-    const int gsz = min(32, x.slots);
-    for (int base = 0; base < x.npieces; base += gsz) {
+    copy_h(0, pre);
+    q += (unsigned)pre;
+    for (int base = pre; base < x.npieces; base += gsz) {
         const int nmine = min(gsz, x.npieces - base);
-        const bool mine = lane < nmine;
-        const unsigned qq = q + (unsigned)lane;
-        const int slot = (int)(qq % (unsigned)x.slots);
-        const unsigned round = qq / (unsigned)x.slots;
-        bool ok = true;
-        if (mine) ok = mbar_wait(&x.empty[slot], (round & 1u) ^ 1u, p.status, abort_flag, p.spin_limit_ns);
-        if (!__all_sync(0xffffffffu, ok)) return false;
-        if (mine) {
-            const int c0 = (base + lane) * x.cpb;           // first chunk of the piece
-            const int nc = min(x.cpb, x.nchunks - c0);      // R chunks to copy (h: the whole box)
-            const unsigned hbytes = (unsigned)x.NRP * x.cpb * (kDfPitch * 4u);
-            const bool rstream = base + lane >= x.rpieces;
-            const unsigned rbytes = rstream ? (unsigned)(nc * ng * x.umax) * (kDfPitch * 4u) : 0u;
-            mbar_arrive_expect_tx(&x.full[slot], hbytes + rbytes);
-            tma_load_4d(x.Hring + (size_t)slot * x.hslot, map, 0, 0, c0, z, &x.full[slot]);
-            if (rstream)
-                for (int cl = 0; cl < nc; ++cl)
-                    tma_load_4d(x.Rring + (size_t)slot * x.rslot + (size_t)cl * x.rsub, rmap, (c0 + cl) * kRecKC,
-                                x.u0, g0, x.d, &x.full[slot]);
-        }
+        if (!claim(base, nmine)) return false;
+        copy_h(base, nmine);
         q += (unsigned)nmine;
     }
     return true;
@@ -259,9 +280,9 @@ __device__ __forceinline__ bool consume_product(const RecParams& p, const DfCtx&
             const int hstep = x.NRP * kDfPitch * 4;
             const char* rp[NC];
             if (pc < x.rpieces) {
-                const float* rbase = x.Rs + (size_t)x.ul * x.ugs + (size_t)col_off * x.KR + k0;
+                const float* rbase = x.Rs + (size_t)x.ul * x.ugs + (size_t)col_off * x.KRP + k0;
 #pragma unroll
-                for (int g = 0; g < NC; ++g) rp[g] = reinterpret_cast<const char*>(rbase + (size_t)g * x.KR);
+                for (int g = 0; g < NC; ++g) rp[g] = reinterpret_cast<const char*>(rbase + (size_t)g * x.KRP);
                 df_piece<TN, NC, EXACT, true>(hp, hstep, rp, kRecKC * 4, ngroups, acc);
             } else {
                 const char* rbox = x.Rring + (size_t)slot * x.rslot;
@@ -359,10 +380,10 @@ __device__ __forceinline__ void cl_product(const DfCtx& x, const char* hbox, int
     const char* hp[TN];
 #pragma unroll
     for (int i = 0; i < TN; ++i) hp[i] = hbox + (size_t)(x.rb * TN + i) * (kDfPitch * 4);
-    const float* rbase = x.Rs + (size_t)x.ul * x.ugs + (size_t)col_off * x.KR;
+    const float* rbase = x.Rs + (size_t)x.ul * x.ugs + (size_t)col_off * x.KRP;
     const char* rp[NC];
 #pragma unroll
-    for (int g = 0; g < NC; ++g) rp[g] = reinterpret_cast<const char*>(rbase + (size_t)g * x.KR);
+    for (int g = 0; g < NC; ++g) rp[g] = reinterpret_cast<const char*>(rbase + (size_t)g * x.KRP);
     df_piece<TN, NC, EXACT, true>(hp, x.NRP * kDfPitch * 4, rp, kRecKC * 4, (x.H + 3) / 4, acc);
 }
 
@@ -440,6 +461,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     x.rslot = p.r_resident ? 0 : x.cpb * x.rsub;
     // R resident in full, or its leading res_chunks 32-k chunks (whole pieces)
     x.KR = p.r_resident ? p.H : p.res_chunks * kRecKC;
+    x.KRP = df_gate_stride(x.KR);
     x.rpieces = p.r_resident ? x.npieces : p.res_chunks / x.cpb;
     x.ncompute = blockDim.x - 32;
     x.ctid = (int)threadIdx.x - 32;
@@ -509,7 +531,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
     // CL: every peer's barriers are initialised before any arrival on them
     if constexpr (CL) cluster_sync_all();
     if (x.KR > 0 && threadIdx.x < 32) {
-        // R[d][g*H + u][k] -> Rs[(u - u0) * ugs + g*KR + k], k < KR: one bulk copy of
+        // R[d][g*H + u][k] -> Rs[(u - u0) * ugs + g*KRP + k], k < KR: one bulk copy of
         // a row of KR floats per (unit, gate), all completing on s_rfill
         // (H is a multiple of 4 and ugs*4 of 16, so every copy is 16-byte
         // aligned at both ends)
@@ -522,7 +544,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
         if (CL && lane == 0) bulk_g2s(clbuf(0), hblock(0), hb0, &s_rfill);
         for (int j = lane; j < x.U * G; j += 32) {
             const int ul = j / G, g = j - ul * G;
-            bulk_g2s(x.Rs + (size_t)ul * x.ugs + (size_t)g * x.KR, src + ((size_t)g * p.H + x.u0 + ul) * p.H,
+            bulk_g2s(x.Rs + (size_t)ul * x.ugs + (size_t)g * x.KRP, src + ((size_t)g * p.H + x.u0 + ul) * p.H,
                      (unsigned)x.KR * 4u, &s_rfill);
         }
     }

@@ -139,12 +139,16 @@ inline size_t rec_smem_bytes(int H, int umax, int G, int npad, int res_chunks)
     return rres + rring + hbytes;
 }
 
-// Dataflow kernel: floats per unit of the resident R slice (G rows of H,
-// padded so that consecutive units start 16 bytes apart modulo the 128-byte
-// bank window: conflict-free 16-byte loads across units).
-inline int df_unit_stride(int H, int G)
+// Dataflow kernel: floats between the gate rows of a unit in the resident R
+// slice (rows of kr k, 12 floats apart modulo the 32 banks, so the lanes of
+// a gate-split group, one gate each, read different banks), and per unit
+// (G rows, padded so that consecutive units start 16 bytes apart modulo the
+// 128-byte bank window: conflict-free 16-byte loads across units).
+constexpr int kDfGatePad = 12;
+__host__ __device__ inline int df_gate_stride(int kr) { return kr + kDfGatePad; }
+inline int df_unit_stride(int kr, int G)
 {
-    const int gh = G * H;
+    const int gh = G * df_gate_stride(kr);
     return gh + (((4 - gh) % 32) + 32) % 32;
 }
 
