@@ -596,6 +596,8 @@ def run_ours(args, ws, rank, local):
     dominant = max(avg, key=avg.get)
 
     traffic_name = args.workload + (f"-lbr{args.lbr}" if args.lbr else "")   # the workload as profiles name it
+    if isinstance(job, StackJob) and not job.wavefront():
+        traffic_name += "-layers"      # a stack run layer by layer (its launches summed), not its wavefront
 
     def roof(kernel):
         ms = avg[kernel]
@@ -619,8 +621,9 @@ def run_ours(args, ws, rank, local):
                     "kernel": "rnn_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": rec_flops,
                     "peak_note": "of measured bf16 burst (fp16 operands, same nominal rate)"}
         if kernel == "recurrence":
-            name = {2: "rnn_dataflow_kernel", 4: "rnn_wavefront_kernel"}.get(geometry.get("kernel"),
-                                                                            "rnn_recurrent_kernel")
+            # kernel 5: the dataflow kernel's in-cluster instance (same name)
+            name = {2: "rnn_dataflow_kernel", 4: "rnn_wavefront_kernel",
+                    5: "rnn_dataflow_kernel"}.get(geometry.get("kernel"), "rnn_recurrent_kernel")
             traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel))
             sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm)
                   if isinstance(job, SequenceJob) else None)
