@@ -2,7 +2,7 @@
 oracle's rnn_io: X, initial_h, initial_c given in the 2-byte type and Y,
 Y_h, Y_c written in it, the arithmetic fp32.  EXACT mode is compared bit for
 bit (the fp32 result is the oracle's, rounded once to nearest even), on the
-staged and the dataflow kernels, with sequence_lens, the masked tail, the
+staged and the dataflow kernels (the latter also with the in-cluster exchange), with sequence_lens, the masked tail, the
 zero-size path and the static-scratch entry point; the tensor-core modes
 within their bound plus one unit in the last place of the output type."""
 import numpy as np
@@ -105,8 +105,9 @@ def test_random_exact_io_bits(io, seed):
 
 
 @pytest.mark.parametrize("io", IOS)
-@pytest.mark.parametrize("launch", [(0, 0, -1, 0, 1), (0, 0, -1, 0, 2), (3, 2, 0, 0, 1), (3, 1, 0, 2, 2)],
-                         ids=["staged", "dataflow", "staged-streamed", "dataflow-streamed"])
+@pytest.mark.parametrize("launch", [(0, 0, -1, 0, 1), (0, 0, -1, 0, 2), (3, 2, 0, 0, 1), (3, 1, 0, 2, 2),
+                                    (6, 0, -1, 0, 5)],
+                         ids=["staged", "dataflow", "staged-streamed", "dataflow-streamed", "cluster"])
 @pytest.mark.parametrize("op", ["GRU", "LSTM"])
 def test_each_kernel_writes_the_io_type(io, launch, op):
     # lengths below seq: the masked tail and the per-row freeze both write 2-byte zeros

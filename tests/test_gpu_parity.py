@@ -207,6 +207,29 @@ def test_cluster_exchange(op, lbr, H, launch):
             assert float(np.abs(g.astype(np.float64) - r.astype(np.float64)).max(initial=0.0)) <= 1e-5
 
 
+# The in-cluster exchange across the attribute space: one direction or both,
+# layouts 0 and 1, named activations with their alpha / beta, clip,
+# input_forget, GRU's two products, lengths with empty rows.
+@pytest.mark.parametrize("op,direction,layout,attrs", [
+    ("LSTM", "forward", 1, dict(activations=["HardSigmoid", "LeakyRelu", "ScaledTanh"], alpha=[0.25, 0.05, 1.5],
+                                beta=[0.45, 0.8], input_forget=1, clip=3.0)),
+    ("GRU", "reverse", 0, dict(activations=["HardSigmoid", "Softsign"], alpha=[0.2], beta=[0.5],
+                               linear_before_reset=0)),
+    ("GRU", "bidirectional", 1, dict(linear_before_reset=1, clip=1.5)),
+    ("RNN", "bidirectional", 1, dict(activations=["Relu", "Elu"], alpha=[0.7])),
+])
+def test_cluster_exchange_attributes(op, direction, layout, attrs):
+    c = make_case(op, direction, 6, 9, 20, 96, seed=47, layout=layout, with_P=True, h0_scale=0.5,
+                  c0_scale=0.5, lens=[6, 0, 3, 6, 1, 5, 6, 2, 4], **attrs)
+    ref = oracle_case(c)
+    for launch in [(12, 0, -1, 0, 5), (5, 2, -1, 2, 5)]:
+        Y, Yh, Yc, plan = gpu_case(c, "exact", launch=launch, keep_plan=True)
+        got = orc.rnn_plan_get_launch(plan)
+        orc.rnn_plan_destroy(plan)
+        assert got["kernel"] == 5 and got["unit_groups"] == launch[0]
+        _compare_exact(c, (Y, Yh, Yc), ref, f"{op} {direction} layout {layout} {launch}")
+
+
 def test_cluster_exchange_refuses_streamed_r():
     c = make_case("LSTM", "forward", 3, 4, 8, 64, seed=3)
     with pytest.raises(orc.RNNError) as e:
