@@ -761,7 +761,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 if (fixed_acts) epi_r(std::true_type{});
                 else epi_r(std::false_type{});
                 if constexpr (CL) {
-                    cl_publish(x, &s_rhready, true);
+                    cl_publish(x, &s_rhready, !(skip_first && s == 0));
                     cl_wait(&s_rhready, (unsigned)s & 1u, p.status, &s_abort, p.spin_limit_ns);
                 } else if (!publish(x, counter, &s_abort, skip_first && s == 0)) {
                     return;
@@ -798,7 +798,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
                 };
                 if (fixed_acts) epi(std::true_type{});
                 else epi(std::false_type{});
-                if constexpr (CL) cl_publish(x, &s_hready[(s + 1) & 1], cl_send);
+                if constexpr (CL) cl_publish(x, &s_hready[(s + 1) & 1], cl_send && !(skip_first && s == 0));
                 else if (!publish(x, counter, &s_abort, false)) return;
             }
         } else {
@@ -879,7 +879,7 @@ __global__ void __launch_bounds__(DfBounds<TN>::threads, 1) rnn_dataflow_kernel(
             };
             if (fixed_acts) epi(std::true_type{});
             else epi(std::false_type{});
-            if constexpr (CL) cl_publish(x, &s_hready[(s + 1) & 1], cl_send);
+            if constexpr (CL) cl_publish(x, &s_hready[(s + 1) & 1], cl_send && !(skip_first && s == 0));
             else if (!publish(x, counter, &s_abort, skip_first && s == 0)) return;
         }
     }

@@ -291,11 +291,13 @@ def test_invalid_lengths_write_nothing():
     orc.rnn_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("kernel,lbr", [(1, 0), (2, 0), (2, 1)])
+@pytest.mark.parametrize("kernel,lbr", [(1, 0), (2, 0), (2, 1), (5, 0), (5, 1)])
 def test_barrier_timeout_is_reported_and_the_device_stays_usable(kernel, lbr):
-    # One CTA withholds its first arrival (staged kernel) or its first flag
-    # (dataflow kernel); every wait is bounded (50 ms here), so the grid exits
-    # and the status says TIMEOUT.
+    # One CTA withholds its first arrival (staged kernel), its first flag
+    # (dataflow kernel) or its first arrivals on its cluster peers' barriers
+    # (in-cluster exchange); every wait is bounded (50 ms here), so the grid
+    # exits (a cluster only after all its CTAs have met) and the status says
+    # TIMEOUT.
     op = "LSTM" if lbr == 0 else "GRU"
     c = make_case(op, "forward", 5, 4, 8, 64, seed=9, h0_scale=0.5, linear_before_reset=lbr)
     plan = orc.rnn_plan_create(op, "forward", 64, 8, linear_before_reset=lbr)
