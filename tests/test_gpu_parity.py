@@ -329,13 +329,16 @@ def test_timing_and_launch_count():
 
 CONCURRENT = {
     # recurrent grids that fill the GPU: the staged kernel, the dataflow
-    # kernel, the tensor-core kernel
+    # kernel, the tensor-core kernel; and clusters of the in-cluster exchange
     "staged": (dict(op="GRU", direction="bidirectional", seq=24, batch=64, input_size=32, hidden_size=1024,
                     lens=("uniform", 1, 24)), "exact", 1),
     "dataflow": (dict(op="LSTM", direction="forward", seq=24, batch=32, input_size=32, hidden_size=512,
                       with_P=True), "exact", 2),
     "tensor_core": (dict(op="GRU", direction="bidirectional", seq=24, batch=64, input_size=32, hidden_size=512,
                          linear_before_reset=1), "tf32", 3),
+    # the in-cluster exchange (the planner's choice here: 4 clusters of 16 CTAs)
+    "cluster": (dict(op="LSTM", direction="forward", seq=24, batch=32, input_size=32, hidden_size=256,
+                     with_P=True), "exact", 5),
 }
 
 
