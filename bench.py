@@ -193,6 +193,12 @@ def live_rows_per_step(case):
     return [int((L > s).sum()) for s in range(steps)]
 
 
+# Dependent-issue latency of an FP32 add or fused multiply-add on one
+# accumulator (cycles): 4 nominal; 4.24 measured on this GPU by a chain of
+# 8192 dependent adds in one warp (the chain bound below uses 4).
+FP32_CHAIN_CYCLES = 4.0
+
+
 def step_roofline(case, mode, rec_ms, sms, clock_mhz, l2_gbs, smem_per_sm):
     """The recurrent kernel's per-step roofline (per launch): every step takes
     at least the largest of
@@ -202,7 +208,11 @@ def step_roofline(case, mode, rec_ms, sms, clock_mhz, l2_gbs, smem_per_sm):
             over SMs * 128 bytes per clock;
       l2    the part of R that cannot stay resident in the SMs' shared memory
             (D * 4 * G * H^2 - SMs * smem_per_sm, if positive), streamed from L2
-            every step, over the measured L2 copy bandwidth.
+            every step, over the measured L2 copy bandwidth;
+      chain every output is one accumulator over k = 0..H-1 in order (exact
+            and fast mode alike), H dependent adds a step (2H for GRU with
+            linear_before_reset = 0, whose second product needs the first's
+            result) at FP32_CHAIN_CYCLES each.
     Returns the terms per step (microseconds, averaged over the steps), the
     binding term, the roofline time of the launch and its fraction of the
     measured time."""
@@ -215,22 +225,26 @@ def step_roofline(case, mode, rec_ms, sms, clock_mhz, l2_gbs, smem_per_sm):
     streamed = max(0.0, r_bytes - float(sms) * smem_per_sm)
     t_smem = r_bytes / smem_bw
     t_l2 = streamed / (l2_gbs * 1e9) if l2_gbs else 0.0
-    roof, terms = 0.0, {"alu": 0.0, "smem": 0.0, "l2": 0.0}
+    two = case.op == "GRU" and case.linear_before_reset == 0
+    t_chain = (2 if two else 1) * H * FP32_CHAIN_CYCLES / clock
+    roof, terms = 0.0, {"alu": 0.0, "smem": 0.0, "l2": 0.0, "chain": 0.0}
     for n in live:
         t_alu = 2.0 * n * D * G * H * H / alu_peak
-        roof += max(t_alu, t_smem, t_l2)
+        roof += max(t_alu, t_smem, t_l2, t_chain)
         terms["alu"] += t_alu
         terms["smem"] += t_smem
         terms["l2"] += t_l2
+        terms["chain"] += t_chain
     steps = max(1, len(live))
     binding = max(terms, key=terms.get)
     return {"terms_us_per_step": {k: round(v / steps * 1e6, 4) for k, v in terms.items()},
             "binding": binding, "steps": len(live), "roof_ms": round(roof * 1e3, 5),
             "measured_ms": round(rec_ms, 5), "frac": round(roof * 1e3 / rec_ms, 4) if rec_ms else 0.0,
             "peaks": {"alu_tflops": round(alu_peak / 1e12, 3), "smem_tbs": round(smem_bw / 1e12, 3),
-                      "l2_gbs": round(l2_gbs, 1) if l2_gbs else None,
+                      "l2_gbs": round(l2_gbs, 1) if l2_gbs else None, "chain_cycles": FP32_CHAIN_CYCLES,
                       "note": "alu and smem derived (SMs x 128 lanes or bytes per clock x max SM clock); "
-                              "l2 measured by an elementwise kernel over a buffer pair that fits in L2"},
+                              "l2 measured by an elementwise kernel over a buffer pair that fits in L2; "
+                              "chain: H dependent FP32 adds a step at the pipe's latency"},
             "r_bytes_per_step": r_bytes, "r_streamed_bytes_per_step": streamed}
 
 
@@ -627,6 +641,19 @@ def run_ours(args, ws, rank, local):
             traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel))
             sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm)
                   if isinstance(job, SequenceJob) else None)
+            if sr and sr["binding"] == "chain":
+                # each output's dependent adds bound the step: their rate
+                # against one add per FP32_CHAIN_CYCLES at the SM clock
+                adds = (sr["terms_us_per_step"]["chain"] * 1e-6 * clock_mhz * 1e6 / FP32_CHAIN_CYCLES) * sr["steps"]
+                rate = adds / (ms / 1e3) if ms else 0.0
+                peak = clock_mhz * 1e6 / FP32_CHAIN_CYCLES
+                return {"bound": "latency", "achieved": round(rate / 1e6, 2), "peak": round(peak / 1e6, 2),
+                        "unit": "M dependent adds/s per output", "frac": sr["frac"], "traffic": traffic,
+                        "kernel": name, "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": rec_flops,
+                        "step_roofline": sr,
+                        "peak_note": f"one FP32 add (or fused multiply-add) per {FP32_CHAIN_CYCLES:.0f} cycles "
+                                     f"on each output's chain (k ascending) at {clock_mhz:.0f} MHz; frac is the "
+                                     "step roofline's (per-step max of the ALU, shared-memory, L2 and chain terms)"}
             if sr and sr["binding"] == "l2":
                 # R does not fit in the SMs' shared memory and its streamed part
                 # bounds the step: bytes from L2 against the measured L2 copy rate

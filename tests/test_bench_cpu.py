@@ -93,12 +93,17 @@ def test_step_roofline_terms():
     assert sr["terms_us_per_step"]["alu"] == pytest.approx(alu_us, rel=1e-3)
     assert sr["terms_us_per_step"]["smem"] == pytest.approx(smem_us, rel=1e-3)
     assert sr["terms_us_per_step"]["l2"] == 0.0 and sr["r_streamed_bytes_per_step"] == 0.0
-    assert sr["binding"] == "alu"
-    assert sr["roof_ms"] == pytest.approx(64 * max(alu_us, smem_us) / 1e3, rel=1e-3)
+    # 512 dependent fused multiply-adds per output and step (0.99 us) bind
+    # before the fused ALU peak (0.83 us) in fast mode
+    chain_us = 512 * bench.FP32_CHAIN_CYCLES / 2070e6 * 1e6
+    assert sr["terms_us_per_step"]["chain"] == pytest.approx(chain_us, rel=1e-3)
+    assert sr["binding"] == "chain"
+    assert sr["roof_ms"] == pytest.approx(64 * max(alu_us, smem_us, chain_us) / 1e3, rel=1e-3)
     assert sr["frac"] == pytest.approx(sr["roof_ms"] / 1.0, rel=1e-3)
-    # exact mode halves the ALU peak (no fused multiply-add)
+    # exact mode halves the ALU peak (no fused multiply-add): the ALU binds
     ex = bench.step_roofline(c, "exact", 1.0, 152, 2070.0, 20000.0, 232448)
     assert ex["terms_us_per_step"]["alu"] == pytest.approx(2 * alu_us, rel=1e-3)
+    assert ex["binding"] == "alu"
 
 
 def test_step_roofline_streams_what_does_not_fit():
@@ -111,6 +116,20 @@ def test_step_roofline_streams_what_does_not_fit():
     assert sr["r_streamed_bytes_per_step"] == r - 152 * 232448
     assert sr["terms_us_per_step"]["l2"] == pytest.approx((r - 152 * 232448) / 10000e9 * 1e6, rel=1e-3)
     assert sr["steps"] == 4096
+    # every output's 2048 dependent adds a step: 2048 * 4 cycles at 2070 MHz
+    chain_us = 2048 * bench.FP32_CHAIN_CYCLES / 2070e6 * 1e6
+    assert sr["terms_us_per_step"]["chain"] == pytest.approx(chain_us, rel=1e-3)
+    assert sr["binding"] == "chain"
+    assert sr["roof_ms"] == pytest.approx(4096 * chain_us / 1e3, rel=1e-3)
+
+
+def test_step_roofline_chain_doubles_for_two_gru_products():
+    from onnx_recurrent_gb300.synth import make_case
+    a = make_case("GRU", "forward", 3, 2, 4, 256, linear_before_reset=0)
+    b = make_case("GRU", "forward", 3, 2, 4, 256, linear_before_reset=1)
+    ca = bench.step_roofline(a, "exact", 1.0, 152, 2070.0, 10000.0, 232448)["terms_us_per_step"]["chain"]
+    cb = bench.step_roofline(b, "exact", 1.0, 152, 2070.0, 10000.0, 232448)["terms_us_per_step"]["chain"]
+    assert ca == pytest.approx(2 * cb, rel=1e-3)
 
 
 def test_traffic_lookup_reads_every_key_of_a_summary(tmp_path, monkeypatch):
