@@ -277,14 +277,40 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(text):
+    """C/C++/CUDA source without its comments and blank space: two sources
+    that differ only there build the same kernels (line numbers aside)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":                      # a string or character literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_digest(kernel):
-    """Digest of the sources a kernel is built from: a committed ncu traffic
-    figure applies only while they are unchanged."""
+    """Digest of the code a kernel is built from (comments and blank space
+    dropped): a committed ncu traffic figure applies only while it is
+    unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "onnx_recurrent_gb300", "csrc")
     for name in KERNEL_SOURCES.get(kernel, sorted(os.listdir(csrc))):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -32,12 +32,18 @@
 //     every CTA of the row group has published `target` times.
 //   Two h buffers suffice: a CTA can only overwrite buffer b after every
 //   producer of its row group has published the step that reads b.
+//   * With the in-cluster exchange (CL instances) a row group is one
+//     thread-block cluster: every CTA keeps the row group's whole h in its own
+//     shared memory and writes the h it computes into every peer's copy
+//     (distributed shared memory); arrivals on the peers' mbarriers replace
+//     the counter, the loader and the tensor copies of h.
 //
 // Every wait is bounded (globaltimer): a CTA that gives up records
 // RNN_ERR_TIMEOUT in the status word; CTAs that see a non-zero status stop.
 // The compute warps leave only at a publish barrier, so no warp is left
 // waiting on a named barrier, and the loader waits for its own copies in
-// flight before it exits.
+// flight before it exits.  A CL CTA does not leave early at all: it runs its
+// remaining steps without waiting and meets its cluster at the end.
 #pragma once
 
 #include <cstdint>

@@ -143,3 +143,12 @@ def test_traffic_lookup_reads_every_key_of_a_summary(tmp_path, monkeypatch):
     assert bench.profiled_traffic("recurrence", "short", "fast", d) == 10
     assert bench.profiled_traffic("recurrence", "long", "fast", d) == 80
 
+
+
+def test_source_digest_ignores_comments_and_blank_space():
+    a = 'int f(int x) {  // one\n  return x + 1; /* two */ }\nconst char* s = "a // not a comment";\n'
+    b = 'int f(int x) {\n\n    return x + 1;   }\nconst char* s = "a // not a comment";'
+    c = 'int f(int x) { return x + 2; }\nconst char* s = "a // not a comment";'
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+    assert "not a comment" in bench.code_only(a)
