@@ -230,6 +230,38 @@ def test_cluster_exchange_attributes(op, direction, layout, attrs):
         _compare_exact(c, (Y, Yh, Yc), ref, f"{op} {direction} layout {layout} {launch}")
 
 
+# Gate split (GRU, linear_before_reset 1, one row per thread): three lanes per
+# (unit, row), a gate column each over all k in order, the sums gathered by
+# shuffles; the launch shows it as 3x the compute threads (ten groups of three
+# lanes per warp).  GRU with linear_before_reset 0 (two products) does not
+# split.  Both give the oracle's bits.
+@pytest.mark.parametrize("lbr,threads", [(1, 6 * 32 + 32), (0, 2 * 32 + 32)])
+def test_dataflow_gate_split(lbr, threads):
+    c = make_case("GRU", "bidirectional", 9, 4, 20, 56, seed=48, h0_scale=0.5, lens=[9, 0, 4, 7],
+                  linear_before_reset=lbr, clip=2.0)
+    Y, Yh, Yc, plan = gpu_case(c, "exact", launch=(4, 1, 1, 1, 2), keep_plan=True)
+    got = orc.rnn_plan_get_launch(plan)
+    orc.rnn_plan_destroy(plan)
+    assert got["kernel"] == 2 and got["threads"] == threads
+    ref = oracle_case(c)
+    _compare_exact(c, (Y, Yh, Yc), ref, f"gate split, lbr {lbr}")
+    for g, r in zip(gpu_case(c, "fast", launch=(4, 1, 1, 1, 2)), ref):
+        if g is not None:
+            assert float(np.abs(g.astype(np.float64) - r.astype(np.float64)).max(initial=0.0)) <= 1e-5
+
+
+def test_cluster_exchange_more_clusters_than_fit():
+    # 16 row groups x 2 directions of 13-CTA clusters: 416 CTAs for 152 SMs;
+    # clusters are independent, so the later ones run after the first finish
+    c = make_case("LSTM", "bidirectional", 12, 128, 24, 256, seed=49, with_P=True, h0_scale=0.5, c0_scale=0.5,
+                  lens=("uniform", 0, 12))
+    Y, Yh, Yc, plan = gpu_case(c, "exact", launch=(13, 1, -1, 16, 5), keep_plan=True)
+    got = orc.rnn_plan_get_launch(plan)
+    orc.rnn_plan_destroy(plan)
+    assert got["kernel"] == 5 and got["unit_groups"] == 13 and got["row_groups"] == 16
+    _compare_exact(c, (Y, Yh, Yc), oracle_case(c), "416 CTAs in clusters of 13")
+
+
 def test_cluster_exchange_refuses_streamed_r():
     c = make_case("LSTM", "forward", 3, 4, 8, 64, seed=3)
     with pytest.raises(orc.RNNError) as e:
