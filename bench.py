@@ -199,41 +199,49 @@ def live_rows_per_step(case):
 FP32_CHAIN_CYCLES = 4.0
 
 
-def step_roofline(case, mode, rec_ms, sms, clock_mhz, l2_gbs, smem_per_sm):
+def step_roofline(case, mode, rec_ms, sms, clock_mhz, l2_gbs, smem_per_sm, h_bytes=0.0, tensor_tflops=None):
     """The recurrent kernel's per-step roofline (per launch): every step takes
     at least the largest of
       alu   2 * live rows * D * G * H^2 FLOP over the FP32 peak (fused
-            multiply-add in the fast modes, separate multiply and add in exact);
-      smem  the R slices read once from shared memory, D * 4 * G * H^2 bytes,
-            over SMs * 128 bytes per clock;
+            multiply-add in the fast modes, separate multiply and add in exact),
+            or over `tensor_tflops` for the tensor-core recurrence;
+      smem  the R slices read once from shared memory, D * 4 * G * H^2 bytes
+            (2 per element on the tensor cores), over SMs * 128 bytes per clock;
       l2    the part of R that cannot stay resident in the SMs' shared memory
             (D * 4 * G * H^2 - SMs * smem_per_sm, if positive), streamed from L2
             every step, over the measured L2 copy bandwidth;
+      h     the copies of h that the launch's CTAs need from L2 (every CTA
+            holding a slice of R needs h of every row it multiplies): `h_bytes`
+            for all rows, counted for the live rows only, over the same
+            bandwidth;
       chain every output is one accumulator over k = 0..H-1 in order (exact
             and fast mode alike), H dependent adds a step (2H for GRU with
             linear_before_reset = 0, whose second product needs the first's
-            result) at FP32_CHAIN_CYCLES each.
+            result) at FP32_CHAIN_CYCLES each (not on the tensor cores).
     Returns the terms per step (microseconds, averaged over the steps), the
     binding term, the roofline time of the launch and its fraction of the
     measured time."""
     G, H, D = case.gates, case.hidden_size, case.dirs
     live = live_rows_per_step(case)
     clock = clock_mhz * 1e6
-    alu_peak = sms * 128 * (1 if mode == "exact" else 2) * clock
+    alu_peak = (tensor_tflops * 1e12 if tensor_tflops else sms * 128 * (1 if mode == "exact" else 2) * clock)
     smem_bw = sms * 128 * clock
-    r_bytes = 4.0 * D * G * H * H
+    r_bytes = (2.0 if tensor_tflops else 4.0) * D * G * H * H
     streamed = max(0.0, r_bytes - float(sms) * smem_per_sm)
     t_smem = r_bytes / smem_bw
     t_l2 = streamed / (l2_gbs * 1e9) if l2_gbs else 0.0
+    t_h_all = h_bytes / (l2_gbs * 1e9) if l2_gbs else 0.0
     two = case.op == "GRU" and case.linear_before_reset == 0
-    t_chain = (2 if two else 1) * H * FP32_CHAIN_CYCLES / clock
-    roof, terms = 0.0, {"alu": 0.0, "smem": 0.0, "l2": 0.0, "chain": 0.0}
+    t_chain = 0.0 if tensor_tflops else (2 if two else 1) * H * FP32_CHAIN_CYCLES / clock
+    roof, terms = 0.0, {"alu": 0.0, "smem": 0.0, "l2": 0.0, "h": 0.0, "chain": 0.0}
     for n in live:
         t_alu = 2.0 * n * D * G * H * H / alu_peak
-        roof += max(t_alu, t_smem, t_l2, t_chain)
+        t_h = t_h_all * n / case.batch
+        roof += max(t_alu, t_smem, t_l2, t_h, t_chain)
         terms["alu"] += t_alu
         terms["smem"] += t_smem
         terms["l2"] += t_l2
+        terms["h"] += t_h
         terms["chain"] += t_chain
     steps = max(1, len(live))
     binding = max(terms, key=terms.get)
@@ -245,7 +253,28 @@ def step_roofline(case, mode, rec_ms, sms, clock_mhz, l2_gbs, smem_per_sm):
                       "note": "alu and smem derived (SMs x 128 lanes or bytes per clock x max SM clock); "
                               "l2 measured by an elementwise kernel over a buffer pair that fits in L2; "
                               "chain: H dependent FP32 adds a step at the pipe's latency"},
-            "r_bytes_per_step": r_bytes, "r_streamed_bytes_per_step": streamed}
+            "r_bytes_per_step": r_bytes, "r_streamed_bytes_per_step": streamed, "h_bytes_per_step": h_bytes}
+
+
+def h_bytes_per_step(geometry, case):
+    """Bytes of h the recurrent launch's CTAs read from L2 each step: every CTA
+    of a direction copies the h of the rows it multiplies (the staged kernel
+    all rows, the dataflow kernel its row group's, the tensor-core kernel all
+    rows in fp16); the in-cluster exchange moves h through shared memory."""
+    def up(a, b):
+        return (a + b - 1) // b * b
+    k = geometry.get("kernel")
+    D, H, N = case.dirs, case.hidden_size, case.batch
+    ctas = geometry.get("unit_groups", 0)
+    if k == 1:
+        return float(D * ctas * up(N, 8) * H * 4)
+    if k == 2:
+        cr = max(1, geometry.get("row_groups", 1))
+        nrp = up((N + cr - 1) // cr, 4 if (cr == 1 and N <= 4) else 8)   # rows per group, padded
+        return float(D * ctas * cr * nrp * H * 4)
+    if k == 3:
+        return float(D * ctas * up(N, 8) * H * 2)
+    return 0.0
 
 
 def measure_l2_gbs(torch, nbytes=32 << 20, reps=50):
@@ -654,18 +683,36 @@ def run_ours(args, ws, rank, local):
             # fp16 tensor-core products (tcgen05 kind::f16): the measured bf16
             # burst peak, fp16 and bf16 having the same nominal dense rate
             peak = float(peaks.get("bf16_tflops", 1900.0))
+            traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel))
+            sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm,
+                                h_bytes_per_step(geometry, job.case), tensor_tflops=peak)
+                  if isinstance(job, SequenceJob) else None)
+            if sr and sr["binding"] == "h":
+                # every CTA copies all of h (fp16) each step: those bytes over L2
+                nbytes = sr["h_bytes_per_step"] * sr["steps"]
+                ach = nbytes / (ms / 1e3) / 1e9 if ms else 0.0
+                return {"bound": "l2", "achieved": round(ach, 1), "peak": round(l2_gbs, 1), "unit": "GB/s",
+                        "frac": sr["frac"], "traffic": traffic, "kernel": "rnn_tc_kernel", "avg_ms": round(ms, 5),
+                        "algorithmic_bytes_per_launch": nbytes, "step_roofline": sr,
+                        "peak_note": "of measured L2 bandwidth (an elementwise kernel, read + write, a 32 MiB "
+                                     "pair); the tensor-core products alone would take "
+                                     f"{sr['terms_us_per_step']['alu']:.2f} us a step against the measured bf16 "
+                                     f"burst ({peak:.0f} TFLOP/s)"}
             ach = rec_flops / (ms / 1e3) / 1e12 if ms else 0.0
-            return {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
-                    "frac": round(ach / peak, 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
-                    "kernel": "rnn_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": rec_flops,
-                    "peak_note": "of measured bf16 burst (fp16 operands, same nominal rate)"}
+            out = {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
+                   "frac": round(ach / peak, 4) if ms else 0.0, "traffic": traffic,
+                   "kernel": "rnn_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": rec_flops,
+                   "peak_note": "of measured bf16 burst (fp16 operands, same nominal rate)"}
+            if sr:
+                out["step_roofline"] = sr
+            return out
         if kernel == "recurrence":
             # kernel 5: the dataflow kernel's in-cluster instance (same name)
             name = {2: "rnn_dataflow_kernel", 4: "rnn_wavefront_kernel",
                     5: "rnn_dataflow_kernel"}.get(geometry.get("kernel"), "rnn_recurrent_kernel")
             traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel))
-            sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm)
+            sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm,
+                                h_bytes_per_step(geometry, job.case))
                   if isinstance(job, SequenceJob) else None)
             if sr and sr["binding"] == "chain":
                 # each output's dependent adds bound the step: their rate
@@ -680,10 +727,12 @@ def run_ours(args, ws, rank, local):
                         "peak_note": f"one FP32 add (or fused multiply-add) per {FP32_CHAIN_CYCLES:.0f} cycles "
                                      f"on each output's chain (k ascending) at {clock_mhz:.0f} MHz; frac is the "
                                      "step roofline's (per-step max of the ALU, shared-memory, L2 and chain terms)"}
-            if sr and sr["binding"] == "l2":
-                # R does not fit in the SMs' shared memory and its streamed part
-                # bounds the step: bytes from L2 against the measured L2 copy rate
-                nbytes = sr["r_streamed_bytes_per_step"] * sr["steps"]
+            if sr and sr["binding"] in ("l2", "h"):
+                # R's streamed part (it does not fit in the SMs' shared memory)
+                # or the copies of h bound the step: bytes from L2 against the
+                # measured L2 copy rate
+                nbytes = (sr["r_streamed_bytes_per_step"] if sr["binding"] == "l2"
+                          else sr["h_bytes_per_step"]) * sr["steps"]
                 ach = nbytes / (ms / 1e3) / 1e9 if ms else 0.0
                 return {"bound": "l2", "achieved": round(ach, 1), "peak": round(l2_gbs, 1), "unit": "GB/s",
                         "frac": sr["frac"], "traffic": traffic, "kernel": name, "avg_ms": round(ms, 5),

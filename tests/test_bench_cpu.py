@@ -152,3 +152,27 @@ def test_source_digest_ignores_comments_and_blank_space():
     assert bench.code_only(a) == bench.code_only(b)
     assert bench.code_only(a) != bench.code_only(c)
     assert "not a comment" in bench.code_only(a)
+
+
+def test_h_bytes_per_step_and_its_term():
+    # LSTM bidirectional, batch 128, hidden 1024 on the staged kernel with 74
+    # CTAs per direction: every CTA copies all 128 rows of h (fp32) each step
+    c = workload("lstm_bidi_s512_b128_i1024_h1024")
+    geo = {"kernel": 1, "unit_groups": 74, "row_groups": 1}
+    hb = bench.h_bytes_per_step(geo, c)
+    assert hb == 2 * 74 * 128 * 1024 * 4
+    # the tensor-core kernel copies them in fp16; the in-cluster exchange none
+    assert bench.h_bytes_per_step({"kernel": 3, "unit_groups": 74}, c) == hb / 2
+    assert bench.h_bytes_per_step({"kernel": 5, "unit_groups": 16}, c) == 0.0
+    # dataflow, batch 32 in 4 row groups of 8: each CTA its group's rows
+    c2 = workload("lstm_fwd_s64_b32_i256_h512")
+    assert bench.h_bytes_per_step({"kernel": 2, "unit_groups": 37, "row_groups": 4}, c2) == 37 * 4 * 8 * 512 * 4
+    sr = bench.step_roofline(c, "fast", 10.0, 152, 2070.0, 7000.0, 232448, hb)
+    # counted for the live rows only: on average the live fraction of the batch
+    live = bench.live_rows_per_step(c)
+    mean_live = sum(live) / len(live) / 128
+    assert sr["terms_us_per_step"]["h"] == pytest.approx(hb / 7000e9 * 1e6 * mean_live, rel=1e-3)
+    assert sr["h_bytes_per_step"] == hb
+    # on the tensor cores (the measured bf16 burst) the h term binds
+    st = bench.step_roofline(c, "tf32", 10.0, 152, 2070.0, 7000.0, 232448, hb / 2, tensor_tflops=1874.7)
+    assert st["binding"] == "h" and st["terms_us_per_step"]["chain"] == 0.0
