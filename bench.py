@@ -296,13 +296,20 @@ def measure_l2_gbs(torch, nbytes=32 << 20, reps=50):
     return 2.0 * nbytes * reps / (ms / 1e3) / 1e9
 
 
+# The sources each kernel is compiled from (its translation units and the
+# headers its code comes from): a committed traffic figure is keyed by their
+# digest, so it stays valid while that kernel's code is unchanged.
+_COMMON = ["tma.cuh", "exact_math.cuh", "io_types.cuh", "rnn_internal.h"]
 KERNEL_SOURCES = {
-    "recurrence": ["k_recur.cuh", "k_recur2.cuh", "k_recur_rnn.cu", "k_recur_gru.cu", "k_recur_lstm.cu",
-                   "k_recur_tc.cu", "k_wave.cuh", "k_wave_rnn.cu", "k_wave_gru.cu", "k_wave_lstm.cu",
-                   "k_clus_rnn.cu", "k_clus_gru.cu", "k_clus_lstm.cu", "tma.cuh",
-                   "exact_math.cuh", "io_types.cuh", "rnn_internal.h"],
-    "projection": ["k_proj.cu", "k_proj_tc.cu", "tma.cuh", "rnn_internal.h"],
-    "cell": ["k_cell.cu", "exact_math.cuh", "rnn_internal.h"],
+    "rnn_recurrent_kernel": ["k_recur.cuh", "k_recur_rnn.cu", "k_recur_gru.cu", "k_recur_lstm.cu"] + _COMMON,
+    "rnn_dataflow_kernel": ["k_recur.cuh", "k_recur2.cuh", "k_recur_rnn.cu", "k_recur_gru.cu", "k_recur_lstm.cu",
+                            "k_clus_rnn.cu", "k_clus_gru.cu", "k_clus_lstm.cu"] + _COMMON,
+    "rnn_tc_kernel": ["k_recur_tc.cu", "k_recur.cuh"] + _COMMON,
+    "rnn_wavefront_kernel": ["k_wave.cuh", "k_wave_rnn.cu", "k_wave_gru.cu", "k_wave_lstm.cu",
+                             "k_recur.cuh"] + _COMMON,
+    "proj_tma_kernel": ["k_proj.cu", "exact_math.cuh", "tma.cuh", "rnn_internal.h"],
+    "proj_tc_kernel": ["k_proj_tc.cu", "tma.cuh", "rnn_internal.h"],
+    "rnn_cell_kernel": ["k_cell.cu", "exact_math.cuh", "rnn_internal.h"],
 }
 
 
@@ -331,15 +338,19 @@ def code_only(text):
     return " ".join("".join(out).split())
 
 
-def source_digest(kernel):
-    """Digest of the code a kernel is built from (comments and blank space
-    dropped): a committed ncu traffic figure applies only while it is
-    unchanged."""
+def source_digest(kernel, read=None):
+    """Digest of the code a kernel (by its name) is built from, comments and
+    blank space dropped: a committed ncu traffic figure applies only while
+    it is unchanged.  `read(name)` supplies a source's text (default: the
+    tree's file)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "onnx_recurrent_gb300", "csrc")
-    for name in KERNEL_SOURCES.get(kernel, sorted(os.listdir(csrc))):
-        with open(os.path.join(csrc, name), encoding="utf-8") as f:
-            h.update(name.encode() + code_only(f.read()).encode())
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                return f.read()
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode() + code_only(read(name)).encode())
     return h.hexdigest()[:16]
 
 
@@ -675,7 +686,7 @@ def run_ours(args, ws, rank, local):
             ach = flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
                     "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
+                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest("rnn_cell_kernel")),
                     "kernel": "rnn_cell_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": flops,
                     "peak_note": f"{'no' if exact else 'fused'} multiply-add: {sms} SMs x 128 FP32 "
                                  f"lanes x {'1' if exact else '2'} FLOP x {clock_mhz:.0f} MHz (derived)"}
@@ -683,7 +694,7 @@ def run_ours(args, ws, rank, local):
             # fp16 tensor-core products (tcgen05 kind::f16): the measured bf16
             # burst peak, fp16 and bf16 having the same nominal dense rate
             peak = float(peaks.get("bf16_tflops", 1900.0))
-            traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel))
+            traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest("rnn_tc_kernel"))
             sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm,
                                 h_bytes_per_step(geometry, job.case), tensor_tflops=peak)
                   if isinstance(job, SequenceJob) else None)
@@ -710,7 +721,7 @@ def run_ours(args, ws, rank, local):
             # kernel 5: the dataflow kernel's in-cluster instance (same name)
             name = {2: "rnn_dataflow_kernel", 4: "rnn_wavefront_kernel",
                     5: "rnn_dataflow_kernel"}.get(geometry.get("kernel"), "rnn_recurrent_kernel")
-            traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel))
+            traffic = profiled_traffic(kernel, traffic_name, args.mode, source_digest(name))
             sr = (step_roofline(job.case, args.mode, ms, sms, clock_mhz, l2_gbs, smem_per_sm,
                                 h_bytes_per_step(geometry, job.case))
                   if isinstance(job, SequenceJob) else None)
@@ -757,7 +768,7 @@ def run_ours(args, ws, rank, local):
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "tensor", "achieved": round(ach, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
                     "frac": round(ach / peak, 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
+                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest("proj_tc_kernel")),
                     "kernel": "proj_tc_kernel", "avg_ms": round(ms, 5), "algorithmic_flops_per_launch": proj_flops,
                     "peak_note": "of measured bf16 burst" + ("" if args.mode == "bf16" else
                                                              " x 1.1/2.25 (TF32: derived from the bf16 "
@@ -766,7 +777,7 @@ def run_ours(args, ws, rank, local):
             ach = proj_flops / (ms / 1e3) / 1e12 if ms else 0.0
             return {"bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak / 1e12, 3),
                     "unit": "TFLOP/s", "frac": round(ach / (alu_peak / 1e12), 4) if ms else 0.0,
-                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest(kernel)),
+                    "traffic": profiled_traffic(kernel, traffic_name, args.mode, source_digest("proj_tma_kernel")),
                     "kernel": "proj_tma_kernel", "avg_ms": round(ms, 5),
                     "algorithmic_flops_per_launch": proj_flops}
         return {"kernel": kernel, "avg_ms": round(ms, 5)}

@@ -535,7 +535,6 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                     const int tot = p.N * U;
                     for (int i = threadIdx.x; i < tot; i += 128) {
                         const int rn = i / U, ul = i - rn * U;
-                        if (p.Y) io_store(p.Y, y_index(p, s_t[rn], d, rn, u0 + ul), s_y[rn * p.umax + ul], p.io);
                         hdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
                     }
                 }
@@ -547,6 +546,17 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                 if (threadIdx.x == 0 && !(skip_first && s == 0)) {
                     fence_proxy_async_global();
                     red_release_add_u32(counter, 1u);
+                }
+                // Y is read by no other CTA: its stores follow the publication,
+                // off the exchange's critical path; the staged tiles are reused
+                // only after every epilogue thread has read them
+                if (p.Y) {
+                    const int tot = p.N * U;
+                    for (int i = threadIdx.x; i < tot; i += 128) {
+                        const int rn = i / U, ul = i - rn * U;
+                        io_store(p.Y, y_index(p, s_t[rn], d, rn, u0 + ul), s_y[rn * p.umax + ul], p.io);
+                    }
+                    tr_bar(1, 128);
                 }
             }
         } else {
@@ -686,7 +696,6 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                     const int tot = p.N * U;
                     for (int i = threadIdx.x; i < tot; i += 128) {
                         const int rn = i / U, ul = i - rn * U;
-                        if (p.Y) io_store(p.Y, y_index(p, s_t[rn], d, rn, u0 + ul), s_y[rn * p.umax + ul], p.io);
                         hdst[(size_t)rn * H + ul] = s_h[rn * p.umax + ul];
                     }
                 }
@@ -699,6 +708,17 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                 if (threadIdx.x == 0 && !(skip_first && s == 0)) {
                     fence_proxy_async_global();
                     red_release_add_u32(counter, 1u);
+                }
+                // Y is read by no other CTA: its stores follow the publication,
+                // off the exchange's critical path; the staged tiles are reused
+                // only after every epilogue thread has read them
+                if (p.Y) {
+                    const int tot = p.N * U;
+                    for (int i = threadIdx.x; i < tot; i += 128) {
+                        const int rn = i / U, ul = i - rn * U;
+                        io_store(p.Y, y_index(p, s_t[rn], d, rn, u0 + ul), s_y[rn * p.umax + ul], p.io);
+                    }
+                    tr_bar(1, 128);
                 }
             }
         }

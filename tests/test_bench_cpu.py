@@ -33,8 +33,8 @@ def test_algorithmic_flops_count_valid_steps_only():
 
 
 def test_traffic_lookup_follows_the_source_digest(tmp_path, monkeypatch):
-    d = bench.source_digest("recurrence")
-    assert len(d) == 16 and d != bench.source_digest("cell")
+    d = bench.source_digest("rnn_recurrent_kernel")
+    assert len(d) == 16 and d != bench.source_digest("rnn_cell_kernel")
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "x.md").write_text(f"summary\n\ntraffic_key: recurrence wl exact {d} 1234\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
@@ -49,9 +49,11 @@ def test_committed_profiles_parse():
         with open(os.path.join(ROOT, "profiles", name)) as f:
             for line in f:
                 if line.startswith("traffic_key:"):
-                    kernel, wl, mode, digest, nbytes = line.split()[1:]
-                    assert kernel in bench.KERNEL_SOURCES and int(nbytes) > 0 and len(digest) == 16
-                    keys.append((kernel, wl, mode))
+                    kind, wl, mode, digest, nbytes = line.split()[1:]
+                    assert kind in ("recurrence", "projection", "cell") and int(nbytes) > 0 and len(digest) == 16
+                    # the summary's kernel (its file name) is one the digests know
+                    assert any(name.startswith(k + "_") for k in bench.KERNEL_SOURCES)
+                    keys.append((kind, wl, mode))
     assert ("recurrence", "lstm_fwd_s64_b32_i256_h512", "exact") in keys
 
 
@@ -135,7 +137,7 @@ def test_step_roofline_chain_doubles_for_two_gru_products():
 def test_traffic_lookup_reads_every_key_of_a_summary(tmp_path, monkeypatch):
     # a summary captured on a shorter sequence carries a key for that case
     # and a scaled one for the bench workload
-    d = bench.source_digest("recurrence")
+    d = bench.source_digest("rnn_recurrent_kernel")
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "x.md").write_text(f"traffic_key: recurrence short fast {d} 10\\n"
                                                 f"traffic_key: recurrence long fast {d} 80\\n")
@@ -143,6 +145,34 @@ def test_traffic_lookup_reads_every_key_of_a_summary(tmp_path, monkeypatch):
     assert bench.profiled_traffic("recurrence", "short", "fast", d) == 10
     assert bench.profiled_traffic("recurrence", "long", "fast", d) == 80
 
+
+
+def test_source_digest_is_per_kernel():
+    # a change to one kernel's code leaves the digests of kernels built from
+    # other sources (and so their committed traffic figures) as they are
+    csrc = os.path.join(ROOT, "onnx_recurrent_gb300", "csrc")
+
+    def read(changed):
+        def r(name):
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                t = f.read()
+            return t + "\nint changed_here;\n" if name == changed else t
+        return r
+
+    for k, srcs in bench.KERNEL_SOURCES.items():
+        assert all(os.path.exists(os.path.join(csrc, n)) for n in srcs)
+    tc = read("k_recur_tc.cu")
+    assert bench.source_digest("rnn_tc_kernel", tc) != bench.source_digest("rnn_tc_kernel")
+    for k in ("rnn_recurrent_kernel", "rnn_dataflow_kernel", "rnn_wavefront_kernel", "proj_tc_kernel"):
+        assert bench.source_digest(k, tc) == bench.source_digest(k)
+    # a header every recurrent kernel is built from changes them all
+    shared = read("k_recur.cuh")
+    for k in ("rnn_recurrent_kernel", "rnn_dataflow_kernel", "rnn_wavefront_kernel", "rnn_tc_kernel"):
+        assert bench.source_digest(k, shared) != bench.source_digest(k)
+    # every translation unit of the library is some kernel's source, or host code
+    from onnx_recurrent_gb300 import _build
+    covered = set().union(*bench.KERNEL_SOURCES.values())
+    assert set(_build.SOURCES) - covered == {"rnn_api.cpp", "k_misc.cu", "rnn_static.cu"}
 
 
 def test_source_digest_ignores_comments_and_blank_space():
