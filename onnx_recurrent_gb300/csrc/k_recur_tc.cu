@@ -181,6 +181,24 @@ __device__ __forceinline__ void tc_act_array(const ActSpec& a, float (&v)[K], co
     }
 }
 
+// A row's XW columns [0, n) into registers (zero past n): 16-byte loads when
+// `vec` (start 16-byte aligned, n a multiple of 4), else 4-byte loads.
+template <int NMAX>
+__device__ __forceinline__ void tc_load_xw(float (&xw)[NMAX], const float* src, int n, bool vec)
+{
+    if (vec) {
+#pragma unroll
+        for (int j = 0; j < NMAX / 4; ++j) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (4 * j < n) v = __ldg(reinterpret_cast<const float4*>(src) + j);
+            xw[4 * j] = v.x; xw[4 * j + 1] = v.y; xw[4 * j + 2] = v.z; xw[4 * j + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < NMAX; ++j) xw[j] = j < n ? __ldg(src + j) : 0.f;
+    }
+}
+
 // TWO (GRU with linear_before_reset = 0): two products per step, z and r
 // over h, then the candidate over r (.) h once every CTA has published its
 // units' r (.) h; R's rows are packed z/r first, candidate rows after.
@@ -414,6 +432,10 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
         }
         const size_t xw_ld = (size_t)p.D * GH;
         const size_t xw_col = (size_t)d * GH + (size_t)u0 * G;
+        // a row's columns are one contiguous run: 16-byte loads where it is
+        // aligned (each lane reads another row, so fewer, wider requests)
+        const bool xw_vec = OP == 2 && ((xw_ld | xw_col | (size_t)(U * G)) % 4 == 0) &&
+                            (reinterpret_cast<uintptr_t>(p.XW) % 16 == 0);
         __half* hx = reinterpret_cast<__half*>(p.hbuf);
         const bool skip_first = p.debug_skip_cta == (int)blockIdx.x;
         bool alive = true;
@@ -426,8 +448,7 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                 if (live) {
                     const size_t xrow = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
                     const float* src = p.XW + xrow * xw_ld + xw_col;
-#pragma unroll
-                    for (int j = 0; j < TR_NPMAX; ++j) xw[j] = j < U * G ? __ldg(src + j) : 0.f;
+                    tc_load_xw<TR_NPMAX>(xw, src, U * G, xw_vec);
                 }
                 // ---- z and r: accumulators j = 2 ul + g in columns 0 .. NP-1
                 const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
@@ -568,8 +589,7 @@ __global__ void __launch_bounds__(TR_THREADS, 1) rnn_tc_kernel(const __grid_cons
                 if (live) {
                     const size_t xrow = p.layout == 0 ? (size_t)t * p.N + n : (size_t)n * p.S + t;
                     const float* src = p.XW + xrow * xw_ld + xw_col;
-    #pragma unroll
-                    for (int j = 0; j < TR_NPMAX; ++j) xw[j] = j < U * G ? __ldg(src + j) : 0.f;
+                    tc_load_xw<TR_NPMAX>(xw, src, U * G, xw_vec);
                 }
                 // accumulators (warp-collective loads: the decision is warp-uniform)
                 const bool got = __all_sync(0xffffffffu, alive && tr_wait(&acc_ready, (unsigned)s & 1u, p, &s_abort));
