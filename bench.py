@@ -277,11 +277,12 @@ def h_bytes_per_step(geometry, case):
     return 0.0
 
 
-def measure_l2_gbs(torch, nbytes=32 << 20, reps=50, trials=5):
+def measure_l2_gbs(torch, nbytes=32 << 20, reps=10, trials=5):
     """Bandwidth (read + write bytes per second) of an elementwise kernel over
     a buffer pair that fits in the L2 (b = a * 1, so the SMs move the data),
     timed with CUDA events after warm-up passes; the best of a few trials
-    (a peak for the roofline, not a mean disturbed by whatever else runs)."""
+    (a peak for the roofline, not a mean disturbed by whatever else runs).
+    55 launches in all (5 warm-up, 5 x 10 timed)."""
     a = torch.empty(nbytes // 4, device="cuda")
     b = torch.empty_like(a)
     a.fill_(1.0)
