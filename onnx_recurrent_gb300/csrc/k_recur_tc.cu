@@ -24,12 +24,14 @@
 //     K 16) per block into tensor memory, commits each ring slot back to the
 //     producer and, after the last block, the accumulators to the epilogue;
 //   * warps 0-3 are the epilogue: thread t owns batch row t (tensor-memory
-//     lane t), reads its NP accumulators, adds XW and the biases, runs the
-//     gate arithmetic (FMA-based, hardware tanh) with its cell state kept in
+//     lane t), reads its NP accumulators, adds XW (its row's columns, 16
+//     bytes per load where they are aligned) and the biases, runs the gate
+//     arithmetic (FMA-based, hardware tanh) with its cell state kept in
 //     registers (h kept in fp32 too), and stages its row of Y and of the
-//     fp16 h in shared memory; the four warps then write both tiles with
+//     fp16 h in shared memory; the four warps then write the h tile with
 //     consecutive threads on consecutive units (a thread per row would make
-//     every store instruction touch 32 rows), and the CTA publishes.
+//     every store instruction touch 32 rows), the CTA publishes, and only
+//     then is the Y tile written (no other CTA reads Y).
 // Every wait is bounded; on a failure the CTA records RNN_ERR_TIMEOUT and
 // its roles leave at the next uniform point, waiting (bounded) for their
 // copies and MMAs in flight before the tensor memory is freed.
