@@ -72,6 +72,26 @@ MUTANTS = [
      "int fn = activation ? o_name_to_fn(activation) : OA_SIGMOID;"),
     ("cell accepts affine", "if (fn != OA_RELU && fn != OA_SIGMOID && fn != OA_TANH) return 1;",
      "if (fn < 0) return 1;"),
+    ("LSTM drops Pi", "pi = pi + Pi[u] * c[u];", "pi = pi;"),
+    ("LSTM Pf takes Pi", "pf = pf + Pf[u] * c[u];", "pf = pf + Pi[u] * c[u];"),
+    ("LSTM cell state clipped", "hn[u] = og * o_act(&acts[2], cn[u]);",
+     "hn[u] = og * o_act(&acts[2], o_clip(a, cn[u]));"),
+    ("GRU lbr0 drops Rb", "if (a->B) { ph = ph + Wb[2 * H + u]; ph = ph + Rb[2 * H + u]; }",
+     "if (a->B) { ph = ph + Wb[2 * H + u]; }"),
+    ("thresholdedrelu boundary", "case OA_THRESHOLDEDRELU: return x > alpha ? x : 0.0f;",
+     "case OA_THRESHOLDEDRELU: return x >= alpha ? x : 0.0f;"),
+    ("scaledtanh alpha and beta swapped", "case OA_SCALEDTANH:      return alpha * oracle_tanh(beta * x);",
+     "case OA_SCALEDTANH:      return beta * oracle_tanh(alpha * x);"),
+    ("hardsigmoid lower clamp", "return v < 0.0f ? 0.0f : (v > 1.0f ? 1.0f : v);",
+     "return v < 0.0f ? v : (v > 1.0f ? 1.0f : v);"),
+    ("hardsigmoid default beta", "case OA_HARDSIGMOID: return 0.5f;", "case OA_HARDSIGMOID: return 0.0f;"),
+    ("hardsigmoid default alpha", "case OA_HARDSIGMOID: return 0.2f;", "case OA_HARDSIGMOID: return 1.0f;"),
+    ("softsign drops abs", "case OA_SOFTSIGN:        return x / (1.0f + o_fabs(x));",
+     "case OA_SOFTSIGN:        return x / (1.0f + x);"),
+    ("affine drops beta", "case OA_AFFINE:          return alpha * x + beta;",
+     "case OA_AFFINE:          return alpha * x;"),
+    ("scaledtanh takes no beta", "return fn == OA_AFFINE || fn == OA_SCALEDTANH || fn == OA_HARDSIGMOID;",
+     "return fn == OA_AFFINE || fn == OA_HARDSIGMOID;"),
 ]
 
 
