@@ -53,6 +53,31 @@ def test_nan_outputs_are_canonical():
     assert np.all(Y.view(np.uint32) == 0x7FC00000)
 
 
+def test_accumulation_starts_from_plus_zero():
+    # Computation: one accumulator per output, k increasing from +0.  Every
+    # product here is 0 * -1 = -0; from +0 each sum is +0 + -0 = +0, Relu
+    # keeps it, and Y is +0 bit for bit (a sum started from -0 would stay -0
+    # and Relu would pass the -0 on).
+    X = np.zeros((1, 1, 1), np.float32)
+    W = np.full((1, 1, 1), -1.0, np.float32)
+    R = np.full((1, 1, 1), -1.0, np.float32)
+    Y, Yh, _ = oracle.rnn("RNN", "forward", 1, 1, X, W, R, activations=["Relu"])
+    assert Y.view(np.uint32).tolist() == [[[[0]]]] and Yh.view(np.uint32).tolist() == [[[0]]]
+
+
+def test_nan_passes_through_clip():
+    # Computation: clip clamps the pre-activation to [-clip, clip], a NaN
+    # passing through: with Affine the NaN reaches Y (canonical in exact
+    # mode), where a clamp that caught it would give the bound.
+    X = np.array([[[np.nan]]], np.float32)
+    W = np.ones((1, 1, 1), np.float32)
+    R = np.zeros((1, 1, 1), np.float32)
+    for clip in (0.5, 2.0):
+        Y, Yh, _ = oracle.rnn("RNN", "forward", 1, 1, X, W, R, activations=["Affine"], alpha=[1.0], beta=[0.0],
+                              clip=clip)
+        assert Y.view(np.uint32).tolist() == [[[[0x7FC00000]]]] and Yh.view(np.uint32).tolist() == [[[0x7FC00000]]]
+
+
 def test_bidirectional_lens_combines_both_hand_cases():
     fwd = load(os.path.join(GOLDEN, "rnn_lens_forward.json"))
     rev = load(os.path.join(GOLDEN, "rnn_lens_reverse.json"))

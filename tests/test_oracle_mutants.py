@@ -92,6 +92,18 @@ MUTANTS = [
      "case OA_AFFINE:          return alpha * x;"),
     ("scaledtanh takes no beta", "return fn == OA_AFFINE || fn == OA_SCALEDTANH || fn == OA_HARDSIGMOID;",
      "return fn == OA_AFFINE || fn == OA_HARDSIGMOID;"),
+    ("GRU lbr0 reset by z", "for (long k = 0; k < H; ++k) rh[k] = r[k] * h[k];",
+     "for (long k = 0; k < H; ++k) rh[k] = z[k] * h[k];"),
+    ("GRU candidate takes f", "float ht = o_act(&acts[1], o_clip(a, ph));", "float ht = o_act(&acts[0], o_clip(a, ph));"),
+    ("LSTM candidate takes f", "float ct = o_act(&acts[1], o_clip(a, pc));", "float ct = o_act(&acts[0], o_clip(a, pc));"),
+    ("RNN takes g", "hn[u] = o_act(&acts[0], o_clip(a, pre));", "hn[u] = o_act(&acts[1], o_clip(a, pre));"),
+    ("len-0 row returns initial cell", "for (long u = 0; u < H; ++u) yc[u] = L > 0 ? o_canon(c[u]) : 0.0f;",
+     "for (long u = 0; u < H; ++u) yc[u] = o_canon(c[u]);"),
+    ("dot starts from -0", "    float acc = 0.0f;\n    for (long k = 0; k < K; ++k) acc = acc + x[k] * w[k];",
+     "    float acc = -0.0f;\n    for (long k = 0; k < K; ++k) acc = acc + x[k] * w[k];"),
+    ("clip turns NaN into the bound", "    if (v > a->clip) return a->clip;", "    if (!(v <= a->clip)) return a->clip;"),
+    ("clip before the peepholes", "                float ig = o_act(&acts[0], o_clip(a, pi));",
+     "                float ig = o_act(&acts[0], o_clip(a, a->P ? pi - Pi[u] * c[u] : pi) + (a->P ? Pi[u] * c[u] : 0.0f));"),
 ]
 
 
@@ -101,6 +113,8 @@ def _battery():
     for p in th.FILES:
         checks.append((f"golden {os.path.basename(p)}", lambda p=p: th.test_golden_case(p)))
     checks.append(("nan canonical", th.test_nan_outputs_are_canonical))
+    checks.append(("plus zero start", th.test_accumulation_starts_from_plus_zero))
+    checks.append(("nan through clip", th.test_nan_passes_through_clip))
     checks.append(("bidi lens hand", th.test_bidirectional_lens_combines_both_hand_cases))
     for s in range(25):
         checks.append((f"brute {s}", lambda s=s: tb.test_oracle_matches_float64_brute_force(s)))
