@@ -233,6 +233,22 @@ def test_resolve_defaults_and_case_and_single_set():
     assert r == [[("elu", 0.5, 0.0)]]
 
 
+def test_resolve_every_default_the_page_lists():
+    # Activations: missing values take the activation's own defaults, as the
+    # page lists them: LeakyRelu 0.01, ThresholdedRelu 1, Elu 1, HardSigmoid
+    # 0.2 and 0.5, Affine and ScaledTanh 1 and 0.
+    f32 = lambda v: float(np.float32(v))
+    page = {"LeakyRelu": (f32(0.01), 0.0), "ThresholdedRelu": (1.0, 0.0), "Elu": (1.0, 0.0),
+            "HardSigmoid": (f32(0.2), 0.5), "Affine": (1.0, 0.0), "ScaledTanh": (1.0, 0.0)}
+    for name, (alpha, beta) in page.items():
+        r = oracle.resolve_activations("RNN", "forward", [name])
+        assert r == [[(name.lower(), alpha, beta)]], name
+    # one of the pair given: the other keeps its default
+    assert oracle.resolve_activations("RNN", "forward", ["ScaledTanh"], None, [0.5]) == \
+        [[("scaledtanh", 1.0, 0.5)]]
+    assert oracle.resolve_activations("RNN", "forward", ["Affine"], [3.0]) == [[("affine", 3.0, 0.0)]]
+
+
 # ------------------------------------------------------ cross-statements
 
 def _np_act(name, x):

@@ -104,6 +104,20 @@ MUTANTS = [
     ("clip turns NaN into the bound", "    if (v > a->clip) return a->clip;", "    if (!(v <= a->clip)) return a->clip;"),
     ("clip before the peepholes", "                float ig = o_act(&acts[0], o_clip(a, pi));",
      "                float ig = o_act(&acts[0], o_clip(a, a->P ? pi - Pi[u] * c[u] : pi) + (a->P ? Pi[u] * c[u] : 0.0f));"),
+    ("names case-sensitive", "            if (c >= 'A' && c <= 'Z') c = (char)(c - 'A' + 'a');\n", ""),
+    ("elu default alpha", "    case OA_ELU: return 1.0f;", "    case OA_ELU: return 0.5f;"),
+    ("thresholdedrelu default alpha", "    case OA_THRESHOLDEDRELU: return 1.0f;", "    case OA_THRESHOLDEDRELU: return 0.5f;"),
+    ("scaledtanh default alpha", "    case OA_SCALEDTANH: return 1.0f;", "    case OA_SCALEDTANH: return 0.5f;"),
+    ("affine default alpha", "    case OA_AFFINE: return 1.0f;", "    case OA_AFFINE: return 0.5f;"),
+    ("affine default beta 1", "    default: return 0.0f;   /* Affine and ScaledTanh default beta is 0 */",
+     "    default: return 1.0f;   /* Affine and ScaledTanh default beta is 0 */"),
+    ("LSTM default h activation sigmoid", "list[1].fn = OA_TANH; list[2].fn = OA_TANH; }",
+     "list[1].fn = OA_TANH; list[2].fn = OA_SIGMOID; }"),
+    ("GRU default g activation sigmoid", "else if (op == 1) { list[0].fn = OA_SIGMOID; list[1].fn = OA_TANH; }",
+     "else if (op == 1) { list[0].fn = OA_SIGMOID; list[1].fn = OA_SIGMOID; }"),
+    ("lengths above seq accepted", "if (lens[n] < 0 || (long)lens[n] > seq) return 2;", "if (lens[n] < 0) return 2;"),
+    ("alpha cursor advances without a taker", "            if (o_takes_alpha(fn)) {\n                if (alpha && ca < n_alpha) list[i].alpha = alpha[ca];\n                ca++;\n            }",
+     "            if (o_takes_alpha(fn)) {\n                if (alpha && ca < n_alpha) list[i].alpha = alpha[ca];\n            }\n            ca++;"),
 ]
 
 
@@ -128,6 +142,8 @@ def _battery():
     checks.append(("resolve page case", ti.test_resolve_page_black_box_case))
     checks.append(("resolve workload", ti.test_resolve_lstm_bidi_workload))
     checks.append(("resolve defaults", ti.test_resolve_defaults_and_case_and_single_set))
+    checks.append(("resolve page defaults", ti.test_resolve_every_default_the_page_lists))
+    checks.append(("invalid lengths", ti.test_invalid_lengths_and_arguments))
     checks.append(("rnncell3", lambda: ti.test_rnncell3_one_step("tanh")))
     checks.append(("bnns gru", ti.test_bnns_gru_reset_after_matmul))
     for p in tcell.FILES:
