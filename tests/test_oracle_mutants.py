@@ -115,7 +115,13 @@ MUTANTS = [
      "list[1].fn = OA_TANH; list[2].fn = OA_SIGMOID; }"),
     ("GRU default g activation sigmoid", "else if (op == 1) { list[0].fn = OA_SIGMOID; list[1].fn = OA_TANH; }",
      "else if (op == 1) { list[0].fn = OA_SIGMOID; list[1].fn = OA_SIGMOID; }"),
-    ("lengths above seq accepted", "if (lens[n] < 0 || (long)lens[n] > seq) return 2;", "if (lens[n] < 0) return 2;"),
+    ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
+     "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
+    ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
+    ("exp drops the ln2 tail", "float r = (x - kf * LN2_HEAD) - kf * LN2_TAIL;", "float r = x - kf * LN2_HEAD;"),
+    ("log subnormal exponent", "        eadj = -24;", "        eadj = -23;"),
+    ("tanh loses the sign", "    return o_from_bits(o_to_bits(y) | sign);", "    return y;"),
+    ("tanh saturates early", "if (a > 9.1f) {", "if (a > 5.0f) {"),
     ("alpha cursor advances without a taker", "            if (o_takes_alpha(fn)) {\n                if (alpha && ca < n_alpha) list[i].alpha = alpha[ca];\n                ca++;\n            }",
      "            if (o_takes_alpha(fn)) {\n                if (alpha && ca < n_alpha) list[i].alpha = alpha[ca];\n            }\n            ca++;"),
 ]
@@ -164,6 +170,8 @@ def _battery():
                tm.test_hardsigmoid_affine_softsign_points, tm.test_softplus_points,
                tm.test_elu_scaledtanh_points):
         checks.append((fn.__name__, fn))
+    checks.append(("exp sweep", tm.test_exp_accuracy_sweep))
+    checks.append(("log sweep", tm.test_log_accuracy_sweep))
     checks.append(("sigmoid sweep", tm.test_sigmoid_accuracy_sweep))
     checks.append(("tanh sweep", tm.test_tanh_accuracy_sweep))
     checks.append(("softplus elu sweep", tm.test_softplus_elu_softsign_sweeps))
