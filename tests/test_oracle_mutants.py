@@ -115,6 +115,17 @@ MUTANTS = [
      "list[1].fn = OA_TANH; list[2].fn = OA_SIGMOID; }"),
     ("GRU default g activation sigmoid", "else if (op == 1) { list[0].fn = OA_SIGMOID; list[1].fn = OA_TANH; }",
      "else if (op == 1) { list[0].fn = OA_SIGMOID; list[1].fn = OA_SIGMOID; }"),
+    ("Wb and Rb exchanged", "const float* Wb = a->B ? a->B + d * 2 * GH : NULL;\n    const float* Rb = a->B ? a->B + d * 2 * GH + GH : NULL;",
+     "const float* Wb = a->B ? a->B + d * 2 * GH + GH : NULL;\n    const float* Rb = a->B ? a->B + d * 2 * GH : NULL;"),
+    ("Po and Pf exchanged", "const float* Po = a->P ? a->P + d * 3 * H + H : NULL;\n    const float* Pf = a->P ? a->P + d * 3 * H + 2 * H : NULL;",
+     "const float* Po = a->P ? a->P + d * 3 * H + 2 * H : NULL;\n    const float* Pf = a->P ? a->P + d * 3 * H + H : NULL;"),
+    ("both directions start from direction 0's state", "h[u] = a->h0 ? a->h0[o_sidx(a, d, n) + u] : 0.0f;",
+     "h[u] = a->h0 ? a->h0[o_sidx(a, 0, n) + u] : 0.0f;"),
+    ("both directions use direction 0's R", "const float* Rd = a->R + d * GH * H;", "const float* Rd = a->R;"),
+    ("layout-0 Y direction and batch axes exchanged", "return a->layout == 0 ? ((t * a->dirs + d) * a->N + n) * a->H",
+     "return a->layout == 0 ? ((t * a->N + n) * a->dirs + d) * a->H"),
+    ("layout-0 state direction and batch axes exchanged", "return a->layout == 0 ? (d * a->N + n) * a->H : (n * a->dirs + d) * a->H;",
+     "return a->layout == 0 ? (n * a->dirs + d) * a->H : (n * a->dirs + d) * a->H;"),
     ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
      "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
     ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
