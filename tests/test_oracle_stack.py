@@ -95,3 +95,38 @@ def test_shared_lengths_mask_every_layer():
     Y, yh, _ = oracle.rnn_stack(layers, c0.X, sequence_lens=c0.sequence_lens)
     assert np.all(Y[2:, :, 1] == 0) and np.all(Y[:, :, 2] == 0)
     assert np.all(yh[1][:, 2] == 0)
+
+
+_STACK_INPUT = oracle.stack_input
+
+
+def _stack_input_directions_swapped(Y, layout):
+    Y = np.asarray(Y, np.float32)
+    return _STACK_INPUT(Y[:, ::-1] if layout == 0 else Y[:, :, ::-1], layout)
+
+
+def _stack_input_batch_major(Y, layout):
+    Y = np.asarray(Y, np.float32)
+    if layout == 0:
+        S, D, N, H = Y.shape
+        return np.ascontiguousarray(Y.reshape(S, N, D * H))   # the directions' planes read as rows
+    return _STACK_INPUT(Y, layout)
+
+
+@pytest.mark.parametrize("mistake", [_stack_input_directions_swapped, _stack_input_batch_major])
+def test_planted_handoff_mistakes_are_caught(mistake, monkeypatch):
+    # a plausible misreading of the handoff, planted in the oracle: the
+    # golden cases or the independent transpose formula must reject it
+    monkeypatch.setattr(oracle, "stack_input", mistake)
+    failed = 0
+    for p in FILES:
+        try:
+            test_stack_golden(p)
+        except AssertionError:
+            failed += 1
+    for layout in (0, 1):
+        try:
+            test_stack_input_matches_transpose_reshape(layout)
+        except AssertionError:
+            failed += 1
+    assert failed > 0
