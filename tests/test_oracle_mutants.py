@@ -126,6 +126,11 @@ MUTANTS = [
      "return a->layout == 0 ? ((t * a->N + n) * a->dirs + d) * a->H"),
     ("layout-0 state direction and batch axes exchanged", "return a->layout == 0 ? (d * a->N + n) * a->H : (n * a->dirs + d) * a->H;",
      "return a->layout == 0 ? (n * a->dirs + d) * a->H : (n * a->dirs + d) * a->H;"),
+    ("bidirectional second direction forward", "int reverse = direction == 1 || (direction == 2 && d == 1);",
+     "int reverse = direction == 1;"),
+    ("GRU lbr1 without B resets xw too", "else ph = xw[2 * H + u] + r[u] * rec;", "else ph = r[u] * (xw[2 * H + u] + rec);"),
+    ("GRU lbr0 Wb inside the reset", "ph = xw[2 * H + u] + o_dot(rh, Rh, H);\n                    if (a->B) { ph = ph + Wb[2 * H + u]; ph = ph + Rb[2 * H + u]; }",
+     "ph = xw[2 * H + u] + o_dot(rh, Rh, H);\n                    if (a->B) { ph = ph + r[u] * Wb[2 * H + u]; ph = ph + Rb[2 * H + u]; }"),
     ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
      "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
     ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
