@@ -302,8 +302,10 @@ def measure_l2_gbs(torch, nbytes=32 << 20, reps=10, trials=5):
 
 
 # The sources each kernel is compiled from (its translation units and the
-# headers its code comes from): a committed traffic figure is keyed by their
-# digest, so it stays valid while that kernel's code is unchanged.
+# headers its code comes from; the staged kernel's units also include the
+# dataflow header, none of whose code the staged kernel uses): a committed
+# traffic figure is keyed by their digest, so it stays valid while that
+# kernel's code is unchanged.
 _COMMON = ["tma.cuh", "exact_math.cuh", "io_types.cuh", "rnn_internal.h"]
 KERNEL_SOURCES = {
     "rnn_recurrent_kernel": ["k_recur.cuh", "k_recur_rnn.cu", "k_recur_gru.cu", "k_recur_lstm.cu"] + _COMMON,

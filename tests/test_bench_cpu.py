@@ -175,6 +175,30 @@ def test_source_digest_is_per_kernel():
     assert set(_build.SOURCES) - covered == {"rnn_api.cpp", "k_misc.cu", "rnn_static.cu"}
 
 
+def test_kernel_sources_cover_their_includes():
+    # every header a kernel's translation units include (transitively) is in
+    # its digest, except the dataflow header in the staged kernel's units
+    import re
+    csrc = os.path.join(ROOT, "onnx_recurrent_gb300", "csrc")
+
+    def closure(name, seen):
+        if name in seen:
+            return seen
+        seen.add(name)
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            for m in re.finditer(r'#include\s+"([^"]+)"', f.read()):
+                if os.path.exists(os.path.join(csrc, m.group(1))):
+                    closure(m.group(1), seen)
+        return seen
+
+    allowed = {"rnn_recurrent_kernel": {"k_recur2.cuh"}}
+    for k, srcs in bench.KERNEL_SOURCES.items():
+        inc = set()
+        for tu in (s for s in srcs if s.endswith(".cu")):
+            inc |= closure(tu, set())
+        assert inc - set(srcs) <= allowed.get(k, set()), k
+
+
 def test_source_digest_ignores_comments_and_blank_space():
     a = 'int f(int x) {  // one\n  return x + 1; /* two */ }\nconst char* s = "a // not a comment";\n'
     b = 'int f(int x) {\n\n    return x + 1;   }\nconst char* s = "a // not a comment";'
