@@ -97,10 +97,12 @@ def test_cell_clip_saturates_exactly():
 
 
 def test_cell_nan_is_canonical():
-    X = np.array([[np.nan]], np.float32)
-    Ho = oracle.rnn_cell(1, 1, X, np.zeros((1, 1), np.float32), np.ones((1, 1), np.float32),
-                         np.ones((1, 1), np.float32), np.zeros(1, np.float32), "Relu")
-    assert Ho.view(np.uint32)[0, 0] == 0x7FC00000
+    # the quiet NaN and a negative NaN with a payload both come out as 0x7FC00000
+    for bits in (0x7FC00000, 0xFFA00001):
+        X = np.array([[bits]], np.uint32).view(np.float32)
+        Ho = oracle.rnn_cell(1, 1, X, np.zeros((1, 1), np.float32), np.ones((1, 1), np.float32),
+                             np.ones((1, 1), np.float32), np.zeros(1, np.float32), "Relu")
+        assert Ho.view(np.uint32)[0, 0] == 0x7FC00000, hex(bits)
 
 
 @pytest.mark.parametrize("bad", [dict(activation="Affine"), dict(activation="LeakyRelu"),

@@ -131,6 +131,11 @@ MUTANTS = [
     ("GRU lbr1 without B resets xw too", "else ph = xw[2 * H + u] + r[u] * rec;", "else ph = r[u] * (xw[2 * H + u] + rec);"),
     ("GRU lbr0 Wb inside the reset", "ph = xw[2 * H + u] + o_dot(rh, Rh, H);\n                    if (a->B) { ph = ph + Wb[2 * H + u]; ph = ph + Rb[2 * H + u]; }",
      "ph = xw[2 * H + u] + o_dot(rh, Rh, H);\n                    if (a->B) { ph = ph + r[u] * Wb[2 * H + u]; ph = ph + Rb[2 * H + u]; }"),
+    ("cell accepts clip 0", "if (!(clip > 0.0f)) return 1;", "if (clip < 0.0f) return 1;"),
+    ("cell clips NaN to the bound", "            if (pre > clip) pre = clip;", "            if (!(pre <= clip)) pre = clip;"),
+    ("cell batch rows share Hprev", "float rec = o_dot(Hprev + n * H, R + j * H, H);", "float rec = o_dot(Hprev, R + j * H, H);"),
+    ("cell NaN not canonical", "Ho[n * H + j] = o_canon(oracle_activation(fn, 0.0f, 0.0f, pre));",
+     "Ho[n * H + j] = oracle_activation(fn, 0.0f, 0.0f, pre);"),
     ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
      "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
     ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
@@ -179,8 +184,8 @@ def _battery():
                            lambda a=act, c=clip: tcell.test_cell_is_the_sequence_operator_at_one_step(a, c)))
     checks.append(("cell clip", tcell.test_cell_clip_saturates_exactly))
     checks.append(("cell nan", tcell.test_cell_nan_is_canonical))
-    checks.append(("cell rejects affine", lambda: tcell.test_cell_rejects_what_the_page_excludes(
-        dict(activation="Affine"))))
+    for bad in (dict(activation="Affine"), dict(clip=0.0), dict(clip=-1.0), dict(clip=float("nan"))):
+        checks.append((f"cell rejects {bad}", lambda b=bad: tcell.test_cell_rejects_what_the_page_excludes(b)))
     for fn in (tm.test_exp_special_values, tm.test_log_special_values, tm.test_tanh_special_values,
                tm.test_relu_points, tm.test_leaky_thresholded_points,
                tm.test_hardsigmoid_affine_softsign_points, tm.test_softplus_points,
