@@ -136,6 +136,10 @@ MUTANTS = [
     ("cell batch rows share Hprev", "float rec = o_dot(Hprev + n * H, R + j * H, H);", "float rec = o_dot(Hprev, R + j * H, H);"),
     ("cell NaN not canonical", "Ho[n * H + j] = o_canon(oracle_activation(fn, 0.0f, 0.0f, pre));",
      "Ho[n * H + j] = oracle_activation(fn, 0.0f, 0.0f, pre);"),
+    ("LSTM Rb before Wb", "pi = pi + Wb[u];         pi = pi + Rb[u];", "pi = pi + Rb[u];         pi = pi + Wb[u];"),
+    ("GRU Rb before Wb", "pz = pz + Wb[u]; pz = pz + Rb[u];", "pz = pz + Rb[u]; pz = pz + Wb[u];"),
+    ("LSTM bias before rec", "float pc = xw[3 * H + u] + o_dot(h, Rd + (3 * H + u) * H, H);",
+     "float pc = (a->B ? xw[3 * H + u] + Wb[3 * H + u] : xw[3 * H + u]) + o_dot(h, Rd + (3 * H + u) * H, H);"),
     ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
      "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
     ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
