@@ -140,6 +140,8 @@ MUTANTS = [
     ("GRU Rb before Wb", "pz = pz + Wb[u]; pz = pz + Rb[u];", "pz = pz + Rb[u]; pz = pz + Wb[u];"),
     ("LSTM bias before rec", "float pc = xw[3 * H + u] + o_dot(h, Rd + (3 * H + u) * H, H);",
      "float pc = (a->B ? xw[3 * H + u] + Wb[3 * H + u] : xw[3 * H + u]) + o_dot(h, Rd + (3 * H + u) * H, H);"),
+    ("GRU lbr0 candidate Rb before Wb", "if (a->B) { ph = ph + Wb[2 * H + u]; ph = ph + Rb[2 * H + u]; }",
+     "if (a->B) { ph = ph + Rb[2 * H + u]; ph = ph + Wb[2 * H + u]; }"),
     ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
      "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
     ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
