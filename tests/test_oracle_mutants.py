@@ -142,6 +142,28 @@ MUTANTS = [
      "float pc = (a->B ? xw[3 * H + u] + Wb[3 * H + u] : xw[3 * H + u]) + o_dot(h, Rd + (3 * H + u) * H, H);"),
     ("GRU lbr0 candidate Rb before Wb", "if (a->B) { ph = ph + Wb[2 * H + u]; ph = ph + Rb[2 * H + u]; }",
      "if (a->B) { ph = ph + Rb[2 * H + u]; ph = ph + Wb[2 * H + u]; }"),
+    ("GRU update as ht + z*(h - ht)", "hn[u] = (1.0f - z[u]) * ht + z[u] * h[u];", "hn[u] = ht + z[u] * (h[u] - ht);"),
+    ("LSTM peephole before the biases",
+     "                if (a->B) {\n"
+     "                    pi = pi + Wb[u];         pi = pi + Rb[u];\n"
+     "                    po = po + Wb[H + u];     po = po + Rb[H + u];\n"
+     "                    pf = pf + Wb[2 * H + u]; pf = pf + Rb[2 * H + u];\n"
+     "                    pc = pc + Wb[3 * H + u]; pc = pc + Rb[3 * H + u];\n"
+     "                }\n"
+     "                if (a->P) {\n"
+     "                    pi = pi + Pi[u] * c[u];\n"
+     "                    pf = pf + Pf[u] * c[u];\n"
+     "                }\n",
+     "                if (a->P) {\n"
+     "                    pi = pi + Pi[u] * c[u];\n"
+     "                    pf = pf + Pf[u] * c[u];\n"
+     "                }\n"
+     "                if (a->B) {\n"
+     "                    pi = pi + Wb[u];         pi = pi + Rb[u];\n"
+     "                    po = po + Wb[H + u];     po = po + Rb[H + u];\n"
+     "                    pf = pf + Wb[2 * H + u]; pf = pf + Rb[2 * H + u];\n"
+     "                    pc = pc + Wb[3 * H + u]; pc = pc + Rb[3 * H + u];\n"
+     "                }\n"),
     ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
      "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
     ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
