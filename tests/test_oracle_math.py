@@ -97,6 +97,9 @@ def test_relu_points():
 
 def test_leaky_thresholded_points():
     assert list(_a("leakyrelu", [-2.0, 3.0], 0.5)) == [-1.0, 3.0]
+    # x < 0 ? alpha*x : x: a NaN is not < 0, so it is returned; -0 likewise
+    y = _a("leakyrelu", [np.nan, -0.0], 0.5)
+    assert np.isnan(y[0]) and y.view(np.uint32)[1] == 0x80000000
     y = _a("thresholdedrelu", [1.0, 1.5, -3.0, np.nan], 1.0)
     assert y[0] == 0.0 and y[1] == 1.5 and y[2] == 0.0 and y[3] == 0.0
 

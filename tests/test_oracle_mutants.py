@@ -164,6 +164,12 @@ MUTANTS = [
      "                    pf = pf + Wb[2 * H + u]; pf = pf + Rb[2 * H + u];\n"
      "                    pc = pc + Wb[3 * H + u]; pc = pc + Rb[3 * H + u];\n"
      "                }\n"),
+    ("elu at -0 takes the exp branch", "case OA_ELU:             return x >= 0.0f ? x : alpha * (oracle_exp(x) - 1.0f);",
+     "case OA_ELU:             return x > 0.0f ? x : alpha * (oracle_exp(x) - 1.0f);"),
+    ("relu turns -0 into +0", "case OA_RELU:            return x < 0.0f ? 0.0f : x;", "case OA_RELU:            return x <= 0.0f ? 0.0f : x;"),
+    ("hardsigmoid drops NaN", "return v < 0.0f ? 0.0f : (v > 1.0f ? 1.0f : v);", "return !(v >= 0.0f) ? 0.0f : (v > 1.0f ? 1.0f : v);"),
+    ("softplus drops the 1", "x > 20.0f ? x : oracle_log(1.0f + oracle_exp(x))", "x > 20.0f ? x : oracle_log(oracle_exp(x))"),
+    ("leakyrelu NaN to 0", "case OA_LEAKYRELU:       return x < 0.0f ? alpha * x : x;", "case OA_LEAKYRELU:       return x >= 0.0f ? x : alpha * (x != x ? 0.0f : x);"),
     ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
      "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
     ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
