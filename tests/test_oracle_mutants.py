@@ -170,6 +170,11 @@ MUTANTS = [
     ("hardsigmoid drops NaN", "return v < 0.0f ? 0.0f : (v > 1.0f ? 1.0f : v);", "return !(v >= 0.0f) ? 0.0f : (v > 1.0f ? 1.0f : v);"),
     ("softplus drops the 1", "x > 20.0f ? x : oracle_log(1.0f + oracle_exp(x))", "x > 20.0f ? x : oracle_log(oracle_exp(x))"),
     ("leakyrelu NaN to 0", "case OA_LEAKYRELU:       return x < 0.0f ? alpha * x : x;", "case OA_LEAKYRELU:       return x >= 0.0f ? x : alpha * (x != x ? 0.0f : x);"),
+    ("reverse Y written in step order", "            float* y = a->Y + o_yidx(a, t, d, n);\n            for (long u = 0; u < H; ++u) y[u] = o_canon(h[u]);",
+     "            float* y = a->Y + o_yidx(a, s, d, n);\n            for (long u = 0; u < H; ++u) y[u] = o_canon(h[u]);"),
+    ("layout-0 X index batch-major", "return a->layout == 0 ? (t * a->N + n) * a->I : (n * a->S + t) * a->I;",
+     "return a->layout == 0 ? (n * a->S + t) * a->I : (n * a->S + t) * a->I;"),
+    ("reverse projects step s", "        o_project(a, d, t, n, xw);", "        o_project(a, d, s, n, xw);"),
     ("exp overflow threshold 88", "if (x > 89.0f) return o_from_bits(0x7F800000u);",
      "if (x > 88.0f) return o_from_bits(0x7F800000u);"),
     ("exp underflow threshold -100", "if (x < -110.0f) return 0.0f;", "if (x < -100.0f) return 0.0f;"),
